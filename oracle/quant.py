@@ -1,0 +1,223 @@
+"""Quantizer arithmetic of the oracle (fp64 NumPy; test infrastructure only).
+
+Sources, by page and section:
+
+* AngelSlim mcore_qad walkthrough (nxmr.cn/news/131691), section 二.3: the weight
+  seen by the matmul is quantize->dequantize(W; s) with s the trainable quantity;
+  activations are fake-quantized by a pre-hook before each quantized matmul.
+* Same article, section 三, and "MCoreQAD Backend" (mcore_qad.md), "Support Matrix":
+  the formats nvfp4 (FP4 E2M1 weights and activations), w4a16 (INT4 weights,
+  BF16 activations) and fp8 (E4M3 weights and activations).
+
+The pages never write the quantizer formulas down.  The readings used here:
+
+* E2M1 grid {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6} (OCP Microscaling Formats
+  v1.0, E2M1 element type), round to nearest with ties to the even code
+  (IEEE 754 roundTiesToEven), saturating at +-6.
+* E4M3 ("fn" variant: max finite 448, subnormals spaced 2^-9), ties to even,
+  saturating at +-448.
+* INT4 symmetric grid {-8, ..., 7}: round half to even, then clamp.
+* The weight scale is one fp32 number per block of B consecutive elements along K
+  (B = 16 for nvfp4, 128 for INT4 group-128, B = K for fp8 per output row), not
+  itself rounded to a narrower format.
+* x = fp32(w / s) is an IEEE fp32 division; the dequantized product q(x)*s is
+  rounded to fp32 and then to bf16.  Division of two fp32 values done in fp64 and
+  rounded once to fp32 equals the IEEE fp32 quotient (53 >= 2*24 + 2), so these
+  steps are bit-exact while everything else runs in fp64.
+* s == 0 (an all-zero block) gives x = +-0 (the sign of w), output +-0 and a zero
+  LSQ factor.
+* The LSQ straight-through factor (Esser et al., "Learned Step Size
+  Quantization", 2019) is phi = q(x) - x inside the CLOSED clip range and the
+  violated bound outside it.  No 1/sqrt(N*Qp) gradient scale is applied.
+
+Parity pins for every function here live in tests/test_oracle_pins.py.
+"""
+import numpy as np
+
+FMT_NVFP4 = 0       # nvfp4 W4A4: E2M1, block 16 along K, activations block-16 amax/6
+FMT_INT4_G128 = 1   # w4a16: INT4, group 128 along K, activations left in bf16
+FMT_FP8_ROW = 2     # fp8 W8A8: E4M3, one scale per output row, activations per-row amax/448
+
+# (lower clip bound, upper clip bound, divisor used to turn an amax into a scale)
+CLIP = {FMT_NVFP4: (-6.0, 6.0), FMT_INT4_G128: (-8.0, 7.0), FMT_FP8_ROW: (-448.0, 448.0)}
+AMAX_DIV = {FMT_NVFP4: 6.0, FMT_INT4_G128: 7.0, FMT_FP8_ROW: 448.0}
+
+
+def weight_block(fmt, K):
+    """Elements of K that share one weight scale."""
+    return {FMT_NVFP4: 16, FMT_INT4_G128: 128, FMT_FP8_ROW: K}[fmt]
+
+
+# --------------------------------------------------------------------------------------
+# bf16 / fp32 storage
+# --------------------------------------------------------------------------------------
+
+def bf16_to_f64(bits):
+    """uint16 bf16 bit patterns -> exact fp64 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def round_bf16(x):
+    """Round fp64 (or fp32) values ONCE to the nearest bf16 (ties to even).
+
+    bf16 keeps 8 significant bits and fp32's exponent range (normal floor 2^-126,
+    subnormal spacing 2^-133); values that round to 2^128 or beyond become inf.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)                       # |x| = m * 2^e with 0.5 <= m < 1
+    qexp = np.maximum(e - 8, -133)            # spacing of bf16 numbers near x
+    r = np.ldexp(np.rint(np.ldexp(x, -qexp)), qexp)
+    r = np.where(np.abs(r) >= 2.0 ** 128, np.copysign(np.inf, x), r)
+    return np.where(np.isfinite(x), r, x)
+
+
+def f64_to_bf16_bits(x):
+    """fp64 values -> bf16 bit patterns (rounding once, ties to even)."""
+    r = round_bf16(x).astype(np.float32)     # exact: r already lies on the bf16 grid
+    return (r.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def round_f32(x):
+    """Round fp64 values once to fp32 (NumPy's cast is round-to-nearest-even)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------------------
+# Element quantizers q(x): values on the format's grid, as fp64
+# --------------------------------------------------------------------------------------
+
+def e2m1_decode(code):
+    """4-bit E2M1 code (sign, 2 exponent bits, 1 mantissa bit, bias 1) -> value."""
+    code = np.asarray(code, dtype=np.int64)
+    sign = np.where(code & 8, -1.0, 1.0)
+    ex = (code >> 1) & 3
+    man = code & 1
+    mag = np.where(ex == 0, 0.5 * man, (1.0 + 0.5 * man) * np.ldexp(1.0, ex - 1))
+    return sign * mag
+
+
+def q_e2m1(x):
+    """Round to the E2M1 grid, ties to even code, saturating at +-6.
+
+    For |x| the decision points are the midpoints between neighbouring grid values:
+    0.25 (0|0.5), 0.75 (0.5|1), 1.25 (1|1.5), 1.75 (1.5|2), 2.5 (2|3), 3.5 (3|4), 5 (4|6).
+    At a midpoint the result is the neighbour whose mantissa bit is 0 (0, 1, 2, 4 are
+    even; 0.5, 1.5, 3, 6 are odd), so 0.25->0, 0.75->1, 1.25->1, 1.75->2, 2.5->2,
+    3.5->4, 5->4.  Anything above 5 rounds to 6 (satfinite).  The sign is kept, so a
+    negative input that rounds to zero gives -0.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    mag = np.select(
+        [a <= 0.25, a < 0.75, a <= 1.25, a < 1.75, a <= 2.5, a < 3.5, a <= 5.0],
+        [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0],
+        default=6.0)
+    return np.copysign(mag, x)
+
+
+def q_e4m3(x):
+    """Round to the E4M3 (fn) grid, ties to even, saturating at +-448.
+
+    Normal binades [2^e, 2^(e+1)) for e >= -6 hold 8 values spaced 2^(e-3); below
+    2^-6 the subnormals are spaced 2^-9.  Scaling by a power of two is exact, so
+    rint(|x| / spacing) * spacing is the tie-to-even rounding on that binade; a
+    result that carries to 2^(e+1) is still on the grid.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                       # a = m * 2^e, 0.5 <= m < 1 -> binade e-1
+    binade = np.maximum(e - 1, -6)
+    spacing = np.ldexp(1.0, binade - 3)
+    mag = np.minimum(np.rint(a / spacing) * spacing, 448.0)
+    mag = np.where(a == 0, 0.0, mag)
+    return np.copysign(mag, x)
+
+
+def q_int4(x):
+    """Round half to even to an integer, then clamp to the INT4 range [-8, 7]."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.clip(np.rint(x), -8.0, 7.0)
+
+
+def q_fmt(fmt, x):
+    return {FMT_NVFP4: q_e2m1, FMT_INT4_G128: q_int4, FMT_FP8_ROW: q_e4m3}[fmt](x)
+
+
+# --------------------------------------------------------------------------------------
+# Fake quantization
+# --------------------------------------------------------------------------------------
+
+def _quotient(w, s):
+    """x = fp32(w / s) with IEEE fp32 rounding; s == 0 gives +-0 with w's sign."""
+    with np.errstate(divide="ignore", invalid="ignore"):
+        x = round_f32(w / np.where(s == 0, 1.0, s))
+    return np.where(s == 0, np.copysign(0.0, w), x)
+
+
+def _dequant(qx, s):
+    """bf16(fp32(q * s)): the product rounded to fp32, then to bf16."""
+    return round_bf16(round_f32(qx * s))
+
+
+def weight_quotient(fmt, w_bits, scale):
+    """x = fp32(W / s) for stacked weights [..., N, K] and scales [..., N, K / B]."""
+    w = bf16_to_f64(w_bits)
+    K = w.shape[-1]
+    s = np.repeat(np.asarray(scale, dtype=np.float64), weight_block(fmt, K), axis=-1)
+    return w, s, _quotient(w, s)
+
+
+def fakequant_weight(fmt, w_bits, scale):
+    """W_hat = bf16(fp32(q(fp32(W / s)) * s)), element by element (section 二.3/二.4).
+
+    w_bits: uint16 bf16 [..., N, K]; scale: fp32 [..., N, K / B].  Returns fp64 values
+    that all lie on the bf16 grid.
+    """
+    _, s, x = weight_quotient(fmt, w_bits, scale)
+    return _dequant(q_fmt(fmt, x), s)
+
+
+def act_scale(fmt, a):
+    """Dynamic activation scale per block along the last axis (detached, not learnable).
+
+    nvfp4: one scale per 16 elements, fp32(amax / 6).  fp8: one per row, fp32(amax / 448).
+    Returns the scale broadcast to a's shape.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    if fmt == FMT_NVFP4:
+        blocks = a.reshape(a.shape[:-1] + (a.shape[-1] // 16, 16))
+        amax = np.abs(blocks).max(axis=-1)
+        return np.repeat(round_f32(amax / 6.0), 16, axis=-1)
+    if fmt == FMT_FP8_ROW:
+        amax = np.abs(a).max(axis=-1, keepdims=True)
+        return np.broadcast_to(round_f32(amax / 448.0), a.shape)
+    raise ValueError("format has no activation quantizer")
+
+
+def fakequant_act(fmt, a):
+    """Activation fake-quant a_hat = bf16(fp32(q(fp32(a / s_a)) * s_a)); identity for w4a16."""
+    a = np.asarray(a, dtype=np.float64)
+    if fmt == FMT_INT4_G128:
+        return a.copy()
+    s = act_scale(fmt, a)
+    return _dequant(q_fmt(fmt, _quotient(a, s)), s)
+
+
+def lsq_factor(fmt, x):
+    """LSQ straight-through derivative of s*q(w/s) with respect to s, given x = fp32(w/s).
+
+    Inside the closed clip range [lo, hi] it is q(x) - x; below it lo, above it hi.
+    """
+    lo, hi = CLIP[fmt]
+    x = np.asarray(x, dtype=np.float64)
+    return np.where(x < lo, lo, np.where(x > hi, hi, q_fmt(fmt, x) - x))
+
+
+def scale_grad_from_wgrad(fmt, dw, w_bits, scale):
+    """g_s[..., n, b] = sum over k in block b of dW[..., n, k] * phi(W[..., n, k], s[..., n, b])."""
+    _, _, x = weight_quotient(fmt, w_bits, scale)
+    prod = np.asarray(dw, dtype=np.float64) * lsq_factor(fmt, x)
+    K = prod.shape[-1]
+    B = weight_block(fmt, K)
+    return prod.reshape(prod.shape[:-1] + (K // B, B)).sum(axis=-1)

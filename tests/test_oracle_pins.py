@@ -1,0 +1,432 @@
+"""Pins of the oracle against facts fixed outside it (CPU only).
+
+Each test checks the oracle against something it does not itself contain: golden
+values worked by hand from a format's definition (tests/golden/, cited there), a
+library routine (torch's float8_e4m3fn cast, NumPy's stable argsort, torch's silu),
+brute-force enumeration of a grid, autograd of the straight-through definition,
+or central finite differences.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe as M
+from oracle import quant as Q
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+def _f32_sweep(lo, hi, n, rng):
+    """Random fp32 values in [lo, hi] plus the fp32 neighbours of every quarter-integer and grid point."""
+    x = rng.uniform(lo, hi, n).astype(np.float32)
+    marks = np.arange(lo * 64, hi * 64 + 1) / 64.0
+    m32 = marks.astype(np.float32)
+    near = np.concatenate([m32, np.nextafter(m32, np.float32(np.inf)), np.nextafter(m32, np.float32(-np.inf))])
+    return np.concatenate([x, near, -x, -near]).astype(np.float64)
+
+
+def _brute_nearest(x, grid, even):
+    """Nearest grid value to each x; ties go to the value whose `even` flag is set."""
+    grid = np.asarray(grid, dtype=np.float64)
+    even = np.asarray(even, dtype=bool)
+    dist = np.abs(x[:, None] - grid[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    pick_even = cand & even[None, :]
+    use = np.where(pick_even.any(axis=1, keepdims=True), pick_even, cand)
+    return grid[np.argmax(use, axis=1)]
+
+
+# ------------------------------------------------------------------------------ E2M1
+
+def test_e2m1_decode_matches_spec_table():
+    rows = _rows("e2m1_grid.txt")
+    codes = np.array([int(r[0]) for r in rows])
+    want = np.array([float(r[1]) for r in rows])
+    got = Q.e2m1_decode(codes)
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
+def test_e2m1_tie_table():
+    rows = _rows("e2m1_ties.txt")
+    x = np.array([float.fromhex(r[0]) for r in rows])
+    want = np.array([float(r[1]) for r in rows])
+    got = Q.q_e2m1(x)
+    assert np.array_equal(got, want), list(zip(x, got, want))
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
+def test_e2m1_bruteforce_nearest_even_code():
+    rng = np.random.default_rng(1)
+    x = _f32_sweep(-8.0, 8.0, 20000, rng)
+    codes = np.arange(16)
+    grid = Q.e2m1_decode(codes)
+    even = (codes & 1) == 0
+    want = _brute_nearest(np.abs(x), grid[:8], even[:8]) * np.where(np.signbit(x), -1.0, 1.0)
+    got = Q.q_e2m1(x)
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(x))
+
+
+# ------------------------------------------------------------------------------ E4M3
+
+def _e4m3_positive_grid():
+    vals, even = [], []
+    for code in range(0x7F):          # 0x7F is NaN in the fn variant
+        ex, man = code >> 3, code & 7
+        vals.append(man * 2.0 ** -9 if ex == 0 else (1 + man / 8) * 2.0 ** (ex - 7))
+        even.append(man % 2 == 0)
+    return np.array(vals), np.array(even)
+
+
+def test_e4m3_golden_points():
+    rows = _rows("e4m3_points.txt")
+    x = np.array([float.fromhex(r[0]) for r in rows])
+    want = np.array([float.fromhex(r[1]) for r in rows])
+    got = Q.q_e4m3(x)
+    assert np.array_equal(got, want), list(zip(x, got, want))
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
+def test_e4m3_matches_torch_cast_inside_range():
+    rng = np.random.default_rng(2)
+    x = np.concatenate([_f32_sweep(-8.0, 8.0, 20000, rng),
+                        rng.uniform(-448, 448, 20000).astype(np.float32).astype(np.float64),
+                        (rng.standard_normal(20000) * 1e-3).astype(np.float32).astype(np.float64)])
+    x = x[np.abs(x) <= 448]
+    lib = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(Q.q_e4m3(x), lib)
+
+
+def test_e4m3_bruteforce_with_saturation():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-600, 600, 5000), rng.standard_normal(5000) * 0.01]).astype(np.float32)
+    x = x.astype(np.float64)
+    grid, even = _e4m3_positive_grid()
+    want = _brute_nearest(np.abs(x), grid, even) * np.where(np.signbit(x), -1.0, 1.0)
+    assert np.array_equal(Q.q_e4m3(x), want)
+
+
+# ------------------------------------------------------------------------------ INT4
+
+def test_int4_bruteforce_nearest_even():
+    rng = np.random.default_rng(4)
+    x = np.concatenate([rng.uniform(-12, 12, 20000), np.arange(-24, 25) / 2.0])
+    grid = np.arange(-8, 8, dtype=np.float64)
+    want = _brute_nearest(x, grid, grid % 2 == 0)
+    assert np.array_equal(Q.q_int4(x), want)
+
+
+# ------------------------------------------------------------------------------ bf16 rounding
+
+def test_round_bf16_fp32_inputs_match_torch():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(50000) * 10.0 ** rng.integers(-30, 30, 50000),
+                        [0.0, -0.0, 3.0e38, -3.0e38, 1e-40]]).astype(np.float32)
+    lib = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(Q.round_bf16(x.astype(np.float64)), lib)
+
+
+def test_round_bf16_fp64_is_single_rounding():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal(50000) * 10.0 ** rng.integers(-20, 20, 50000)
+    got = Q.round_bf16(x)
+    # the three bf16 numbers around the truncation of fp32(x)
+    t = (x.astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000))
+    cands = []
+    for dlt in (-1, 0, 1):
+        c = (t.astype(np.int64) + dlt * 0x10000).astype(np.uint32).view(np.float32).astype(np.float64)
+        cands.append(c)
+    cands = np.stack(cands, 1)
+    dist = np.abs(cands - x[:, None])
+    best = dist.min(1, keepdims=True)
+    tie_even = (dist == best) & (((cands.astype(np.float32).view(np.uint32) >> 16) & 1) == 0)
+    use = np.where(tie_even.any(1, keepdims=True), tie_even, dist == best)
+    want = cands[np.arange(x.size), np.argmax(use, 1)]
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------------------------ fake quant
+
+def _weights(fmt, E=2, N=8, K=256, seed=7, outliers=True):
+    g = torch.Generator().manual_seed(seed)
+    w = torch.randn((E, N, K), generator=g) * 0.02
+    if outliers:
+        w[0, 0, :5] = torch.tensor([0.5, -0.5, 0.0, -0.0, 1e-30])
+        w[1, 1, :16] = 0.0                       # an all-zero block -> zero scale
+    w = w.to(torch.bfloat16)
+    B = Q.weight_block(fmt, K)
+    amax = w.float().abs().reshape(E, N, K // B, B).amax(-1)
+    s = (amax / Q.AMAX_DIV[fmt] * (1 + (torch.rand(amax.shape, generator=g) * 0.2 - 0.1))).float()
+    bits = w.view(torch.int16).numpy().view(np.uint16)
+    return bits, s.numpy()
+
+
+@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+def test_fakequant_idempotent(fmt):
+    bits, s = _weights(fmt)
+    w1 = Q.fakequant_weight(fmt, bits, s)
+    w2 = Q.fakequant_weight(fmt, Q.f64_to_bf16_bits(w1), s)
+    assert np.array_equal(Q.f64_to_bf16_bits(w1), Q.f64_to_bf16_bits(w2))
+    assert np.all(np.isfinite(w1))
+
+
+@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+def test_fakequant_outputs_lie_on_scaled_grid(fmt):
+    bits, s = _weights(fmt, N=4, K=128)
+    what = Q.fakequant_weight(fmt, bits, s)
+    K = bits.shape[-1]
+    sf = np.repeat(s.astype(np.float64), Q.weight_block(fmt, K), axis=-1)
+    if fmt == Q.FMT_NVFP4:
+        grid = Q.e2m1_decode(np.arange(16))
+    elif fmt == Q.FMT_INT4_G128:
+        grid = np.arange(-8, 8, dtype=np.float64)
+    else:
+        pos, _ = _e4m3_positive_grid()
+        grid = np.concatenate([pos, -pos])
+    # every output equals bf16(fp32(g * s)) for some g of the grid (enumerated, not computed by q)
+    cand = Q.round_bf16(Q.round_f32(grid[None, :] * sf.reshape(-1)[:, None]))
+    hit = (cand == what.reshape(-1)[:, None]).any(axis=1)
+    assert hit.all()
+
+
+def test_fakequant_zero_scale_block_gives_signed_zero():
+    bits, s = _weights(Q.FMT_NVFP4)
+    assert s[1, 1, 0] == 0
+    what = Q.fakequant_weight(Q.FMT_NVFP4, bits, s)
+    blk = what[1, 1, :16]
+    assert np.all(blk == 0)
+    w = Q.bf16_to_f64(bits)[1, 1, :16]
+    assert np.array_equal(np.signbit(blk), np.signbit(w))
+
+
+@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_FP8_ROW])
+def test_act_fakequant_properties(fmt):
+    rng = np.random.default_rng(8)
+    a = Q.round_bf16(rng.standard_normal((6, 64)))
+    a[2, :16] = 0.0
+    ah = Q.fakequant_act(fmt, a)
+    assert np.all(np.isfinite(ah))
+    assert np.all(ah[2, :16] == 0)
+    # the block maximum maps to the top of the grid, so it is kept to bf16 accuracy
+    blk = 16 if fmt == Q.FMT_NVFP4 else 64
+    ab = np.abs(a).reshape(6, -1, blk)
+    hb = np.abs(ah).reshape(6, -1, blk)
+    i = ab.argmax(-1)
+    amax = np.take_along_axis(ab, i[..., None], -1)[..., 0]
+    hmax = np.take_along_axis(hb, i[..., None], -1)[..., 0]
+    assert np.allclose(hmax, amax, rtol=2 ** -7, atol=0)
+    # idempotent up to the dynamic scale being recomputed from the quantized block
+    assert np.array_equal(Q.fakequant_act(fmt, ah), ah)
+
+
+def test_int4_has_no_activation_quant():
+    a = Q.round_bf16(np.random.default_rng(9).standard_normal((3, 256)))
+    assert np.array_equal(Q.fakequant_act(Q.FMT_INT4_G128, a), a)
+
+
+# ------------------------------------------------------------------------------ LSQ factor
+
+@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+def test_scale_grad_zero_for_weights_on_grid_points(fmt):
+    E, N, K = 2, 4, 256
+    B = Q.weight_block(fmt, K)
+    rng = np.random.default_rng(10)
+    if fmt == Q.FMT_NVFP4:
+        grid = Q.e2m1_decode(np.arange(16))
+    elif fmt == Q.FMT_INT4_G128:
+        grid = np.arange(-8, 8, dtype=np.float64)
+    else:
+        pos, _ = _e4m3_positive_grid()
+        grid = np.concatenate([pos, -pos])
+    s = 2.0 ** rng.integers(-8, -2, (E, N, K // B))        # powers of two: g * s exact in bf16
+    g = rng.choice(grid, (E, N, K))
+    lo, hi = Q.CLIP[fmt]
+    g[0, 0, 0], g[0, 0, 1] = lo, hi                         # the clip bounds themselves (closed range)
+    w = g * np.repeat(s, B, -1)
+    bits = Q.f64_to_bf16_bits(w)
+    assert np.array_equal(Q.bf16_to_f64(bits), w)
+    dw = rng.standard_normal((E, N, K))
+    ds = Q.scale_grad_from_wgrad(fmt, dw, bits, s.astype(np.float32))
+    assert np.all(ds == 0.0)
+
+
+@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+def test_lsq_factor_structure(fmt):
+    lo, hi = Q.CLIP[fmt]
+    rng = np.random.default_rng(11)
+    x = Q.round_f32(rng.uniform(2 * lo, 2 * hi, 20000))
+    phi = Q.lsq_factor(fmt, x)
+    inside = (x >= lo) & (x <= hi)
+    assert np.all(phi[x < lo] == lo) and np.all(phi[x > hi] == hi)
+    # inside the range x + phi is the quantized value: on the grid and the nearest grid point
+    if fmt == Q.FMT_NVFP4:
+        grid = Q.e2m1_decode(np.arange(16))
+    elif fmt == Q.FMT_INT4_G128:
+        grid = np.arange(-8, 8, dtype=np.float64)
+    else:
+        pos, _ = _e4m3_positive_grid()
+        grid = np.concatenate([pos, -pos])
+    xin, qin = x[inside], x[inside] + phi[inside]
+    assert np.isin(qin, grid).all()
+    nearest = np.abs(xin[:, None] - grid[None, :]).min(1)
+    assert np.allclose(np.abs(phi[inside]), nearest, rtol=0, atol=1e-12)
+
+
+def _ste_fakequant_torch(fmt, w, s):
+    """s * q_ste(w / s) with autograd: inside the clip range the rounding residual is
+    detached (straight-through), outside the clamp has zero slope."""
+    lo, hi = Q.CLIP[fmt]
+    xd = w / s
+    x = xd + (xd.float().double() - xd).detach()          # the fp32 quotient, same slope
+    if fmt == Q.FMT_FP8_ROW:
+        qx = x.detach().float().to(torch.float8_e4m3fn).double()
+    elif fmt == Q.FMT_INT4_G128:
+        qx = torch.round(x.detach())                       # half to even
+    else:
+        grid = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64)
+        a = x.detach().abs().clamp(max=6.0)
+        d = (a[..., None] - grid).abs()
+        best = d.min(-1, keepdim=True).values
+        evenmask = torch.tensor([1, 0, 1, 0, 1, 0, 1, 0], dtype=torch.bool)
+        tie = (d == best) & evenmask
+        use = torch.where(tie.any(-1, keepdim=True), tie, d == best)
+        qx = grid[use.float().argmax(-1)] * torch.sign(x.detach())
+    inside = (x >= lo) & (x <= hi)
+    xq = torch.where(inside, x + (qx - x).detach(), x.clamp(lo, hi))
+    return s * xq
+
+
+@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+def test_scale_grad_matches_autograd_of_ste_definition(fmt):
+    bits, s = _weights(fmt, E=2, N=4, K=256, seed=12)
+    s = s * np.float32(0.7)                                 # push some weights past the clip bound
+    s = s.astype(np.float32)
+    K = bits.shape[-1]
+    B = Q.weight_block(fmt, K)
+    rng = np.random.default_rng(13)
+    dw = rng.standard_normal(bits.shape)
+    w_t = torch.from_numpy(Q.bf16_to_f64(bits))
+    s_t = torch.from_numpy(s.astype(np.float64)).requires_grad_(True)
+    s_full = s_t.repeat_interleave(B, dim=-1)
+    safe = torch.where(s_full == 0, torch.ones_like(s_full), s_full)
+    what = _ste_fakequant_torch(fmt, w_t, safe)
+    what = torch.where(s_full == 0, torch.zeros_like(what), what)
+    (what * torch.from_numpy(dw)).sum().backward()
+    want = s_t.grad.numpy()
+    got = Q.scale_grad_from_wgrad(fmt, dw, bits, s)
+    # autograd's slope uses the fp64 quotient w/s, the oracle's the fp32 one: they differ
+    # by ~1e-7 relative; a dropped term or a wrong sign would differ by O(1)
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-5)
+
+
+# ------------------------------------------------------------------------------ routing
+
+def test_route_matches_stable_argsort():
+    rng = np.random.default_rng(14)
+    T, E, k = 300, 7, 3
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    rt = M.route(idx, E)
+    order = np.argsort(idx.reshape(-1), kind="stable")
+    assert np.array_equal(rt["row_token"] * k + rt["row_slot"], order)
+    assert np.array_equal(rt["counts"], np.bincount(idx.reshape(-1), minlength=E))
+    assert rt["error"] == 0
+
+
+def test_route_hand_worked_example_with_invalid_pairs():
+    rows = _rows("route_small.txt")
+    idx = np.array([[int(v) for v in r[1:]] for r in rows if r[0] == "idx"])
+    want_rows = [(int(r[1]), int(r[2])) for r in rows if r[0] == "row"]
+    counts = [int(v) for r in rows if r[0] == "counts" for v in r[1:]]
+    err = [int(r[1]) for r in rows if r[0] == "error"][0]
+    rt = M.route(idx, 3)
+    assert list(zip(rt["row_token"], rt["row_slot"])) == want_rows
+    assert list(rt["counts"]) == counts
+    assert rt["error"] == err
+    assert rt["row_of"][3, 0] == -1 and rt["row_of"][2, 1] == -1
+
+
+# ------------------------------------------------------------------------------ grouped GEMM
+
+def test_grouped_gemm_against_triple_loops():
+    rng = np.random.default_rng(15)
+    counts = [0, 1, 5]
+    off = np.concatenate([[0], np.cumsum(counts)])
+    R, E, N, K = off[-1], 3, 4, 6
+    a = rng.standard_normal((R, K))
+    w = rng.standard_normal((E, N, K))
+    b = rng.standard_normal((R, N))
+    nt = M.grouped_gemm_nt(a, w, off)
+    nn = M.grouped_gemm_nn(b, w, off)
+    wg = M.grouped_wgrad(b, a, off, E)
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            for n in range(N):
+                assert abs(nt[r, n] - sum(a[r, kk] * w[e, n, kk] for kk in range(K))) < 1e-12
+            for kk in range(K):
+                assert abs(nn[r, kk] - sum(b[r, n] * w[e, n, kk] for n in range(N))) < 1e-12
+        for n in range(N):
+            for kk in range(K):
+                want = sum(b[r, n] * a[r, kk] for r in range(off[e], off[e + 1]))
+                assert abs(wg[e, n, kk] - want) < 1e-12
+
+
+# ------------------------------------------------------------------------------ the layer
+
+def _layer(T=24, E=3, d=32, F=16, k=2, seed=16):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((T, d), generator=g, dtype=torch.float64)
+    w13 = torch.randn((E, 2 * F, d), generator=g, dtype=torch.float64) * 0.3
+    w2 = torch.randn((E, d, F), generator=g, dtype=torch.float64) * 0.3
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).numpy()
+    p = torch.softmax(torch.randn((T, k), generator=g, dtype=torch.float64), 1).numpy()
+    dout = torch.randn((T, d), generator=g, dtype=torch.float64).numpy()
+    return x.numpy(), w13.numpy(), w2.numpy(), idx, p, dout
+
+
+def _fwd(x, w13, w2, idx, p):
+    return M.moe_forward(Q.FMT_NVFP4, x, idx, p, w13, None, w2, None, quant=False, round_bf16=False)
+
+
+def test_dense_special_case_matches_torch_swiglu_mlp():
+    x, w13, w2, _, _, _ = _layer(E=1, k=1)
+    T = x.shape[0]
+    out = _fwd(x, w13, w2, np.zeros((T, 1), np.int64), np.ones((T, 1)))["out"]
+    xt = torch.from_numpy(x)
+    F_ = w2.shape[2]
+    gate = xt @ torch.from_numpy(w13[0, :F_]).T
+    up = xt @ torch.from_numpy(w13[0, F_:]).T
+    want = (torch.nn.functional.silu(gate) * up) @ torch.from_numpy(w2[0]).T
+    assert np.allclose(out, want.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_finite_differences_of_the_ste_free_layer():
+    x, w13, w2, idx, p, dout = _layer()
+    fwd = _fwd(x, w13, w2, idx, p)
+    bwd = M.moe_dgrad(dout, p, fwd, round_bf16=False)
+    dw13, dw2 = M.moe_weight_grads(fwd, bwd)
+
+    def loss(x_, w13_, w2_, p_):
+        return float((_fwd(x_, w13_, w2_, idx, p_)["out"] * dout).sum())
+
+    h = 1e-6
+    rng = np.random.default_rng(17)
+    for arr, grad, name in ((x, bwd["dx"], "x"), (w13, dw13, "w13"), (w2, dw2, "w2"), (p, bwd["dprobs"], "p")):
+        for _ in range(6):
+            i = tuple(rng.integers(0, s) for s in arr.shape)
+            args = {"x": x, "w13": w13, "w2": w2, "p": p}
+            plus = {kk: v.copy() for kk, v in args.items()}
+            minus = {kk: v.copy() for kk, v in args.items()}
+            plus[name][i] += h
+            minus[name][i] -= h
+            fd = (loss(plus["x"], plus["w13"], plus["w2"], plus["p"])
+                  - loss(minus["x"], minus["w13"], minus["w2"], minus["p"])) / (2 * h)
+            assert abs(fd - grad[i]) <= 1e-6 * max(1.0, abs(fd)), (name, i, fd, grad[i])
