@@ -1,0 +1,393 @@
+"""Benchmark of one scale-only QAD MoE layer step (fwd + input grad + scale grad) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch: qad_moe_fwd, qad_moe_bwd_dgrad and
+qad_moe_bwd_scalegrad through the C ABI.  `value` is tokens/s with inputs resident in HBM;
+`e2e` adds, every step, the host->device copy of the step's activations and routing from
+pinned memory and the device->host read of out, dx and the scale gradients.  Every step
+streams far more than the 129 MB L2 (weights alone are 1.2 GB at the default workload),
+so no explicit flush is used.  Under torchrun each rank runs its own replica on its own
+batch (weak scaling) and the scale gradients are averaged over ranks, as data-parallel
+training does.  `--impl reference` times the fp64 CPU oracle on a bounded sample of the
+same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "qwen3_30b_a3b_nvfp4"
+METRIC = "MoE-layer fwd+bwd tokens/s (nvfp4, 1 GB300); % HBM / tensor-core roofline"
+FMT_NAME = {0: "nvfp4", 1: "w4a16", 2: "fp8"}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_per_launch(cfg):
+    """FLOPs per GEMM launch (routed rows only) and bytes per weight-fake-quant launch."""
+    R = cfg["T"] * cfg["topk"]
+    d, F, E = cfg["d"], cfg["F"], cfg["E"]
+    fc1 = 2.0 * R * 2 * F * d
+    fc2 = 2.0 * R * d * F
+    bpe = {0: 2 + 4.0 / 16 + 2, 1: 2 + 4.0 / 128 + 2, 2: None}[cfg["fmt"]]
+    n13, n2 = E * 2 * F * d, E * d * F
+    if bpe is None:  # one fp32 scale per row
+        fq = (4.0 * n13 + 4 * E * 2 * F + 4.0 * n2 + 4 * E * d) / 2
+    else:
+        fq = bpe * (n13 + n2) / 2  # average of the two launches
+    return {"gemm_fc1_swiglu_aq": ("tensor", fc1), "gemm_fc2": ("tensor", fc2),
+            "gemm_dgrad_fc2_swiglu_bwd": ("tensor", fc2), "gemm_dgrad_fc1": ("tensor", fc1),
+            "gemm_wgrad_fc2_scalegrad": ("tensor", fc2), "gemm_wgrad_fc1_scalegrad": ("tensor", fc1),
+            "fakequant_w": ("hbm", fq)}
+
+
+def _traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if its source hash still matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+    for ln in open(path):
+        f = ln.split()
+        if len(f) >= 4 and not ln.startswith("#") and f[0] == kernel and f[1] == workload:
+            src = os.path.join(ROOT, "scale_only_quantization_gb300", "csrc", f[3].split(":")[0])
+            if not os.path.exists(src):
+                return None
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            return float(f[2]) if h == f[3].split(":")[1] else None
+    return None
+
+
+def run_ours(args):
+    import scale_only_quantization_gb300 as Q
+    from scale_only_quantization_gb300 import build as B
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    Q.lib()
+    cfg = synth.workload(args.workload)
+    inp = synth.make_inputs(cfg, seed=rank, device=dev)
+    T, d, F, E, k, fmt = inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"]
+    s = Q.shape(T, d, F, E, k, fmt)
+    ws = torch.empty(Q.qad_moe_workspace_bytes(s), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty_like(out)
+    dprobs = torch.empty((T, k), dtype=torch.float32, device=dev)
+    ds13 = torch.empty_like(inp["s13"])
+    ds2 = torch.empty_like(inp["s2"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x, idx, p, dout):
+        Q.qad_moe_fwd(s, x, idx, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], out, ws, stream)
+        Q.qad_moe_bwd_dgrad(s, dout, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], dx, dprobs, ws, stream)
+        Q.qad_moe_bwd_scalegrad(s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], ds13, ds2, 0, ws, stream)
+        if world > 1:
+            import torch.distributed as dist
+            dist.all_reduce(ds13)
+            dist.all_reduce(ds2)
+            ds13.div_(world)
+            ds2.div_(world)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    args_dev = (inp["x"], inp["topk_idx"], inp["topk_w"], inp["dout"])
+    for _ in range(args.warmup):
+        step(*args_dev)
+    err = Q.qad_check_device_error(ws, stream)
+    if err:
+        raise RuntimeError("device error word %d after warm-up" % err)
+    barrier()
+
+    # ---- device-resident timed region (kernel timing on, clocks sampled)
+    Q.qad_profile_reset()
+    Q.qad_profile_enable(True)
+    n0 = Q.qad_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(*args_dev)
+        e1.record(stream)
+        barrier()
+    launches = Q.qad_launch_count() - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    prof = Q.qad_profile_read()
+    Q.qad_profile_enable(False)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API with pinned host buffers
+    host_in = [a.cpu().pin_memory() for a in args_dev]
+    host_out = [torch.empty(a.shape, dtype=a.dtype, pin_memory=True) for a in (out, dx, ds13, ds2)]
+    dev_in = [torch.empty_like(a) for a in args_dev]
+    h2d = sum(a.numel() * a.element_size() for a in host_in)
+    d2h = sum(a.numel() * a.element_size() for a in host_out)
+
+    def e2e_step():
+        for dst, src in zip(dev_in, host_in):
+            dst.copy_(src, non_blocking=True)
+        step(*dev_in)
+        for dst, src in zip(host_out, (out, dx, ds13, ds2)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    # ---- roofline of the dominant kernel (largest share of the timed region)
+    hbm, tf_burst, tf_sust, peak_src = _peaks()
+    alg = algorithmic_per_launch(cfg)
+    kernels = {}
+    for name, (tot, n) in prof.items():
+        if n == 0:
+            continue
+        entry = {"ms_per_launch": tot / n, "launches_per_step": n / args.steps, "share": None}
+        if name in alg:
+            bound, amount = alg[name]
+            per_s = amount / (tot / n / 1e3)
+            if bound == "tensor":
+                entry.update(achieved_tflops=per_s / 1e12, frac=per_s / 1e12 / tf_sust)
+            else:
+                entry.update(achieved_gbs=per_s / 1e9, frac=per_s / 1e9 / hbm)
+        kernels[name] = entry
+    total_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values())
+    for v in kernels.values():
+        v["share"] = v["ms_per_launch"] * v["launches_per_step"] / total_ms if total_ms else None
+    dom = max((nm for nm in kernels if nm in alg), key=lambda nm: kernels[nm]["share"])
+    bound, amount = alg[dom]
+    dur = kernels[dom]["ms_per_launch"] / 1e3
+    if bound == "tensor":
+        roof = {"bound": "tensor", "kernel": dom, "achieved": amount / dur / 1e12, "peak": tf_sust,
+                "unit": "TFLOP/s", "peak_source": peak_src + " bf16_tflops_sustained"}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": amount / dur / 1e9, "peak": hbm, "unit": "GB/s",
+                "peak_source": peak_src + " hbm_gbs"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = _traffic(dom, args.workload)
+    flops_step = synth.tokens_to_flops(cfg)
+
+    line = {
+        "metric": METRIC, "value": T * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "format": FMT_NAME[fmt], "E": E, "d": d, "F": F, "topk": k,
+                   "tokens_per_gpu": T, "global_batch": T * world, "parallelism": "dp%d" % world,
+                   "l2": "inputs larger than L2 (weights %.2f GB streamed per pass), no flush" %
+                         (2 * 3 * E * F * d / 1e9)},
+        "step_tflops": flops_step / (ms / 1e3) / 1e12,
+        "step_tensor_frac_of_sustained": flops_step / (ms / 1e3) / 1e12 / tf_sust,
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "e2e": {"value": T * world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _oracle_sample(cfg, host, n_experts):
+    """The oracle's fwd + dgrad + scalegrad restricted to experts [0, n_experts): pairs routed
+    elsewhere are dropped.  Returns (routed pairs processed, seconds)."""
+    from oracle import moe as OM
+    idx = host["topk_idx"]
+    keep = (idx >= 0) & (idx < n_experts)
+    toks = np.nonzero(keep.any(axis=1))[0]
+    sub_idx = np.where(keep[toks], idx[toks], -1)
+    p = host["topk_w"][toks]
+    E = n_experts
+    t0 = time.perf_counter()
+    fwd = OM.moe_forward(cfg["fmt"], host["x"][toks], sub_idx, p, host["w13"][:E], host["s13"][:E], host["w2"][:E],
+                         host["s2"][:E])
+    bwd = OM.moe_dgrad(host["dout"][toks], p, fwd)
+    OM.moe_scalegrad(cfg["fmt"], fwd, bwd, host["w13"][:E], host["s13"][:E], host["w2"][:E], host["s2"][:E])
+    return int(keep.sum()), time.perf_counter() - t0
+
+
+def _host_inputs(inp, n_experts):
+    to_bits = synth.to_numpy_bits
+    return {"x": to_bits(inp["x"]), "dout": to_bits(inp["dout"]), "topk_idx": synth.to_numpy(inp["topk_idx"]),
+            "topk_w": synth.to_numpy(inp["topk_w"]), "w13": to_bits(inp["w13"][:n_experts]),
+            "w2": to_bits(inp["w2"][:n_experts]), "s13": synth.to_numpy(inp["s13"][:n_experts]),
+            "s2": synth.to_numpy(inp["s2"][:n_experts])}
+
+
+def cpu_baseline(cfg, inp, budget_s=15.0):
+    """Time the oracle as it stands on this host's cores on a bounded sample: the experts
+    [0, n) with every pair routed to them, n grown until ~budget_s of work."""
+    n, pairs, secs = 1, 0, 0.0
+    host = _host_inputs(inp, min(cfg["E"], 64))
+    while True:
+        pr, dt = _oracle_sample(cfg, host, n)
+        pairs, secs = pr, dt
+        if dt * 2 > budget_s or n * 2 > min(cfg["E"], 64):
+            break
+        n *= 2
+    return {"value": pairs / cfg["topk"] / secs, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "fp64 NumPy oracle, fwd+dgrad+scalegrad of experts 0..%d (%d routed rows = %.0f token-"
+                      "equivalents) of %s; %.1f s" % (n - 1, pairs, pairs / cfg["topk"], cfg["name"], secs)}
+
+
+def run_reference(args):
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    cfg = synth.workload(args.workload)
+    inp = synth.make_inputs(cfg, seed=0, device="cpu")
+    host = _host_inputs(inp, min(cfg["E"], 64))
+    n = 4 if cfg["E"] >= 4 else cfg["E"]
+    for _ in range(args.warmup):
+        _oracle_sample(cfg, host, 1)
+    tot_pairs, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        pr, dt = _oracle_sample(cfg, host, n)
+        tot_pairs += pr
+        tot_s += dt
+    value = tot_pairs / cfg["topk"] / tot_s
+    ms = tot_s / args.steps * 1e3
+    sample = ("fp64 NumPy oracle on the host cores, each step fwd+dgrad+scalegrad of experts 0..%d (all pairs "
+              "routed to them) of %s" % (n - 1, cfg["name"]))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "format": FMT_NAME[cfg["fmt"]], "E": cfg["E"], "d": cfg["d"],
+                   "F": cfg["F"], "topk": cfg["topk"], "tokens_per_gpu": cfg["T"], "parallelism": "none (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * qad.h -- C ABI of the scale-only QAD MoE-layer library for one GB300 (sm_103a).
+ *
+ * What the library computes.  Scale-only quantization-aware training/distillation
+ * keeps the BF16 weights frozen, fake-quantizes them (quantize then dequantize) and
+ * optimises only the quantizer scales ("MCoreQAD Backend", mcore_qad.md, opening
+ * section).  The weight a matmul sees is quantize->dequantize(W; s) with gradients
+ * reaching s, and each quantized matmul's input is fake-quantized first (AngelSlim
+ * mcore_qad walkthrough, nxmr.cn/news/131691, section 二.3).  The routed experts of a
+ * MoE layer are 3D-stacked, fake-quantized in one pass and run as one grouped GEMM
+ * (same article, section 二.4).  Formats: nvfp4 (W4A4), w4a16 (INT4) and fp8 (W8A8)
+ * ("MCoreQAD Backend", Support Matrix; article section 三).
+ *
+ * Layer (per token t, routed to k distinct experts j with weights p[t, j]):
+ *   A1  = AQ(x[t])                                  activation fake-quant
+ *   Z1  = A1 . W13_hat[e]^T          [2F]           rows [0, F) gate, [F, 2F) up
+ *   H   = silu(gate) * up;  H_hat = AQ(H)           [F]
+ *   Y   = H_hat . W2_hat[e]^T        [d]
+ *   out = sum_j p[t, j] * Y_j                       [d]
+ * W_hat = bf16(fp32(q(fp32(W / s)) * s)) element by element, s broadcast over its block.
+ * Backward: straight-through estimator for both quantizers; the weights get no
+ * gradient; the scale gradient is
+ *   ds[e, n, b] = sum_{kappa in block b} dW_hat[e, n, kappa] * phi(W[e, n, kappa], s[e, n, b])
+ * with the LSQ factor phi = q(x) - x inside the closed clip range, the clip bound
+ * outside it (x = fp32(W / s)).
+ *
+ * Conventions for every call:
+ *   - pointers are DEVICE pointers unless stated; bf16 tensors are passed as void*;
+ *     every pointer must be 16-byte aligned;
+ *   - every call is asynchronous on `stream` and allocates nothing; the caller owns
+ *     all memory, including the workspace;
+ *   - a call returns QAD_OK, or a negative qad_status BEFORE launching anything when
+ *     an argument is invalid; CUDA launch failures return QAD_ERR_CUDA;
+ *   - problems found on the device (a routing index out of range or repeated within a
+ *     token, a pipeline wait that timed out) set bits in the workspace's device error
+ *     word, which qad_check_device_error() reads; no kernel traps or aborts.
+ */
+#ifndef QAD_H_
+#define QAD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* qad_stream_t; /* the same type as cudaStream_t; NULL = legacy stream */
+
+typedef enum {
+  QAD_OK = 0,
+  QAD_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size, bad flag */
+  QAD_ERR_UNSUPPORTED = -2, /* shape outside the supported set (divisibility, limits) */
+  QAD_ERR_WORKSPACE = -3,   /* workspace smaller than qad_moe_workspace_bytes() */
+  QAD_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+  QAD_ERR_DEVICE = -5       /* the device error word is non-zero (see QAD_DEV_*) */
+} qad_status;
+
+/* Weight formats (the pages' format names) */
+typedef enum {
+  QAD_FMT_NVFP4 = 0,     /* nvfp4 W4A4: E2M1 weights, one fp32 scale per 16 along K;
+                            activations E2M1 with dynamic per-16 scale amax/6 */
+  QAD_FMT_INT4_G128 = 1, /* w4a16: INT4 {-8..7} weights, one fp32 scale per 128 along K;
+                            activations stay bf16 */
+  QAD_FMT_FP8_ROW = 2    /* fp8 W8A8: E4M3 weights, one fp32 scale per output row;
+                            activations E4M3 with dynamic per-row scale amax/448 */
+} qad_fmt;
+
+/* Bits of the device error word */
+enum {
+  QAD_DEV_BAD_INDEX = 1, /* a topk index outside [0, E): that (token, slot) pair is dropped */
+  QAD_DEV_DUP_INDEX = 2, /* a token names the same expert twice: the later slot is dropped */
+  QAD_DEV_TIMEOUT = 4    /* a bounded pipeline wait expired; outputs of that call are invalid */
+};
+
+/* qad_moe_shape.flags */
+enum {
+  QAD_FLAG_STASH_H = 1   /* also store the un-quantized SwiGLU output H in the workspace */
+};
+
+/* Shape of one MoE layer. T tokens, hidden d, expert FFN width F, E experts, top-k. */
+typedef struct {
+  int64_t T, d, F, E;
+  int32_t topk;
+  int32_t fmt;   /* qad_fmt */
+  int32_t flags; /* QAD_FLAG_* */
+  int32_t reserved; /* must be 0 */
+} qad_moe_shape;
+
+/*
+ * Weight fake-quant of a stack of E matrices [N, K] (article section 二.3/二.4: the whole
+ * expert stack in one vectorised pass).
+ *   w      bf16 [E, N, K] row-major (read only)
+ *   scale  fp32 [E, N, K / B] with B = 16 (nvfp4), 128 (int4), K (fp8 per row)
+ *   w_hat  bf16 [E, N, K] (written; may not overlap w)
+ * Requires K % 16 == 0 (nvfp4, fp8) or K % 128 == 0 (int4), scales >= 0 and finite.
+ * Output is bit-exact: w_hat = bf16(fp32(q(fp32(w / s)) * s)).
+ */
+int qad_fakequant_fwd(int fmt, const void* w, const float* scale, void* w_hat,
+                      int64_t E, int64_t N, int64_t K, qad_stream_t stream);
+
+/* Bytes of workspace the three layer calls need for this shape; 0 if the shape is
+ * not supported.  Host-only, no CUDA call. */
+size_t qad_moe_workspace_bytes(const qad_moe_shape* s);
+
+/*
+ * Forward of one MoE layer.
+ *   x        bf16 [T, d]        topk_idx int32 [T, topk]     topk_w fp32 [T, topk]
+ *   w13      bf16 [E, 2F, d]    s13 fp32 [E, 2F, d / B]      (rows [0,F) gate, [F,2F) up)
+ *   w2       bf16 [E, d, F]     s2  fp32 [E, d, F / B]
+ *   out      bf16 [T, d] (written)
+ *   ws       workspace (256-byte aligned) of ws_bytes >= qad_moe_workspace_bytes(s); it keeps what the
+ *            backward calls need (routing maps, fake-quantized weights, activations).
+ * Supported: d % 128 == 0, F % 128 == 0, 1 <= topk <= min(E, 32), 1 <= E <= 1024,
+ * T * topk < 2^31.  The error word is cleared at the start of this call.
+ */
+int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, const float* topk_w,
+                const void* w13, const float* s13, const void* w2, const float* s2,
+                void* out, void* ws, size_t ws_bytes, qad_stream_t stream);
+
+/*
+ * Input gradient of the layer (straight-through both quantizers).
+ *   dout   bf16 [T, d]; topk_w as in the forward; w13/s13/w2/s2 as in the forward
+ *   dx     bf16 [T, d] (written)
+ *   dprobs fp32 [T, topk] (written, may be NULL): dL/dtopk_w[t, j] = <dout[t], Y_j>
+ * Must follow qad_moe_fwd on the same workspace, inputs and stream.
+ */
+int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* topk_w,
+                      const void* w13, const float* s13, const void* w2, const float* s2,
+                      void* dx, float* dprobs, void* ws, size_t ws_bytes, qad_stream_t stream);
+
+/*
+ * Scale gradients (the only trainable parameters).
+ *   ds13 fp32 [E, 2F, d / B], ds2 fp32 [E, d, F / B]: overwritten, or added to when
+ *   accumulate != 0.
+ * The weight gradient is reduced into the scale gradient inside the GEMM epilogue and
+ * never stored.  Must follow qad_moe_bwd_dgrad on the same workspace and stream.
+ */
+int qad_moe_bwd_scalegrad(const qad_moe_shape* s, const void* w13, const float* s13,
+                          const void* w2, const float* s2, float* ds13, float* ds2,
+                          int accumulate, void* ws, size_t ws_bytes, qad_stream_t stream);
+
+/* Synchronises `stream`, copies the device error word of `ws` into *code (host
+ * pointer, may be NULL) and returns QAD_OK if it is zero, QAD_ERR_DEVICE otherwise. */
+int qad_check_device_error(void* ws, qad_stream_t stream, int32_t* code);
+
+/* Static English text for a qad_status value. */
+const char* qad_status_string(int status);
+
+/* Views into the workspace for stage-by-stage testing.  Writes the byte offset of
+ * region `which` from the workspace base and its element count.  Host-only. */
+enum {
+  QAD_VIEW_HEADER = 0,     /* int32[64]: [0] error word, [1] routed-row tiles, [2] padded rows */
+  QAD_VIEW_OFFSETS = 1,    /* int32 [E + 1]: first padded row of each expert (multiples of 128) */
+  QAD_VIEW_COUNTS = 2,     /* int32 [E]: routed rows per expert */
+  QAD_VIEW_ROW_TOKEN = 3,  /* int32 [Rmax]: token of each padded row, -1 for padding */
+  QAD_VIEW_ROW_SLOT = 4,   /* int32 [Rmax]: top-k slot of each padded row, -1 for padding */
+  QAD_VIEW_ROW_OF = 5,     /* int32 [T * topk]: padded row of each pair, -1 if dropped */
+  QAD_VIEW_W13_HAT = 6,    /* bf16 [E, 2F, d] */
+  QAD_VIEW_W2_HAT = 7,     /* bf16 [E, d, F] */
+  QAD_VIEW_A1 = 8,         /* bf16 [Rmax, d] */
+  QAD_VIEW_Z1 = 9,         /* bf16 [Rmax, 2F] */
+  QAD_VIEW_H = 10,         /* bf16 [Rmax, F] (QAD_FLAG_STASH_H, or fp8) */
+  QAD_VIEW_H_HAT = 11,     /* bf16 [Rmax, F] */
+  QAD_VIEW_Y = 12,         /* bf16 [Rmax, d] */
+  QAD_VIEW_DY = 13,        /* bf16 [Rmax, d] */
+  QAD_VIEW_DZ1 = 14,       /* bf16 [Rmax, 2F] */
+  QAD_VIEW_DA1 = 15,       /* bf16 [Rmax, d] */
+  QAD_VIEW_XQ = 16,        /* bf16 [T, d]: AQ(x) per token */
+  QAD_VIEW_COUNT = 17
+};
+int qad_moe_debug_view(const qad_moe_shape* s, int which, size_t* byte_offset, int64_t* numel);
+
+/*
+ * Kernel timing.  While enabled, every kernel launch of the library is bracketed by
+ * CUDA events on its stream.  qad_profile_read() synchronises the device and returns,
+ * per kernel id, the summed milliseconds and the launch count since the last reset.
+ * qad_launch_count() counts all launches of the library, enabled or not.
+ */
+enum {
+  QAD_K_FAKEQUANT = 0, QAD_K_ROUTE = 1, QAD_K_ACT_QUANT = 2, QAD_K_GATHER = 3,
+  QAD_K_GEMM_FC1 = 4, QAD_K_GEMM_FC2 = 5, QAD_K_COMBINE = 6, QAD_K_DY_GATHER = 7,
+  QAD_K_GEMM_DGRAD_FC2 = 8, QAD_K_GEMM_DGRAD_FC1 = 9, QAD_K_DX_COMBINE = 10,
+  QAD_K_GEMM_WGRAD_FC2 = 11, QAD_K_GEMM_WGRAD_FC1 = 12, QAD_K_SCALE_REDUCE = 13,
+  QAD_K_COUNT = 14
+};
+int qad_profile_enable(int on);
+int qad_profile_reset(void);
+int qad_profile_read(float* ms, int64_t* launches, int n);
+const char* qad_kernel_name(int id);
+int64_t qad_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QAD_H_ */

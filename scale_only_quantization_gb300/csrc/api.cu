@@ -1,0 +1,352 @@
+// C ABI of the scale-only QAD MoE library: argument checks, workspace layout, the call
+// sequences of the forward / input-gradient / scale-gradient passes, and kernel timing.
+//
+// The passes follow the AngelSlim mcore_qad walkthrough (nxmr.cn/news/131691): weights
+// fake-quantized as quantize->dequantize(W; s) with gradients reaching only s, activations
+// fake-quantized before each quantized matmul, router unquantized (section 二.3); the
+// whole expert stack fake-quantized in one pass and every expert run as one grouped GEMM
+// (section 二.4).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace qad {
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------- profiler
+
+struct Pending {
+  int id;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<Pending> g_pending;
+std::vector<cudaEvent_t> g_free_events;
+double g_ms[QAD_K_COUNT];
+int64_t g_launches[QAD_K_COUNT];
+std::atomic<int64_t> g_launch_total{0};
+thread_local Pending t_open = {-1, nullptr, nullptr};
+
+cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+int g_sms[64] = {0};
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+void prof_begin(int id, cudaStream_t st) {
+  g_launch_total.fetch_add(1, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  t_open.id = id;
+  t_open.a = take_event();
+  t_open.b = take_event();
+  cudaEventRecord(t_open.a, st);
+}
+
+void note_launches(int n) { g_launch_total.fetch_add(n, std::memory_order_relaxed); }
+
+void prof_end(int id, cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on || t_open.id != id || !t_open.a) return;
+  cudaEventRecord(t_open.b, st);
+  g_pending.push_back(t_open);
+  t_open = {-1, nullptr, nullptr};
+}
+
+int layout_of(const qad_moe_shape& s, Layout* L) {
+  if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
+  if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_FP8_ROW) return QAD_ERR_INVALID_ARG;
+  if (s.reserved != 0 || (s.flags & ~QAD_FLAG_STASH_H)) return QAD_ERR_INVALID_ARG;
+  if (s.d % 128 || s.F % 128) return QAD_ERR_UNSUPPORTED;
+  if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
+  const int64_t R = s.T * (int64_t)s.topk;
+  const int64_t Rmax = (R + (int64_t)(kTileRows - 1) * s.E + kTileRows - 1) / kTileRows * kTileRows;
+  if (Rmax >= (int64_t(1) << 31) || s.E * 2 * s.F >= (int64_t(1) << 31) || s.E * s.d >= (int64_t(1) << 31))
+    return QAD_ERR_UNSUPPORTED;
+  L->T = s.T; L->d = s.d; L->F = s.F; L->E = s.E; L->k = s.topk; L->R = R; L->Rmax = Rmax;
+  L->nchunks = (R + kRouteChunk - 1) / kRouteChunk;
+  const int64_t d = s.d, F = s.F, E = s.E;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = up(o + bytes); return at; };
+  L->header = take(256);
+  L->counts = take(4 * E);
+  L->offs = take(4 * (E + 1));
+  L->chunk_counts = take(4 * (size_t)(L->nchunks * E));
+  L->chunk_base = take(4 * (size_t)(L->nchunks * E));
+  L->mtile_expert = take(4 * (size_t)(Rmax / kTileRows));
+  L->row_token = take(4 * (size_t)Rmax);
+  L->row_slot = take(4 * (size_t)Rmax);
+  L->row_of = take(4 * (size_t)R);
+  L->xq = take(2 * (size_t)(s.T * d));
+  L->w13h = take(2 * (size_t)(E * 2 * F * d));
+  L->w2h = take(2 * (size_t)(E * d * F));
+  L->a1 = take(2 * (size_t)(Rmax * d));
+  L->z1 = take(2 * (size_t)(Rmax * 2 * F));
+  L->h = take(2 * (size_t)(Rmax * F));
+  L->hh = take(2 * (size_t)(Rmax * F));
+  L->y = take(2 * (size_t)(Rmax * d));
+  L->dy = take(2 * (size_t)(Rmax * d));
+  L->dz1 = take(2 * (size_t)(Rmax * 2 * F));
+  L->da1 = take(2 * (size_t)(Rmax * d));
+  L->part13 = take(4 * (size_t)(E * 2 * F * (d / 128)));
+  L->part2 = take(4 * (size_t)(E * d * (F / 128)));
+  L->total = o;
+  return QAD_OK;
+}
+
+}  // namespace qad
+
+using namespace qad;
+
+namespace {
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? QAD_OK : QAD_ERR_CUDA; }
+
+#define QAD_TRY(expr)                     \
+  do {                                    \
+    cudaError_t e_ = (expr);              \
+    if (e_ != cudaSuccess) return QAD_ERR_CUDA; \
+  } while (0)
+
+int check_layer(const qad_moe_shape* s, void* ws, size_t ws_bytes, Layout* L) {
+  if (!s) return QAD_ERR_INVALID_ARG;
+  const int rc = layout_of(*s, L);
+  if (rc != QAD_OK) return rc;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return QAD_ERR_INVALID_ARG;
+  if (ws_bytes < L->total) return QAD_ERR_WORKSPACE;
+  return QAD_OK;
+}
+
+bool ok_ptr(const void* p) { return p && aligned16(p); }
+
+}  // namespace
+
+extern "C" {
+
+const char* qad_status_string(int status) {
+  switch (status) {
+    case QAD_OK: return "ok";
+    case QAD_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size or flag)";
+    case QAD_ERR_UNSUPPORTED: return "unsupported shape (needs d % 128 == 0, F % 128 == 0, topk <= min(E, 32), E <= 1024)";
+    case QAD_ERR_WORKSPACE: return "workspace smaller than qad_moe_workspace_bytes()";
+    case QAD_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case QAD_ERR_DEVICE: return "device error word set (bad or repeated routing index, or a pipeline timeout)";
+    default: return "unknown status";
+  }
+}
+
+int qad_fakequant_fwd(int fmt, const void* w, const float* scale, void* w_hat, int64_t E, int64_t N, int64_t K,
+                      qad_stream_t stream) {
+  if (fmt < QAD_FMT_NVFP4 || fmt > QAD_FMT_FP8_ROW) return QAD_ERR_INVALID_ARG;
+  if (E < 0 || N < 0 || K <= 0) return QAD_ERR_INVALID_ARG;
+  if (K % 16 || (fmt == QAD_FMT_INT4_G128 && K % 128)) return QAD_ERR_UNSUPPORTED;
+  if (E * N == 0) return QAD_OK;
+  if (!ok_ptr(w) || !ok_ptr(scale) || !ok_ptr(w_hat)) return QAD_ERR_INVALID_ARG;
+  return to_status(launch_fakequant(fmt, w, scale, w_hat, E * N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qad_moe_workspace_bytes(const qad_moe_shape* s) {
+  if (!s) return 0;
+  Layout L;
+  return layout_of(*s, &L) == QAD_OK ? L.total : 0;
+}
+
+int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, const float* topk_w,
+                const void* w13, const float* s13, const void* w2, const float* s2, void* out, void* ws,
+                size_t ws_bytes, qad_stream_t stream) {
+  Layout L;
+  int rc = check_layer(s, ws, ws_bytes, &L);
+  if (rc != QAD_OK) return rc;
+  if (L.T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx) || !ok_ptr(topk_w) || !ok_ptr(out))) return QAD_ERR_INVALID_ARG;
+  if (!ok_ptr(w13) || !ok_ptr(s13) || !ok_ptr(w2) || !ok_ptr(s2)) return QAD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int32_t* hdr = reinterpret_cast<int32_t*>(wsb + L.header);
+  const int32_t* rpad = hdr + HDR_RPAD;
+  const int fmt = s->fmt;
+  QAD_TRY(cudaMemsetAsync(hdr, 0, 256, st));
+  QAD_TRY(launch_route(topk_idx, L, wsb, st));
+  QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st));
+  QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st));
+  const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
+  if (fmt == QAD_FMT_INT4_G128) {
+    QAD_TRY(launch_gather_rows(x, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
+  } else {
+    QAD_TRY(launch_act_quant_rows(fmt, x, wsb + L.xq, L.T, L.d, nullptr, st));
+    QAD_TRY(launch_gather_rows(wsb + L.xq, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
+  }
+  GemmCtx c = {&L, wsb, fmt, s->flags, st};
+  QAD_TRY(gemm_fc1(c));
+  if (fmt == QAD_FMT_FP8_ROW) QAD_TRY(launch_act_quant_rows(fmt, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
+  QAD_TRY(gemm_fc2(c));
+  QAD_TRY(launch_combine(wsb + L.y, reinterpret_cast<const int32_t*>(wsb + L.row_of), topk_w, out, L.T, (int)L.k,
+                         L.d, st));
+  return QAD_OK;
+}
+
+int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* topk_w, const void* w13,
+                      const float* s13, const void* w2, const float* s2, void* dx, float* dprobs, void* ws,
+                      size_t ws_bytes, qad_stream_t stream) {
+  Layout L;
+  int rc = check_layer(s, ws, ws_bytes, &L);
+  if (rc != QAD_OK) return rc;
+  if (L.T > 0 && (!ok_ptr(dout) || !ok_ptr(topk_w) || !ok_ptr(dx))) return QAD_ERR_INVALID_ARG;
+  if (dprobs && !ok_ptr(dprobs)) return QAD_ERR_INVALID_ARG;
+  if (!ok_ptr(w13) || !ok_ptr(s13) || !ok_ptr(w2) || !ok_ptr(s2)) return QAD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int32_t* hdr = reinterpret_cast<int32_t*>(wsb + L.header);
+  const int32_t* rpad = hdr + HDR_RPAD;
+  if (dprobs && L.R > 0) QAD_TRY(cudaMemsetAsync(dprobs, 0, sizeof(float) * L.R, st));
+  QAD_TRY(launch_dy_gather(dout, topk_w, reinterpret_cast<const int32_t*>(wsb + L.row_token),
+                           reinterpret_cast<const int32_t*>(wsb + L.row_slot), wsb + L.y, wsb + L.dy, dprobs, L.Rmax,
+                           (int)L.k, L.d, rpad, st));
+  GemmCtx c = {&L, wsb, s->fmt, s->flags, st};
+  QAD_TRY(gemm_dgrad_fc2(c));
+  QAD_TRY(gemm_dgrad_fc1(c));
+  QAD_TRY(launch_combine(wsb + L.da1, reinterpret_cast<const int32_t*>(wsb + L.row_of), nullptr, dx, L.T, (int)L.k,
+                         L.d, st));
+  return QAD_OK;
+}
+
+int qad_moe_bwd_scalegrad(const qad_moe_shape* s, const void* w13, const float* s13, const void* w2, const float* s2,
+                          float* ds13, float* ds2, int accumulate, void* ws, size_t ws_bytes, qad_stream_t stream) {
+  Layout L;
+  int rc = check_layer(s, ws, ws_bytes, &L);
+  if (rc != QAD_OK) return rc;
+  if (!ok_ptr(w13) || !ok_ptr(s13) || !ok_ptr(w2) || !ok_ptr(s2) || !ok_ptr(ds13) || !ok_ptr(ds2))
+    return QAD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  GemmCtx c = {&L, static_cast<uint8_t*>(ws), s->fmt, s->flags, st};
+  QAD_TRY(gemm_wgrad_fc2(c, w2, s2, ds2, accumulate ? 1 : 0));
+  QAD_TRY(gemm_wgrad_fc1(c, w13, s13, ds13, accumulate ? 1 : 0));
+  return QAD_OK;
+}
+
+int qad_check_device_error(void* ws, qad_stream_t stream, int32_t* code) {
+  if (!ws) return QAD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess) return QAD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QAD_ERR_CUDA;
+  if (code) *code = v;
+  return v == 0 ? QAD_OK : QAD_ERR_DEVICE;
+}
+
+int qad_moe_debug_view(const qad_moe_shape* s, int which, size_t* byte_offset, int64_t* numel) {
+  if (!s || !byte_offset || !numel) return QAD_ERR_INVALID_ARG;
+  Layout L;
+  const int rc = layout_of(*s, &L);
+  if (rc != QAD_OK) return rc;
+  const int64_t d = L.d, F = L.F, E = L.E, Rm = L.Rmax;
+  size_t off = 0;
+  int64_t n = 0;
+  switch (which) {
+    case QAD_VIEW_HEADER: off = L.header; n = 64; break;
+    case QAD_VIEW_OFFSETS: off = L.offs; n = E + 1; break;
+    case QAD_VIEW_COUNTS: off = L.counts; n = E; break;
+    case QAD_VIEW_ROW_TOKEN: off = L.row_token; n = Rm; break;
+    case QAD_VIEW_ROW_SLOT: off = L.row_slot; n = Rm; break;
+    case QAD_VIEW_ROW_OF: off = L.row_of; n = L.R; break;
+    case QAD_VIEW_W13_HAT: off = L.w13h; n = E * 2 * F * d; break;
+    case QAD_VIEW_W2_HAT: off = L.w2h; n = E * d * F; break;
+    case QAD_VIEW_A1: off = L.a1; n = Rm * d; break;
+    case QAD_VIEW_Z1: off = L.z1; n = Rm * 2 * F; break;
+    case QAD_VIEW_H: off = L.h; n = Rm * F; break;
+    case QAD_VIEW_H_HAT: off = L.hh; n = Rm * F; break;
+    case QAD_VIEW_Y: off = L.y; n = Rm * d; break;
+    case QAD_VIEW_DY: off = L.dy; n = Rm * d; break;
+    case QAD_VIEW_DZ1: off = L.dz1; n = Rm * 2 * F; break;
+    case QAD_VIEW_DA1: off = L.da1; n = Rm * d; break;
+    case QAD_VIEW_XQ: off = L.xq; n = L.T * d; break;
+    default: return QAD_ERR_INVALID_ARG;
+  }
+  *byte_offset = off;
+  *numel = n;
+  return QAD_OK;
+}
+
+int qad_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return QAD_OK;
+}
+
+int qad_profile_reset(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return QAD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& pe : g_pending) {
+    g_free_events.push_back(pe.a);
+    g_free_events.push_back(pe.b);
+  }
+  g_pending.clear();
+  memset(g_ms, 0, sizeof(g_ms));
+  memset(g_launches, 0, sizeof(g_launches));
+  return QAD_OK;
+}
+
+int qad_profile_read(float* ms, int64_t* launches, int n) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return QAD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& pe : g_pending) {
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, pe.a, pe.b) == cudaSuccess && pe.id >= 0 && pe.id < QAD_K_COUNT) {
+      g_ms[pe.id] += t;
+      g_launches[pe.id] += 1;
+    }
+    g_free_events.push_back(pe.a);
+    g_free_events.push_back(pe.b);
+  }
+  g_pending.clear();
+  for (int i = 0; i < n && i < QAD_K_COUNT; ++i) {
+    if (ms) ms[i] = (float)g_ms[i];
+    if (launches) launches[i] = g_launches[i];
+  }
+  return QAD_OK;
+}
+
+const char* qad_kernel_name(int id) {
+  static const char* names[QAD_K_COUNT] = {"fakequant_w", "route_permute", "act_quant", "gather_rows",
+                                           "gemm_fc1_swiglu_aq", "gemm_fc2", "combine", "dy_gather",
+                                           "gemm_dgrad_fc2_swiglu_bwd", "gemm_dgrad_fc1", "dx_combine",
+                                           "gemm_wgrad_fc2_scalegrad", "gemm_wgrad_fc1_scalegrad", "scale_reduce"};
+  return (id >= 0 && id < QAD_K_COUNT) ? names[id] : "unknown";
+}
+
+int64_t qad_launch_count(void) { return g_launch_total.load(); }
+
+}  // extern "C"

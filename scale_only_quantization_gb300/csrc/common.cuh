@@ -1,0 +1,132 @@
+// Device helpers shared by the kernels of the scale-only QAD MoE library (sm_103a).
+//
+// Quantizer readings (the pages name the formats but print no formula):
+//   nvfp4  - E2M1 grid {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}, round to nearest even,
+//            saturating (PTX cvt.rn.satfinite.e2m1x2.f32), one fp32 scale per 16 along K;
+//   w4a16  - INT4 grid {-8..7}: rintf (half to even) then clamp, one scale per 128 along K;
+//   fp8    - E4M3 (max 448), round to nearest even, saturating (cvt.rn.satfinite.e4m3x2.f32),
+//            one scale per output row.
+// x = w / s is the IEEE fp32 quotient (__fdiv_rn); the dequantized value is
+// bf16(fp32(q(x) * s)); s == 0 gives x = +-0 with the sign of w.
+// Formats: "MCoreQAD Backend" (mcore_qad.md), Support Matrix; AngelSlim mcore_qad
+// walkthrough (nxmr.cn/news/131691), sections 二.3 and 三.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qad.h"
+
+namespace qad {
+
+constexpr int kFmtNvfp4 = QAD_FMT_NVFP4;
+constexpr int kFmtInt4 = QAD_FMT_INT4_G128;
+constexpr int kFmtFp8 = QAD_FMT_FP8_ROW;
+
+// ---------------------------------------------------------------------------------- bf16
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half), .y = hi
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// 8 bf16 in a uint4 <-> 8 floats
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+}
+
+// ---------------------------------------------------------------------------------- quantizers
+
+// E2M1 rounding of two values; returns the decoded grid values (exact in fp32).
+__device__ __forceinline__ float2 q_e2m1x2(float a, float b) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2) : "f"(a), "f"(b));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);   // low half <- a, high half <- b
+  return make_float2(__low2float(h), __high2float(h));
+}
+
+// E4M3 rounding of two values; returns the decoded grid values (exact in fp32).
+__device__ __forceinline__ float2 q_e4m3x2(float a, float b) {
+  uint16_t p;
+  uint32_t h2;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p) : "f"(a), "f"(b));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(p));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return make_float2(__low2float(h), __high2float(h));
+}
+
+__device__ __forceinline__ float q_int4(float x) { return fminf(fmaxf(rintf(x), -8.0f), 7.0f); }
+
+template <int FMT>
+__device__ __forceinline__ float2 q_pair(float a, float b) {
+  float2 r;
+  if constexpr (FMT == kFmtNvfp4) {
+    r = q_e2m1x2(a, b);
+  } else if constexpr (FMT == kFmtFp8) {
+    r = q_e4m3x2(a, b);
+  } else {
+    r = make_float2(q_int4(a), q_int4(b));
+  }
+  // the grid value keeps the sign of its input, also when it rounds to zero
+  return make_float2(copysignf(r.x, a), copysignf(r.y, b));
+}
+
+template <int FMT> struct Clip;
+template <> struct Clip<kFmtNvfp4> { static constexpr float lo = -6.0f, hi = 6.0f; };
+template <> struct Clip<kFmtInt4> { static constexpr float lo = -8.0f, hi = 7.0f; };
+template <> struct Clip<kFmtFp8> { static constexpr float lo = -448.0f, hi = 448.0f; };
+
+// x = fp32(w / s); s == 0 -> +-0 with the sign of w
+__device__ __forceinline__ float quotient(float w, float s) {
+  return s == 0.0f ? copysignf(0.0f, w) : __fdiv_rn(w, s);
+}
+
+// Fake-quantize n (even) values that share scale s, in place: v <- bf16(fp32(q(v / s) * s)).
+template <int FMT, int N>
+__device__ __forceinline__ void fakequant_inplace(float* v, float s) {
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    float2 q = q_pair<FMT>(quotient(v[i], s), quotient(v[i + 1], s));
+    v[i] = round_bf16(__fmul_rn(q.x, s));
+    v[i + 1] = round_bf16(__fmul_rn(q.y, s));
+  }
+}
+
+// LSQ straight-through factor phi(x): q(x) - x inside the closed clip range, else the bound.
+template <int FMT>
+__device__ __forceinline__ float2 lsq_pair(float xa, float xb) {
+  float2 q = q_pair<FMT>(xa, xb);
+  float pa = xa < Clip<FMT>::lo ? Clip<FMT>::lo : (xa > Clip<FMT>::hi ? Clip<FMT>::hi : q.x - xa);
+  float pb = xb < Clip<FMT>::lo ? Clip<FMT>::lo : (xb > Clip<FMT>::hi ? Clip<FMT>::hi : q.y - xb);
+  return make_float2(pa, pb);
+}
+
+// ---------------------------------------------------------------------------------- misc
+
+__device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdiv_rn(1.0f, 1.0f + expf(-g)); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace qad

@@ -1,0 +1,432 @@
+// Memory-bound kernels of the scale-only QAD MoE path: weight fake-quant, routing
+// permutation, activation fake-quant, row gather, combine, dY gather, scale reduce.
+//
+// Weight fake-quant: the whole stacked expert weight is fake-quantized in one vectorised
+// pass (AngelSlim mcore_qad walkthrough, nxmr.cn/news/131691, section 二.4); the weight a
+// matmul sees is quantize->dequantize(W; s) (section 二.3).  Activations are fake-quantized
+// before each quantized matmul with a dynamic (detached) scale (section 二.3).  The routed
+// rows are grouped by expert for one grouped GEMM (section 二.4); routing indices and
+// weights come from the unquantized router and are inputs here.
+#include "common.cuh"
+#include "internal.h"
+
+namespace qad {
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
+
+int grid_for(int64_t items, int threads, int per_sm) {
+  int64_t want = (items + threads - 1) / threads;
+  int64_t cap = (int64_t)num_sms() * per_sm;
+  if (want > cap) want = cap;
+  return want < 1 ? 1 : (int)want;
+}
+
+// ------------------------------------------------------------------------- weight fake-quant
+
+// One thread per 16 consecutive elements of a row (16 | K, and every scale block is a
+// whole number of 16-element chunks).  `cps` = chunks per scale (1, 8 or K / 16).
+template <int FMT>
+__global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict__ w, const float* __restrict__ s,
+                                                        uint4* __restrict__ out, uint64_t nchunks, uint32_t cps) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
+    const uint4 u0 = ld_stream(w + 2 * c);
+    const uint4 u1 = ld_stream(w + 2 * c + 1);
+    const float sc = __ldg(s + (cps == 1 ? c : c / cps));
+    float v[16];
+    unpack8(u0, v);
+    unpack8(u1, v + 8);
+    fakequant_inplace<FMT, 16>(v, sc);
+    st_stream(out + 2 * c, pack8(v));
+    st_stream(out + 2 * c + 1, pack8(v + 8));
+  }
+}
+
+// ------------------------------------------------------------------------- routing
+
+// Expert of pair i = t * k + j, or -1 when the pair is dropped (index outside [0, E), or
+// the same expert as an earlier slot of the token); sets error bits in *err.
+__device__ __forceinline__ int pair_expert(const int32_t* __restrict__ idx, int64_t i, int k, int E, int* err) {
+  const int64_t t = i / k;
+  const int j = (int)(i - t * k);
+  const int e = idx[i];
+  if (e < 0 || e >= E) {
+    *err |= QAD_DEV_BAD_INDEX;
+    return -1;
+  }
+  for (int jj = 0; jj < j; ++jj)
+    if (idx[t * k + jj] == e) {
+      *err |= QAD_DEV_DUP_INDEX;
+      return -1;
+    }
+  return e;
+}
+
+__global__ void __launch_bounds__(256) route_hist_kernel(const int32_t* __restrict__ idx, int64_t R, int k, int E,
+                                                         int32_t* __restrict__ chunk_counts, int32_t* hdr) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  int err = 0;
+  const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
+  for (int i = threadIdx.x; i < kRouteChunk; i += blockDim.x) {
+    const int64_t g = base + i;
+    if (g < R) {
+      const int e = pair_expert(idx, g, k, E, &err);
+      if (e >= 0) atomicAdd(&hist[e], 1);
+    }
+  }
+  if (err) atomicOr(&hdr[HDR_ERR], err);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One block of 1024 threads, thread e owns expert e (E <= 1024).  Produces per-expert
+// counts, padded offsets (multiples of 128 rows), each chunk's first row per expert, the
+// expert of every 128-row tile, and marks padding rows with token -1.
+__global__ void __launch_bounds__(1024) route_scan_kernel(int64_t nchunks, int E, const int32_t* __restrict__ chunk_counts,
+                                                          int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offs, int32_t* __restrict__ mtile_expert,
+                                                          int32_t* __restrict__ row_token, int32_t* __restrict__ row_slot,
+                                                          int32_t* hdr) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t valid_tot[32];
+  const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+  int32_t total = 0;
+  if (e < E) {
+#pragma unroll 8
+    for (int64_t c = 0; c < nchunks; ++c) {
+      const int32_t v = chunk_counts[c * E + e];
+      chunk_base[c * E + e] = total;
+      total += v;
+    }
+    counts[e] = total;
+  }
+  const int32_t padded = (total + kTileRows - 1) / kTileRows * kTileRows;
+  int32_t v = padded, nv = total;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+  if (lane == 31) warp_tot[w] = v;
+  if (lane == 0) valid_tot[w] = nv;
+  __syncthreads();
+  if (w == 0) {
+    int32_t t = warp_tot[lane], s = valid_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    warp_tot[lane] = t;
+    if (lane == 0) valid_tot[0] = s;
+  }
+  __syncthreads();
+  const int32_t incl = v + (w > 0 ? warp_tot[w - 1] : 0);
+  const int32_t excl = incl - padded;
+  if (e < E) {
+    offs[e] = excl;
+    if (e == E - 1) {
+      offs[E] = incl;
+      hdr[HDR_NMTILES] = incl / kTileRows;
+      hdr[HDR_RPAD] = incl;
+      hdr[HDR_NVALID] = valid_tot[0];
+    }
+    for (int64_t c = 0; c < nchunks; ++c) chunk_base[c * E + e] += excl;
+    for (int32_t r = excl + total; r < incl; ++r) {
+      row_token[r] = -1;
+      row_slot[r] = -1;
+    }
+    for (int32_t mb = excl / kTileRows; mb < incl / kTileRows; ++mb) mtile_expert[mb] = e;
+  }
+}
+
+// One warp per chunk of 1024 pairs, 32 at a time in order; a pair's row is its chunk's
+// first row for the expert plus the number of earlier pairs of the chunk with that expert.
+__global__ void __launch_bounds__(32) route_scatter_kernel(const int32_t* __restrict__ idx, int64_t R, int k, int E,
+                                                           const int32_t* __restrict__ chunk_base,
+                                                           int32_t* __restrict__ row_token, int32_t* __restrict__ row_slot,
+                                                           int32_t* __restrict__ row_of) {
+  extern __shared__ int32_t seen[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) seen[e] = 0;
+  __syncwarp();
+  const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
+  const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
+  for (int step = 0; step < kRouteChunk / 32; ++step) {
+    const int64_t g = base + step * 32 + lane;
+    int err = 0;
+    const int e = g < R ? pair_expert(idx, g, k, E, &err) : -1;
+    const int key = e >= 0 ? e : -1 - lane;  // unmatched keys for dropped pairs
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int before = __popc(peers & ((1u << lane) - 1u));
+    int pos = -1;
+    if (e >= 0) pos = cb[e] + seen[e] + before;
+    __syncwarp();
+    if (e >= 0 && before == 0) seen[e] += __popc(peers);
+    __syncwarp();
+    if (g < R) {
+      row_of[g] = pos;
+      if (pos >= 0) {
+        const int64_t t = g / k;
+        row_token[pos] = (int32_t)t;
+        row_slot[pos] = (int32_t)(g - t * k);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------- activations
+
+// nvfp4: one thread per 16-element block, scale fp32(amax / 6)
+__global__ void __launch_bounds__(256) act_quant_nvfp4_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                                              int64_t rows, int64_t cols, const int32_t* dev_rows) {
+  const int64_t nrows = dev_rows ? (int64_t)*dev_rows : rows;
+  const int64_t nblk = nrows * (cols / 16);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride) {
+    float v[16];
+    unpack8(in[2 * b], v);
+    unpack8(in[2 * b + 1], v + 8);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    fakequant_inplace<kFmtNvfp4, 16>(v, __fdiv_rn(amax, 6.0f));
+    out[2 * b] = pack8(v);
+    out[2 * b + 1] = pack8(v + 8);
+  }
+}
+
+// fp8: one warp per row, scale fp32(row amax / 448)
+__global__ void __launch_bounds__(256) act_quant_fp8_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                                            int64_t rows, int64_t cols, const int32_t* dev_rows) {
+  const int64_t nrows = dev_rows ? (int64_t)*dev_rows : rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t c8 = cols / 8;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows; r += warps) {
+    const uint4* src = in + r * c8;
+    float amax = 0.0f;
+    for (int64_t c = lane; c < c8; c += 32) {
+      float v[8];
+      unpack8(src[c], v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 448.0f);
+    for (int64_t c = lane; c < c8; c += 32) {
+      float v[8];
+      unpack8(src[c], v);
+      fakequant_inplace<kFmtFp8, 8>(v, s);
+      out[r * c8 + c] = pack8(v);
+    }
+  }
+}
+
+// one warp per destination row
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                          const int32_t* __restrict__ row_token, int64_t c8,
+                                                          const int32_t* dev_rows) {
+  const int64_t nrows = *dev_rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows; r += warps) {
+    const int32_t t = row_token[r];
+    uint4* d = dst + r * c8;
+    if (t < 0) {
+      for (int64_t c = lane; c < c8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
+    } else {
+      const uint4* s = src + (int64_t)t * c8;
+      for (int64_t c = lane; c < c8; c += 32) d[c] = __ldg(s + c);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------- combine
+
+// one warp per token; fixed slot order j = 0..k-1, fp32 sums
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
+                                                      const float* __restrict__ p, uint4* __restrict__ out, int64_t T,
+                                                      int k, int64_t c8) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T; t += warps) {
+    for (int64_t c = lane; c < c8; c += 32) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = __ldg(row_of + t * k + j);
+        if (r < 0) continue;
+        const float pj = p ? __ldg(p + t * k + j) : 1.0f;
+        float v[8];
+        unpack8(__ldg(y + (int64_t)r * c8 + c), v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(pj, v[i], acc[i]);
+      }
+      out[t * c8 + c] = pack8(acc);
+    }
+  }
+}
+
+// one warp per padded row: dy[r] = bf16(fp32(p * dout[t])), dprobs[t, j] = <dout[t], y[r]>
+__global__ void __launch_bounds__(256) dy_gather_kernel(const uint4* __restrict__ dout, const float* __restrict__ p,
+                                                        const int32_t* __restrict__ row_token,
+                                                        const int32_t* __restrict__ row_slot, const uint4* __restrict__ y,
+                                                        uint4* __restrict__ dy, float* __restrict__ dprobs, int k,
+                                                        int64_t c8, const int32_t* dev_rows) {
+  const int64_t nrows = *dev_rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows; r += warps) {
+    const int32_t t = row_token[r];
+    uint4* d = dy + r * c8;
+    if (t < 0) {
+      for (int64_t c = lane; c < c8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const int j = row_slot[r];
+    const float pj = __ldg(p + (int64_t)t * k + j);
+    const uint4* g = dout + (int64_t)t * c8;
+    float dot = 0.0f;
+    for (int64_t c = lane; c < c8; c += 32) {
+      float v[8];
+      unpack8(__ldg(g + c), v);
+      if (dprobs) {
+        float yv[8];
+        unpack8(__ldg(y + r * c8 + c), yv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dot = fmaf(v[i], yv[i], dot);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(pj, v[i]);
+      d[c] = pack8(v);
+    }
+    if (dprobs) {
+      dot = warp_sum(dot);
+      if (lane == 0) dprobs[(int64_t)t * k + j] = dot;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) scale_reduce_kernel(const float* __restrict__ part, float* __restrict__ ds,
+                                                           int64_t n, int nparts, int accumulate) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    float acc = accumulate ? ds[i] : 0.0f;
+    for (int j = 0; j < nparts; ++j) acc += part[i * nparts + j];
+    ds[i] = acc;
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------- launchers
+
+cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, int64_t rows, int64_t K,
+                             cudaStream_t st) {
+  const uint64_t nchunks = (uint64_t)rows * (uint64_t)(K / 16);
+  if (nchunks == 0) return cudaSuccess;
+  const int grid = grid_for((int64_t)nchunks, 256, 8);
+  const uint4* wi = static_cast<const uint4*>(w);
+  uint4* o = static_cast<uint4*>(out);
+  prof_begin(QAD_K_FAKEQUANT, st);
+  if (fmt == kFmtNvfp4) {
+    fakequant_kernel<kFmtNvfp4><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 1u);
+  } else if (fmt == kFmtInt4) {
+    fakequant_kernel<kFmtInt4><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 8u);
+  } else {
+    fakequant_kernel<kFmtFp8><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16));
+  }
+  prof_end(QAD_K_FAKEQUANT, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st) {
+  int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.header);
+  int32_t* cc = reinterpret_cast<int32_t*>(ws + L.chunk_counts);
+  int32_t* cb = reinterpret_cast<int32_t*>(ws + L.chunk_base);
+  int32_t* row_token = reinterpret_cast<int32_t*>(ws + L.row_token);
+  int32_t* row_slot = reinterpret_cast<int32_t*>(ws + L.row_slot);
+  const int E = (int)L.E, k = (int)L.k;
+  prof_begin(QAD_K_ROUTE, st);
+  if (L.nchunks > 0) {
+    route_hist_kernel<<<(unsigned)L.nchunks, 256, E * sizeof(int32_t), st>>>(idx, L.R, k, E, cc, hdr);
+  }
+  route_scan_kernel<<<1, 1024, 0, st>>>(L.nchunks, E, cc, cb, reinterpret_cast<int32_t*>(ws + L.counts),
+                                        reinterpret_cast<int32_t*>(ws + L.offs),
+                                        reinterpret_cast<int32_t*>(ws + L.mtile_expert), row_token, row_slot, hdr);
+  if (L.nchunks > 0) {
+    route_scatter_kernel<<<(unsigned)L.nchunks, 32, E * sizeof(int32_t), st>>>(
+        idx, L.R, k, E, cb, row_token, row_slot, reinterpret_cast<int32_t*>(ws + L.row_of));
+  }
+  prof_end(QAD_K_ROUTE, st);
+  if (L.nchunks > 0) note_launches(2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_rows(int fmt, const void* in, void* out, int64_t rows, int64_t cols,
+                                  const int32_t* dev_rows, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  prof_begin(QAD_K_ACT_QUANT, st);
+  if (fmt == kFmtNvfp4) {
+    act_quant_nvfp4_kernel<<<grid_for(rows * (cols / 16), 256, 8), 256, 0, st>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
+  } else {
+    act_quant_fp8_kernel<<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
+  }
+  prof_end(QAD_K_ACT_QUANT, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* row_token, int64_t rmax, int64_t cols,
+                               const int32_t* dev_rows, cudaStream_t st) {
+  if (rmax == 0) return cudaSuccess;
+  prof_begin(QAD_K_GATHER, st);
+  gather_rows_kernel<<<grid_for(rmax * 32, 256, 8), 256, 0, st>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), row_token, cols / 8, dev_rows);
+  prof_end(QAD_K_GATHER, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* p, void* out, int64_t T, int k,
+                           int64_t d, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int id = p ? QAD_K_COMBINE : QAD_K_DX_COMBINE;
+  prof_begin(id, st);
+  combine_kernel<<<grid_for(T * 32, 256, 8), 256, 0, st>>>(static_cast<const uint4*>(y), row_of, p,
+                                                            static_cast<uint4*>(out), T, k, d / 8);
+  prof_end(id, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dy_gather(const void* dout, const float* p, const int32_t* row_token, const int32_t* row_slot,
+                             const void* y, void* dy, float* dprobs, int64_t rmax, int k, int64_t d,
+                             const int32_t* dev_rows, cudaStream_t st) {
+  if (rmax == 0) return cudaSuccess;
+  prof_begin(QAD_K_DY_GATHER, st);
+  dy_gather_kernel<<<grid_for(rmax * 32, 256, 8), 256, 0, st>>>(
+      static_cast<const uint4*>(dout), p, row_token, row_slot, static_cast<const uint4*>(y), static_cast<uint4*>(dy),
+      dprobs, k, d / 8, dev_rows);
+  prof_end(QAD_K_DY_GATHER, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_reduce(const float* part, float* ds, int64_t n, int nparts, int accumulate,
+                                cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  prof_begin(QAD_K_SCALE_REDUCE, st);
+  scale_reduce_kernel<<<grid_for(n, 256, 8), 256, 0, st>>>(part, ds, n, nparts, accumulate);
+  prof_end(QAD_K_SCALE_REDUCE, st);
+  return cudaGetLastError();
+}
+
+}  // namespace qad

@@ -1,0 +1,736 @@
+// Grouped GEMMs of the scale-only QAD MoE layer on the 5th-generation tensor cores.
+//
+// "All experts in one grouped GEMM over the token-routed rows" (AngelSlim mcore_qad
+// walkthrough, nxmr.cn/news/131691, section 二.4).  One persistent kernel template serves
+// the six GEMMs of a fwd + bwd step:
+//
+//   fc1    Z1 = A1 . W13_hat[e]^T   epilogue: bf16 Z1, SwiGLU, activation fake-quant -> H_hat
+//   fc2    Y  = H_hat . W2_hat[e]^T  epilogue: bf16 store
+//   dgrad  dH = dY . W2_hat[e]       epilogue: SwiGLU backward -> dZ1 (dH never stored)
+//   dgrad  dA1 = dZ1 . W13_hat[e]    epilogue: bf16 store
+//   wgrad  dW2 = dY_e^T . H_hat_e    epilogue: x LSQ factor, per-block sums -> ds2 (dW never stored)
+//   wgrad  dW13 = dZ1_e^T . A1_e     epilogue: same -> ds13
+//
+// Rows of each expert are padded to a multiple of 128 (zero rows), so a 128-row tile never
+// straddles two experts and a wgrad contraction runs over whole 64-row blocks.
+//
+// Per CTA (one per SM, persistent over tiles): warp 0 issues TMA loads (128B-swizzled
+// tiles) into a STAGES-deep ring guarded by mbarriers; warp 1 owns the tensor memory and
+// issues tcgen05.mma (M=128, N=BN, K=16, bf16 x bf16 -> fp32) from one thread; warps 2-5
+// read the accumulator (two TMEM buffers, so the next tile's MMAs overlap this epilogue)
+// with tcgen05.ld and run the fused epilogue.  Every wait is bounded: on expiry the CTA
+// raises QAD_DEV_TIMEOUT in the workspace error word, drains what it issued and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qad {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+enum { EPI_FC1 = 0, EPI_STORE = 1, EPI_SWIGLU_BWD = 2, EPI_SCALEGRAD = 3 };
+
+struct Params {
+  int32_t* hdr;                 // workspace header ([HDR_ERR], [HDR_NMTILES])
+  const int32_t* mtile_expert;  // expert of each 128-row tile
+  const int32_t* poff;          // padded expert offsets [E + 1]
+  int E;
+  int wgrad;                    // 0: output rows grouped by expert; 1: contraction over an expert's rows
+  int n_ntiles;                 // tiles along the GEMM's N
+  int n_mtiles_w;               // wgrad: tiles along the GEMM's M (weight rows / 128)
+  int num_kb;                   // rows mode: K / 64
+  int b_rows;                   // rows of the B tensor map per expert
+  int F;                        // expert FFN width (fc1 / SwiGLU epilogues)
+  int fmt, flags;
+  __nv_bfloat16* out;  int64_t ld_out;   // STORE: out; FC1: Z1; SWIGLU_BWD: dZ1
+  __nv_bfloat16* out2; int64_t ld_out2;  // FC1: H_hat
+  __nv_bfloat16* out3;                   // FC1: H (same leading dimension as out2)
+  const __nv_bfloat16* aux; int64_t ld_aux;  // SWIGLU_BWD: Z1
+  const __nv_bfloat16* w;  const float* s;   // SCALEGRAD: raw weights [E, Mw, Kw] and scales
+  int64_t w_rows, w_cols;
+  float* ds; float* part; int accumulate;
+};
+
+template <int BN> struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int RING = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int SMEM = RING + 256 + 1024;  // + barriers, + alignment slack
+  static constexpr int TMEM_COLS = 2 * BN;
+};
+
+// ---------------------------------------------------------------------------------- PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with parity `parity` of barrier `bar`.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicOr(err, QAD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4 in [0,14), leading byte offset
+// >> 4 in [16,30), stride byte offset >> 4 in [32,46), the fixed 0b001 in [46,49),
+// base offset 0 (tiles are 1024-byte aligned), swizzle mode 2 = 128-byte in [61,64).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12
+// = 1), A/B major in bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 in [17,23),
+// M >> 4 in [24,29).
+template <int N, bool A_MN, bool B_MN>
+__host__ __device__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = pack8(v + 8 * i);
+}
+__device__ __forceinline__ void load32(const __nv_bfloat16* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack8(__ldg(s + i), v + 8 * i);
+}
+
+// ---------------------------------------------------------------------------------- tiles
+
+struct Tile {
+  int e, mb, nb, nkb, r0;
+};
+
+__device__ __forceinline__ int tile_count(const Params& p) {
+  return p.wgrad ? p.E * p.n_mtiles_w * p.n_ntiles : p.hdr[HDR_NMTILES] * p.n_ntiles;
+}
+
+__device__ __forceinline__ Tile tile_of(const Params& p, int t) {
+  Tile ti;
+  if (p.wgrad) {
+    const int per_e = p.n_mtiles_w * p.n_ntiles;
+    ti.e = t / per_e;
+    const int rem = t - ti.e * per_e;
+    ti.mb = rem / p.n_ntiles;
+    ti.nb = rem - ti.mb * p.n_ntiles;
+    ti.r0 = __ldg(p.poff + ti.e);
+    ti.nkb = (__ldg(p.poff + ti.e + 1) - ti.r0) / BK;
+  } else {
+    ti.mb = t / p.n_ntiles;
+    ti.nb = t - ti.mb * p.n_ntiles;
+    ti.e = __ldg(p.mtile_expert + ti.mb);
+    ti.r0 = ti.mb * BM;
+    ti.nkb = p.num_kb;
+  }
+  return ti;
+}
+
+// ---------------------------------------------------------------------------------- epilogues
+
+template <int FMT>
+__device__ __forceinline__ void fc1_aq(float* h) {
+  if constexpr (FMT == kFmtNvfp4) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[16 * b + i]));
+      fakequant_inplace<kFmtNvfp4, 16>(h + 16 * b, __fdiv_rn(amax, 6.0f));
+    }
+  }
+}
+
+// Z1 (bf16) and H = bf16(silu(gate) * up) for 128 FFN columns; H_hat = AQ(H) for nvfp4,
+// = H for w4a16; fp8 needs the row amax over all F columns, so H goes to the H buffer
+// and a separate pass quantizes it.
+template <int BN>
+__device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+  const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
+  const int fcol0 = ti.nb * 128;
+  __nv_bfloat16* z1 = p.out + row * p.ld_out;
+  const bool stash_h = (p.flags & QAD_FLAG_STASH_H) || p.fmt == kFmtFp8;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float g[32], u[32];
+    tmem_ld32(tbase + 32 * c, g);
+    tmem_ld32(tbase + 128 + 32 * c, u);
+    const int f0 = fcol0 + 32 * c;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      g[i] = round_bf16(g[i]);
+      u[i] = round_bf16(u[i]);
+    }
+    store32(z1 + f0, g);
+    store32(z1 + p.F + f0, u);
+    float h[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) h[i] = round_bf16(__fmul_rn(silu_f(g[i]), u[i]));
+    if (stash_h) store32(p.out3 + row * p.ld_out2 + f0, h);
+    if (p.fmt == kFmtFp8) continue;
+    if (p.fmt == kFmtNvfp4) fc1_aq<kFmtNvfp4>(h);
+    store32(p.out2 + row * p.ld_out2 + f0, h);
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+  const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
+  __nv_bfloat16* dst = p.out + row * p.ld_out + (int64_t)ti.nb * BN;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(tbase + 32 * c, v);
+    store32(dst + 32 * c, v);
+  }
+}
+
+// dZ1 = [dH * up * sig(g) * (1 + g (1 - sig(g))), dH * g * sig(g)] from the stored bf16 Z1
+template <int BN>
+__device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+  const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
+  const __nv_bfloat16* z1 = p.aux + row * p.ld_aux;
+  __nv_bfloat16* dz1 = p.out + row * p.ld_out;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int f0 = ti.nb * BN + 32 * c;
+    float dh[32], g[32], u[32];
+    tmem_ld32(tbase + 32 * c, dh);
+    load32(z1 + f0, g);
+    load32(z1 + p.F + f0, u);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float sg = sigmoid_f(g[i]);
+      const float dgi = dh[i] * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+      const float dui = dh[i] * g[i] * sg;
+      g[i] = dgi;
+      u[i] = dui;
+    }
+    store32(dz1 + f0, g);
+    store32(dz1 + p.F + f0, u);
+  }
+}
+
+// ds[e, n, b] (+)= sum_{kappa in b} dW[n, kappa] * phi(W[e, n, kappa], s[e, n, b]); for fp8
+// (one scale per row) the tile's partial row sum goes to part[(e * Mw + n) * n_ntiles + nb].
+template <int BN, int FMT>
+__device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+  const int64_t n = (int64_t)ti.mb * BM + row_in_tile;
+  const int64_t wrow = (int64_t)ti.e * p.w_rows + n;
+  const __nv_bfloat16* wr = p.w + wrow * p.w_cols;
+  const int64_t k0 = (int64_t)ti.nb * BN;
+  float row_sum = 0.0f, grp = 0.0f;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float acc[32], wv[32];
+    if (ti.nkb > 0) {
+      tmem_ld32(tbase + 32 * c, acc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+    }
+    const int64_t kc = k0 + 32 * c;
+    load32(wr + kc, wv);
+    if constexpr (FMT == kFmtNvfp4) {
+      const int64_t sidx = wrow * (p.w_cols / 16) + kc / 16;
+      float sum[2];
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const float sc = __ldg(p.s + sidx + b);
+        float t = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const float2 ph = lsq_pair<FMT>(quotient(wv[16 * b + i], sc), quotient(wv[16 * b + i + 1], sc));
+          t = fmaf(acc[16 * b + i], ph.x, t);
+          t = fmaf(acc[16 * b + i + 1], ph.y, t);
+        }
+        sum[b] = t;
+      }
+      float* dst = p.ds + sidx;
+      if (p.accumulate) {
+        dst[0] += sum[0];
+        dst[1] += sum[1];
+      } else {
+        dst[0] = sum[0];
+        dst[1] = sum[1];
+      }
+    } else {
+      const float sc = (FMT == kFmtInt4) ? __ldg(p.s + wrow * (p.w_cols / 128) + kc / 128) : __ldg(p.s + wrow);
+      float t = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float2 ph = lsq_pair<FMT>(quotient(wv[i], sc), quotient(wv[i + 1], sc));
+        t = fmaf(acc[i], ph.x, t);
+        t = fmaf(acc[i + 1], ph.y, t);
+      }
+      if constexpr (FMT == kFmtInt4) {
+        grp += t;
+        if ((c & 3) == 3) {
+          float* dst = p.ds + wrow * (p.w_cols / 128) + kc / 128;
+          *dst = p.accumulate ? *dst + grp : grp;
+          grp = 0.0f;
+        }
+      } else {
+        row_sum += t;
+      }
+    }
+  }
+  if constexpr (FMT == kFmtFp8) p.part[wrow * p.n_ntiles + ti.nb] = row_sum;
+}
+
+template <int BN, int EPI>
+__device__ __forceinline__ void run_epilogue(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+  if constexpr (EPI == EPI_FC1) {
+    epi_fc1<BN>(p, ti, tbase, row_in_tile);
+  } else if constexpr (EPI == EPI_STORE) {
+    epi_store<BN>(p, ti, tbase, row_in_tile);
+  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+    epi_swiglu_bwd<BN>(p, ti, tbase, row_in_tile);
+  } else {
+    if (p.fmt == kFmtNvfp4) epi_scalegrad_fmt<BN, kFmtNvfp4>(p, ti, tbase, row_in_tile);
+    else if (p.fmt == kFmtInt4) epi_scalegrad_fmt<BN, kFmtInt4>(p, ti, tbase, row_in_tile);
+    else epi_scalegrad_fmt<BN, kFmtFp8>(p, ti, tbase, row_in_tile);
+  }
+}
+
+// ---------------------------------------------------------------------------------- kernel
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Params p) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN>();
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t a_ring = smem_u32(smem);
+  const uint32_t b_ring = a_ring + STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* err = p.hdr + HDR_ERR;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4 * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_count(p);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_parity = 0;  // stages with a load in flight, and its phase parity
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      const Tile ti = tile_of(p, t);
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full_bar(stage);
+        mbar_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+        const uint32_t sa = a_ring + stage * C::A_BYTES;
+        const uint32_t sb = b_ring + stage * C::B_BYTES;
+        if (!p.wgrad) {
+          tma_load_2d(sa, &tmA, kb * BK, ti.r0, fb);
+          if constexpr (!B_MN) {
+            if constexpr (EPI == EPI_FC1) {
+              tma_load_2d(sb, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * 128, fb);
+              tma_load_2d(sb + 128 * 128, &tmB, kb * BK, ti.e * p.b_rows + p.F + ti.nb * 128, fb);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / 128; ++i)
+                tma_load_2d(sb + i * 128 * 128, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * BN + i * 128, fb);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + i * 64, ti.e * p.b_rows + kb * BK, fb);
+          }
+        } else {
+          const int y = ti.r0 + kb * BK;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) tma_load_2d(sa + i * 64 * 128, &tmA, ti.mb * BM + i * 64, y, fb);
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + i * 64, y, fb);
+        }
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (*abort_flag) {
+      // let every load this thread issued land before the CTA releases its shared memory
+      int32_t dummy = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) {
+          volatile int zero = 0;
+          mbar_wait(full_bar(s), (armed_parity >> s) & 1u, &zero, &dummy);
+        }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    int acc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      const Tile ti = tile_of(p, t);
+      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, err)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = a_ring + stage * C::A_BYTES;
+        const uint32_t sb = b_ring + stage * C::B_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, 64 * 128, 1024) : smem_desc(sa + k * 32, 16, 1024);
+          const uint64_t bd = B_MN ? smem_desc(sb + k * 2048, 64 * 128, 1024) : smem_desc(sb + k * 32, 16, 1024);
+          mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+        }
+        mma_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(tfull_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    // every MMA this thread issued has finished before TMEM and shared memory are released
+    mma_commit(drain_bar);
+    volatile int zero = 0;
+    int32_t dummy = 0;
+    mbar_wait(drain_bar, 0, &zero, &dummy);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile ti = tile_of(p, t);
+      const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      run_epilogue<BN, EPI>(p, ti, tbase, row_in_tile);
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [outer, inner] (row-major, `ld` elements per row), box {64, box_rows}, 128B swizzle
+bool make_tmap(CUtensorMap* tm, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int64_t max_tiles, int kid,
+                   cudaStream_t st) {
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+  if (e != cudaSuccess) return e;
+  int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
+  if (grid < 1) return cudaSuccess;
+  prof_begin(kid, st);
+  kern<<<(unsigned)grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, p);
+  prof_end(kid, st);
+  return cudaGetLastError();
+}
+
+template <typename T>
+T* at(uint8_t* ws, size_t off) {
+  return reinterpret_cast<T*>(ws + off);
+}
+
+Params base_params(const GemmCtx& c) {
+  const Layout& L = *c.L;
+  Params p = {};
+  p.hdr = at<int32_t>(c.ws, L.header);
+  p.mtile_expert = at<int32_t>(c.ws, L.mtile_expert);
+  p.poff = at<int32_t>(c.ws, L.offs);
+  p.E = (int)L.E;
+  p.F = (int)L.F;
+  p.fmt = c.fmt;
+  p.flags = c.flags;
+  return p;
+}
+
+inline int pick_bn(int64_t n) { return n % 256 == 0 ? 256 : 128; }
+
+}  // namespace
+
+cudaError_t gemm_fc1(const GemmCtx& c) {
+  const Layout& L = *c.L;
+  Params p = base_params(c);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, c.ws + L.a1, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.ws + L.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
+  p.n_ntiles = (int)(L.F / 128);
+  p.num_kb = (int)(L.d / BK);
+  p.b_rows = (int)(2 * L.F);
+  p.out = at<__nv_bfloat16>(c.ws, L.z1);
+  p.ld_out = 2 * L.F;
+  p.out2 = at<__nv_bfloat16>(c.ws, L.hh);
+  p.ld_out2 = L.F;
+  p.out3 = at<__nv_bfloat16>(c.ws, L.h);
+  return launch<256, false, false, EPI_FC1>(ta, tb, p, (L.Rmax / BM) * p.n_ntiles, QAD_K_GEMM_FC1, c.st);
+}
+
+cudaError_t gemm_fc2(const GemmCtx& c) {
+  const Layout& L = *c.L;
+  Params p = base_params(c);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, c.ws + L.hh, L.F, L.Rmax, L.F, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.ws + L.w2h, L.F, L.E * L.d, L.F, 128)) return cudaErrorInvalidValue;
+  const int bn = pick_bn(L.d);
+  p.n_ntiles = (int)(L.d / bn);
+  p.num_kb = (int)(L.F / BK);
+  p.b_rows = (int)L.d;
+  p.out = at<__nv_bfloat16>(c.ws, L.y);
+  p.ld_out = L.d;
+  const int64_t tiles = (L.Rmax / BM) * p.n_ntiles;
+  return bn == 256 ? launch<256, false, false, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_FC2, c.st)
+                   : launch<128, false, false, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_FC2, c.st);
+}
+
+cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
+  const Layout& L = *c.L;
+  Params p = base_params(c);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, c.ws + L.dy, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
+  // W2_hat viewed as [E * d (GEMM K), F (GEMM N)], N contiguous
+  if (!make_tmap(&tb, c.ws + L.w2h, L.F, L.E * L.d, L.F, 64)) return cudaErrorInvalidValue;
+  const int bn = pick_bn(L.F);
+  p.n_ntiles = (int)(L.F / bn);
+  p.num_kb = (int)(L.d / BK);
+  p.b_rows = (int)L.d;
+  p.out = at<__nv_bfloat16>(c.ws, L.dz1);
+  p.ld_out = 2 * L.F;
+  p.aux = at<__nv_bfloat16>(c.ws, L.z1);
+  p.ld_aux = 2 * L.F;
+  const int64_t tiles = (L.Rmax / BM) * p.n_ntiles;
+  return bn == 256 ? launch<256, false, true, EPI_SWIGLU_BWD>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st)
+                   : launch<128, false, true, EPI_SWIGLU_BWD>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st);
+}
+
+cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
+  const Layout& L = *c.L;
+  Params p = base_params(c);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, c.ws + L.dz1, 2 * L.F, L.Rmax, 2 * L.F, 128)) return cudaErrorInvalidValue;
+  // W13_hat viewed as [E * 2F (GEMM K), d (GEMM N)], N contiguous
+  if (!make_tmap(&tb, c.ws + L.w13h, L.d, L.E * 2 * L.F, L.d, 64)) return cudaErrorInvalidValue;
+  const int bn = pick_bn(L.d);
+  p.n_ntiles = (int)(L.d / bn);
+  p.num_kb = (int)(2 * L.F / BK);
+  p.b_rows = (int)(2 * L.F);
+  p.out = at<__nv_bfloat16>(c.ws, L.da1);
+  p.ld_out = L.d;
+  const int64_t tiles = (L.Rmax / BM) * p.n_ntiles;
+  return bn == 256 ? launch<256, false, true, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st)
+                   : launch<128, false, true, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st);
+}
+
+namespace {
+cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int64_t k_w, const void* w,
+                  const float* s, float* ds, size_t part_off, int accumulate, int kid) {
+  const Layout& L = *c.L;
+  Params p = base_params(c);
+  CUtensorMap ta, tb;
+  // A = dZ [Rmax, Mw] (M contiguous), B = A_hat [Rmax, Kw] (N contiguous)
+  if (!make_tmap(&ta, c.ws + a_off, m_w, L.Rmax, m_w, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.ws + b_off, k_w, L.Rmax, k_w, 64)) return cudaErrorInvalidValue;
+  const int bn = pick_bn(k_w);
+  p.wgrad = 1;
+  p.n_mtiles_w = (int)(m_w / BM);
+  p.n_ntiles = (int)(k_w / bn);
+  p.w = static_cast<const __nv_bfloat16*>(w);
+  p.s = s;
+  p.w_rows = m_w;
+  p.w_cols = k_w;
+  p.ds = ds;
+  p.part = at<float>(c.ws, part_off);
+  p.accumulate = accumulate;
+  const int64_t tiles = L.E * p.n_mtiles_w * p.n_ntiles;
+  cudaError_t e = bn == 256 ? launch<256, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st)
+                            : launch<128, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st);
+  if (e != cudaSuccess) return e;
+  if (c.fmt == kFmtFp8) return launch_scale_reduce(p.part, ds, L.E * m_w, p.n_ntiles, accumulate, c.st);
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t gemm_wgrad_fc2(const GemmCtx& c, const void* w2, const float* s2, float* ds2, int accumulate) {
+  const Layout& L = *c.L;
+  return wgrad(c, L.dy, L.d, L.hh, L.F, w2, s2, ds2, L.part2, accumulate, QAD_K_GEMM_WGRAD_FC2);
+}
+
+cudaError_t gemm_wgrad_fc1(const GemmCtx& c, const void* w13, const float* s13, float* ds13, int accumulate) {
+  const Layout& L = *c.L;
+  return wgrad(c, L.dz1, 2 * L.F, L.a1, L.d, w13, s13, ds13, L.part13, accumulate, QAD_K_GEMM_WGRAD_FC1);
+}
+
+}  // namespace qad

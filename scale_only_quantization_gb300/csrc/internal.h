@@ -1,0 +1,70 @@
+// Internal interfaces of the scale-only QAD MoE library: workspace layout and launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/qad.h"
+
+namespace qad {
+
+constexpr int kTileRows = 128;     // rows per GEMM tile; every expert's rows are padded to a multiple
+constexpr int kRouteChunk = 1024;  // (token, slot) pairs per routing chunk
+
+// Byte offsets of the workspace regions (each 1024-byte aligned).
+struct Layout {
+  int64_t T, d, F, E, k, R, Rmax, nchunks;
+  size_t header, counts, offs, chunk_counts, chunk_base, mtile_expert, row_token, row_slot, row_of;
+  size_t xq, w13h, w2h, a1, z1, h, hh, y, dy, dz1, da1, part13, part2;
+  size_t total;
+};
+
+// Header words (int32) at the start of the workspace
+enum { HDR_ERR = 0, HDR_NMTILES = 1, HDR_RPAD = 2, HDR_NVALID = 3 };
+
+// Returns a negative qad_status for an unsupported or invalid shape.
+int layout_of(const qad_moe_shape& s, Layout* L);
+
+// Profiler / launch accounting (api.cu)
+void prof_begin(int kernel_id, cudaStream_t st);
+void prof_end(int kernel_id, cudaStream_t st);
+void note_launches(int n);  // extra kernels launched inside one profiled region
+int num_sms();
+
+// ---- kernels (each returns the launch's cudaError_t) ----
+cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, int64_t rows, int64_t K,
+                             cudaStream_t st);
+cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st);
+// out[r, :] = AQ(in[r, :]) for r < rows (or < *dev_rows when dev_rows != nullptr)
+cudaError_t launch_act_quant_rows(int fmt, const void* in, void* out, int64_t rows, int64_t cols,
+                                  const int32_t* dev_rows, cudaStream_t st);
+// dst[r, :] = src[row_token[r], :], zeros where row_token[r] < 0, for r < *dev_rows
+cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* row_token, int64_t rmax, int64_t cols,
+                               const int32_t* dev_rows, cudaStream_t st);
+// out[t, :] = bf16(sum_j p[t, j] * y[row_of[t, j], :]) (p == nullptr: weight 1)
+cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* p, void* out, int64_t T, int k,
+                           int64_t d, cudaStream_t st);
+// dy[r] = bf16(p[t, j] * dout[t]); dprobs[t, j] = <dout[t], y[r]> (dprobs may be null)
+cudaError_t launch_dy_gather(const void* dout, const float* p, const int32_t* row_token, const int32_t* row_slot,
+                             const void* y, void* dy, float* dprobs, int64_t rmax, int k, int64_t d,
+                             const int32_t* dev_rows, cudaStream_t st);
+// ds[i] = (accumulate ? ds[i] : 0) + sum_j part[i * nparts + j]
+cudaError_t launch_scale_reduce(const float* part, float* ds, int64_t n, int nparts, int accumulate,
+                                cudaStream_t st);
+
+// ---- grouped GEMMs (gemm.cu) ----
+struct GemmCtx {
+  const Layout* L;
+  uint8_t* ws;
+  int fmt, flags;
+  cudaStream_t st;
+};
+cudaError_t gemm_fc1(const GemmCtx& c);         // Z1, H, H_hat  <- A1 . W13_hat^T (+ SwiGLU, AQ)
+cudaError_t gemm_fc2(const GemmCtx& c);         // Y <- H_hat . W2_hat^T
+cudaError_t gemm_dgrad_fc2(const GemmCtx& c);   // dZ1 <- SwiGLU'(dY . W2_hat)
+cudaError_t gemm_dgrad_fc1(const GemmCtx& c);   // dA1 <- dZ1 . W13_hat
+cudaError_t gemm_wgrad_fc2(const GemmCtx& c, const void* w2, const float* s2, float* ds2, int accumulate);
+cudaError_t gemm_wgrad_fc1(const GemmCtx& c, const void* w13, const float* s13, float* ds13, int accumulate);
+
+}  // namespace qad

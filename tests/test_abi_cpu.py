@@ -1,0 +1,90 @@
+"""The C ABI library loads without a GPU, exports every function include/qad.h declares,
+and rejects bad arguments on the host before touching CUDA (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import scale_only_quantization_gb300 as Q
+from scale_only_quantization_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return Q.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "qad.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qad_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_layer_calls():
+    names = _declared()
+    for n in ("qad_fakequant_fwd", "qad_moe_fwd", "qad_moe_bwd_dgrad", "qad_moe_bwd_scalegrad"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(Q.EXPORTS) == _declared()
+
+
+def test_workspace_size_and_views(lib):
+    s = Q.shape(512, 256, 128, 4, 2, Q.QAD_FMT_NVFP4)
+    ws = Q.qad_moe_workspace_bytes(s)
+    assert ws > 0 and ws % 1024 == 0
+    off, n = Q.qad_moe_debug_view(s, "W13_HAT")
+    assert off % 1024 == 0 and n == 4 * 256 * 256
+    off2, n2 = Q.qad_moe_debug_view(s, "ROW_TOKEN")
+    Rmax = (512 * 2 + 127 * 4 + 127) // 128 * 128
+    assert n2 == Rmax
+    for v in range(len(Q.VIEWS)):
+        o, k = Q.qad_moe_debug_view(s, v)
+        assert o + k <= ws
+
+
+@pytest.mark.parametrize("bad, status", [
+    (dict(d=200), Q.QAD_ERR_UNSUPPORTED),
+    (dict(F=96), Q.QAD_ERR_UNSUPPORTED),
+    (dict(topk=5, E=4), Q.QAD_ERR_UNSUPPORTED),
+    (dict(E=2000), Q.QAD_ERR_UNSUPPORTED),
+    (dict(fmt=7), Q.QAD_ERR_INVALID_ARG),
+    (dict(T=-1), Q.QAD_ERR_INVALID_ARG),
+])
+def test_bad_shapes_rejected_on_host(lib, bad, status):
+    kw = dict(T=512, d=256, F=128, E=4, topk=2, fmt=0)
+    kw.update(bad)
+    s = Q.shape(**kw)
+    assert Q.qad_moe_workspace_bytes(s) == 0
+    rc = lib.qad_moe_fwd(ctypes.byref(s), None, None, None, None, None, None, None, None, None, 0, None)
+    assert rc == status
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch(lib):
+    s = Q.shape(512, 256, 128, 4, 2, Q.QAD_FMT_NVFP4)
+    P = ctypes.c_void_p
+    assert lib.qad_moe_fwd(ctypes.byref(s), None, None, None, None, None, None, None, None, None, 0,
+                           None) == Q.QAD_ERR_INVALID_ARG
+    ws = P(1 << 20)
+    need = Q.qad_moe_workspace_bytes(s)
+    assert lib.qad_moe_fwd(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16), ws,
+                           need - 1, None) == Q.QAD_ERR_WORKSPACE
+    assert lib.qad_moe_fwd(ctypes.byref(s), P(8), P(16), P(16), P(16), P(16), P(16), P(16), P(16), ws, need,
+                           None) == Q.QAD_ERR_INVALID_ARG
+    assert lib.qad_fakequant_fwd(0, P(16), P(16), P(16), 1, 4, 24, None) == Q.QAD_ERR_UNSUPPORTED
+    assert lib.qad_fakequant_fwd(1, P(16), P(16), P(16), 1, 4, 64, None) == Q.QAD_ERR_UNSUPPORTED
+    assert lib.qad_fakequant_fwd(0, P(16), P(16), P(17), 1, 4, 64, None) == Q.QAD_ERR_INVALID_ARG
+    assert lib.qad_fakequant_fwd(0, None, None, None, 0, 4, 64, None) == Q.QAD_OK   # empty: nothing to do
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5):
+        assert Q.status_string(st)
+    assert Q.qad_kernel_name(4) == "gemm_fc1_swiglu_aq"

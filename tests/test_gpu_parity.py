@@ -1,0 +1,292 @@
+"""GPU parity of the CUDA path against the fp64 oracle, through the C ABI (small cases).
+
+Protocol (stage by stage, "teacher forced"): quantized values and routing maps are
+compared bit for bit; each floating-point stage is compared with the oracle applied to
+the GPU's own bf16 output of the previous stage, within the tolerances of gpu_util.
+The activation quantizer is discontinuous, so a one-ulp difference in H may move one
+FP4 code; the end-to-end comparison from raw inputs only reports how many moved.
+"""
+import numpy as np
+import pytest
+import torch
+
+import scale_only_quantization_gb300 as Q
+from oracle import moe as OM
+from oracle import quant as OQ
+import synth
+
+from gpu_util import Run, assert_close, assert_scale_grad, bits, host_inputs, unpadded_row_of, vals
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from scale_only_quantization_gb300 import build
+    build.build()
+    Q.lib()
+
+
+# ------------------------------------------------------------------------------ weight fake-quant
+
+def _special_weights(E, N, K, fmt, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    w = torch.randn((E, N, K), generator=g, device="cuda") * 0.02
+    w[0, 0, :8] = torch.tensor([0.5, -0.5, 0.0, -0.0, 1e-30, -1e-30, 3.0, -3.0], device="cuda")
+    w[0, 1, :] = 0.0                                   # all-zero rows -> zero scales
+    w[-1, -1, ::7] *= 40.0                             # outliers inside their block
+    w = w.to(torch.bfloat16)
+    s = synth.init_scales(w, fmt, g)
+    s[0, 2] *= 0.25                                    # clipped weights
+    return w.contiguous(), s.contiguous()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("E,N,K", [(3, 64, 512), (1, 5, 256), (2, 128, 2048)])
+def test_fakequant_bit_exact(fmt, E, N, K):
+    w, s = _special_weights(E, N, K, fmt, seed=100 + fmt)
+    out = torch.empty_like(w)
+    Q.qad_fakequant_fwd(fmt, w, s, out, E, N, K)
+    torch.cuda.synchronize()
+    want = OQ.f64_to_bf16_bits(OQ.fakequant_weight(fmt, bits(w), synth.to_numpy(s)))
+    got = bits(out)
+    bad = np.count_nonzero(got != want)
+    assert bad == 0, "%d of %d fake-quant outputs differ" % (bad, got.size)
+
+
+def test_fakequant_empty_is_a_no_op():
+    Q.qad_fakequant_fwd(0, None, None, None, 0, 16, 64)
+
+
+# ------------------------------------------------------------------------------ routing
+
+def _check_routing(run, host):
+    rt = run.routing()
+    ref = OM.route(host["topk_idx"], run.inp["E"])
+    real = rt["real"]
+    assert np.array_equal(rt["row_token"][real], ref["row_token"])
+    assert np.array_equal(rt["row_slot"][real], ref["row_slot"])
+    assert np.array_equal(rt["counts"], ref["counts"])
+    padded = (ref["counts"] + 127) // 128 * 128
+    assert np.array_equal(rt["offs"], np.concatenate([[0], np.cumsum(padded)]))
+    assert np.array_equal(unpadded_row_of(rt), ref["row_of"])
+    assert rt["hdr"][0] == ref["error"] == run.error
+    assert rt["rpad"] == padded.sum() and rt["hdr"][1] == padded.sum() // 128
+    return rt, ref
+
+
+# ------------------------------------------------------------------------------ the layer, stage by stage
+
+def _stagewise(run, host, check_h=True):
+    """Teacher-forced comparison of every stage; returns the GPU stages for further use."""
+    inp = run.inp
+    fmt, T, d, F, E, k = inp["fmt"], inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"]
+    rt, ref = _check_routing(run, host)
+    real, off = rt["real"], ref["offsets"]
+    row_of = ref["row_of"]
+    p = host["topk_w"].astype(np.float64)
+
+    # fake-quantized weights (bit exact)
+    w13h_b = bits(run.view("W13_HAT", torch.bfloat16)).reshape(E, 2 * F, d)
+    w2h_b = bits(run.view("W2_HAT", torch.bfloat16)).reshape(E, d, F)
+    assert np.array_equal(w13h_b, OQ.f64_to_bf16_bits(OQ.fakequant_weight(fmt, host["w13"], host["s13"])))
+    assert np.array_equal(w2h_b, OQ.f64_to_bf16_bits(OQ.fakequant_weight(fmt, host["w2"], host["s2"])))
+    w13h, w2h = OQ.bf16_to_f64(w13h_b), OQ.bf16_to_f64(w2h_b)
+
+    # A1 = AQ(x) gathered (bit exact); padding rows are zero
+    a1_all = run.rows("A1", d)
+    a1 = a1_all[real]
+    want_a1 = OQ.fakequant_act(fmt, OQ.bf16_to_f64(host["x"]))[ref["row_token"]]
+    assert np.array_equal(OQ.f64_to_bf16_bits(a1), OQ.f64_to_bf16_bits(want_a1))
+    assert np.all(a1_all[~real] == 0)
+
+    # Z1 = A1 . W13_hat^T
+    z1_all = run.rows("Z1", 2 * F)
+    z1 = z1_all[real]
+    assert_close(z1, OQ.round_bf16(OM.grouped_gemm_nt(a1, w13h, off)), "Z1")
+    assert np.all(z1_all[~real] == 0)
+
+    # H and H_hat = AQ(H): bit exact given the GPU's H
+    hh = run.rows("H_HAT", F)[real]
+    if check_h:
+        h = run.rows("H", F)[real]
+        assert_close(h, OQ.round_bf16(OM.swiglu(z1)), "H")
+        assert np.array_equal(OQ.f64_to_bf16_bits(hh), OQ.f64_to_bf16_bits(OQ.fakequant_act(fmt, h)))
+
+    # Y = H_hat . W2_hat^T, out = sum_j p Y
+    y = run.rows("Y", d)[real]
+    assert_close(y, OQ.round_bf16(OM.grouped_gemm_nt(hh, w2h, off)), "Y")
+    out = vals(run.out)
+    assert_close(out, OQ.round_bf16(OM.combine(y, p, row_of)), "out")
+
+    # dY = bf16(fp32(p * dout)) (bit exact), padding rows zero
+    dy_all = run.rows("DY", d)
+    dy = dy_all[real]
+    dout = OQ.bf16_to_f64(host["dout"])
+    want_dy = OQ.round_bf16(OQ.round_f32(dout[ref["row_token"]] * p[ref["row_token"], ref["row_slot"]][:, None]))
+    assert np.array_equal(OQ.f64_to_bf16_bits(dy), OQ.f64_to_bf16_bits(want_dy))
+    assert np.all(dy_all[~real] == 0)
+
+    # dZ1 = SwiGLU'(dY . W2_hat) given the GPU's Z1
+    dz1 = run.rows("DZ1", 2 * F)[real]
+    assert_close(dz1, OQ.round_bf16(OM.swiglu_bwd(OM.grouped_gemm_nn(dy, w2h, off), z1)), "dZ1")
+    da1 = run.rows("DA1", d)[real]
+    assert_close(da1, OQ.round_bf16(OM.grouped_gemm_nn(dz1, w13h, off)), "dA1")
+    assert_close(vals(run.dx), OQ.round_bf16(OM.combine(da1, np.ones((T, k)), row_of)), "dx")
+    if run.dprobs is not None:
+        dp = np.zeros((T, k))
+        for j in range(k):
+            r = row_of[:, j]
+            ok = r >= 0
+            dp[ok, j] = np.einsum("td,td->t", dout[ok], y[r[ok]])
+        assert_close(synth.to_numpy(run.dprobs).astype(np.float64), dp, "dprobs")
+
+    # scale gradients from the GPU's stored operands
+    dw2 = OM.grouped_wgrad(dy, hh, off, E)
+    dw13 = OM.grouped_wgrad(dz1, a1, off, E)
+    ds2 = OQ.scale_grad_from_wgrad(fmt, dw2, host["w2"], host["s2"])
+    ds13 = OQ.scale_grad_from_wgrad(fmt, dw13, host["w13"], host["s13"])
+    assert_scale_grad(synth.to_numpy(run.ds2), ds2.reshape(host["s2"].shape), "ds2")
+    assert_scale_grad(synth.to_numpy(run.ds13), ds13.reshape(host["s13"].shape), "ds13")
+    return dict(y=y, ds2=ds2, ds13=ds13)
+
+
+def _tiny(fmt, **over):
+    cfg = synth.workload("tiny_nvfp4", fmt=fmt, **over)
+    return synth.make_inputs(cfg, seed=0, device="cuda")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_layer_stagewise_tiny(fmt):
+    inp = _tiny(fmt)
+    host = host_inputs(inp)
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    _stagewise(run, host)
+
+    # end to end from raw inputs: report moved activation codes, check the outputs loosely
+    fwd = OM.moe_forward(fmt, host["x"], host["topk_idx"], host["topk_w"], host["w13"], host["s13"], host["w2"],
+                         host["s2"])
+    rt = run.routing()
+    hh_gpu = run.rows("H_HAT", inp["F"])[rt["real"]]
+    moved = int(np.count_nonzero(OQ.f64_to_bf16_bits(hh_gpu) != OQ.f64_to_bf16_bits(fwd["hh"])))
+    print("fmt %d: %d of %d H_hat codes differ end to end" % (fmt, moved, hh_gpu.size))
+    assert moved <= 0.01 * hh_gpu.size
+    out_ref = fwd["out"]
+    rel = np.max(np.abs(vals(run.out) - out_ref)) / np.sqrt(np.mean(out_ref ** 2))
+    assert rel < 0.5
+
+
+def test_stash_h_flag_off_matches_on():
+    inp = _tiny(Q.QAD_FMT_NVFP4)
+    a = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    b = Run(inp, flags=0)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
+    assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
+
+
+def test_runs_are_deterministic():
+    inp = _tiny(Q.QAD_FMT_NVFP4)
+    a, b = Run(inp), Run(inp)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
+    assert torch.equal(a.dprobs, b.dprobs)
+    assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_scalegrad_accumulate_adds(fmt):
+    inp = _tiny(fmt)
+    a = Run(inp)
+    base = (torch.full_like(inp["s13"], 0.5), torch.full_like(inp["s2"], -0.25))
+    b = Run(inp, accumulate=1, ds_init=base)
+    assert torch.allclose(b.ds13, a.ds13 + 0.5, rtol=0, atol=1e-6 * float(a.ds13.abs().max()) + 1e-6)
+    assert torch.allclose(b.ds2, a.ds2 - 0.25, rtol=0, atol=1e-6 * float(a.ds2.abs().max()) + 1e-6)
+
+
+# ------------------------------------------------------------------------------ edge cases
+
+def _custom_routing(inp, idx):
+    inp = dict(inp)
+    T, k = idx.shape
+    g = torch.Generator(device="cuda").manual_seed(7)
+    inp["topk_idx"] = torch.as_tensor(idx, dtype=torch.int32, device="cuda").contiguous()
+    inp["topk_w"] = torch.softmax(torch.randn((T, k), generator=g, device="cuda"), 1).contiguous()
+    inp["x"] = inp["x"][:T].contiguous()
+    inp["dout"] = inp["dout"][:T].contiguous()
+    inp["T"], inp["topk"] = T, k
+    return inp
+
+
+def test_empty_experts_single_row_expert_and_small_batch():
+    base = synth.make_inputs(synth.workload("tiny_nvfp4", E=8, T=300), seed=1, device="cuda")
+    rng = np.random.default_rng(3)
+    T, k = 300, 2
+    idx = np.stack([rng.choice([0, 3, 5], 2, replace=False) for _ in range(T)])
+    idx[17] = [6, 0]                                  # expert 6 gets exactly one row
+    inp = _custom_routing(base, idx)
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    res = _stagewise(run, host_inputs(inp))
+    # experts that received no rows get a zero scale gradient
+    for e in (1, 2, 4, 7):
+        assert np.all(synth.to_numpy(run.ds13)[e] == 0) and np.all(synth.to_numpy(run.ds2)[e] == 0)
+    assert np.count_nonzero(synth.to_numpy(run.ds13)[6]) > 0
+
+
+def test_fewer_rows_than_one_tile():
+    base = synth.make_inputs(synth.workload("tiny_nvfp4"), seed=2, device="cuda")
+    idx = np.array([[1, 2], [2, 3], [0, 1], [3, 0], [1, 3]])
+    inp = _custom_routing(base, idx)
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    _stagewise(run, host_inputs(inp))
+
+
+def test_zero_tokens():
+    base = synth.make_inputs(synth.workload("tiny_nvfp4"), seed=3, device="cuda")
+    inp = _custom_routing(base, np.zeros((0, 2), dtype=np.int64))
+    run = Run(inp)
+    assert run.error == 0
+    assert torch.all(run.ds13 == 0) and torch.all(run.ds2 == 0)
+
+
+def test_invalid_routing_indices_are_dropped_and_flagged():
+    base = synth.make_inputs(synth.workload("tiny_nvfp4"), seed=4, device="cuda")
+    rng = np.random.default_rng(5)
+    idx = np.stack([rng.permutation(4)[:2] for _ in range(512)])
+    idx[3] = [9, 1]            # out of range
+    idx[10] = [2, 2]           # repeated expert
+    idx[11] = [-1, -7]         # negative
+    inp = _custom_routing(base, idx)
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == (Q.QAD_DEV_BAD_INDEX | Q.QAD_DEV_DUP_INDEX)
+    _stagewise(run, host_inputs(inp))
+    dp = synth.to_numpy(run.dprobs)
+    assert dp[3, 0] == 0 and dp[10, 1] == 0 and np.all(dp[11] == 0)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Guard bands around every output keep their sentinel values."""
+    inp = _tiny(Q.QAD_FMT_NVFP4)
+    T, d, k = inp["T"], inp["d"], inp["topk"]
+    G = 256
+    s = Q.shape(T, d, inp["F"], inp["E"], k, 0)
+    ws = torch.empty(Q.qad_moe_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    big_out = torch.full((T * d + 2 * G,), 7.0, dtype=torch.bfloat16, device="cuda")
+    big_dx = torch.full((T * d + 2 * G,), 7.0, dtype=torch.bfloat16, device="cuda")
+    big_dp = torch.full((T * k + 2 * G,), 7.0, dtype=torch.float32, device="cuda")
+    n13, n2 = inp["s13"].numel(), inp["s2"].numel()
+    big13 = torch.full((n13 + 2 * G,), 7.0, dtype=torch.float32, device="cuda")
+    big2 = torch.full((n2 + 2 * G,), 7.0, dtype=torch.float32, device="cuda")
+    Q.qad_moe_fwd(s, inp["x"], inp["topk_idx"], inp["topk_w"], inp["w13"], inp["s13"], inp["w2"], inp["s2"],
+                  big_out[G:G + T * d], ws)
+    Q.qad_moe_bwd_dgrad(s, inp["dout"], inp["topk_w"], inp["w13"], inp["s13"], inp["w2"], inp["s2"],
+                        big_dx[G:G + T * d], big_dp[G:G + T * k], ws)
+    Q.qad_moe_bwd_scalegrad(s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], big13[G:G + n13], big2[G:G + n2], 0, ws)
+    torch.cuda.synchronize()
+    for t, n in ((big_out, T * d), (big_dx, T * d), (big_dp, T * k), (big13, n13), (big2, n2)):
+        assert torch.all(t[:G] == 7.0) and torch.all(t[G + n:] == 7.0)
+        assert torch.all(torch.isfinite(t[G:G + n].float()))
