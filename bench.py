@@ -151,7 +151,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     B.build()
     Q.lib()
-    cfg = synth.workload(args.workload)
+    cfg = synth.workload(args.workload, **({"T": args.tokens} if args.tokens else {}))
     inp = synth.make_inputs(cfg, seed=rank, device=dev)
     T, d, F, E, k, fmt = inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"]
     s = Q.shape(T, d, F, E, k, fmt)
@@ -276,7 +276,8 @@ def run_ours(args):
         "metric": METRIC, "value": T * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "format": FMT_NAME[fmt], "E": E, "d": d, "F": F, "topk": k,
+        "config": {"workload": args.workload if not args.tokens else "%s_T%d" % (args.workload, T),
+                   "format": FMT_NAME[fmt], "E": E, "d": d, "F": F, "topk": k,
                    "tokens_per_gpu": T, "global_batch": T * world, "parallelism": "dp%d" % world,
                    "l2": "inputs larger than L2 (weights %.2f GB streamed per pass), no flush" %
                          (2 * 3 * E * F * d / 1e9)},
@@ -374,12 +375,14 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (small cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

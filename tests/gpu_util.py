@@ -2,9 +2,16 @@
 stages back to the host, and the tolerance rules.
 
 Tolerances: floating-point layer outputs and input gradients must satisfy
-max |gpu - oracle| <= 2e-2 * RMS(oracle); scale gradients relative L2 <= 1e-2.
+|gpu - oracle| <= 2e-2 * RMS(oracle) + 2^-8 * |oracle| element by element: the stated
+2e-2 x RMS bound on the arithmetic, plus the rounding of each stored bf16 value
+(at most half a bf16 ulp, i.e. 2^-8 of its magnitude), which on its own exceeds
+2e-2 x RMS for any element larger than ~5 x RMS.  Scale gradients: relative L2 <= 1e-2.
 Quantized values (fake-quant weights/activations), routing maps and the bf16(p * dout)
-rows are compared bit for bit.
+rows are compared bit for bit.  A tolerance check compares the GPU's stored bf16 value
+with the oracle's value BEFORE the oracle's own final bf16 rounding: the GPU rounds an
+fp32 sum and the oracle an fp64 one, so near a rounding midpoint the two stored values
+may legitimately differ by one bf16 ulp, which for an element far above the RMS exceeds
+2e-2 x RMS on its own.
 """
 import numpy as np
 import torch
@@ -15,6 +22,7 @@ from oracle import quant as OQ
 import synth
 
 MAXABS_REL = 2e-2
+BF16_HALF_ULP_REL = 2.0 ** -8
 SCALE_REL_L2 = 1e-2
 
 
@@ -34,10 +42,13 @@ def assert_close(gpu, ref, what):
     if ref.size == 0:
         return 0.0
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    err = float(np.max(np.abs(gpu - ref)))
     assert np.all(np.isfinite(gpu)), what
-    assert err <= MAXABS_REL * rms + 1e-30, "%s: max abs err %.3e > %.1e x rms %.3e" % (what, err, MAXABS_REL, rms)
-    return err / max(rms, 1e-30)
+    diff = np.abs(gpu - ref)
+    excess = diff - (MAXABS_REL * rms + BF16_HALF_ULP_REL * np.abs(ref))
+    i = int(np.argmax(excess))
+    assert excess.flat[i] <= 1e-30, "%s: |err| %.3e at |ref| %.3e exceeds %.1e x rms %.3e + 2^-8 |ref|" % (
+        what, diff.flat[i], abs(ref.flat[i]), MAXABS_REL, rms)
+    return float(diff.max()) / max(rms, 1e-30)
 
 
 def assert_scale_grad(gpu, ref, what):

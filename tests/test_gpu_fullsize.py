@@ -93,20 +93,20 @@ def test_full_size_sampled(name):
         a1 = _rows(run, "A1", d, pick)
         assert np.array_equal(OQ.f64_to_bf16_bits(a1), OQ.f64_to_bf16_bits(OQ.fakequant_act(fmt, x)))
         z1 = _rows(run, "Z1", 2 * F, pick)
-        assert_close(z1, OQ.round_bf16(a1 @ w13h.T), "Z1 rows e%d" % e)
+        assert_close(z1, a1 @ w13h.T, "Z1 rows e%d" % e)
         h = _rows(run, "H", F, pick)
-        assert_close(h, OQ.round_bf16(OM.swiglu(z1)), "H rows e%d" % e)
+        assert_close(h, OM.swiglu(z1), "H rows e%d" % e)
         hh = _rows(run, "H_HAT", F, pick)
         assert np.array_equal(OQ.f64_to_bf16_bits(hh), OQ.f64_to_bf16_bits(OQ.fakequant_act(fmt, h)))
         y = _rows(run, "Y", d, pick)
-        assert_close(y, OQ.round_bf16(hh @ w2h.T), "Y rows e%d" % e)
+        assert_close(y, hh @ w2h.T, "Y rows e%d" % e)
         dy = _rows(run, "DY", d, pick)
         want_dy = OQ.round_bf16(OQ.round_f32(dout * p[toks, slots][:, None]))
         assert np.array_equal(OQ.f64_to_bf16_bits(dy), OQ.f64_to_bf16_bits(want_dy))
         dz1 = _rows(run, "DZ1", 2 * F, pick)
-        assert_close(dz1, OQ.round_bf16(OM.swiglu_bwd(dy @ w2h, z1)), "dZ1 rows e%d" % e)
+        assert_close(dz1, OM.swiglu_bwd(dy @ w2h, z1), "dZ1 rows e%d" % e)
         da1 = _rows(run, "DA1", d, pick)
-        assert_close(da1, OQ.round_bf16(dz1 @ w13h), "dA1 rows e%d" % e)
+        assert_close(da1, dz1 @ w13h, "dA1 rows e%d" % e)
 
     # 64 sampled tokens: combine, input gradient and routing-weight gradient
     toks = rng.choice(T, size=64, replace=False)
@@ -114,8 +114,8 @@ def test_full_size_sampled(name):
     ys = _rows(run, "Y", d, np.maximum(ro, 0).reshape(-1)).reshape(64, k, d)
     das = _rows(run, "DA1", d, np.maximum(ro, 0).reshape(-1)).reshape(64, k, d)
     dout = OQ.bf16_to_f64(bits(inp["dout"][torch.as_tensor(toks, device="cuda")]))
-    out_ref = OQ.round_bf16(np.einsum("tj,tjd->td", p[toks], ys))
-    dx_ref = OQ.round_bf16(das.sum(axis=1))
+    out_ref = np.einsum("tj,tjd->td", p[toks], ys)
+    dx_ref = das.sum(axis=1)
     dp_ref = np.einsum("td,tjd->tj", dout, ys)
     sel = torch.as_tensor(toks, device="cuda")
     assert_close(vals(run.out[sel]), out_ref, "out (sampled tokens)")
