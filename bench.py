@@ -151,7 +151,12 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     B.build()
     Q.lib()
-    cfg = synth.workload(args.workload, **({"T": args.tokens} if args.tokens else {}))
+    over = {}
+    if args.tokens:
+        over["T"] = args.tokens
+    if args.experts:
+        over["E"] = args.experts
+    cfg = synth.workload(args.workload, **over)
     inp = synth.make_inputs(cfg, seed=rank, device=dev)
     T, d, F, E, k, fmt = inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"]
     s = Q.shape(T, d, F, E, k, fmt)
@@ -276,7 +281,7 @@ def run_ours(args):
         "metric": METRIC, "value": T * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload if not args.tokens else "%s_T%d" % (args.workload, T),
+        "config": {"workload": args.workload + ("" if not over else "_T%d_E%d" % (T, E)),
                    "format": FMT_NAME[fmt], "E": E, "d": d, "F": F, "topk": k,
                    "tokens_per_gpu": T, "global_batch": T * world, "parallelism": "dp%d" % world,
                    "l2": "inputs larger than L2 (weights %.2f GB streamed per pass), no flush" %
@@ -383,6 +388,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the workload's expert count (small cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -191,6 +191,16 @@ int qad_profile_read(float* ms, int64_t* launches, int n);
 const char* qad_kernel_name(int id);
 int64_t qad_launch_count(void);
 
+/*
+ * Self-check of the division inside the quantizers (not an operation of the method).
+ * The kernels compute x = fp32(w / s) from the correctly rounded reciprocal of s and one
+ * FMA correction (Markstein's theorem) instead of a division per element.  For each i
+ * this writes x_fast[i] (that computation) and x_ieee[i] (CUDA's IEEE division); the two
+ * must agree bit for bit.  w, s, x_fast, x_ieee: fp32 [n], device pointers.
+ */
+int qad_debug_quotient(const float* w, const float* s, float* x_fast, float* x_ieee, int64_t n,
+                       qad_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

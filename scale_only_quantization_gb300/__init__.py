@@ -24,7 +24,8 @@ KERNELS = 14
 
 EXPORTS = ["qad_fakequant_fwd", "qad_moe_workspace_bytes", "qad_moe_fwd", "qad_moe_bwd_dgrad",
            "qad_moe_bwd_scalegrad", "qad_check_device_error", "qad_status_string", "qad_moe_debug_view",
-           "qad_profile_enable", "qad_profile_reset", "qad_profile_read", "qad_kernel_name", "qad_launch_count"]
+           "qad_profile_enable", "qad_profile_reset", "qad_profile_read", "qad_kernel_name", "qad_launch_count",
+           "qad_debug_quotient"]
 
 
 class QADError(RuntimeError):
@@ -70,6 +71,7 @@ def lib():
                                                 ctypes.c_int]),
             "qad_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
             "qad_launch_count": (ctypes.c_int64, []),
+            "qad_debug_quotient": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -171,6 +173,11 @@ def qad_kernel_name(i):
 
 def qad_launch_count():
     return int(lib().qad_launch_count())
+
+
+def qad_debug_quotient(w, s, x_fast, x_ieee, n, stream=None):
+    return _check(lib().qad_debug_quotient(_ptr(w), _ptr(s), _ptr(x_fast), _ptr(x_ieee), int(n), _stream(stream)),
+                  "qad_debug_quotient")
 
 
 def workspace_view(ws, s, which, dtype):

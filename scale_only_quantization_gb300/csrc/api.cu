@@ -122,8 +122,8 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->dy = take(2 * (size_t)(Rmax * d));
   L->dz1 = take(2 * (size_t)(Rmax * 2 * F));
   L->da1 = take(2 * (size_t)(Rmax * d));
-  L->part13 = take(4 * (size_t)(E * 2 * F * (d / 128)));
-  L->part2 = take(4 * (size_t)(E * d * (F / 128)));
+  L->part13 = take(4 * (size_t)(E * 2 * F * (d / 128) * 2));
+  L->part2 = take(4 * (size_t)(E * d * (F / 128) * 2));
   L->total = o;
   return QAD_OK;
 }
@@ -348,5 +348,12 @@ const char* qad_kernel_name(int id) {
 }
 
 int64_t qad_launch_count(void) { return g_launch_total.load(); }
+
+int qad_debug_quotient(const float* w, const float* s, float* x_fast, float* x_ieee, int64_t n, qad_stream_t stream) {
+  if (n < 0) return QAD_ERR_INVALID_ARG;
+  if (n == 0) return QAD_OK;
+  if (!w || !s || !x_fast || !x_ieee) return QAD_ERR_INVALID_ARG;
+  return to_status(launch_quotient_check(w, s, x_fast, x_ieee, n, reinterpret_cast<cudaStream_t>(stream)));
+}
 
 }  // extern "C"

@@ -88,35 +88,72 @@ template <> struct Clip<kFmtNvfp4> { static constexpr float lo = -6.0f, hi = 6.0
 template <> struct Clip<kFmtInt4> { static constexpr float lo = -8.0f, hi = 7.0f; };
 template <> struct Clip<kFmtFp8> { static constexpr float lo = -448.0f, hi = 448.0f; };
 
-// x = fp32(w / s); s == 0 -> +-0 with the sign of w
+// x = fp32(w / s); s == 0 -> +-0 with the sign of w (IEEE division, the reference path)
 __device__ __forceinline__ float quotient(float w, float s) {
   return s == 0.0f ? copysignf(0.0f, w) : __fdiv_rn(w, s);
+}
+
+// The same correctly rounded quotients from r = RN(1 / s), without a division per element.
+// Markstein's theorem (P. Markstein, "IA-64 and Elementary Functions", 2000; also
+// Cornea, Golliver and Markstein 1999): if r is the correctly rounded reciprocal of s and
+// q approximates w / s within one ulp, the remainder e = w - s q is exact (one FMA) and
+// RN(q + e r) is the correctly rounded quotient; q = RN(w r) is within one ulp.  The
+// theorem needs the remainder and the quotient in the normal range.  With s in
+// [2^-126, 2^20] and |w| >= 2^-80 the remainder (>= 2^-46 |w| when non-zero) and the
+// quotient (>= 2^-100) are normal; w = +-0 gives +-0 (sign restored below); an overflow
+// is checked.  If any element of the block falls outside, the whole block is recomputed
+// with the division (rare: tiny non-zero weights or extreme scales).  The GPU tests
+// compare the result with CUDA's own division bit for bit.
+template <int N>
+__device__ __forceinline__ void quotients(const float* w, float s, float* x) {
+  const float r = __frcp_rn(s);
+  bool ok = s >= 1.17549435e-38f && s <= 0x1p20f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float q = __fmul_rn(w[i], r);
+    const float e = __fmaf_rn(-q, s, w[i]);
+    const float xi = copysignf(__fmaf_rn(e, r, q), w[i]);
+    const float aw = fabsf(w[i]);
+    ok = ok && (aw >= 0x1p-80f || aw == 0.0f) && fabsf(xi) <= 3.0e38f;
+    x[i] = xi;
+  }
+  if (__builtin_expect(!ok, 0)) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = quotient(w[i], s);
+  }
 }
 
 // Fake-quantize n (even) values that share scale s, in place: v <- bf16(fp32(q(v / s) * s)).
 template <int FMT, int N>
 __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
+  float x[N];
+  quotients<N>(v, s, x);
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
-    float2 q = q_pair<FMT>(quotient(v[i], s), quotient(v[i + 1], s));
+    const float2 q = q_pair<FMT>(x[i], x[i + 1]);
     v[i] = round_bf16(__fmul_rn(q.x, s));
     v[i + 1] = round_bf16(__fmul_rn(q.y, s));
   }
 }
 
-// LSQ straight-through factor phi(x): q(x) - x inside the closed clip range, else the bound.
+// LSQ straight-through factor phi(x): q(x) - x inside the closed clip range, else the
+// violated bound.  q saturates (E2M1, E4M3) or clamps (INT4) to exactly that bound
+// outside the range, so phi = q(x) - (x inside ? x : 0).
 template <int FMT>
 __device__ __forceinline__ float2 lsq_pair(float xa, float xb) {
-  float2 q = q_pair<FMT>(xa, xb);
-  float pa = xa < Clip<FMT>::lo ? Clip<FMT>::lo : (xa > Clip<FMT>::hi ? Clip<FMT>::hi : q.x - xa);
-  float pb = xb < Clip<FMT>::lo ? Clip<FMT>::lo : (xb > Clip<FMT>::hi ? Clip<FMT>::hi : q.y - xb);
-  return make_float2(pa, pb);
+  const float2 q = q_pair<FMT>(xa, xb);
+  const float ia = (xa >= Clip<FMT>::lo && xa <= Clip<FMT>::hi) ? xa : 0.0f;
+  const float ib = (xb >= Clip<FMT>::lo && xb <= Clip<FMT>::hi) ? xb : 0.0f;
+  return make_float2(q.x - ia, q.y - ib);
 }
 
 // ---------------------------------------------------------------------------------- misc
 
-__device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
-__device__ __forceinline__ float sigmoid_f(float g) { return __fdiv_rn(1.0f, 1.0f + expf(-g)); }
+// sigmoid(g) = 1 / (1 + exp(-g)) from CUDA's fast exponential and the correctly rounded
+// reciprocal (exp(-g) = inf gives 0).  Used only where the result is compared with the
+// oracle by tolerance.
+__device__ __forceinline__ float sigmoid_f(float g) { return __frcp_rn(1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return __fmul_rn(g, sigmoid_f(g)); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

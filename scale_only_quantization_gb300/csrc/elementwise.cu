@@ -326,7 +326,27 @@ __global__ void __launch_bounds__(256) scale_reduce_kernel(const float* __restri
   }
 }
 
+__global__ void __launch_bounds__(256) quotient_check_kernel(const float* __restrict__ w, const float* __restrict__ s,
+                                                             float* __restrict__ fast, float* __restrict__ ieee,
+                                                             int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float wi = w[i];
+    float x;
+    quotients<1>(&wi, s[i], &x);
+    fast[i] = x;
+    ieee[i] = quotient(wi, s[i]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, float* ieee, int64_t n,
+                                  cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  quotient_check_kernel<<<grid_for(n, 256, 8), 256, 0, st>>>(w, s, fast, ieee, n);
+  return cudaGetLastError();
+}
 
 // ------------------------------------------------------------------------- launchers
 

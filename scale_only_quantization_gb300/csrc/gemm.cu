@@ -16,9 +16,11 @@
 //
 // Per CTA (one per SM, persistent over tiles): warp 0 issues TMA loads (128B-swizzled
 // tiles) into a STAGES-deep ring guarded by mbarriers; warp 1 owns the tensor memory and
-// issues tcgen05.mma (M=128, N=BN, K=16, bf16 x bf16 -> fp32) from one thread; warps 2-5
+// issues tcgen05.mma (M=128, N=BN, K=16, bf16 x bf16 -> fp32) from one thread; warps 2-9
 // read the accumulator (two TMEM buffers, so the next tile's MMAs overlap this epilogue)
-// with tcgen05.ld and run the fused epilogue.  Every wait is bounded: on expiry the CTA
+// with tcgen05.ld and run the fused epilogue: a warp may only read the 32 TMEM lanes of
+// its quadrant (warp id mod 4), so each quadrant has two warps, one per column half.
+// Every wait is bounded: on expiry the CTA
 // raises QAD_DEV_TIMEOUT in the workspace error word, drains what it issued and exits.
 #include <cuda.h>
 
@@ -30,7 +32,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;       // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-9 epilogue
+constexpr int kEpiThreads = 256;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 enum { EPI_FC1 = 0, EPI_STORE = 1, EPI_SWIGLU_BWD = 2, EPI_SCALEGRAD = 3 };
@@ -150,20 +153,30 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+// tcgen05.ld is asynchronous until tcgen05.wait::ld: the loads of the next chunk are issued
+// before the current chunk is processed.  The wait takes the destination registers as
+// in/out operands so the compiler keeps them untouched until the data has landed.
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (issue only)
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+// 16 consecutive fp32 columns (issue only)
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) :: "memory");
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t (&a)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]) :: "memory");
+}
+__device__ __forceinline__ void tmem_wait16x2(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]) :: "memory");
 }
 
 __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v) {
@@ -171,10 +184,15 @@ __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) d[i] = pack8(v + 8 * i);
 }
-__device__ __forceinline__ void load32(const __nv_bfloat16* src, float* v) {
+__device__ __forceinline__ void ldraw16(const __nv_bfloat16* src, uint4 (&u)[2]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) unpack8(__ldg(s + i), v + 8 * i);
+  u[0] = __ldg(s);
+  u[1] = __ldg(s + 1);
+}
+__device__ __forceinline__ void store16(__nv_bfloat16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = pack8(v);
+  d[1] = pack8(v + 8);
 }
 
 // ---------------------------------------------------------------------------------- tiles
@@ -209,168 +227,241 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
 
 // ---------------------------------------------------------------------------------- epilogues
 
-template <int FMT>
-__device__ __forceinline__ void fc1_aq(float* h) {
-  if constexpr (FMT == kFmtNvfp4) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[16 * b + i]));
-      fakequant_inplace<kFmtNvfp4, 16>(h + 16 * b, __fdiv_rn(amax, 6.0f));
-    }
-  }
-}
-
-// Z1 (bf16) and H = bf16(silu(gate) * up) for 128 FFN columns; H_hat = AQ(H) for nvfp4,
-// = H for w4a16; fp8 needs the row amax over all F columns, so H goes to the H buffer
-// and a separate pass quantizes it.
+// Z1 (bf16) and H = bf16(silu(gate) * up) for 64 of the tile's 128 FFN columns (this warp's
+// half), 16 at a time (one activation-quant block); H_hat = AQ(H) for nvfp4, = H for
+// w4a16; fp8 needs the row amax over all F columns, so H goes to the H buffer and a
+// separate pass quantizes it.
 template <int BN>
-__device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+__device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
   const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
-  const int fcol0 = ti.nb * 128;
   __nv_bfloat16* z1 = p.out + row * p.ld_out;
+  __nv_bfloat16* hrow = p.out3 + row * p.ld_out2;
+  __nv_bfloat16* hhrow = p.out2 + row * p.ld_out2;
   const bool stash_h = (p.flags & QAD_FLAG_STASH_H) || p.fmt == kFmtFp8;
+  const int c0 = 64 * half;  // first of this warp's 64 columns within the tile's 128
+  uint32_t g[16], u[16], gn[16], un[16];
+  tmem_ld16_issue(tbase + c0, g);
+  tmem_ld16_issue(tbase + 128 + c0, u);
+  tmem_wait16x2(g, u);
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    float g[32], u[32];
-    tmem_ld32(tbase + 32 * c, g);
-    tmem_ld32(tbase + 128 + 32 * c, u);
-    const int f0 = fcol0 + 32 * c;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      g[i] = round_bf16(g[i]);
-      u[i] = round_bf16(u[i]);
+  for (int j = 0; j < 4; ++j) {
+    const int cc = c0 + 16 * j;
+    if (j < 3) {
+      tmem_ld16_issue(tbase + cc + 16, gn);
+      tmem_ld16_issue(tbase + 128 + cc + 16, un);
     }
-    store32(z1 + f0, g);
-    store32(z1 + p.F + f0, u);
-    float h[32];
+    const int f0 = ti.nb * 128 + cc;
+    float gv[16], uv[16], h[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) h[i] = round_bf16(__fmul_rn(silu_f(g[i]), u[i]));
-    if (stash_h) store32(p.out3 + row * p.ld_out2 + f0, h);
-    if (p.fmt == kFmtFp8) continue;
-    if (p.fmt == kFmtNvfp4) fc1_aq<kFmtNvfp4>(h);
-    store32(p.out2 + row * p.ld_out2 + f0, h);
+    for (int i = 0; i < 16; ++i) {
+      gv[i] = round_bf16(__uint_as_float(g[i]));
+      uv[i] = round_bf16(__uint_as_float(u[i]));
+      h[i] = round_bf16(__fmul_rn(silu_f(gv[i]), uv[i]));
+    }
+    uint4* zg = reinterpret_cast<uint4*>(z1 + f0);
+    uint4* zu = reinterpret_cast<uint4*>(z1 + p.F + f0);
+    zg[0] = pack8(gv);
+    zg[1] = pack8(gv + 8);
+    zu[0] = pack8(uv);
+    zu[1] = pack8(uv + 8);
+    if (stash_h) {
+      uint4* hs = reinterpret_cast<uint4*>(hrow + f0);
+      hs[0] = pack8(h);
+      hs[1] = pack8(h + 8);
+    }
+    if (p.fmt != kFmtFp8) {
+      if (p.fmt == kFmtNvfp4) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[i]));
+        fakequant_inplace<kFmtNvfp4, 16>(h, __fdiv_rn(amax, 6.0f));
+      }
+      uint4* hh = reinterpret_cast<uint4*>(hhrow + f0);
+      hh[0] = pack8(h);
+      hh[1] = pack8(h + 8);
+    }
+    if (j < 3) {
+      tmem_wait16x2(gn, un);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        g[i] = gn[i];
+        u[i] = un[i];
+      }
+    }
   }
 }
 
 template <int BN>
-__device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+__device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
   const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
   __nv_bfloat16* dst = p.out + row * p.ld_out + (int64_t)ti.nb * BN;
+  constexpr int NH = BN / 64;
+  uint32_t r[32], rn[32];
+  tmem_ld32_issue(tbase + 32 * half * NH, r);
+  tmem_wait32(r);
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = half * NH; c < (half + 1) * NH; ++c) {
+    const bool more = c + 1 < (half + 1) * NH;
+    if (more) tmem_ld32_issue(tbase + 32 * (c + 1), rn);
     float v[32];
-    tmem_ld32(tbase + 32 * c, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
     store32(dst + 32 * c, v);
+    if (more) {
+      tmem_wait32(rn);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = rn[i];
+    }
   }
 }
 
-// dZ1 = [dH * up * sig(g) * (1 + g (1 - sig(g))), dH * g * sig(g)] from the stored bf16 Z1
+// dZ1 = [dH * up * sig(g) * (1 + g (1 - sig(g))), dH * g * sig(g)] from the stored bf16 Z1,
+// 16 columns at a time
 template <int BN>
-__device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+__device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
+                                               int half) {
   const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
   const __nv_bfloat16* z1 = p.aux + row * p.ld_aux;
   __nv_bfloat16* dz1 = p.out + row * p.ld_out;
+  constexpr int STEPS = BN / 32;  // 16-column steps per half
+  const int col0 = half * (BN / 2);
+  uint32_t r[16], rn[16];
+  uint4 gr[2], ur[2], grn[2], urn[2];
+  ldraw16(z1 + ti.nb * BN + col0, gr);
+  ldraw16(z1 + p.F + ti.nb * BN + col0, ur);
+  tmem_ld16_issue(tbase + col0, r);
+  tmem_wait16(r);
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    const int f0 = ti.nb * BN + 32 * c;
-    float dh[32], g[32], u[32];
-    tmem_ld32(tbase + 32 * c, dh);
-    load32(z1 + f0, g);
-    load32(z1 + p.F + f0, u);
+  for (int j = 0; j < STEPS; ++j) {
+    const bool more = j + 1 < STEPS;
+    const int f0 = ti.nb * BN + col0 + 16 * j;
+    if (more) {
+      ldraw16(z1 + f0 + 16, grn);
+      ldraw16(z1 + p.F + f0 + 16, urn);
+      tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
+    }
+    float g[16], u[16];
+    unpack8(gr[0], g);
+    unpack8(gr[1], g + 8);
+    unpack8(ur[0], u);
+    unpack8(ur[1], u + 8);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 16; ++i) {
+      const float dh = __uint_as_float(r[i]);
       const float sg = sigmoid_f(g[i]);
-      const float dgi = dh[i] * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
-      const float dui = dh[i] * g[i] * sg;
+      const float dgi = dh * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+      const float dui = dh * g[i] * sg;
       g[i] = dgi;
       u[i] = dui;
     }
-    store32(dz1 + f0, g);
-    store32(dz1 + p.F + f0, u);
+    store16(dz1 + f0, g);
+    store16(dz1 + p.F + f0, u);
+    if (more) {
+      tmem_wait16(rn);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = rn[i];
+      gr[0] = grn[0];
+      gr[1] = grn[1];
+      ur[0] = urn[0];
+      ur[1] = urn[1];
+    }
   }
 }
 
-// ds[e, n, b] (+)= sum_{kappa in b} dW[n, kappa] * phi(W[e, n, kappa], s[e, n, b]); for fp8
-// (one scale per row) the tile's partial row sum goes to part[(e * Mw + n) * n_ntiles + nb].
+// ds[e, n, b] (+)= sum_{kappa in b} dW[n, kappa] * phi(W[e, n, kappa], s[e, n, b]), 16
+// columns at a time.  nvfp4 blocks (16) and INT4 groups (128, when a column half holds a
+// whole group) are reduced here; otherwise (fp8's whole-row block, INT4 with 128-column
+// tiles) each column half writes its partial sum to
+// part[ds_index * parts + (tile in block) * 2 + half] and a reduction kernel adds the
+// parts in a fixed order.
 template <int BN, int FMT>
-__device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+__device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
+                                                  int half) {
+  constexpr int STEPS = BN / 32;  // 16-column steps per half
   const int64_t n = (int64_t)ti.mb * BM + row_in_tile;
   const int64_t wrow = (int64_t)ti.e * p.w_rows + n;
   const __nv_bfloat16* wr = p.w + wrow * p.w_cols;
-  const int64_t k0 = (int64_t)ti.nb * BN;
-  float row_sum = 0.0f, grp = 0.0f;
+  constexpr bool kDirectGroups = (FMT == kFmtInt4) && (BN == 256);
+  const bool have_acc = ti.nkb > 0;
+  const int col0 = half * (BN / 2);
+  float part_sum = 0.0f;
+  uint32_t r[16], rn[16];
+  uint4 wraw[2], wrawn[2];
+  ldraw16(wr + (int64_t)ti.nb * BN + col0, wraw);
+  if (have_acc) {
+    tmem_ld16_issue(tbase + col0, r);
+    tmem_wait16(r);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = 0u;
+  }
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    float acc[32], wv[32];
-    if (ti.nkb > 0) {
-      tmem_ld32(tbase + 32 * c, acc);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  for (int j = 0; j < STEPS; ++j) {
+    const bool more = j + 1 < STEPS;
+    const int64_t kc = (int64_t)ti.nb * BN + col0 + 16 * j;
+    if (more) {
+      ldraw16(wr + kc + 16, wrawn);
+      if (have_acc) tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
     }
-    const int64_t kc = k0 + 32 * c;
-    load32(wr + kc, wv);
+    float wv[16], x[16];
+    unpack8(wraw[0], wv);
+    unpack8(wraw[1], wv + 8);
+    float sc;
+    if constexpr (FMT == kFmtNvfp4) sc = __ldg(p.s + wrow * (p.w_cols / 16) + kc / 16);
+    else if constexpr (FMT == kFmtInt4) sc = __ldg(p.s + wrow * (p.w_cols / 128) + kc / 128);
+    else sc = __ldg(p.s + wrow);
+    quotients<16>(wv, sc, x);
+    float t = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 ph = lsq_pair<FMT>(x[i], x[i + 1]);
+      t = fmaf(__uint_as_float(r[i]), ph.x, t);
+      t = fmaf(__uint_as_float(r[i + 1]), ph.y, t);
+    }
     if constexpr (FMT == kFmtNvfp4) {
-      const int64_t sidx = wrow * (p.w_cols / 16) + kc / 16;
-      float sum[2];
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const float sc = __ldg(p.s + sidx + b);
-        float t = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const float2 ph = lsq_pair<FMT>(quotient(wv[16 * b + i], sc), quotient(wv[16 * b + i + 1], sc));
-          t = fmaf(acc[16 * b + i], ph.x, t);
-          t = fmaf(acc[16 * b + i + 1], ph.y, t);
-        }
-        sum[b] = t;
-      }
-      float* dst = p.ds + sidx;
-      if (p.accumulate) {
-        dst[0] += sum[0];
-        dst[1] += sum[1];
-      } else {
-        dst[0] = sum[0];
-        dst[1] = sum[1];
-      }
+      float* dst = p.ds + wrow * (p.w_cols / 16) + kc / 16;
+      *dst = p.accumulate ? *dst + t : t;
     } else {
-      const float sc = (FMT == kFmtInt4) ? __ldg(p.s + wrow * (p.w_cols / 128) + kc / 128) : __ldg(p.s + wrow);
-      float t = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float2 ph = lsq_pair<FMT>(quotient(wv[i], sc), quotient(wv[i + 1], sc));
-        t = fmaf(acc[i], ph.x, t);
-        t = fmaf(acc[i + 1], ph.y, t);
-      }
-      if constexpr (FMT == kFmtInt4) {
-        grp += t;
-        if ((c & 3) == 3) {
+      part_sum += t;
+      if constexpr (kDirectGroups) {
+        if ((j & 7) == 7) {
           float* dst = p.ds + wrow * (p.w_cols / 128) + kc / 128;
-          *dst = p.accumulate ? *dst + grp : grp;
-          grp = 0.0f;
+          *dst = p.accumulate ? *dst + part_sum : part_sum;
+          part_sum = 0.0f;
         }
-      } else {
-        row_sum += t;
       }
+    }
+    if (more) {
+      if (have_acc) {
+        tmem_wait16(rn);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = rn[i];
+      }
+      wraw[0] = wrawn[0];
+      wraw[1] = wrawn[1];
     }
   }
-  if constexpr (FMT == kFmtFp8) p.part[wrow * p.n_ntiles + ti.nb] = row_sum;
+  if constexpr (FMT != kFmtNvfp4 && !kDirectGroups) {
+    const int64_t B = (FMT == kFmtInt4) ? 128 : p.w_cols;  // elements per scale
+    const int tiles_per_block = (int)(B / BN);
+    const int64_t ds_index = wrow * (p.w_cols / B) + ((int64_t)ti.nb * BN) / B;
+    p.part[ds_index * (2 * tiles_per_block) + (ti.nb % tiles_per_block) * 2 + half] = part_sum;
+  }
 }
 
 template <int BN, int EPI>
-__device__ __forceinline__ void run_epilogue(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile) {
+__device__ __forceinline__ void run_epilogue(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
+                                             int half) {
   if constexpr (EPI == EPI_FC1) {
-    epi_fc1<BN>(p, ti, tbase, row_in_tile);
+    epi_fc1<BN>(p, ti, tbase, row_in_tile, half);
   } else if constexpr (EPI == EPI_STORE) {
-    epi_store<BN>(p, ti, tbase, row_in_tile);
+    epi_store<BN>(p, ti, tbase, row_in_tile, half);
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-    epi_swiglu_bwd<BN>(p, ti, tbase, row_in_tile);
+    epi_swiglu_bwd<BN>(p, ti, tbase, row_in_tile, half);
   } else {
-    if (p.fmt == kFmtNvfp4) epi_scalegrad_fmt<BN, kFmtNvfp4>(p, ti, tbase, row_in_tile);
-    else if (p.fmt == kFmtInt4) epi_scalegrad_fmt<BN, kFmtInt4>(p, ti, tbase, row_in_tile);
-    else epi_scalegrad_fmt<BN, kFmtFp8>(p, ti, tbase, row_in_tile);
+    if (p.fmt == kFmtNvfp4) epi_scalegrad_fmt<BN, kFmtNvfp4>(p, ti, tbase, row_in_tile, half);
+    else if (p.fmt == kFmtInt4) epi_scalegrad_fmt<BN, kFmtInt4>(p, ti, tbase, row_in_tile, half);
+    else epi_scalegrad_fmt<BN, kFmtFp8>(p, ti, tbase, row_in_tile, half);
   }
 }
 
@@ -406,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4 * 32);
+      mbar_init(tempty_bar(a), kEpiThreads);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -527,7 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(drain_bar, 0, &zero, &dummy);
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;            // TMEM lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns it handles
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -537,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      run_epilogue<BN, EPI>(p, ti, tbase, row_in_tile);
+      run_epilogue<BN, EPI>(p, ti, tbase, row_in_tile, half);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;
@@ -718,7 +810,10 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   cudaError_t e = bn == 256 ? launch<256, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st)
                             : launch<128, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st);
   if (e != cudaSuccess) return e;
-  if (c.fmt == kFmtFp8) return launch_scale_reduce(p.part, ds, L.E * m_w, p.n_ntiles, accumulate, c.st);
+  if (c.fmt == kFmtFp8 || (c.fmt == kFmtInt4 && bn == 128)) {
+    const int64_t B = c.fmt == kFmtInt4 ? 128 : k_w;  // elements per scale
+    return launch_scale_reduce(p.part, ds, L.E * m_w * (k_w / B), (int)(2 * (B / bn)), accumulate, c.st);
+  }
   return cudaSuccess;
 }
 }  // namespace

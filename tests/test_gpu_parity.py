@@ -290,3 +290,36 @@ def test_outputs_stay_inside_their_buffers():
     for t, n in ((big_out, T * d), (big_dx, T * d), (big_dp, T * k), (big13, n13), (big2, n2)):
         assert torch.all(t[:G] == 7.0) and torch.all(t[G + n:] == 7.0)
         assert torch.all(torch.isfinite(t[G:G + n].float()))
+
+
+# ------------------------------------------------------------------------------ the quotient
+
+def test_reciprocal_quotient_matches_cuda_division():
+    """The quantizers' x = w / s (correctly rounded reciprocal + one FMA correction) equals
+    CUDA's IEEE division bit for bit, on hard cases and 32M random pairs."""
+    g = torch.Generator(device="cuda").manual_seed(11)
+    n = 1 << 25
+    w = torch.randn(n, generator=g, device="cuda") * torch.exp2(torch.randint(-40, 12, (n,), generator=g,
+                                                                              device="cuda").float())
+    w = w.to(torch.bfloat16).float()
+    s = torch.rand(n, generator=g, device="cuda") * torch.exp2(torch.randint(-30, 4, (n,), generator=g,
+                                                                            device="cuda").float())
+    # hard cases: all-ones mantissas, powers of two, exact multiples, signed zeros, tiny/huge
+    ones = torch.tensor([1.9999999, 1.0, 1.5, 1.9999998], device="cuda")
+    m = 1 << 16
+    s[:m] = ones[torch.arange(m, device="cuda") % 4] * torch.exp2(torch.randint(-20, 4, (m,), generator=g,
+                                                                                device="cuda").float())
+    w[m:2 * m] = s[m:2 * m] * torch.randint(-8, 8, (m,), generator=g, device="cuda").float()
+    w[2 * m:2 * m + 8] = torch.tensor([0.0, -0.0, 3e38, -3e38, 1e-38, -1e-38, 6.0, -0.5], device="cuda")
+    s[2 * m:2 * m + 8] = torch.tensor([0.25, 0.25, 1e-3, 1e-3, 0.5, 2e-38, 1.0, 0.0], device="cuda")
+    s[2 * m + 8:2 * m + 12] = torch.tensor([1e-40, 3e-39, 0.0, 1e-45], device="cuda")   # subnormal / zero scales
+    fast = torch.empty_like(w)
+    ieee = torch.empty_like(w)
+    Q.qad_debug_quotient(w, s, fast, ieee, n)
+    torch.cuda.synchronize()
+    same = fast.view(torch.int32) == ieee.view(torch.int32)
+    assert bool(same.all()), "%d mismatches, e.g. w=%r s=%r" % (int((~same).sum()), w[~same][:3].tolist(),
+                                                                s[~same][:3].tolist())
+    nz = s != 0
+    torch_div = w[nz] / s[nz]
+    assert torch.equal(ieee[nz].view(torch.int32), torch_div.view(torch.int32))
