@@ -54,7 +54,8 @@ typedef enum {
   QAD_ERR_UNSUPPORTED = -2, /* shape outside the supported set (divisibility, limits) */
   QAD_ERR_WORKSPACE = -3,   /* workspace smaller than qad_moe_workspace_bytes() */
   QAD_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
-  QAD_ERR_DEVICE = -5       /* the device error word is non-zero (see QAD_DEV_*) */
+  QAD_ERR_DEVICE = -5,      /* the device error word is non-zero (see QAD_DEV_*) */
+  QAD_ERR_SCRATCH_LIMIT = -6 /* larger than the fixed scratch of qad_route_permute_noalloc */
 } qad_status;
 
 /* Weight formats (the pages' format names) */
@@ -190,6 +191,37 @@ int qad_profile_reset(void);
 int qad_profile_read(float* ms, int64_t* launches, int n);
 const char* qad_kernel_name(int id);
 int64_t qad_launch_count(void);
+
+/*
+ * Routing permutation that allocates nothing (the pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory, e.g. code running inside
+ * a CUDA-graph stream capture where cudaMalloc is not allowed, or a runtime that owns all
+ * device memory and gives a plugin only its inputs and outputs).
+ *
+ * Computes the same maps as the routing step of qad_moe_fwd: the T * topk (token, slot)
+ * pairs grouped by expert in (token, slot) order, each expert's rows padded to a
+ * multiple of 128; out-of-range or repeated indices are dropped and flagged.
+ *   topk_idx  int32 [T, topk]                        (read)
+ *   row_token int32 [Rmax], row_slot int32 [Rmax]     token / slot of each padded row, -1 = padding,
+ *             Rmax = round_up(T * topk + 127 * E, 128); only the first header[2] are written
+ *   row_of    int32 [T * topk]                        padded row of each pair, -1 if dropped
+ *   offsets   int32 [E + 1]                           first padded row of each expert
+ *   counts    int32 [E]                               routed rows per expert
+ *   header    int32 [4]                               device error word (QAD_DEV_*), 128-row
+ *                                                     tiles, padded rows, routed rows
+ * All pointers are device pointers; nothing is allocated.  The library's own scratch for
+ * this call is a file-scope device array of 534 KB per GPU (held until the process
+ * exits), sized for E <= QAD_NOALLOC_MAX_EXPERTS and T * topk <= QAD_NOALLOC_MAX_PAIRS;
+ * larger problems return QAD_ERR_SCRATCH_LIMIT before anything is launched.  The first
+ * call on a device looks up the scratch's device address (cudaGetSymbolAddress), so make
+ * that first call before any stream capture.  Every call shares the one scratch array:
+ * calls whose execution overlaps on the GPU (different streams, or different host threads)
+ * race and give undefined results; the header is cleared at the start of each call.
+ */
+enum { QAD_NOALLOC_MAX_EXPERTS = 256, QAD_NOALLOC_MAX_PAIRS = 262144 };
+int qad_route_permute_noalloc(const int32_t* topk_idx, int64_t T, int32_t topk, int32_t E,
+                              int32_t* row_token, int32_t* row_slot, int32_t* row_of, int32_t* offsets,
+                              int32_t* counts, int32_t* header, qad_stream_t stream);
 
 /*
  * Self-check of the division inside the quantizers (not an operation of the method).

@@ -14,6 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqad_gb300.so")
 
 QAD_OK, QAD_ERR_INVALID_ARG, QAD_ERR_UNSUPPORTED, QAD_ERR_WORKSPACE, QAD_ERR_CUDA, QAD_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+QAD_ERR_SCRATCH_LIMIT = -6
+QAD_NOALLOC_MAX_EXPERTS, QAD_NOALLOC_MAX_PAIRS = 256, 262144
 QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW = 0, 1, 2
 QAD_DEV_BAD_INDEX, QAD_DEV_DUP_INDEX, QAD_DEV_TIMEOUT = 1, 2, 4
 QAD_FLAG_STASH_H = 1
@@ -25,7 +27,7 @@ KERNELS = 14
 EXPORTS = ["qad_fakequant_fwd", "qad_moe_workspace_bytes", "qad_moe_fwd", "qad_moe_bwd_dgrad",
            "qad_moe_bwd_scalegrad", "qad_check_device_error", "qad_status_string", "qad_moe_debug_view",
            "qad_profile_enable", "qad_profile_reset", "qad_profile_read", "qad_kernel_name", "qad_launch_count",
-           "qad_debug_quotient"]
+           "qad_debug_quotient", "qad_route_permute_noalloc"]
 
 
 class QADError(RuntimeError):
@@ -72,6 +74,8 @@ def lib():
             "qad_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
             "qad_launch_count": (ctypes.c_int64, []),
             "qad_debug_quotient": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P]),
+            "qad_route_permute_noalloc": (ctypes.c_int, [_P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P,
+                                                         _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -178,6 +182,14 @@ def qad_launch_count():
 def qad_debug_quotient(w, s, x_fast, x_ieee, n, stream=None):
     return _check(lib().qad_debug_quotient(_ptr(w), _ptr(s), _ptr(x_fast), _ptr(x_ieee), int(n), _stream(stream)),
                   "qad_debug_quotient")
+
+
+def qad_route_permute_noalloc(topk_idx, T, topk, E, row_token, row_slot, row_of, offsets, counts, header,
+                              stream=None):
+    """Routing maps without any device allocation by the library (see include/qad.h)."""
+    return _check(lib().qad_route_permute_noalloc(_ptr(topk_idx), int(T), int(topk), int(E), _ptr(row_token),
+                                                  _ptr(row_slot), _ptr(row_of), _ptr(offsets), _ptr(counts),
+                                                  _ptr(header), _stream(stream)), "qad_route_permute_noalloc")
 
 
 def workspace_view(ws, s, which, dtype):

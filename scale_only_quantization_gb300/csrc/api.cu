@@ -165,6 +165,7 @@ const char* qad_status_string(int status) {
     case QAD_ERR_WORKSPACE: return "workspace smaller than qad_moe_workspace_bytes()";
     case QAD_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case QAD_ERR_DEVICE: return "device error word set (bad or repeated routing index, or a pipeline timeout)";
+    case QAD_ERR_SCRATCH_LIMIT: return "problem larger than the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }

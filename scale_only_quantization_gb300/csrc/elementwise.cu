@@ -392,6 +392,25 @@ cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaS
   return cudaGetLastError();
 }
 
+cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64_t nchunks, int32_t* hdr,
+                              int32_t* chunk_counts, int32_t* chunk_base, int32_t* counts, int32_t* offs,
+                              int32_t* mtile_expert, int32_t* row_token, int32_t* row_slot, int32_t* row_of,
+                              cudaStream_t st) {
+  prof_begin(QAD_K_ROUTE, st);
+  if (nchunks > 0) {
+    route_hist_kernel<<<(unsigned)nchunks, 256, E * sizeof(int32_t), st>>>(idx, R, k, E, chunk_counts, hdr);
+  }
+  route_scan_kernel<<<1, 1024, 0, st>>>(nchunks, E, chunk_counts, chunk_base, counts, offs, mtile_expert, row_token,
+                                        row_slot, hdr);
+  if (nchunks > 0) {
+    route_scatter_kernel<<<(unsigned)nchunks, 32, E * sizeof(int32_t), st>>>(idx, R, k, E, chunk_base, row_token,
+                                                                            row_slot, row_of);
+  }
+  prof_end(QAD_K_ROUTE, st);
+  if (nchunks > 0) note_launches(2);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_act_quant_rows(int fmt, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;

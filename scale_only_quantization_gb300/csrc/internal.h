@@ -36,6 +36,12 @@ int num_sms();
 cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, int64_t rows, int64_t K,
                              cudaStream_t st);
 cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st);
+// the same three routing kernels on explicit buffers (hdr: int32[64], zeroed by the caller;
+// chunk_counts / chunk_base: int32[nchunks * E]; mtile_expert: int32[Rmax / 128])
+cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64_t nchunks, int32_t* hdr,
+                              int32_t* chunk_counts, int32_t* chunk_base, int32_t* counts, int32_t* offs,
+                              int32_t* mtile_expert, int32_t* row_token, int32_t* row_slot, int32_t* row_of,
+                              cudaStream_t st);
 // out[r, :] = AQ(in[r, :]) for r < rows (or < *dev_rows when dev_rows != nullptr)
 cudaError_t launch_act_quant_rows(int fmt, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st);
