@@ -124,19 +124,24 @@ def algorithmic_per_launch(cfg):
 
 
 def _traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if its source hash still matches."""
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.txt), or None
+    when the kernel's sources have changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     import hashlib
     for ln in open(path):
         f = ln.split()
-        if len(f) >= 4 and not ln.startswith("#") and f[0] == kernel and f[1] == workload:
-            src = os.path.join(ROOT, "scale_only_quantization_gb300", "csrc", f[3].split(":")[0])
+        if len(f) < 4 or ln.startswith("#") or f[0] != kernel or f[1] != workload:
+            continue
+        files, want = f[3].split(":")
+        h = hashlib.sha256()
+        for name in files.split("+"):
+            src = os.path.join(ROOT, "scale_only_quantization_gb300", "csrc", name)
             if not os.path.exists(src):
                 return None
-            h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-            return float(f[2]) if h == f[3].split(":")[1] else None
+            h.update(open(src, "rb").read())
+        return float(f[2]) if h.hexdigest()[:16] == want else None
     return None
 
 
