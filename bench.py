@@ -148,6 +148,7 @@ def _traffic(kernel, workload):
 def run_ours(args):
     import scale_only_quantization_gb300 as Q
     from scale_only_quantization_gb300 import build as B
+    from scale_only_quantization_gb300 import dp
     world, rank, local = _dist()
     if world > 1:
         import torch.distributed as dist
@@ -178,11 +179,7 @@ def run_ours(args):
         Q.qad_moe_bwd_dgrad(s, dout, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], dx, dprobs, ws, stream)
         Q.qad_moe_bwd_scalegrad(s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], ds13, ds2, 0, ws, stream)
         if world > 1:
-            import torch.distributed as dist
-            dist.all_reduce(ds13)
-            dist.all_reduce(ds2)
-            ds13.div_(world)
-            ds2.div_(world)
+            dp.average_scale_grads([ds13, ds2])
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -215,11 +212,7 @@ def run_ours(args):
     ms = e0.elapsed_time(e1) / args.steps
     prof = Q.qad_profile_read()
     Q.qad_profile_enable(False)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = dp.max_over_ranks(ms, device=dev)
 
     # ---- end to end through the public API with pinned host buffers
     host_in = [a.cpu().pin_memory() for a in args_dev]
@@ -244,11 +237,7 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     ms_e2e = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = dp.max_over_ranks(ms_e2e, device=dev)
 
     # ---- roofline of the dominant kernel (largest share of the timed region)
     hbm, tf_burst, tf_sust, peak_src = _peaks()
