@@ -113,7 +113,7 @@ size_t qad_moe_workspace_bytes(const qad_moe_shape* s);
  *   out      bf16 [T, d] (written)
  *   ws       workspace (256-byte aligned) of ws_bytes >= qad_moe_workspace_bytes(s); it keeps what the
  *            backward calls need (routing maps, fake-quantized weights, activations).
- * Supported: d % 128 == 0, F % 128 == 0, 1 <= topk <= min(E, 32), 1 <= E <= 1024,
+ * Supported: d % 256 == 0, F % 128 == 0, 1 <= topk <= min(E, 32), 1 <= E <= 1024,
  * T * topk < 2^31.  The error word is cleared at the start of this call.
  */
 int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, const float* topk_w,

@@ -91,7 +91,7 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
   if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_FP8_ROW) return QAD_ERR_INVALID_ARG;
   if (s.reserved != 0 || (s.flags & ~QAD_FLAG_STASH_H)) return QAD_ERR_INVALID_ARG;
-  if (s.d % 128 || s.F % 128) return QAD_ERR_UNSUPPORTED;
+  if (s.d % 256 || s.F % 128) return QAD_ERR_UNSUPPORTED;
   if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
   const int64_t R = s.T * (int64_t)s.topk;
   const int64_t Rmax = (R + (int64_t)(kTileRows - 1) * s.E + kTileRows - 1) / kTileRows * kTileRows;
@@ -108,6 +108,8 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->chunk_counts = take(4 * (size_t)(L->nchunks * E));
   L->chunk_base = take(4 * (size_t)(L->nchunks * E));
   L->mtile_expert = take(4 * (size_t)(Rmax / kTileRows));
+  L->ptile_row0 = take(4 * (size_t)(Rmax / kTileRows));
+  L->ptile_expert = take(4 * (size_t)(Rmax / kTileRows));
   L->row_token = take(4 * (size_t)Rmax);
   L->row_slot = take(4 * (size_t)Rmax);
   L->row_of = take(4 * (size_t)R);
@@ -161,7 +163,7 @@ const char* qad_status_string(int status) {
   switch (status) {
     case QAD_OK: return "ok";
     case QAD_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size or flag)";
-    case QAD_ERR_UNSUPPORTED: return "unsupported shape (needs d % 128 == 0, F % 128 == 0, topk <= min(E, 32), E <= 1024)";
+    case QAD_ERR_UNSUPPORTED: return "unsupported shape (needs d % 256 == 0, F % 128 == 0, topk <= min(E, 32), E <= 1024)";
     case QAD_ERR_WORKSPACE: return "workspace smaller than qad_moe_workspace_bytes()";
     case QAD_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case QAD_ERR_DEVICE: return "device error word set (bad or repeated routing index, or a pipeline timeout)";
@@ -211,6 +213,7 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
     QAD_TRY(launch_gather_rows(wsb + L.xq, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
   }
   GemmCtx c = {&L, wsb, fmt, s->flags, st};
+  QAD_TRY(gemm_prepare(c));
   QAD_TRY(gemm_fc1(c));
   if (fmt == QAD_FMT_FP8_ROW) QAD_TRY(launch_act_quant_rows(fmt, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
   QAD_TRY(gemm_fc2(c));

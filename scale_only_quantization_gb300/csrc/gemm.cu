@@ -11,16 +11,28 @@
 //   wgrad  dW2 = dY_e^T . H_hat_e    epilogue: x LSQ factor, per-block sums -> ds2 (dW never stored)
 //   wgrad  dW13 = dZ1_e^T . A1_e     epilogue: same -> ds13
 //
-// Rows of each expert are padded to a multiple of 128 (zero rows), so a 128-row tile never
-// straddles two experts and a wgrad contraction runs over whole 64-row blocks.
+// Rows of each expert are padded to a multiple of 128 (zero rows), so a 128-row half tile
+// never straddles two experts and a wgrad contraction runs over whole 64-row blocks.
 //
-// Per CTA (one per SM, persistent over tiles): warp 0 issues TMA loads (128B-swizzled
-// tiles) into a STAGES-deep ring guarded by mbarriers; warp 1 owns the tensor memory and
-// issues tcgen05.mma (M=128, N=BN, K=16, bf16 x bf16 -> fp32) from one thread; warps 2-9
-// read the accumulator (two TMEM buffers, so the next tile's MMAs overlap this epilogue)
-// with tcgen05.ld and run the fused epilogue: a warp may only read the 32 TMEM lanes of
-// its quadrant (warp id mod 4), so each quadrant has two warps, one per column half.
-// Every wait is bounded: on expiry the CTA
+// The MMAs run on SM pairs (a cluster of two CTAs, tcgen05 cta_group::2): one
+// 256 x BN x 16 MMA issued by the pair's leader reads the 256 rows of A from the two CTAs'
+// shared memory (128 each) and the BN columns of B from both (BN/2 each), and writes each
+// CTA's 128 rows of the accumulator into that CTA's tensor memory.  Each SM therefore
+// loads only half of the B tile: a third fewer operand bytes per FLOP than a one-SM
+// 128 x BN tile, which matters because these GEMMs are limited by L2-to-SM bandwidth.
+// A row-mode pair tile is two consecutive 128-row blocks of one expert; when an expert
+// has an odd number of blocks the second CTA's half of its last tile is dead (computed,
+// not stored).
+//
+// Per CTA (persistent over the pair's tiles): warp 0 issues TMA loads (128B-swizzled
+// tiles) into a STAGES-deep ring; the pair's TMA bytes complete on the leader's "full"
+// barrier; warp 1 of each CTA owns the pair's tensor memory allocation and, in the
+// leader, one thread issues the MMAs and commits to both CTAs' "empty" (ring slot free)
+// and "full accumulator" barriers at once (multicast); warps 2-9 read their CTA's
+// accumulator (two TMEM buffers, so the next tile's MMAs overlap this epilogue) with
+// tcgen05.ld and run the fused epilogue, then arrive on the leader's "empty accumulator"
+// barrier.  A warp may only read the 32 TMEM lanes of its quadrant (warp id mod 4), so
+// each quadrant has two warps, one per column half.  Every wait is bounded: on expiry the CTA
 // raises QAD_DEV_TIMEOUT in the workspace error word, drains what it issued and exits.
 #include <cuda.h>
 
@@ -39,13 +51,14 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 enum { EPI_FC1 = 0, EPI_STORE = 1, EPI_SWIGLU_BWD = 2, EPI_SCALEGRAD = 3 };
 
 struct Params {
-  int32_t* hdr;                 // workspace header ([HDR_ERR], [HDR_NMTILES])
-  const int32_t* mtile_expert;  // expert of each 128-row tile
+  int32_t* hdr;                 // workspace header ([HDR_ERR], [HDR_NPTILES])
+  const int32_t* ptile_row0;    // first row of each row-mode pair tile
+  const int32_t* ptile_expert;  // expert of each row-mode pair tile
   const int32_t* poff;          // padded expert offsets [E + 1]
   int E;
   int wgrad;                    // 0: output rows grouped by expert; 1: contraction over an expert's rows
   int n_ntiles;                 // tiles along the GEMM's N
-  int n_mtiles_w;               // wgrad: tiles along the GEMM's M (weight rows / 128)
+  int n_mtiles_w;               // wgrad: pair tiles along the GEMM's M (weight rows / 256)
   int num_kb;                   // rows mode: K / 64
   int b_rows;                   // rows of the B tensor map per expert
   int F;                        // expert FFN width (fc1 / SwiGLU epilogues)
@@ -60,10 +73,11 @@ struct Params {
 };
 
 template <int BN> struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr int RING = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int A_BYTES = BM * BK * 2;        // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's half of B
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (192 * 1024) / STAGE;  // 6 (BN = 256) or 8 (BN = 128)
+  static constexpr int RING = STAGES * STAGE;
   static constexpr int SMEM = RING + 256 + 1024;  // + barriers, + alignment slack
   static constexpr int TMEM_COLS = 2 * BN;
 };
@@ -77,9 +91,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -106,12 +117,41 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
+// TMA tile load into this CTA's shared memory; the bytes complete on `bar`, a shared::cluster
+// address that may be the pair leader's barrier (cta_group::2).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
@@ -134,23 +174,27 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12
 // = 1), A/B major in bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 in [17,23),
-// M >> 4 in [24,29).
+// M >> 4 in [24,29); M = 256 for the pair.
 template <int N, bool A_MN, bool B_MN>
 __host__ __device__ constexpr uint32_t instr_desc() {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// arrive on the barrier at offset `bar` in every CTA of `mask` once the MMAs issued so far are done
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
 }
 
 // tcgen05.ld is asynchronous until tcgen05.wait::ld: the loads of the next chunk are issued
@@ -199,13 +243,15 @@ __device__ __forceinline__ void store16(__nv_bfloat16* dst, const float* v) {
 
 struct Tile {
   int e, mb, nb, nkb, r0;
+  int64_t row_base;  // first output row of this CTA's 128-row half (rows mode) / weight row (wgrad)
+  bool live;         // false for the dead second half of an expert's odd last block
 };
 
 __device__ __forceinline__ int tile_count(const Params& p) {
-  return p.wgrad ? p.E * p.n_mtiles_w * p.n_ntiles : p.hdr[HDR_NMTILES] * p.n_ntiles;
+  return p.wgrad ? p.E * p.n_mtiles_w * p.n_ntiles : p.hdr[HDR_NPTILES] * p.n_ntiles;
 }
 
-__device__ __forceinline__ Tile tile_of(const Params& p, int t) {
+__device__ __forceinline__ Tile tile_of(const Params& p, int t, uint32_t rank) {
   Tile ti;
   if (p.wgrad) {
     const int per_e = p.n_mtiles_w * p.n_ntiles;
@@ -215,12 +261,17 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
     ti.nb = rem - ti.mb * p.n_ntiles;
     ti.r0 = __ldg(p.poff + ti.e);
     ti.nkb = (__ldg(p.poff + ti.e + 1) - ti.r0) / BK;
+    ti.row_base = (int64_t)ti.mb * (2 * BM) + (int64_t)rank * BM;
+    ti.live = true;
   } else {
-    ti.mb = t / p.n_ntiles;
-    ti.nb = t - ti.mb * p.n_ntiles;
-    ti.e = __ldg(p.mtile_expert + ti.mb);
-    ti.r0 = ti.mb * BM;
+    const int pt = t / p.n_ntiles;
+    ti.mb = pt;
+    ti.nb = t - pt * p.n_ntiles;
+    ti.e = __ldg(p.ptile_expert + pt);
+    ti.r0 = __ldg(p.ptile_row0 + pt) + (int)rank * BM;
     ti.nkb = p.num_kb;
+    ti.row_base = ti.r0;
+    ti.live = ti.r0 < __ldg(p.poff + ti.e + 1);
   }
   return ti;
 }
@@ -233,7 +284,7 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
 // separate pass quantizes it.
 template <int BN>
 __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
-  const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
+  const int64_t row = ti.row_base + row_in_tile;
   __nv_bfloat16* z1 = p.out + row * p.ld_out;
   __nv_bfloat16* hrow = p.out3 + row * p.ld_out2;
   __nv_bfloat16* hhrow = p.out2 + row * p.ld_out2;
@@ -293,7 +344,7 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_
 
 template <int BN>
 __device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
-  const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
+  const int64_t row = ti.row_base + row_in_tile;
   __nv_bfloat16* dst = p.out + row * p.ld_out + (int64_t)ti.nb * BN;
   constexpr int NH = BN / 64;
   uint32_t r[32], rn[32];
@@ -320,7 +371,7 @@ __device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint3
 template <int BN>
 __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                                int half) {
-  const int64_t row = (int64_t)ti.mb * BM + row_in_tile;
+  const int64_t row = ti.row_base + row_in_tile;
   const __nv_bfloat16* z1 = p.aux + row * p.ld_aux;
   __nv_bfloat16* dz1 = p.out + row * p.ld_out;
   constexpr int STEPS = BN / 32;  // 16-column steps per half
@@ -378,7 +429,7 @@ template <int BN, int FMT>
 __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                                   int half) {
   constexpr int STEPS = BN / 32;  // 16-column steps per half
-  const int64_t n = (int64_t)ti.mb * BM + row_in_tile;
+  const int64_t n = ti.row_base + row_in_tile;
   const int64_t wrow = (int64_t)ti.e * p.w_rows + n;
   const __nv_bfloat16* wr = p.w + wrow * p.w_cols;
   constexpr bool kDirectGroups = (FMT == kFmtInt4) && (BN == 256);
@@ -468,7 +519,7 @@ __device__ __forceinline__ void run_epilogue(const Params& p, const Tile& ti, ui
 // ---------------------------------------------------------------------------------- kernel
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const Params p) {
   using C = Cfg<BN>;
@@ -490,6 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* err = p.hdr + HDR_ERR;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0 = the pair's leader, which issues the MMAs
+  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
@@ -497,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiThreads);
+      mbar_init(tempty_bar(a), 2 * (kEpiThreads / 32));  // one arrival per epilogue warp of either CTA
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -505,58 +558,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"((uint32_t)C::TMEM_COLS)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = tile_count(p);
+  const int first = (int)cluster_id(), step = (int)cluster_count();
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;  // stages with a load in flight, and its phase parity
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      const Tile ti = tile_of(p, t);
+    for (int t = first; ok && t < total; t += step) {
+      const Tile ti = tile_of(p, t, rank);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, err)) {
           ok = false;
           break;
         }
-        const uint32_t fb = full_bar(stage);
-        mbar_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+        if (leader) mbar_expect_tx(full_bar(stage), 2 * C::STAGE);  // both CTAs' bytes
+        const uint32_t fb = peer_addr(full_bar(stage), 0);          // the leader's barrier
         const uint32_t sa = a_ring + stage * C::A_BYTES;
         const uint32_t sb = b_ring + stage * C::B_BYTES;
+        const int half_n = (int)rank * (BN / 2);
         if (!p.wgrad) {
           tma_load_2d(sa, &tmA, kb * BK, ti.r0, fb);
           if constexpr (!B_MN) {
             if constexpr (EPI == EPI_FC1) {
-              tma_load_2d(sb, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * 128, fb);
-              tma_load_2d(sb + 128 * 128, &tmB, kb * BK, ti.e * p.b_rows + p.F + ti.nb * 128, fb);
+              // leader: the 128 gate rows of the tile, peer: the matching 128 up rows
+              tma_load_2d(sb, &tmB, kb * BK, ti.e * p.b_rows + (int)rank * p.F + ti.nb * 128, fb);
             } else {
-#pragma unroll
-              for (int i = 0; i < BN / 128; ++i)
-                tma_load_2d(sb + i * 128 * 128, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * BN + i * 128, fb);
+              tma_load_2d(sb, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * BN + half_n, fb);
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + i * 64, ti.e * p.b_rows + kb * BK, fb);
+            for (int i = 0; i < BN / 128; ++i)
+              tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, ti.e * p.b_rows + kb * BK, fb);
           }
         } else {
           const int y = ti.r0 + kb * BK;
 #pragma unroll
-          for (int i = 0; i < 2; ++i) tma_load_2d(sa + i * 64 * 128, &tmA, ti.mb * BM + i * 64, y, fb);
+          for (int i = 0; i < 2; ++i)
+            tma_load_2d(sa + i * 64 * 128, &tmA, ti.mb * 2 * BM + (int)rank * BM + i * 64, y, fb);
 #pragma unroll
-          for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + i * 64, y, fb);
+          for (int i = 0; i < BN / 128; ++i) tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, y, fb);
         }
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -566,8 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (*abort_flag) {
-      // let every load this thread issued land before the CTA releases its shared memory
+    if (*abort_flag && leader) {
+      // let every load of the pair land before the CTA releases its shared memory
       int32_t dummy = 0;
       for (int s = 0; s < STAGES; ++s)
         if (armed & (1u << s)) {
@@ -575,14 +630,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(full_bar(s), (armed_parity >> s) & 1u, &zero, &dummy);
         }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------------ MMA issuer (leader)
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     int acc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      const Tile ti = tile_of(p, t);
+    for (int t = first; ok && t < total; t += step) {
+      const Tile ti = tile_of(p, t, rank);
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, err)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -600,48 +655,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = B_MN ? smem_desc(sb + k * 2048, 64 * 128, 1024) : smem_desc(sb + k * 32, 16, 1024);
           mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
-        mma_commit(empty_bar(stage));
+        mma_commit(empty_bar(stage), 3);  // frees the slot in both CTAs
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      mma_commit(tfull_bar(acc));
+      mma_commit(tfull_bar(acc), 3);  // both CTAs' accumulators are ready
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    // every MMA this thread issued has finished before TMEM and shared memory are released
-    mma_commit(drain_bar);
+    // every MMA issued has finished before tensor memory and shared memory are released
+    mma_commit(drain_bar, 1);
     volatile int zero = 0;
     int32_t dummy = 0;
     mbar_wait(drain_bar, 0, &zero, &dummy);
   } else if (warp >= 2) {
-    // ------------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // which half of the tile's columns it handles
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile ti = tile_of(p, t);
+    for (int t = first; t < total; t += step) {
+      const Tile ti = tile_of(p, t, rank);
       const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      run_epilogue<BN, EPI>(p, ti, tbase, row_in_tile, half);
+      if (ti.live) run_epilogue<BN, EPI>(p, ti, tbase, row_in_tile, half);
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(peer_addr(tempty_bar(acc), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
 
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers or read its TMEM
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)C::TMEM_COLS)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)C::TMEM_COLS)
                  : "memory");
   }
 }
@@ -684,12 +741,67 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p
   auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
   if (e != cudaSuccess) return e;
-  int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
-  if (grid < 1) return cudaSuccess;
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!max_pairs[dev]) {
+    // SM pairs that can hold one CTA each at the same time (persistent grid)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    max_pairs[dev] = n;
+  }
+  int64_t pairs = max_tiles < max_pairs[dev] ? max_tiles : max_pairs[dev];
+  if (pairs < 1) return cudaSuccess;
   prof_begin(kid, st);
-  kern<<<(unsigned)grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, p);
+  kern<<<(unsigned)(2 * pairs), kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, p);
   prof_end(kid, st);
   return cudaGetLastError();
+}
+
+// Row-mode pair tiles: expert e with m_e padded 128-row blocks gets ceil(m_e / 2) tiles of two
+// consecutive blocks starting at row offs[e] + 256 i.  One block of 1024 threads, one
+// expert per thread (E <= 1024), exclusive scan of the tile counts.
+__global__ void __launch_bounds__(1024) pair_tiles_kernel(const int32_t* __restrict__ offs, int E,
+                                                          int32_t* __restrict__ row0, int32_t* __restrict__ expert,
+                                                          int32_t* hdr) {
+  __shared__ int32_t warp_tot[32];
+  const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+  const int32_t start = e < E ? offs[e] : 0;
+  const int32_t blocks = e < E ? (offs[e + 1] - start) / BM : 0;
+  const int32_t n = (blocks + 1) / 2;
+  int32_t v = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t x = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += x;
+  }
+  if (lane == 31) warp_tot[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int32_t t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t x = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += x;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int32_t incl = v + (w > 0 ? warp_tot[w - 1] : 0);
+  const int32_t excl = incl - n;
+  for (int32_t i = 0; i < n; ++i) {
+    row0[excl + i] = start + 2 * BM * i;
+    expert[excl + i] = e;
+  }
+  if (e == E - 1) hdr[HDR_NPTILES] = incl;
 }
 
 template <typename T>
@@ -701,7 +813,8 @@ Params base_params(const GemmCtx& c) {
   const Layout& L = *c.L;
   Params p = {};
   p.hdr = at<int32_t>(c.ws, L.header);
-  p.mtile_expert = at<int32_t>(c.ws, L.mtile_expert);
+  p.ptile_row0 = at<int32_t>(c.ws, L.ptile_row0);
+  p.ptile_expert = at<int32_t>(c.ws, L.ptile_expert);
   p.poff = at<int32_t>(c.ws, L.offs);
   p.E = (int)L.E;
   p.F = (int)L.F;
@@ -713,6 +826,14 @@ Params base_params(const GemmCtx& c) {
 inline int pick_bn(int64_t n) { return n % 256 == 0 ? 256 : 128; }
 
 }  // namespace
+
+cudaError_t gemm_prepare(const GemmCtx& c) {
+  const Layout& L = *c.L;
+  pair_tiles_kernel<<<1, 1024, 0, c.st>>>(at<int32_t>(c.ws, L.offs), (int)L.E, at<int32_t>(c.ws, L.ptile_row0),
+                                          at<int32_t>(c.ws, L.ptile_expert), at<int32_t>(c.ws, L.header));
+  note_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t gemm_fc1(const GemmCtx& c) {
   const Layout& L = *c.L;
@@ -728,7 +849,7 @@ cudaError_t gemm_fc1(const GemmCtx& c) {
   p.out2 = at<__nv_bfloat16>(c.ws, L.hh);
   p.ld_out2 = L.F;
   p.out3 = at<__nv_bfloat16>(c.ws, L.h);
-  return launch<256, false, false, EPI_FC1>(ta, tb, p, (L.Rmax / BM) * p.n_ntiles, QAD_K_GEMM_FC1, c.st);
+  return launch<256, false, false, EPI_FC1>(ta, tb, p, (L.Rmax / BM) * (int64_t)p.n_ntiles, QAD_K_GEMM_FC1, c.st);
 }
 
 cudaError_t gemm_fc2(const GemmCtx& c) {
@@ -736,14 +857,14 @@ cudaError_t gemm_fc2(const GemmCtx& c) {
   Params p = base_params(c);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.hh, L.F, L.Rmax, L.F, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tb, c.ws + L.w2h, L.F, L.E * L.d, L.F, 128)) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.d);
+  if (!make_tmap(&tb, c.ws + L.w2h, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
   p.n_ntiles = (int)(L.d / bn);
   p.num_kb = (int)(L.F / BK);
   p.b_rows = (int)L.d;
   p.out = at<__nv_bfloat16>(c.ws, L.y);
   p.ld_out = L.d;
-  const int64_t tiles = (L.Rmax / BM) * p.n_ntiles;
+  const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
   return bn == 256 ? launch<256, false, false, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_FC2, c.st)
                    : launch<128, false, false, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_FC2, c.st);
 }
@@ -763,7 +884,7 @@ cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
   p.ld_out = 2 * L.F;
   p.aux = at<__nv_bfloat16>(c.ws, L.z1);
   p.ld_aux = 2 * L.F;
-  const int64_t tiles = (L.Rmax / BM) * p.n_ntiles;
+  const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
   return bn == 256 ? launch<256, false, true, EPI_SWIGLU_BWD>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st)
                    : launch<128, false, true, EPI_SWIGLU_BWD>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st);
 }
@@ -781,7 +902,7 @@ cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
   p.b_rows = (int)(2 * L.F);
   p.out = at<__nv_bfloat16>(c.ws, L.da1);
   p.ld_out = L.d;
-  const int64_t tiles = (L.Rmax / BM) * p.n_ntiles;
+  const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
   return bn == 256 ? launch<256, false, true, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st)
                    : launch<128, false, true, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st);
 }
@@ -797,7 +918,7 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   if (!make_tmap(&tb, c.ws + b_off, k_w, L.Rmax, k_w, 64)) return cudaErrorInvalidValue;
   const int bn = pick_bn(k_w);
   p.wgrad = 1;
-  p.n_mtiles_w = (int)(m_w / BM);
+  p.n_mtiles_w = (int)(m_w / (2 * BM));
   p.n_ntiles = (int)(k_w / bn);
   p.w = static_cast<const __nv_bfloat16*>(w);
   p.s = s;

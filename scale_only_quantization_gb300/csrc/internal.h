@@ -15,13 +15,14 @@ constexpr int kRouteChunk = 1024;  // (token, slot) pairs per routing chunk
 // Byte offsets of the workspace regions (each 1024-byte aligned).
 struct Layout {
   int64_t T, d, F, E, k, R, Rmax, nchunks;
-  size_t header, counts, offs, chunk_counts, chunk_base, mtile_expert, row_token, row_slot, row_of;
+  size_t header, counts, offs, chunk_counts, chunk_base, mtile_expert, ptile_row0, ptile_expert, row_token,
+      row_slot, row_of;
   size_t xq, w13h, w2h, a1, z1, h, hh, y, dy, dz1, da1, part13, part2;
   size_t total;
 };
 
 // Header words (int32) at the start of the workspace
-enum { HDR_ERR = 0, HDR_NMTILES = 1, HDR_RPAD = 2, HDR_NVALID = 3 };
+enum { HDR_ERR = 0, HDR_NMTILES = 1, HDR_RPAD = 2, HDR_NVALID = 3, HDR_NPTILES = 4 };
 
 // Returns a negative qad_status for an unsupported or invalid shape.
 int layout_of(const qad_moe_shape& s, Layout* L);
@@ -70,6 +71,7 @@ struct GemmCtx {
   int fmt, flags;
   cudaStream_t st;
 };
+cudaError_t gemm_prepare(const GemmCtx& c);     // pair-tile table of the row-mode GEMMs (after routing)
 cudaError_t gemm_fc1(const GemmCtx& c);         // Z1, H, H_hat  <- A1 . W13_hat^T (+ SwiGLU, AQ)
 cudaError_t gemm_fc2(const GemmCtx& c);         // Y <- H_hat . W2_hat^T
 cudaError_t gemm_dgrad_fc2(const GemmCtx& c);   // dZ1 <- SwiGLU'(dY . W2_hat)

@@ -52,6 +52,7 @@ def test_workspace_size_and_views(lib):
 
 @pytest.mark.parametrize("bad, status", [
     (dict(d=200), Q.QAD_ERR_UNSUPPORTED),
+    (dict(d=384), Q.QAD_ERR_UNSUPPORTED),
     (dict(F=96), Q.QAD_ERR_UNSUPPORTED),
     (dict(topk=5, E=4), Q.QAD_ERR_UNSUPPORTED),
     (dict(E=2000), Q.QAD_ERR_UNSUPPORTED),
