@@ -227,11 +227,16 @@ int qad_route_permute_noalloc(const int32_t* topk_idx, int64_t T, int32_t topk, 
  * Self-check of the division inside the quantizers (not an operation of the method).
  * The kernels compute x = fp32(w / s) from the correctly rounded reciprocal of s and one
  * FMA correction (Markstein's theorem) instead of a division per element.  For each i
- * this writes x_fast[i] (that computation) and x_ieee[i] (CUDA's IEEE division); the two
- * must agree bit for bit.  w, s, x_fast, x_ieee: fp32 [n], device pointers.
+ * this writes x_ieee[i] (CUDA's IEEE division) and x_fast[i]:
+ *   mode 0: the per-element guarded form used for weights -- must equal x_ieee bit for bit;
+ *   mode 1: the form used for activations and the scale-gradient factor, which checks only
+ *           the block's scale (in [2^-60, 2^60], else mode 0's form) -- must equal x_ieee
+ *           bit for bit wherever 2^-11 <= |x| <= 2^100, and round to zero on every grid
+ *           below (its callers never produce larger quotients: see the kernels).
+ * w, s, x_fast, x_ieee: fp32 [n], device pointers.
  */
 int qad_debug_quotient(const float* w, const float* s, float* x_fast, float* x_ieee, int64_t n,
-                       qad_stream_t stream);
+                       int32_t mode, qad_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -73,7 +73,7 @@ def lib():
                                                 ctypes.c_int]),
             "qad_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
             "qad_launch_count": (ctypes.c_int64, []),
-            "qad_debug_quotient": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P]),
+            "qad_debug_quotient": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int32, _P]),
             "qad_route_permute_noalloc": (ctypes.c_int, [_P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P,
                                                          _P, _P, _P]),
         }
@@ -179,9 +179,9 @@ def qad_launch_count():
     return int(lib().qad_launch_count())
 
 
-def qad_debug_quotient(w, s, x_fast, x_ieee, n, stream=None):
-    return _check(lib().qad_debug_quotient(_ptr(w), _ptr(s), _ptr(x_fast), _ptr(x_ieee), int(n), _stream(stream)),
-                  "qad_debug_quotient")
+def qad_debug_quotient(w, s, x_fast, x_ieee, n, mode=0, stream=None):
+    return _check(lib().qad_debug_quotient(_ptr(w), _ptr(s), _ptr(x_fast), _ptr(x_ieee), int(n), int(mode),
+                                           _stream(stream)), "qad_debug_quotient")
 
 
 def qad_route_permute_noalloc(topk_idx, T, topk, E, row_token, row_slot, row_of, offsets, counts, header,

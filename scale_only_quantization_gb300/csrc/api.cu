@@ -353,11 +353,12 @@ const char* qad_kernel_name(int id) {
 
 int64_t qad_launch_count(void) { return g_launch_total.load(); }
 
-int qad_debug_quotient(const float* w, const float* s, float* x_fast, float* x_ieee, int64_t n, qad_stream_t stream) {
-  if (n < 0) return QAD_ERR_INVALID_ARG;
+int qad_debug_quotient(const float* w, const float* s, float* x_fast, float* x_ieee, int64_t n, int32_t mode,
+                       qad_stream_t stream) {
+  if (n < 0 || mode < 0 || mode > 1) return QAD_ERR_INVALID_ARG;
   if (n == 0) return QAD_OK;
   if (!w || !s || !x_fast || !x_ieee) return QAD_ERR_INVALID_ARG;
-  return to_status(launch_quotient_check(w, s, x_fast, x_ieee, n, reinterpret_cast<cudaStream_t>(stream)));
+  return to_status(launch_quotient_check(w, s, x_fast, x_ieee, n, mode, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

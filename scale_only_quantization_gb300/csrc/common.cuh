@@ -123,6 +123,47 @@ __device__ __forceinline__ void quotients(const float* w, float s, float* x) {
   }
 }
 
+// Quotients for a block whose scale lies in [2^-60, 2^60] (the caller checks, and falls back
+// to quotients<N> otherwise), without per-element guards.  Exactness is only needed where x
+// can change a quantization decision: every grid's smallest decision point is >= 2^-10, and
+// for |x| >= 2^-11 with such a scale, w, q and the remainder (a multiple of
+// ulp(s) ulp(q) >= 2^-117) are normal, so Markstein's theorem gives the correctly rounded
+// quotient; smaller |x| may be off by a subnormal quantum but rounds to zero on every grid
+// either way.  The caller must also rule out an overflowing quotient (finite activations
+// with s = amax / Qmax never overflow; the LSQ reduction checks its block sum).
+template <int N>
+__device__ __forceinline__ void quotients_unguarded(const float* w, float s, float* x) {
+  const float r = __frcp_rn(s);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float q = __fmul_rn(w[i], r);
+    const float e = __fmaf_rn(-q, s, w[i]);
+    x[i] = __fmaf_rn(e, r, q);
+  }
+}
+__device__ __forceinline__ bool scale_in_fast_range(float s) { return s >= 0x1p-60f && s <= 0x1p60f; }
+
+// Activation fake-quant of n values sharing the dynamic scale s = fp32(amax / Qmax): |x| <=
+// amax / s stays near Qmax, so no overflow is possible; the sign of a zero result is w's.
+template <int FMT, int N>
+__device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
+  float x[N];
+  if (scale_in_fast_range(s)) {
+    quotients_unguarded<N>(v, s, x);
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = copysignf(x[i], v[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = quotient(v[i], s);
+  }
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const float2 q = q_pair<FMT>(x[i], x[i + 1]);
+    v[i] = round_bf16(__fmul_rn(q.x, s));
+    v[i + 1] = round_bf16(__fmul_rn(q.y, s));
+  }
+}
+
 // Fake-quantize n (even) values that share scale s, in place: v <- bf16(fp32(q(v / s) * s)).
 template <int FMT, int N>
 __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
@@ -138,21 +179,40 @@ __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
 
 // LSQ straight-through factor phi(x): q(x) - x inside the closed clip range, else the
 // violated bound.  q saturates (E2M1, E4M3) or clamps (INT4) to exactly that bound
-// outside the range, so phi = q(x) - (x inside ? x : 0).
+// outside the range, so phi = q(x) - (x inside ? x : 0).  The sign of a zero q does not
+// matter here, so the grid value is used as the conversion returns it.
 template <int FMT>
 __device__ __forceinline__ float2 lsq_pair(float xa, float xb) {
-  const float2 q = q_pair<FMT>(xa, xb);
-  const float ia = (xa >= Clip<FMT>::lo && xa <= Clip<FMT>::hi) ? xa : 0.0f;
-  const float ib = (xb >= Clip<FMT>::lo && xb <= Clip<FMT>::hi) ? xb : 0.0f;
+  float2 q;
+  if constexpr (FMT == kFmtNvfp4) {
+    q = q_e2m1x2(xa, xb);
+  } else if constexpr (FMT == kFmtFp8) {
+    q = q_e4m3x2(xa, xb);
+  } else {
+    q = make_float2(q_int4(xa), q_int4(xb));
+  }
+  float ia, ib;
+  if constexpr (FMT == kFmtInt4) {
+    ia = (xa >= Clip<FMT>::lo && xa <= Clip<FMT>::hi) ? xa : 0.0f;
+    ib = (xb >= Clip<FMT>::lo && xb <= Clip<FMT>::hi) ? xb : 0.0f;
+  } else {  // symmetric clip range
+    ia = fabsf(xa) <= Clip<FMT>::hi ? xa : 0.0f;
+    ib = fabsf(xb) <= Clip<FMT>::hi ? xb : 0.0f;
+  }
   return make_float2(q.x - ia, q.y - ib);
 }
 
 // ---------------------------------------------------------------------------------- misc
 
-// sigmoid(g) = 1 / (1 + exp(-g)) from CUDA's fast exponential and the correctly rounded
+// sigmoid(g) = 1 / (1 + exp(-g)) from CUDA's fast exponential and the hardware's approximate
 // reciprocal (exp(-g) = inf gives 0).  Used only where the result is compared with the
 // oracle by tolerance.
-__device__ __forceinline__ float sigmoid_f(float g) { return __frcp_rn(1.0f + __expf(-g)); }
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float sigmoid_f(float g) { return rcp_approx(1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return __fmul_rn(g, sigmoid_f(g)); }
 
 __device__ __forceinline__ float warp_max(float v) {

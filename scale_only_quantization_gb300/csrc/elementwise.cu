@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(256) act_quant_nvfp4_kernel(const uint4* __res
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    fakequant_inplace<kFmtNvfp4, 16>(v, __fdiv_rn(amax, 6.0f));
+    fakequant_act_inplace<kFmtNvfp4, 16>(v, __fdiv_rn(amax, 6.0f));
     out[2 * b] = pack8(v);
     out[2 * b + 1] = pack8(v + 8);
   }
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(256) act_quant_fp8_kernel(const uint4* __restr
     for (int64_t c = lane; c < c8; c += 32) {
       float v[8];
       unpack8(src[c], v);
-      fakequant_inplace<kFmtFp8, 8>(v, s);
+      fakequant_act_inplace<kFmtFp8, 8>(v, s);
       out[r * c8 + c] = pack8(v);
     }
   }
@@ -328,23 +328,27 @@ __global__ void __launch_bounds__(256) scale_reduce_kernel(const float* __restri
 
 __global__ void __launch_bounds__(256) quotient_check_kernel(const float* __restrict__ w, const float* __restrict__ s,
                                                              float* __restrict__ fast, float* __restrict__ ieee,
-                                                             int64_t n) {
+                                                             int64_t n, int mode) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const float wi = w[i];
+    const float wi = w[i], si = s[i];
     float x;
-    quotients<1>(&wi, s[i], &x);
+    if (mode == 1 && scale_in_fast_range(si)) {
+      quotients_unguarded<1>(&wi, si, &x);
+    } else {
+      quotients<1>(&wi, si, &x);
+    }
     fast[i] = x;
-    ieee[i] = quotient(wi, s[i]);
+    ieee[i] = quotient(wi, si);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, float* ieee, int64_t n,
+cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, float* ieee, int64_t n, int mode,
                                   cudaStream_t st) {
   if (n == 0) return cudaSuccess;
-  quotient_check_kernel<<<grid_for(n, 256, 8), 256, 0, st>>>(w, s, fast, ieee, n);
+  quotient_check_kernel<<<grid_for(n, 256, 8), 256, 0, st>>>(w, s, fast, ieee, n, mode);
   return cudaGetLastError();
 }
 

@@ -132,8 +132,11 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
+// Arrive on a barrier of either CTA of the pair.  Relaxed: it only tells the MMA issuer that
+// this warp's tensor-memory reads are complete (tcgen05.wait::ld has returned); it must not
+// wait for the epilogue's global stores to become visible, which release semantics would.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
@@ -228,11 +231,6 @@ __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) d[i] = pack8(v + 8 * i);
 }
-__device__ __forceinline__ void ldraw16(const __nv_bfloat16* src, uint4 (&u)[2]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-  u[0] = __ldg(s);
-  u[1] = __ldg(s + 1);
-}
 __device__ __forceinline__ void store16(__nv_bfloat16* dst, const float* v) {
   uint4* d = reinterpret_cast<uint4*>(dst);
   d[0] = pack8(v);
@@ -325,7 +323,7 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[i]));
-        fakequant_inplace<kFmtNvfp4, 16>(h, __fdiv_rn(amax, 6.0f));
+        fakequant_act_inplace<kFmtNvfp4, 16>(h, __fdiv_rn(amax, 6.0f));
       }
       uint4* hh = reinterpret_cast<uint4*>(hhrow + f0);
       hh[0] = pack8(h);
@@ -367,7 +365,7 @@ __device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint3
 }
 
 // dZ1 = [dH * up * sig(g) * (1 + g (1 - sig(g))), dH * g * sig(g)] from the stored bf16 Z1,
-// 16 columns at a time
+// 16 columns at a time; the Z1 loads run two steps ahead, the TMEM loads one step ahead.
 template <int BN>
 __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                                int half) {
@@ -376,26 +374,34 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, 
   __nv_bfloat16* dz1 = p.out + row * p.ld_out;
   constexpr int STEPS = BN / 32;  // 16-column steps per half
   const int col0 = half * (BN / 2);
+  const int f_first = ti.nb * BN + col0;
   uint32_t r[16], rn[16];
-  uint4 gr[2], ur[2], grn[2], urn[2];
-  ldraw16(z1 + ti.nb * BN + col0, gr);
-  ldraw16(z1 + p.F + ti.nb * BN + col0, ur);
+  uint4 z[3][4];  // ring of Z1 (gate 2 x 16 B, up 2 x 16 B) for three steps
+  {
+    const uint4* g0 = reinterpret_cast<const uint4*>(z1 + f_first);
+    const uint4* u0 = reinterpret_cast<const uint4*>(z1 + p.F + f_first);
+    z[0][0] = __ldg(g0); z[0][1] = __ldg(g0 + 1); z[0][2] = __ldg(u0); z[0][3] = __ldg(u0 + 1);
+    if (STEPS > 1) {
+      z[1][0] = __ldg(g0 + 2); z[1][1] = __ldg(g0 + 3); z[1][2] = __ldg(u0 + 2); z[1][3] = __ldg(u0 + 3);
+    }
+  }
   tmem_ld16_issue(tbase + col0, r);
   tmem_wait16(r);
-#pragma unroll 1
+#pragma unroll
   for (int j = 0; j < STEPS; ++j) {
-    const bool more = j + 1 < STEPS;
-    const int f0 = ti.nb * BN + col0 + 16 * j;
-    if (more) {
-      ldraw16(z1 + f0 + 16, grn);
-      ldraw16(z1 + p.F + f0 + 16, urn);
-      tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
+    const int f0 = f_first + 16 * j;
+    if (j + 2 < STEPS) {
+      const uint4* g2 = reinterpret_cast<const uint4*>(z1 + f0 + 32);
+      const uint4* u2 = reinterpret_cast<const uint4*>(z1 + p.F + f0 + 32);
+      z[(j + 2) % 3][0] = __ldg(g2); z[(j + 2) % 3][1] = __ldg(g2 + 1);
+      z[(j + 2) % 3][2] = __ldg(u2); z[(j + 2) % 3][3] = __ldg(u2 + 1);
     }
+    if (j + 1 < STEPS) tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
     float g[16], u[16];
-    unpack8(gr[0], g);
-    unpack8(gr[1], g + 8);
-    unpack8(ur[0], u);
-    unpack8(ur[1], u + 8);
+    unpack8(z[j % 3][0], g);
+    unpack8(z[j % 3][1], g + 8);
+    unpack8(z[j % 3][2], u);
+    unpack8(z[j % 3][3], u + 8);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float dh = __uint_as_float(r[i]);
@@ -407,38 +413,88 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, 
     }
     store16(dz1 + f0, g);
     store16(dz1 + p.F + f0, u);
-    if (more) {
+    if (j + 1 < STEPS) {
       tmem_wait16(rn);
 #pragma unroll
       for (int i = 0; i < 16; ++i) r[i] = rn[i];
-      gr[0] = grn[0];
-      gr[1] = grn[1];
-      ur[0] = urn[0];
-      ur[1] = urn[1];
     }
   }
 }
 
 // ds[e, n, b] (+)= sum_{kappa in b} dW[n, kappa] * phi(W[e, n, kappa], s[e, n, b]), 16
-// columns at a time.  nvfp4 blocks (16) and INT4 groups (128, when a column half holds a
-// whole group) are reduced here; otherwise (fp8's whole-row block, INT4 with 128-column
+// columns at a time.  The half-row's scales are loaded once up front, W runs two steps
+// ahead of the arithmetic, and the TMEM accumulator one step.  nvfp4 blocks (16) are
+// written as vectors at the end; INT4 groups (128, when a column half holds a whole
+// group) are written directly; otherwise (fp8's whole-row block, INT4 with 128-column
 // tiles) each column half writes its partial sum to
 // part[ds_index * parts + (tile in block) * 2 + half] and a reduction kernel adds the
 // parts in a fixed order.
+template <int FMT>
+__device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const uint4 (&wraw)[2], float sc) {
+  float wv[16], x[16];
+  unpack8(wraw[0], wv);
+  unpack8(wraw[1], wv + 8);
+  float t = 0.0f;
+  if (scale_in_fast_range(sc)) {
+    quotients_unguarded<16>(wv, sc, x);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 ph = lsq_pair<FMT>(x[i], x[i + 1]);
+      t = fmaf(__uint_as_float(acc[i]), ph.x, t);
+      t = fmaf(__uint_as_float(acc[i + 1]), ph.y, t);
+    }
+  }
+  if (!scale_in_fast_range(sc) || !isfinite(t)) {  // rare: extreme scale or an overflowing quotient
+    quotients<16>(wv, sc, x);
+    t = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 ph = lsq_pair<FMT>(x[i], x[i + 1]);
+      t = fmaf(__uint_as_float(acc[i]), ph.x, t);
+      t = fmaf(__uint_as_float(acc[i + 1]), ph.y, t);
+    }
+  }
+  return t;
+}
+
 template <int BN, int FMT>
 __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                                   int half) {
-  constexpr int STEPS = BN / 32;  // 16-column steps per half
+  constexpr int STEPS = BN / 32;  // 16-column steps per half (= nvfp4 scales per half)
   const int64_t n = ti.row_base + row_in_tile;
   const int64_t wrow = (int64_t)ti.e * p.w_rows + n;
-  const __nv_bfloat16* wr = p.w + wrow * p.w_cols;
+  const int col0 = half * (BN / 2);
+  const int64_t k_first = (int64_t)ti.nb * BN + col0;
+  const __nv_bfloat16* wr = p.w + wrow * p.w_cols + k_first;
   constexpr bool kDirectGroups = (FMT == kFmtInt4) && (BN == 256);
   const bool have_acc = ti.nkb > 0;
-  const int col0 = half * (BN / 2);
-  float part_sum = 0.0f;
+
+  // scales of this half row
+  float sv[STEPS];
+  float* ds_vec = nullptr;
+  if constexpr (FMT == kFmtNvfp4) {
+    const int64_t sidx = wrow * (p.w_cols / 16) + k_first / 16;  // a multiple of 4
+    const float4* sp = reinterpret_cast<const float4*>(p.s + sidx);
+#pragma unroll
+    for (int i = 0; i < STEPS / 4; ++i) {
+      const float4 v4 = __ldg(sp + i);
+      sv[4 * i] = v4.x; sv[4 * i + 1] = v4.y; sv[4 * i + 2] = v4.z; sv[4 * i + 3] = v4.w;
+    }
+    ds_vec = p.ds + sidx;
+  } else {
+    const float sc = (FMT == kFmtInt4) ? __ldg(p.s + wrow * (p.w_cols / 128) + k_first / 128) : __ldg(p.s + wrow);
+#pragma unroll
+    for (int i = 0; i < STEPS; ++i) sv[i] = sc;
+  }
+
   uint32_t r[16], rn[16];
-  uint4 wraw[2], wrawn[2];
-  ldraw16(wr + (int64_t)ti.nb * BN + col0, wraw);
+  uint4 wq[3][2];
+  wq[0][0] = __ldg(reinterpret_cast<const uint4*>(wr));
+  wq[0][1] = __ldg(reinterpret_cast<const uint4*>(wr) + 1);
+  if (STEPS > 1) {
+    wq[1][0] = __ldg(reinterpret_cast<const uint4*>(wr) + 2);
+    wq[1][1] = __ldg(reinterpret_cast<const uint4*>(wr) + 3);
+  }
   if (have_acc) {
     tmem_ld16_issue(tbase + col0, r);
     tmem_wait16(r);
@@ -446,57 +502,46 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
 #pragma unroll
     for (int i = 0; i < 16; ++i) r[i] = 0u;
   }
-#pragma unroll 1
+  float tsum[STEPS];
+#pragma unroll
   for (int j = 0; j < STEPS; ++j) {
-    const bool more = j + 1 < STEPS;
-    const int64_t kc = (int64_t)ti.nb * BN + col0 + 16 * j;
-    if (more) {
-      ldraw16(wr + kc + 16, wrawn);
-      if (have_acc) tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
+    if (j + 2 < STEPS) {
+      wq[(j + 2) % 3][0] = __ldg(reinterpret_cast<const uint4*>(wr) + 2 * (j + 2));
+      wq[(j + 2) % 3][1] = __ldg(reinterpret_cast<const uint4*>(wr) + 2 * (j + 2) + 1);
     }
-    float wv[16], x[16];
-    unpack8(wraw[0], wv);
-    unpack8(wraw[1], wv + 8);
-    float sc;
-    if constexpr (FMT == kFmtNvfp4) sc = __ldg(p.s + wrow * (p.w_cols / 16) + kc / 16);
-    else if constexpr (FMT == kFmtInt4) sc = __ldg(p.s + wrow * (p.w_cols / 128) + kc / 128);
-    else sc = __ldg(p.s + wrow);
-    quotients<16>(wv, sc, x);
-    float t = 0.0f;
+    if (have_acc && j + 1 < STEPS) tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
+    tsum[j] = lsq_block_sum<FMT>(r, wq[j % 3], sv[j]);
+    if (j + 1 < STEPS && have_acc) {
+      tmem_wait16(rn);
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 ph = lsq_pair<FMT>(x[i], x[i + 1]);
-      t = fmaf(__uint_as_float(r[i]), ph.x, t);
-      t = fmaf(__uint_as_float(r[i + 1]), ph.y, t);
-    }
-    if constexpr (FMT == kFmtNvfp4) {
-      float* dst = p.ds + wrow * (p.w_cols / 16) + kc / 16;
-      *dst = p.accumulate ? *dst + t : t;
-    } else {
-      part_sum += t;
-      if constexpr (kDirectGroups) {
-        if ((j & 7) == 7) {
-          float* dst = p.ds + wrow * (p.w_cols / 128) + kc / 128;
-          *dst = p.accumulate ? *dst + part_sum : part_sum;
-          part_sum = 0.0f;
-        }
-      }
-    }
-    if (more) {
-      if (have_acc) {
-        tmem_wait16(rn);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = rn[i];
-      }
-      wraw[0] = wrawn[0];
-      wraw[1] = wrawn[1];
+      for (int i = 0; i < 16; ++i) r[i] = rn[i];
     }
   }
-  if constexpr (FMT != kFmtNvfp4 && !kDirectGroups) {
-    const int64_t B = (FMT == kFmtInt4) ? 128 : p.w_cols;  // elements per scale
-    const int tiles_per_block = (int)(B / BN);
-    const int64_t ds_index = wrow * (p.w_cols / B) + ((int64_t)ti.nb * BN) / B;
-    p.part[ds_index * (2 * tiles_per_block) + (ti.nb % tiles_per_block) * 2 + half] = part_sum;
+
+  if constexpr (FMT == kFmtNvfp4) {
+    float4* dv = reinterpret_cast<float4*>(ds_vec);
+#pragma unroll
+    for (int i = 0; i < STEPS / 4; ++i) {
+      float4 o = make_float4(tsum[4 * i], tsum[4 * i + 1], tsum[4 * i + 2], tsum[4 * i + 3]);
+      if (p.accumulate) {
+        const float4 old = dv[i];
+        o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+      }
+      dv[i] = o;
+    }
+  } else {
+    float sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < STEPS; ++j) sum += tsum[j];
+    if constexpr (kDirectGroups) {
+      float* dst = p.ds + wrow * (p.w_cols / 128) + k_first / 128;
+      *dst = p.accumulate ? *dst + sum : sum;
+    } else {
+      const int64_t B = (FMT == kFmtInt4) ? 128 : p.w_cols;  // elements per scale
+      const int tiles_per_block = (int)(B / BN);
+      const int64_t ds_index = wrow * (p.w_cols / B) + ((int64_t)ti.nb * BN) / B;
+      p.part[ds_index * (2 * tiles_per_block) + (ti.nb % tiles_per_block) * 2 + half] = sum;
+    }
   }
 }
 

@@ -60,8 +60,9 @@ cudaError_t launch_dy_gather(const void* dout, const float* p, const int32_t* ro
 cudaError_t launch_scale_reduce(const float* part, float* ds, int64_t n, int nparts, int accumulate,
                                 cudaStream_t st);
 
-// fast[i] = the quantizers' reciprocal-based quotient of w[i] / s[i], ieee[i] = IEEE division
-cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, float* ieee, int64_t n,
+// fast[i] = the quantizers' reciprocal-based quotient of w[i] / s[i] (mode 0: per-element
+// guarded form; mode 1: the block-guarded form), ieee[i] = IEEE division
+cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, float* ieee, int64_t n, int mode,
                                   cudaStream_t st);
 
 // ---- grouped GEMMs (gemm.cu) ----

@@ -294,11 +294,8 @@ def test_outputs_stay_inside_their_buffers():
 
 # ------------------------------------------------------------------------------ the quotient
 
-def test_reciprocal_quotient_matches_cuda_division():
-    """The quantizers' x = w / s (correctly rounded reciprocal + one FMA correction) equals
-    CUDA's IEEE division bit for bit, on hard cases and 32M random pairs."""
-    g = torch.Generator(device="cuda").manual_seed(11)
-    n = 1 << 25
+def _quotient_cases(n, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
     w = torch.randn(n, generator=g, device="cuda") * torch.exp2(torch.randint(-40, 12, (n,), generator=g,
                                                                               device="cuda").float())
     w = w.to(torch.bfloat16).float()
@@ -313,11 +310,34 @@ def test_reciprocal_quotient_matches_cuda_division():
     w[2 * m:2 * m + 8] = torch.tensor([0.0, -0.0, 3e38, -3e38, 1e-38, -1e-38, 6.0, -0.5], device="cuda")
     s[2 * m:2 * m + 8] = torch.tensor([0.25, 0.25, 1e-3, 1e-3, 0.5, 2e-38, 1.0, 0.0], device="cuda")
     s[2 * m + 8:2 * m + 12] = torch.tensor([1e-40, 3e-39, 0.0, 1e-45], device="cuda")   # subnormal / zero scales
+    # the activation case: |w| <= amax, s = amax / Qmax
+    k = 1 << 20
+    amax = torch.rand(k, generator=g, device="cuda") * 10.0 + 1e-3
+    w[3 * m:3 * m + k] = ((torch.rand(k, generator=g, device="cuda") * 2 - 1) * amax).to(torch.bfloat16).float()
+    s[3 * m:3 * m + k] = amax.to(torch.bfloat16).float() / 6.0
+    return w, s
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_reciprocal_quotient_matches_cuda_division(mode):
+    """The quantizers' x = w / s (correctly rounded reciprocal + one FMA correction) equals
+    CUDA's IEEE division bit for bit, on hard cases and 32M random pairs; the block-guarded
+    form (mode 1) wherever 2^-11 <= |x| <= 2^100, and below that it still rounds to zero on
+    every grid."""
+    n = 1 << 25
+    w, s = _quotient_cases(n, 11 + mode)
     fast = torch.empty_like(w)
     ieee = torch.empty_like(w)
-    Q.qad_debug_quotient(w, s, fast, ieee, n)
+    Q.qad_debug_quotient(w, s, fast, ieee, n, mode)
     torch.cuda.synchronize()
     same = fast.view(torch.int32) == ieee.view(torch.int32)
+    if mode == 1:
+        # contract of the block-guarded form: exact for 2^-11 <= |x| <= 2^100 (its callers
+        # never produce larger quotients: activations have |x| <= amax / s ~ Qmax, and the
+        # scale-gradient reduction re-runs a block whose sum is not finite with mode 0's form)
+        small = ieee.abs() < 2.0 ** -11
+        assert bool((fast[small].abs() < 2.0 ** -10).all())
+        same = same | small | (ieee.abs() > 2.0 ** 100)
     assert bool(same.all()), "%d mismatches, e.g. w=%r s=%r" % (int((~same).sum()), w[~same][:3].tolist(),
                                                                 s[~same][:3].tolist())
     nz = s != 0
