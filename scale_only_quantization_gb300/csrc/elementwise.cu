@@ -32,7 +32,26 @@ template <int FMT>
 __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict__ w, const float* __restrict__ s,
                                                         uint4* __restrict__ out, uint64_t nchunks, uint32_t cps) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
+  uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; c + stride < nchunks; c += 2 * stride) {  // two chunks (64 bytes) per thread in flight
+    const uint64_t c2 = c + stride;
+    const uint4 u0 = ld_stream(w + 2 * c), u1 = ld_stream(w + 2 * c + 1);
+    const uint4 u2 = ld_stream(w + 2 * c2), u3 = ld_stream(w + 2 * c2 + 1);
+    const float sc = __ldg(s + (cps == 1 ? c : c / cps));
+    const float sc2 = __ldg(s + (cps == 1 ? c2 : c2 / cps));
+    float v[16];
+    unpack8(u0, v);
+    unpack8(u1, v + 8);
+    fakequant_inplace<FMT, 16>(v, sc);
+    st_stream(out + 2 * c, pack8(v));
+    st_stream(out + 2 * c + 1, pack8(v + 8));
+    unpack8(u2, v);
+    unpack8(u3, v + 8);
+    fakequant_inplace<FMT, 16>(v, sc2);
+    st_stream(out + 2 * c2, pack8(v));
+    st_stream(out + 2 * c2 + 1, pack8(v + 8));
+  }
+  for (; c < nchunks; c += stride) {
     const uint4 u0 = ld_stream(w + 2 * c);
     const uint4 u1 = ld_stream(w + 2 * c + 1);
     const float sc = __ldg(s + (cps == 1 ? c : c / cps));
@@ -246,32 +265,68 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
       for (int64_t c = lane; c < c8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
     } else {
       const uint4* s = src + (int64_t)t * c8;
-      for (int64_t c = lane; c < c8; c += 32) d[c] = __ldg(s + c);
+      int64_t c = lane;
+      for (; c + 96 < c8; c += 128) {  // four 16-byte loads in flight per lane
+        const uint4 a0 = __ldg(s + c), a1 = __ldg(s + c + 32), a2 = __ldg(s + c + 64), a3 = __ldg(s + c + 96);
+        d[c] = a0;
+        d[c + 32] = a1;
+        d[c + 64] = a2;
+        d[c + 96] = a3;
+      }
+      for (; c < c8; c += 32) d[c] = __ldg(s + c);
     }
   }
 }
 
 // ------------------------------------------------------------------------- combine
 
-// one warp per token; fixed slot order j = 0..k-1, fp32 sums
+// one warp per token; fixed slot order j = 0..k-1, fp32 sums.  KC > 0 fixes k at compile time
+// so that the k row loads of a column chunk are all in flight together.
+template <int KC>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ p, uint4* __restrict__ out, int64_t T,
-                                                      int k, int64_t c8) {
+                                                      int k_rt, int64_t c8) {
+  const int k = KC > 0 ? KC : k_rt;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T; t += warps) {
-    for (int64_t c = lane; c < c8; c += 32) {
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int j = 0; j < k; ++j) {
-        const int32_t r = __ldg(row_of + t * k + j);
-        if (r < 0) continue;
-        const float pj = p ? __ldg(p + t * k + j) : 1.0f;
-        float v[8];
-        unpack8(__ldg(y + (int64_t)r * c8 + c), v);
+    if constexpr (KC > 0) {
+      int32_t rows[KC];
+      float pw[KC];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(pj, v[i], acc[i]);
+      for (int j = 0; j < KC; ++j) {
+        rows[j] = __ldg(row_of + t * KC + j);
+        pw[j] = p ? __ldg(p + t * KC + j) : 1.0f;
       }
-      out[t * c8 + c] = pack8(acc);
+      for (int64_t c = lane; c < c8; c += 32) {
+        uint4 v[KC];
+#pragma unroll
+        for (int j = 0; j < KC; ++j) v[j] = rows[j] >= 0 ? __ldg(y + (int64_t)rows[j] * c8 + c) : make_uint4(0, 0, 0, 0);
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          if (rows[j] < 0) continue;
+          float f[8];
+          unpack8(v[j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(pw[j], f[i], acc[i]);
+        }
+        out[t * c8 + c] = pack8(acc);
+      }
+    } else {
+      for (int64_t c = lane; c < c8; c += 32) {
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < k; ++j) {
+          const int32_t r = __ldg(row_of + t * k + j);
+          if (r < 0) continue;
+          const float pj = p ? __ldg(p + t * k + j) : 1.0f;
+          float v[8];
+          unpack8(__ldg(y + (int64_t)r * c8 + c), v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(pj, v[i], acc[i]);
+        }
+        out[t * c8 + c] = pack8(acc);
+      }
     }
   }
 }
@@ -295,19 +350,31 @@ __global__ void __launch_bounds__(256) dy_gather_kernel(const uint4* __restrict_
     const int j = row_slot[r];
     const float pj = __ldg(p + (int64_t)t * k + j);
     const uint4* g = dout + (int64_t)t * c8;
+    const uint4* yr = y + r * c8;
     float dot = 0.0f;
-    for (int64_t c = lane; c < c8; c += 32) {
-      float v[8];
-      unpack8(__ldg(g + c), v);
+    for (int64_t c0 = lane; c0 < c8; c0 += 64) {  // two 16-byte chunks per lane in flight
+      const bool two = c0 + 32 < c8;
+      const uint4 g0 = __ldg(g + c0);
+      const uint4 g1 = two ? __ldg(g + c0 + 32) : make_uint4(0, 0, 0, 0);
+      uint4 y0 = make_uint4(0, 0, 0, 0), y1 = make_uint4(0, 0, 0, 0);
       if (dprobs) {
-        float yv[8];
-        unpack8(__ldg(y + r * c8 + c), yv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dot = fmaf(v[i], yv[i], dot);
+        y0 = __ldg(yr + c0);
+        if (two) y1 = __ldg(yr + c0 + 32);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(pj, v[i]);
-      d[c] = pack8(v);
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !two) break;
+        float v[8], yv[8];
+        unpack8(h ? g1 : g0, v);
+        if (dprobs) {
+          unpack8(h ? y1 : y0, yv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dot = fmaf(v[i], yv[i], dot);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(pj, v[i]);
+        d[c0 + 32 * h] = pack8(v);
+      }
     }
     if (dprobs) {
       dot = warp_sum(dot);
@@ -445,8 +512,13 @@ cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* p,
   if (T == 0) return cudaSuccess;
   const int id = p ? QAD_K_COMBINE : QAD_K_DX_COMBINE;
   prof_begin(id, st);
-  combine_kernel<<<grid_for(T * 32, 256, 8), 256, 0, st>>>(static_cast<const uint4*>(y), row_of, p,
-                                                            static_cast<uint4*>(out), T, k, d / 8);
+  const int grid = grid_for(T * 32, 256, 8);
+  const uint4* yy = static_cast<const uint4*>(y);
+  uint4* o = static_cast<uint4*>(out);
+  if (k == 8) combine_kernel<8><<<grid, 256, 0, st>>>(yy, row_of, p, o, T, k, d / 8);
+  else if (k == 2) combine_kernel<2><<<grid, 256, 0, st>>>(yy, row_of, p, o, T, k, d / 8);
+  else if (k == 4) combine_kernel<4><<<grid, 256, 0, st>>>(yy, row_of, p, o, T, k, d / 8);
+  else combine_kernel<0><<<grid, 256, 0, st>>>(yy, row_of, p, o, T, k, d / 8);
   prof_end(id, st);
   return cudaGetLastError();
 }
