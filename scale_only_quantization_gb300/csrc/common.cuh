@@ -165,10 +165,24 @@ __device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
 }
 
 // Fake-quantize n (even) values that share scale s, in place: v <- bf16(fp32(q(v / s) * s)).
+// Weights are arbitrary, so besides the block's scale range the quotients are checked for
+// overflow through one NaN/inf-propagating sum (an overflowing fast quotient gives inf or
+// NaN); a block that fails is recomputed with the per-element guarded form.
 template <int FMT, int N>
 __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
   float x[N];
-  quotients<N>(v, s, x);
+  bool fast = scale_in_fast_range(s);
+  if (fast) {
+    quotients_unguarded<N>(v, s, x);
+    float probe = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      x[i] = copysignf(x[i], v[i]);
+      probe += x[i] * 0.0f;  // 0 unless some x is inf or NaN
+    }
+    fast = probe == 0.0f;
+  }
+  if (!fast) quotients<N>(v, s, x);
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
     const float2 q = q_pair<FMT>(x[i], x[i + 1]);

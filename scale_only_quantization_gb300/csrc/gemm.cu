@@ -340,27 +340,25 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_
   }
 }
 
+// bf16 store of this warp's half of the tile: all its TMEM loads are issued at once, then
+// one wait (a single TMEM latency per tile instead of one per chunk).
 template <int BN>
 __device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
   const int64_t row = ti.row_base + row_in_tile;
-  __nv_bfloat16* dst = p.out + row * p.ld_out + (int64_t)ti.nb * BN;
-  constexpr int NH = BN / 64;
-  uint32_t r[32], rn[32];
-  tmem_ld32_issue(tbase + 32 * half * NH, r);
-  tmem_wait32(r);
-#pragma unroll 1
-  for (int c = half * NH; c < (half + 1) * NH; ++c) {
-    const bool more = c + 1 < (half + 1) * NH;
-    if (more) tmem_ld32_issue(tbase + 32 * (c + 1), rn);
+  constexpr int NH = BN / 64;  // 32-column chunks per half: 4 or 2
+  const int c0 = half * NH;
+  __nv_bfloat16* dst = p.out + row * p.ld_out + (int64_t)ti.nb * BN + 32 * c0;
+  uint32_t r[NH][32];
+#pragma unroll
+  for (int c = 0; c < NH; ++c) tmem_ld32_issue(tbase + 32 * (c0 + c), r[c]);
+#pragma unroll
+  for (int c = 0; c < NH; ++c) tmem_wait32(r[c]);
+#pragma unroll
+  for (int c = 0; c < NH; ++c) {
     float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c][i]);
     store32(dst + 32 * c, v);
-    if (more) {
-      tmem_wait32(rn);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) r[i] = rn[i];
-    }
   }
 }
 
