@@ -77,7 +77,13 @@ enum {
 
 /* qad_moe_shape.flags */
 enum {
-  QAD_FLAG_STASH_H = 1   /* also store the un-quantized SwiGLU output H in the workspace */
+  QAD_FLAG_STASH_H = 1,  /* also store the un-quantized SwiGLU output H in the workspace */
+  QAD_FLAG_NO_QUANT = 2  /* quantizers off: the self-distillation teacher pass ("MCoreQAD
+                            Backend", opening section: the same frozen model with quantization
+                            disabled supplies the teacher logits).  qad_moe_fwd and
+                            qad_moe_bwd_dgrad then use the raw bf16 weights and bf16
+                            activations; the scales are not read (pass any valid pointer)
+                            and qad_moe_bwd_scalegrad returns QAD_ERR_INVALID_ARG. */
 };
 
 /* Shape of one MoE layer. T tokens, hidden d, expert FFN width F, E experts, top-k. */

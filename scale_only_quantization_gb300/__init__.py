@@ -18,7 +18,7 @@ QAD_ERR_SCRATCH_LIMIT = -6
 QAD_NOALLOC_MAX_EXPERTS, QAD_NOALLOC_MAX_PAIRS = 256, 262144
 QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW = 0, 1, 2
 QAD_DEV_BAD_INDEX, QAD_DEV_DUP_INDEX, QAD_DEV_TIMEOUT = 1, 2, 4
-QAD_FLAG_STASH_H = 1
+QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT = 1, 2
 VIEWS = ["HEADER", "OFFSETS", "COUNTS", "ROW_TOKEN", "ROW_SLOT", "ROW_OF", "W13_HAT", "W2_HAT", "A1", "Z1", "H",
          "H_HAT", "Y", "DY", "DZ1", "DA1", "XQ"]
 VIEW = {n: i for i, n in enumerate(VIEWS)}

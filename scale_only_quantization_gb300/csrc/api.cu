@@ -90,7 +90,7 @@ void prof_end(int id, cudaStream_t st) {
 int layout_of(const qad_moe_shape& s, Layout* L) {
   if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
   if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_FP8_ROW) return QAD_ERR_INVALID_ARG;
-  if (s.reserved != 0 || (s.flags & ~QAD_FLAG_STASH_H)) return QAD_ERR_INVALID_ARG;
+  if (s.reserved != 0 || (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT))) return QAD_ERR_INVALID_ARG;
   if (s.d % 256 || s.F % 128) return QAD_ERR_UNSUPPORTED;
   if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
   const int64_t R = s.T * (int64_t)s.topk;
@@ -155,6 +155,23 @@ int check_layer(const qad_moe_shape* s, void* ws, size_t ws_bytes, Layout* L) {
 
 bool ok_ptr(const void* p) { return p && aligned16(p); }
 
+// GEMM context of one call.  With QAD_FLAG_NO_QUANT the GEMMs read the caller's raw weights
+// and the fc1 epilogue applies no activation quantizer (the w4a16 path, whose activations
+// stay bf16); otherwise they read the fake-quantized copies the forward wrote.
+GemmCtx gemm_ctx(const Layout& L, uint8_t* wsb, const qad_moe_shape& s, const void* w13, const void* w2,
+                 cudaStream_t st) {
+  const bool no_quant = (s.flags & QAD_FLAG_NO_QUANT) != 0;
+  GemmCtx c;
+  c.L = &L;
+  c.ws = wsb;
+  c.fmt = no_quant ? QAD_FMT_INT4_G128 : s.fmt;
+  c.flags = s.flags;
+  c.st = st;
+  c.w13h = no_quant ? w13 : static_cast<const void*>(wsb + L.w13h);
+  c.w2h = no_quant ? w2 : static_cast<const void*>(wsb + L.w2h);
+  return c;
+}
+
 }  // namespace
 
 extern "C" {
@@ -201,21 +218,25 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
   int32_t* hdr = reinterpret_cast<int32_t*>(wsb + L.header);
   const int32_t* rpad = hdr + HDR_RPAD;
   const int fmt = s->fmt;
+  const bool no_quant = (s->flags & QAD_FLAG_NO_QUANT) != 0;
   QAD_TRY(cudaMemsetAsync(hdr, 0, 256, st));
   QAD_TRY(launch_route(topk_idx, L, wsb, st));
-  QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st));
-  QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st));
+  if (!no_quant) {
+    QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st));
+    QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st));
+  }
   const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
-  if (fmt == QAD_FMT_INT4_G128) {
+  if (no_quant || fmt == QAD_FMT_INT4_G128) {
     QAD_TRY(launch_gather_rows(x, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
   } else {
     QAD_TRY(launch_act_quant_rows(fmt, x, wsb + L.xq, L.T, L.d, nullptr, st));
     QAD_TRY(launch_gather_rows(wsb + L.xq, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
   }
-  GemmCtx c = {&L, wsb, fmt, s->flags, st};
+  GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
   QAD_TRY(gemm_prepare(c));
   QAD_TRY(gemm_fc1(c));
-  if (fmt == QAD_FMT_FP8_ROW) QAD_TRY(launch_act_quant_rows(fmt, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
+  if (!no_quant && fmt == QAD_FMT_FP8_ROW)
+    QAD_TRY(launch_act_quant_rows(fmt, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
   QAD_TRY(gemm_fc2(c));
   QAD_TRY(launch_combine(wsb + L.y, reinterpret_cast<const int32_t*>(wsb + L.row_of), topk_w, out, L.T, (int)L.k,
                          L.d, st));
@@ -239,7 +260,7 @@ int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* top
   QAD_TRY(launch_dy_gather(dout, topk_w, reinterpret_cast<const int32_t*>(wsb + L.row_token),
                            reinterpret_cast<const int32_t*>(wsb + L.row_slot), wsb + L.y, wsb + L.dy, dprobs, L.Rmax,
                            (int)L.k, L.d, rpad, st));
-  GemmCtx c = {&L, wsb, s->fmt, s->flags, st};
+  GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
   QAD_TRY(gemm_dgrad_fc2(c));
   QAD_TRY(gemm_dgrad_fc1(c));
   QAD_TRY(launch_combine(wsb + L.da1, reinterpret_cast<const int32_t*>(wsb + L.row_of), nullptr, dx, L.T, (int)L.k,
@@ -254,8 +275,9 @@ int qad_moe_bwd_scalegrad(const qad_moe_shape* s, const void* w13, const float* 
   if (rc != QAD_OK) return rc;
   if (!ok_ptr(w13) || !ok_ptr(s13) || !ok_ptr(w2) || !ok_ptr(s2) || !ok_ptr(ds13) || !ok_ptr(ds2))
     return QAD_ERR_INVALID_ARG;
+  if (s->flags & QAD_FLAG_NO_QUANT) return QAD_ERR_INVALID_ARG;  // no scales without quantizers
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  GemmCtx c = {&L, static_cast<uint8_t*>(ws), s->fmt, s->flags, st};
+  GemmCtx c = gemm_ctx(L, static_cast<uint8_t*>(ws), *s, w13, w2, st);
   QAD_TRY(gemm_wgrad_fc2(c, w2, s2, ds2, accumulate ? 1 : 0));
   QAD_TRY(gemm_wgrad_fc1(c, w13, s13, ds13, accumulate ? 1 : 0));
   return QAD_OK;

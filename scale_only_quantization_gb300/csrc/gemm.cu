@@ -883,7 +883,7 @@ cudaError_t gemm_fc1(const GemmCtx& c) {
   Params p = base_params(c);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.a1, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tb, c.ws + L.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
   p.n_ntiles = (int)(L.F / 128);
   p.num_kb = (int)(L.d / BK);
   p.b_rows = (int)(2 * L.F);
@@ -901,7 +901,7 @@ cudaError_t gemm_fc2(const GemmCtx& c) {
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.hh, L.F, L.Rmax, L.F, 128)) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.d);
-  if (!make_tmap(&tb, c.ws + L.w2h, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
   p.n_ntiles = (int)(L.d / bn);
   p.num_kb = (int)(L.F / BK);
   p.b_rows = (int)L.d;
@@ -918,7 +918,7 @@ cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.dy, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
   // W2_hat viewed as [E * d (GEMM K), F (GEMM N)], N contiguous
-  if (!make_tmap(&tb, c.ws + L.w2h, L.F, L.E * L.d, L.F, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, 64)) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.F);
   p.n_ntiles = (int)(L.F / bn);
   p.num_kb = (int)(L.d / BK);
@@ -938,7 +938,7 @@ cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.dz1, 2 * L.F, L.Rmax, 2 * L.F, 128)) return cudaErrorInvalidValue;
   // W13_hat viewed as [E * 2F (GEMM K), d (GEMM N)], N contiguous
-  if (!make_tmap(&tb, c.ws + L.w13h, L.d, L.E * 2 * L.F, L.d, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 64)) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.d);
   p.n_ntiles = (int)(L.d / bn);
   p.num_kb = (int)(2 * L.F / BK);

@@ -69,8 +69,10 @@ cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, f
 struct GemmCtx {
   const Layout* L;
   uint8_t* ws;
-  int fmt, flags;
+  int fmt, flags;  // fmt selects the activation quantizer of the fc1 epilogue and the LSQ grid
   cudaStream_t st;
+  const void* w13h;  // the weights the GEMMs read: the fake-quantized copies in the workspace,
+  const void* w2h;   // or the caller's raw weights for the unquantized teacher pass
 };
 cudaError_t gemm_prepare(const GemmCtx& c);     // pair-tile table of the row-mode GEMMs (after routing)
 cudaError_t gemm_fc1(const GemmCtx& c);         // Z1, H, H_hat  <- A1 . W13_hat^T (+ SwiGLU, AQ)

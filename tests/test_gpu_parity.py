@@ -343,3 +343,53 @@ def test_reciprocal_quotient_matches_cuda_division(mode):
     nz = s != 0
     torch_div = w[nz] / s[nz]
     assert torch.equal(ieee[nz].view(torch.int32), torch_div.view(torch.int32))
+
+
+# ------------------------------------------------------------------------------ teacher pass
+
+@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW])
+def test_teacher_pass_without_quantizers(fmt):
+    """QAD_FLAG_NO_QUANT: the same layer with both quantizers off (the self-distillation
+    teacher) against the oracle with quant=False, stage by stage."""
+    inp = _tiny(fmt)
+    host = host_inputs(inp)
+    s = Q.shape(inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], fmt, Q.QAD_FLAG_NO_QUANT | Q.QAD_FLAG_STASH_H)
+    ws = torch.empty(Q.qad_moe_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    T, d, k, F, E = inp["T"], inp["d"], inp["topk"], inp["F"], inp["E"]
+    out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty_like(out)
+    dprobs = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    Q.qad_moe_fwd(s, inp["x"], inp["topk_idx"], inp["topk_w"], inp["w13"], inp["s13"], inp["w2"], inp["s2"], out, ws)
+    Q.qad_moe_bwd_dgrad(s, inp["dout"], inp["topk_w"], inp["w13"], inp["s13"], inp["w2"], inp["s2"], dx, dprobs, ws)
+    assert Q.qad_check_device_error(ws) == 0
+    with pytest.raises(Q.QADError):
+        Q.qad_moe_bwd_scalegrad(s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], torch.empty_like(inp["s13"]),
+                                torch.empty_like(inp["s2"]), 0, ws)
+    ref = OM.route(host["topk_idx"], E)
+    off, row_of = ref["offsets"], ref["row_of"]
+    token = Q.workspace_view(ws, s, "ROW_TOKEN", torch.int32).cpu().numpy()
+    real = token[:int(Q.workspace_view(ws, s, "HEADER", torch.int32)[2])] >= 0
+    rpad = real.size
+
+    def rows(name, cols):
+        return vals(Q.workspace_view(ws, s, name, torch.bfloat16)[:rpad * cols].view(rpad, cols))[real]
+
+    w13, w2 = OQ.bf16_to_f64(host["w13"]), OQ.bf16_to_f64(host["w2"])
+    a1 = rows("A1", d)
+    assert np.array_equal(a1, OQ.bf16_to_f64(host["x"])[ref["row_token"]])      # no activation quant
+    z1 = rows("Z1", 2 * F)
+    assert_close(z1, OM.grouped_gemm_nt(a1, w13, off), "teacher Z1")
+    h, hh = rows("H", F), rows("H_HAT", F)
+    assert np.array_equal(h, hh)                                                   # H_hat = H
+    y = rows("Y", d)
+    assert_close(y, OM.grouped_gemm_nt(hh, w2, off), "teacher Y")
+    p = host["topk_w"].astype(np.float64)
+    assert_close(vals(out), OM.combine(y, p, row_of), "teacher out")
+    fwd = OM.moe_forward(fmt, host["x"], host["topk_idx"], host["topk_w"], host["w13"], host["s13"], host["w2"],
+                         host["s2"], quant=False)
+    rel = np.max(np.abs(vals(out) - fwd["out"])) / np.sqrt(np.mean(fwd["out"] ** 2))
+    assert rel < 0.05                                                              # end to end, no codes to move
+    dz1 = rows("DZ1", 2 * F)
+    da1 = rows("DA1", d)
+    assert_close(da1, OM.grouped_gemm_nn(dz1, w13, off), "teacher dA1")
+    assert_close(vals(dx), OM.combine(da1, np.ones((T, k)), row_of), "teacher dx")
