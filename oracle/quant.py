@@ -17,6 +17,7 @@ The pages never write the quantizer formulas down.  The readings used here:
 * E4M3 ("fn" variant: max finite 448, subnormals spaced 2^-9), ties to even,
   saturating at +-448.
 * INT4 symmetric grid {-8, ..., 7}: round half to even, then clamp.
+* INT8 (w8a8) grid {-128, ..., 127}: round half to even, then clamp; scales amax/127.
 * The weight scale is one fp32 number per block of B consecutive elements along K
   (B = 16 for nvfp4, 128 for INT4 group-128, B = K for fp8 per output row), not
   itself rounded to a narrower format.
@@ -37,15 +38,31 @@ import numpy as np
 FMT_NVFP4 = 0       # nvfp4 W4A4: E2M1, block 16 along K, activations block-16 amax/6
 FMT_INT4_G128 = 1   # w4a16: INT4, group 128 along K, activations left in bf16
 FMT_FP8_ROW = 2     # fp8 W8A8: E4M3, one scale per output row, activations per-row amax/448
+FMT_NVFP4A16 = 3    # nvfp4a16: E2M1 weights as nvfp4, activations left in bf16
+FMT_W8A8 = 4        # w8a8: INT8 weights, one scale per output row, activations per-row amax/127
+FMT_W4AFP8 = 5      # w4afp8: INT4 weights as w4a16, activations E4M3 per-row amax/448
+FORMATS = (FMT_NVFP4, FMT_INT4_G128, FMT_FP8_ROW, FMT_NVFP4A16, FMT_W8A8, FMT_W4AFP8)
 
-# (lower clip bound, upper clip bound, divisor used to turn an amax into a scale)
-CLIP = {FMT_NVFP4: (-6.0, 6.0), FMT_INT4_G128: (-8.0, 7.0), FMT_FP8_ROW: (-448.0, 448.0)}
-AMAX_DIV = {FMT_NVFP4: 6.0, FMT_INT4_G128: 7.0, FMT_FP8_ROW: 448.0}
+# element grids ("quantizer kinds") and what each format uses for weights / activations
+Q_E2M1, Q_INT4, Q_E4M3, Q_INT8 = "e2m1", "int4", "e4m3", "int8"
+WEIGHT_Q = {FMT_NVFP4: Q_E2M1, FMT_INT4_G128: Q_INT4, FMT_FP8_ROW: Q_E4M3, FMT_NVFP4A16: Q_E2M1,
+            FMT_W8A8: Q_INT8, FMT_W4AFP8: Q_INT4}
+ACT_Q = {FMT_NVFP4: Q_E2M1, FMT_INT4_G128: None, FMT_FP8_ROW: Q_E4M3, FMT_NVFP4A16: None,
+         FMT_W8A8: Q_INT8, FMT_W4AFP8: Q_E4M3}
+# per quantizer kind: (lower clip bound, upper clip bound), the divisor that turns an amax
+# into a scale, and the block of consecutive K elements sharing a scale (None = a whole row)
+Q_CLIP = {Q_E2M1: (-6.0, 6.0), Q_INT4: (-8.0, 7.0), Q_E4M3: (-448.0, 448.0), Q_INT8: (-128.0, 127.0)}
+Q_AMAX_DIV = {Q_E2M1: 6.0, Q_INT4: 7.0, Q_E4M3: 448.0, Q_INT8: 127.0}
+Q_BLOCK = {Q_E2M1: 16, Q_INT4: 128, Q_E4M3: None, Q_INT8: None}
+
+CLIP = {f: Q_CLIP[WEIGHT_Q[f]] for f in FORMATS}
+AMAX_DIV = {f: Q_AMAX_DIV[WEIGHT_Q[f]] for f in FORMATS}
 
 
 def weight_block(fmt, K):
     """Elements of K that share one weight scale."""
-    return {FMT_NVFP4: 16, FMT_INT4_G128: 128, FMT_FP8_ROW: K}[fmt]
+    b = Q_BLOCK[WEIGHT_Q[fmt]]
+    return K if b is None else b
 
 
 # --------------------------------------------------------------------------------------
@@ -140,8 +157,18 @@ def q_int4(x):
     return np.clip(np.rint(x), -8.0, 7.0)
 
 
+def q_int8(x):
+    """Round half to even to an integer, then clamp to the INT8 range [-128, 127]."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.clip(np.rint(x), -128.0, 127.0)
+
+
+Q_FUNC = {Q_E2M1: q_e2m1, Q_INT4: q_int4, Q_E4M3: q_e4m3, Q_INT8: q_int8}
+
+
 def q_fmt(fmt, x):
-    return {FMT_NVFP4: q_e2m1, FMT_INT4_G128: q_int4, FMT_FP8_ROW: q_e4m3}[fmt](x)
+    """The weight quantizer of format `fmt`."""
+    return Q_FUNC[WEIGHT_Q[fmt]](x)
 
 
 # --------------------------------------------------------------------------------------
@@ -181,27 +208,31 @@ def fakequant_weight(fmt, w_bits, scale):
 def act_scale(fmt, a):
     """Dynamic activation scale per block along the last axis (detached, not learnable).
 
-    nvfp4: one scale per 16 elements, fp32(amax / 6).  fp8: one per row, fp32(amax / 448).
-    Returns the scale broadcast to a's shape.
+    E2M1 (nvfp4): one scale per 16 elements, fp32(amax / 6).  E4M3 (fp8, w4afp8): one per
+    row, fp32(amax / 448).  INT8 (w8a8): one per row, fp32(amax / 127).  Returns the scale
+    broadcast to a's shape.
     """
     a = np.asarray(a, dtype=np.float64)
-    if fmt == FMT_NVFP4:
+    kind = ACT_Q[fmt]
+    if kind is None:
+        raise ValueError("format has no activation quantizer")
+    div = Q_AMAX_DIV[kind]
+    if Q_BLOCK[kind] == 16:
         blocks = a.reshape(a.shape[:-1] + (a.shape[-1] // 16, 16))
         amax = np.abs(blocks).max(axis=-1)
-        return np.repeat(round_f32(amax / 6.0), 16, axis=-1)
-    if fmt == FMT_FP8_ROW:
-        amax = np.abs(a).max(axis=-1, keepdims=True)
-        return np.broadcast_to(round_f32(amax / 448.0), a.shape)
-    raise ValueError("format has no activation quantizer")
+        return np.repeat(round_f32(amax / div), 16, axis=-1)
+    amax = np.abs(a).max(axis=-1, keepdims=True)
+    return np.broadcast_to(round_f32(amax / div), a.shape)
 
 
 def fakequant_act(fmt, a):
-    """Activation fake-quant a_hat = bf16(fp32(q(fp32(a / s_a)) * s_a)); identity for w4a16."""
+    """Activation fake-quant a_hat = bf16(fp32(q(fp32(a / s_a)) * s_a)); identity without one."""
     a = np.asarray(a, dtype=np.float64)
-    if fmt == FMT_INT4_G128:
+    kind = ACT_Q[fmt]
+    if kind is None:
         return a.copy()
     s = act_scale(fmt, a)
-    return _dequant(q_fmt(fmt, _quotient(a, s)), s)
+    return _dequant(Q_FUNC[kind](_quotient(a, s)), s)
 
 
 def lsq_factor(fmt, x):

@@ -21,7 +21,7 @@ import math
 
 import torch
 
-FMT_NVFP4, FMT_INT4_G128, FMT_FP8_ROW = 0, 1, 2
+FMT_NVFP4, FMT_INT4_G128, FMT_FP8_ROW, FMT_NVFP4A16, FMT_W8A8, FMT_W4AFP8 = 0, 1, 2, 3, 4, 5
 
 WORKLOADS = {
     "tiny_nvfp4": dict(E=4, d=256, F=128, topk=2, T=512, fmt=FMT_NVFP4, routing="uniform", outliers=0.0),
@@ -35,9 +35,11 @@ WORKLOADS = {
                         outliers=0.001),
 }
 
-# elements per weight scale along K, and the divisor that turns a block amax into a scale
-_BLOCK = {FMT_NVFP4: 16, FMT_INT4_G128: 128}
-_QMAX = {FMT_NVFP4: 6.0, FMT_INT4_G128: 7.0, FMT_FP8_ROW: 448.0}
+# elements per weight scale along K (absent: one per row), and the divisor that turns a
+# block amax into a scale
+_BLOCK = {FMT_NVFP4: 16, FMT_INT4_G128: 128, FMT_NVFP4A16: 16, FMT_W4AFP8: 128}
+_QMAX = {FMT_NVFP4: 6.0, FMT_INT4_G128: 7.0, FMT_FP8_ROW: 448.0, FMT_NVFP4A16: 6.0, FMT_W8A8: 127.0,
+         FMT_W4AFP8: 7.0}
 
 
 def workload(name, **override):

@@ -125,6 +125,27 @@ def test_int4_bruteforce_nearest_even():
     assert np.array_equal(Q.q_int4(x), want)
 
 
+def test_int8_bruteforce_nearest_even():
+    rng = np.random.default_rng(40)
+    x = np.concatenate([rng.uniform(-140, 140, 20000), np.arange(-280, 281) / 2.0])
+    grid = np.arange(-128, 128, dtype=np.float64)
+    want = _brute_nearest(x, grid, grid % 2 == 0)
+    assert np.array_equal(Q.q_int8(x), want)
+
+
+def _grid(fmt):
+    """The weight grid of a format, enumerated (not computed by the quantizer)."""
+    kind = Q.WEIGHT_Q[fmt]
+    if kind == Q.Q_E2M1:
+        return Q.e2m1_decode(np.arange(16))
+    if kind == Q.Q_INT4:
+        return np.arange(-8, 8, dtype=np.float64)
+    if kind == Q.Q_INT8:
+        return np.arange(-128, 128, dtype=np.float64)
+    pos, _ = _e4m3_positive_grid()
+    return np.concatenate([pos, -pos])
+
+
 # ------------------------------------------------------------------------------ bf16 rounding
 
 def test_round_bf16_fp32_inputs_match_torch():
@@ -170,7 +191,7 @@ def _weights(fmt, E=2, N=8, K=256, seed=7, outliers=True):
     return bits, s.numpy()
 
 
-@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", Q.FORMATS)
 def test_fakequant_idempotent(fmt):
     bits, s = _weights(fmt)
     w1 = Q.fakequant_weight(fmt, bits, s)
@@ -179,19 +200,13 @@ def test_fakequant_idempotent(fmt):
     assert np.all(np.isfinite(w1))
 
 
-@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", Q.FORMATS)
 def test_fakequant_outputs_lie_on_scaled_grid(fmt):
     bits, s = _weights(fmt, N=4, K=128)
     what = Q.fakequant_weight(fmt, bits, s)
     K = bits.shape[-1]
     sf = np.repeat(s.astype(np.float64), Q.weight_block(fmt, K), axis=-1)
-    if fmt == Q.FMT_NVFP4:
-        grid = Q.e2m1_decode(np.arange(16))
-    elif fmt == Q.FMT_INT4_G128:
-        grid = np.arange(-8, 8, dtype=np.float64)
-    else:
-        pos, _ = _e4m3_positive_grid()
-        grid = np.concatenate([pos, -pos])
+    grid = _grid(fmt)
     # every output equals bf16(fp32(g * s)) for some g of the grid (enumerated, not computed by q)
     cand = Q.round_bf16(Q.round_f32(grid[None, :] * sf.reshape(-1)[:, None]))
     hit = (cand == what.reshape(-1)[:, None]).any(axis=1)
@@ -208,7 +223,7 @@ def test_fakequant_zero_scale_block_gives_signed_zero():
     assert np.array_equal(np.signbit(blk), np.signbit(w))
 
 
-@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", [f for f in Q.FORMATS if Q.ACT_Q[f] is not None])
 def test_act_fakequant_properties(fmt):
     rng = np.random.default_rng(8)
     a = Q.round_bf16(rng.standard_normal((6, 64)))
@@ -217,36 +232,36 @@ def test_act_fakequant_properties(fmt):
     assert np.all(np.isfinite(ah))
     assert np.all(ah[2, :16] == 0)
     # the block maximum maps to the top of the grid, so it is kept to bf16 accuracy
-    blk = 16 if fmt == Q.FMT_NVFP4 else 64
+    blk = 16 if Q.ACT_Q[fmt] == Q.Q_E2M1 else 64
     ab = np.abs(a).reshape(6, -1, blk)
     hb = np.abs(ah).reshape(6, -1, blk)
     i = ab.argmax(-1)
     amax = np.take_along_axis(ab, i[..., None], -1)[..., 0]
     hmax = np.take_along_axis(hb, i[..., None], -1)[..., 0]
     assert np.allclose(hmax, amax, rtol=2 ** -7, atol=0)
+    # the block maximum divided by its scale is the top of the grid (up to the fp32 scale rounding)
+    s_a = np.take_along_axis(Q.act_scale(fmt, a).reshape(6, -1, blk), i[..., None], -1)[..., 0]
+    top = Q.Q_CLIP[Q.ACT_Q[fmt]][1]
+    nz = amax > 0
+    assert np.allclose(amax[nz] / s_a[nz], top, rtol=1e-6, atol=0)
     # idempotent up to the dynamic scale being recomputed from the quantized block
     assert np.array_equal(Q.fakequant_act(fmt, ah), ah)
 
 
-def test_int4_has_no_activation_quant():
+@pytest.mark.parametrize("fmt", [f for f in Q.FORMATS if Q.ACT_Q[f] is None])
+def test_weight_only_formats_leave_activations_alone(fmt):
     a = Q.round_bf16(np.random.default_rng(9).standard_normal((3, 256)))
-    assert np.array_equal(Q.fakequant_act(Q.FMT_INT4_G128, a), a)
+    assert np.array_equal(Q.fakequant_act(fmt, a), a)
 
 
 # ------------------------------------------------------------------------------ LSQ factor
 
-@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", Q.FORMATS)
 def test_scale_grad_zero_for_weights_on_grid_points(fmt):
     E, N, K = 2, 4, 256
     B = Q.weight_block(fmt, K)
     rng = np.random.default_rng(10)
-    if fmt == Q.FMT_NVFP4:
-        grid = Q.e2m1_decode(np.arange(16))
-    elif fmt == Q.FMT_INT4_G128:
-        grid = np.arange(-8, 8, dtype=np.float64)
-    else:
-        pos, _ = _e4m3_positive_grid()
-        grid = np.concatenate([pos, -pos])
+    grid = _grid(fmt)
     s = 2.0 ** rng.integers(-8, -2, (E, N, K // B))        # powers of two: g * s exact in bf16
     g = rng.choice(grid, (E, N, K))
     lo, hi = Q.CLIP[fmt]
@@ -259,7 +274,7 @@ def test_scale_grad_zero_for_weights_on_grid_points(fmt):
     assert np.all(ds == 0.0)
 
 
-@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", Q.FORMATS)
 def test_lsq_factor_structure(fmt):
     lo, hi = Q.CLIP[fmt]
     rng = np.random.default_rng(11)
@@ -268,13 +283,7 @@ def test_lsq_factor_structure(fmt):
     inside = (x >= lo) & (x <= hi)
     assert np.all(phi[x < lo] == lo) and np.all(phi[x > hi] == hi)
     # inside the range x + phi is the quantized value: on the grid and the nearest grid point
-    if fmt == Q.FMT_NVFP4:
-        grid = Q.e2m1_decode(np.arange(16))
-    elif fmt == Q.FMT_INT4_G128:
-        grid = np.arange(-8, 8, dtype=np.float64)
-    else:
-        pos, _ = _e4m3_positive_grid()
-        grid = np.concatenate([pos, -pos])
+    grid = _grid(fmt)
     xin, qin = x[inside], x[inside] + phi[inside]
     assert np.isin(qin, grid).all()
     nearest = np.abs(xin[:, None] - grid[None, :]).min(1)
@@ -287,9 +296,10 @@ def _ste_fakequant_torch(fmt, w, s):
     lo, hi = Q.CLIP[fmt]
     xd = w / s
     x = xd + (xd.float().double() - xd).detach()          # the fp32 quotient, same slope
-    if fmt == Q.FMT_FP8_ROW:
+    kind = Q.WEIGHT_Q[fmt]
+    if kind == Q.Q_E4M3:
         qx = x.detach().float().to(torch.float8_e4m3fn).double()
-    elif fmt == Q.FMT_INT4_G128:
+    elif kind in (Q.Q_INT4, Q.Q_INT8):
         qx = torch.round(x.detach())                       # half to even
     else:
         grid = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64)
@@ -305,7 +315,7 @@ def _ste_fakequant_torch(fmt, w, s):
     return s * xq
 
 
-@pytest.mark.parametrize("fmt", [Q.FMT_NVFP4, Q.FMT_INT4_G128, Q.FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", Q.FORMATS)
 def test_scale_grad_matches_autograd_of_ste_definition(fmt):
     bits, s = _weights(fmt, E=2, N=4, K=256, seed=12)
     s = s * np.float32(0.7)                                 # push some weights past the clip bound
