@@ -32,7 +32,7 @@ import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "qwen3_30b_a3b_nvfp4"
 METRIC = "MoE-layer fwd+bwd tokens/s (nvfp4, 1 GB300); % HBM / tensor-core roofline"
-FMT_NAME = {0: "nvfp4", 1: "w4a16", 2: "fp8"}
+FMT_NAME = {0: "nvfp4", 1: "w4a16", 2: "fp8", 3: "nvfp4a16", 4: "w8a8", 5: "w4afp8"}
 
 
 def _dist():
@@ -112,7 +112,8 @@ def algorithmic_per_launch(cfg):
     d, F, E = cfg["d"], cfg["F"], cfg["E"]
     fc1 = 2.0 * R * 2 * F * d
     fc2 = 2.0 * R * d * F
-    bpe = {0: 2 + 4.0 / 16 + 2, 1: 2 + 4.0 / 128 + 2, 2: None}[cfg["fmt"]]
+    bpe = {0: 2 + 4.0 / 16 + 2, 1: 2 + 4.0 / 128 + 2, 2: None, 3: 2 + 4.0 / 16 + 2, 4: None,
+           5: 2 + 4.0 / 128 + 2}[cfg["fmt"]]
     n13, n2 = E * 2 * F * d, E * d * F
     if bpe is None:  # one fp32 scale per row
         fq = (4.0 * n13 + 4 * E * 2 * F + 4.0 * n2 + 4 * E * d) / 2

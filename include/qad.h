@@ -58,14 +58,20 @@ typedef enum {
   QAD_ERR_SCRATCH_LIMIT = -6 /* larger than the fixed scratch of qad_route_permute_noalloc */
 } qad_status;
 
-/* Weight formats (the pages' format names) */
+/* Formats: the pages' names ("MCoreQAD Backend", Support Matrix: nvfp4, nvfp4a16, w4a16,
+ * w8a8, fp8, w4afp8).  The element grids, scale granularity and activation scales are
+ * readings of those names (the pages give no formula). */
 typedef enum {
   QAD_FMT_NVFP4 = 0,     /* nvfp4 W4A4: E2M1 weights, one fp32 scale per 16 along K;
                             activations E2M1 with dynamic per-16 scale amax/6 */
   QAD_FMT_INT4_G128 = 1, /* w4a16: INT4 {-8..7} weights, one fp32 scale per 128 along K;
                             activations stay bf16 */
-  QAD_FMT_FP8_ROW = 2    /* fp8 W8A8: E4M3 weights, one fp32 scale per output row;
+  QAD_FMT_FP8_ROW = 2,   /* fp8 W8A8: E4M3 weights, one fp32 scale per output row;
                             activations E4M3 with dynamic per-row scale amax/448 */
+  QAD_FMT_NVFP4A16 = 3,  /* nvfp4a16: E2M1 weights as nvfp4; activations stay bf16 */
+  QAD_FMT_W8A8 = 4,      /* w8a8: INT8 {-128..127} weights, one fp32 scale per output row;
+                            activations INT8 with dynamic per-row scale amax/127 */
+  QAD_FMT_W4AFP8 = 5     /* w4afp8: INT4 weights as w4a16; activations E4M3 per row, amax/448 */
 } qad_fmt;
 
 /* Bits of the device error word */
@@ -99,9 +105,9 @@ typedef struct {
  * Weight fake-quant of a stack of E matrices [N, K] (article section 二.3/二.4: the whole
  * expert stack in one vectorised pass).
  *   w      bf16 [E, N, K] row-major (read only)
- *   scale  fp32 [E, N, K / B] with B = 16 (nvfp4), 128 (int4), K (fp8 per row)
+ *   scale  fp32 [E, N, K / B] with B = 16 (E2M1 formats), 128 (INT4 formats), K (fp8, w8a8)
  *   w_hat  bf16 [E, N, K] (written; may not overlap w)
- * Requires K % 16 == 0 (nvfp4, fp8) or K % 128 == 0 (int4), scales >= 0 and finite.
+ * Requires K % 16 == 0 (K % 128 == 0 for the INT4 formats), scales >= 0 and finite.
  * Output is bit-exact: w_hat = bf16(fp32(q(fp32(w / s)) * s)).
  */
 int qad_fakequant_fwd(int fmt, const void* w, const float* scale, void* w_hat,
@@ -168,7 +174,7 @@ enum {
   QAD_VIEW_W2_HAT = 7,     /* bf16 [E, d, F] */
   QAD_VIEW_A1 = 8,         /* bf16 [Rmax, d] */
   QAD_VIEW_Z1 = 9,         /* bf16 [Rmax, 2F] */
-  QAD_VIEW_H = 10,         /* bf16 [Rmax, F] (QAD_FLAG_STASH_H, or fp8) */
+  QAD_VIEW_H = 10,         /* bf16 [Rmax, F] (QAD_FLAG_STASH_H, or per-row activation grids) */
   QAD_VIEW_H_HAT = 11,     /* bf16 [Rmax, F] */
   QAD_VIEW_Y = 12,         /* bf16 [Rmax, d] */
   QAD_VIEW_DY = 13,        /* bf16 [Rmax, d] */

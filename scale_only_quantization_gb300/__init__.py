@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libqad_gb300.so")
 QAD_OK, QAD_ERR_INVALID_ARG, QAD_ERR_UNSUPPORTED, QAD_ERR_WORKSPACE, QAD_ERR_CUDA, QAD_ERR_DEVICE = 0, -1, -2, -3, -4, -5
 QAD_ERR_SCRATCH_LIMIT = -6
 QAD_NOALLOC_MAX_EXPERTS, QAD_NOALLOC_MAX_PAIRS = 256, 262144
-QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW = 0, 1, 2
+QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW, QAD_FMT_NVFP4A16, QAD_FMT_W8A8, QAD_FMT_W4AFP8 = range(6)
 QAD_DEV_BAD_INDEX, QAD_DEV_DUP_INDEX, QAD_DEV_TIMEOUT = 1, 2, 4
 QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT = 1, 2
 VIEWS = ["HEADER", "OFFSETS", "COUNTS", "ROW_TOKEN", "ROW_SLOT", "ROW_OF", "W13_HAT", "W2_HAT", "A1", "Z1", "H",

@@ -14,6 +14,7 @@
 #include <mutex>
 #include <vector>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace qad {
@@ -89,7 +90,7 @@ void prof_end(int id, cudaStream_t st) {
 
 int layout_of(const qad_moe_shape& s, Layout* L) {
   if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
-  if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_FP8_ROW) return QAD_ERR_INVALID_ARG;
+  if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_W4AFP8) return QAD_ERR_INVALID_ARG;
   if (s.reserved != 0 || (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT))) return QAD_ERR_INVALID_ARG;
   if (s.d % 256 || s.F % 128) return QAD_ERR_UNSUPPORTED;
   if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
@@ -156,15 +157,16 @@ int check_layer(const qad_moe_shape* s, void* ws, size_t ws_bytes, Layout* L) {
 bool ok_ptr(const void* p) { return p && aligned16(p); }
 
 // GEMM context of one call.  With QAD_FLAG_NO_QUANT the GEMMs read the caller's raw weights
-// and the fc1 epilogue applies no activation quantizer (the w4a16 path, whose activations
-// stay bf16); otherwise they read the fake-quantized copies the forward wrote.
+// and the fc1 epilogue applies no activation quantizer; otherwise they read the
+// fake-quantized copies the forward wrote.
 GemmCtx gemm_ctx(const Layout& L, uint8_t* wsb, const qad_moe_shape& s, const void* w13, const void* w2,
                  cudaStream_t st) {
   const bool no_quant = (s.flags & QAD_FLAG_NO_QUANT) != 0;
   GemmCtx c;
   c.L = &L;
   c.ws = wsb;
-  c.fmt = no_quant ? QAD_FMT_INT4_G128 : s.fmt;
+  c.wq = weight_kind(s.fmt);
+  c.aq = no_quant ? kQNone : act_kind(s.fmt);
   c.flags = s.flags;
   c.st = st;
   c.w13h = no_quant ? w13 : static_cast<const void*>(wsb + L.w13h);
@@ -191,9 +193,9 @@ const char* qad_status_string(int status) {
 
 int qad_fakequant_fwd(int fmt, const void* w, const float* scale, void* w_hat, int64_t E, int64_t N, int64_t K,
                       qad_stream_t stream) {
-  if (fmt < QAD_FMT_NVFP4 || fmt > QAD_FMT_FP8_ROW) return QAD_ERR_INVALID_ARG;
+  if (fmt < QAD_FMT_NVFP4 || fmt > QAD_FMT_W4AFP8) return QAD_ERR_INVALID_ARG;
   if (E < 0 || N < 0 || K <= 0) return QAD_ERR_INVALID_ARG;
-  if (K % 16 || (fmt == QAD_FMT_INT4_G128 && K % 128)) return QAD_ERR_UNSUPPORTED;
+  if (K % 16 || (weight_kind(fmt) == kQInt4 && K % 128)) return QAD_ERR_UNSUPPORTED;
   if (E * N == 0) return QAD_OK;
   if (!ok_ptr(w) || !ok_ptr(scale) || !ok_ptr(w_hat)) return QAD_ERR_INVALID_ARG;
   return to_status(launch_fakequant(fmt, w, scale, w_hat, E * N, K, reinterpret_cast<cudaStream_t>(stream)));
@@ -226,17 +228,16 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
     QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st));
   }
   const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
-  if (no_quant || fmt == QAD_FMT_INT4_G128) {
+  GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
+  if (c.aq == kQNone) {
     QAD_TRY(launch_gather_rows(x, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
   } else {
-    QAD_TRY(launch_act_quant_rows(fmt, x, wsb + L.xq, L.T, L.d, nullptr, st));
+    QAD_TRY(launch_act_quant_rows(c.aq, x, wsb + L.xq, L.T, L.d, nullptr, st));
     QAD_TRY(launch_gather_rows(wsb + L.xq, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
   }
-  GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
   QAD_TRY(gemm_prepare(c));
   QAD_TRY(gemm_fc1(c));
-  if (!no_quant && fmt == QAD_FMT_FP8_ROW)
-    QAD_TRY(launch_act_quant_rows(fmt, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
+  if (row_scaled(c.aq)) QAD_TRY(launch_act_quant_rows(c.aq, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
   QAD_TRY(gemm_fc2(c));
   QAD_TRY(launch_combine(wsb + L.y, reinterpret_cast<const int32_t*>(wsb + L.row_of), topk_w, out, L.T, (int)L.k,
                          L.d, st));

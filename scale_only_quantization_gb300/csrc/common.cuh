@@ -1,11 +1,16 @@
 // Device helpers shared by the kernels of the scale-only QAD MoE library (sm_103a).
 //
-// Quantizer readings (the pages name the formats but print no formula):
-//   nvfp4  - E2M1 grid {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}, round to nearest even,
-//            saturating (PTX cvt.rn.satfinite.e2m1x2.f32), one fp32 scale per 16 along K;
-//   w4a16  - INT4 grid {-8..7}: rintf (half to even) then clamp, one scale per 128 along K;
-//   fp8    - E4M3 (max 448), round to nearest even, saturating (cvt.rn.satfinite.e4m3x2.f32),
-//            one scale per output row.
+// Quantizer readings (the pages name the formats but print no formula).  Element grids:
+//   E2M1 - {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}, round to nearest even, saturating
+//          (PTX cvt.rn.satfinite.e2m1x2.f32); weight scale per 16 along K, activations
+//          per 16 with amax / 6;
+//   INT4 - {-8..7}: rintf (half to even) then clamp; weight scale per 128 along K;
+//   E4M3 - max 448, round to nearest even, saturating (cvt.rn.satfinite.e4m3x2.f32);
+//          weight scale per output row, activations per row with amax / 448;
+//   INT8 - {-128..127}: rintf then clamp; weight scale per output row, activations per row
+//          with amax / 127.
+// Formats: nvfp4 = E2M1/E2M1, w4a16 = INT4/bf16, fp8 = E4M3/E4M3, nvfp4a16 = E2M1/bf16,
+// w8a8 = INT8/INT8, w4afp8 = INT4/E4M3 (weights/activations).
 // x = w / s is the IEEE fp32 quotient (__fdiv_rn); the dequantized value is
 // bf16(fp32(q(x) * s)); s == 0 gives x = +-0 with the sign of w.
 // Formats: "MCoreQAD Backend" (mcore_qad.md), Support Matrix; AngelSlim mcore_qad
@@ -21,9 +26,24 @@
 
 namespace qad {
 
-constexpr int kFmtNvfp4 = QAD_FMT_NVFP4;
-constexpr int kFmtInt4 = QAD_FMT_INT4_G128;
-constexpr int kFmtFp8 = QAD_FMT_FP8_ROW;
+// element grids ("quantizer kinds")
+constexpr int kQNone = -1, kQE2M1 = 0, kQInt4 = 1, kQE4M3 = 2, kQInt8 = 3;
+
+// weight and activation grids of each public format (qad_fmt)
+__host__ __device__ constexpr int weight_kind(int fmt) {
+  return fmt == QAD_FMT_NVFP4 || fmt == QAD_FMT_NVFP4A16   ? kQE2M1
+         : fmt == QAD_FMT_INT4_G128 || fmt == QAD_FMT_W4AFP8 ? kQInt4
+         : fmt == QAD_FMT_FP8_ROW                            ? kQE4M3
+                                                             : kQInt8;
+}
+__host__ __device__ constexpr int act_kind(int fmt) {
+  return fmt == QAD_FMT_NVFP4                              ? kQE2M1
+         : fmt == QAD_FMT_FP8_ROW || fmt == QAD_FMT_W4AFP8 ? kQE4M3
+         : fmt == QAD_FMT_W8A8                             ? kQInt8
+                                                           : kQNone;
+}
+// a scale per whole row (E4M3, INT8) rather than per block along K
+__host__ __device__ constexpr bool row_scaled(int kind) { return kind == kQE4M3 || kind == kQInt8; }
 
 // ---------------------------------------------------------------------------------- bf16
 
@@ -68,25 +88,33 @@ __device__ __forceinline__ float2 q_e4m3x2(float a, float b) {
 }
 
 __device__ __forceinline__ float q_int4(float x) { return fminf(fmaxf(rintf(x), -8.0f), 7.0f); }
+__device__ __forceinline__ float q_int8(float x) { return fminf(fmaxf(rintf(x), -128.0f), 127.0f); }
 
-template <int FMT>
-__device__ __forceinline__ float2 q_pair(float a, float b) {
-  float2 r;
-  if constexpr (FMT == kFmtNvfp4) {
-    r = q_e2m1x2(a, b);
-  } else if constexpr (FMT == kFmtFp8) {
-    r = q_e4m3x2(a, b);
+template <int QK>
+__device__ __forceinline__ float2 q_pair_raw(float a, float b) {
+  if constexpr (QK == kQE2M1) {
+    return q_e2m1x2(a, b);
+  } else if constexpr (QK == kQE4M3) {
+    return q_e4m3x2(a, b);
+  } else if constexpr (QK == kQInt4) {
+    return make_float2(q_int4(a), q_int4(b));
   } else {
-    r = make_float2(q_int4(a), q_int4(b));
+    return make_float2(q_int8(a), q_int8(b));
   }
+}
+
+template <int QK>
+__device__ __forceinline__ float2 q_pair(float a, float b) {
+  const float2 r = q_pair_raw<QK>(a, b);
   // the grid value keeps the sign of its input, also when it rounds to zero
   return make_float2(copysignf(r.x, a), copysignf(r.y, b));
 }
 
-template <int FMT> struct Clip;
-template <> struct Clip<kFmtNvfp4> { static constexpr float lo = -6.0f, hi = 6.0f; };
-template <> struct Clip<kFmtInt4> { static constexpr float lo = -8.0f, hi = 7.0f; };
-template <> struct Clip<kFmtFp8> { static constexpr float lo = -448.0f, hi = 448.0f; };
+template <int QK> struct Clip;
+template <> struct Clip<kQE2M1> { static constexpr float lo = -6.0f, hi = 6.0f; };
+template <> struct Clip<kQInt4> { static constexpr float lo = -8.0f, hi = 7.0f; };
+template <> struct Clip<kQE4M3> { static constexpr float lo = -448.0f, hi = 448.0f; };
+template <> struct Clip<kQInt8> { static constexpr float lo = -128.0f, hi = 127.0f; };
 
 // x = fp32(w / s); s == 0 -> +-0 with the sign of w (IEEE division, the reference path)
 __device__ __forceinline__ float quotient(float w, float s) {
@@ -145,7 +173,7 @@ __device__ __forceinline__ bool scale_in_fast_range(float s) { return s >= 0x1p-
 
 // Activation fake-quant of n values sharing the dynamic scale s = fp32(amax / Qmax): |x| <=
 // amax / s stays near Qmax, so no overflow is possible; the sign of a zero result is w's.
-template <int FMT, int N>
+template <int QK, int N>
 __device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
   float x[N];
   if (scale_in_fast_range(s)) {
@@ -158,7 +186,7 @@ __device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
   }
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
-    const float2 q = q_pair<FMT>(x[i], x[i + 1]);
+    const float2 q = q_pair<QK>(x[i], x[i + 1]);
     v[i] = round_bf16(__fmul_rn(q.x, s));
     v[i + 1] = round_bf16(__fmul_rn(q.y, s));
   }
@@ -168,7 +196,7 @@ __device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
 // Weights are arbitrary, so besides the block's scale range the quotients are checked for
 // overflow through one NaN/inf-propagating sum (an overflowing fast quotient gives inf or
 // NaN); a block that fails is recomputed with the per-element guarded form.
-template <int FMT, int N>
+template <int QK, int N>
 __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
   float x[N];
   bool fast = scale_in_fast_range(s);
@@ -185,7 +213,7 @@ __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
   if (!fast) quotients<N>(v, s, x);
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
-    const float2 q = q_pair<FMT>(x[i], x[i + 1]);
+    const float2 q = q_pair<QK>(x[i], x[i + 1]);
     v[i] = round_bf16(__fmul_rn(q.x, s));
     v[i + 1] = round_bf16(__fmul_rn(q.y, s));
   }
@@ -195,23 +223,16 @@ __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
 // violated bound.  q saturates (E2M1, E4M3) or clamps (INT4) to exactly that bound
 // outside the range, so phi = q(x) - (x inside ? x : 0).  The sign of a zero q does not
 // matter here, so the grid value is used as the conversion returns it.
-template <int FMT>
+template <int QK>
 __device__ __forceinline__ float2 lsq_pair(float xa, float xb) {
-  float2 q;
-  if constexpr (FMT == kFmtNvfp4) {
-    q = q_e2m1x2(xa, xb);
-  } else if constexpr (FMT == kFmtFp8) {
-    q = q_e4m3x2(xa, xb);
-  } else {
-    q = make_float2(q_int4(xa), q_int4(xb));
-  }
+  const float2 q = q_pair_raw<QK>(xa, xb);
   float ia, ib;
-  if constexpr (FMT == kFmtInt4) {
-    ia = (xa >= Clip<FMT>::lo && xa <= Clip<FMT>::hi) ? xa : 0.0f;
-    ib = (xb >= Clip<FMT>::lo && xb <= Clip<FMT>::hi) ? xb : 0.0f;
+  if constexpr (QK == kQInt4 || QK == kQInt8) {
+    ia = (xa >= Clip<QK>::lo && xa <= Clip<QK>::hi) ? xa : 0.0f;
+    ib = (xb >= Clip<QK>::lo && xb <= Clip<QK>::hi) ? xb : 0.0f;
   } else {  // symmetric clip range
-    ia = fabsf(xa) <= Clip<FMT>::hi ? xa : 0.0f;
-    ib = fabsf(xb) <= Clip<FMT>::hi ? xb : 0.0f;
+    ia = fabsf(xa) <= Clip<QK>::hi ? xa : 0.0f;
+    ib = fabsf(xb) <= Clip<QK>::hi ? xb : 0.0f;
   }
   return make_float2(q.x - ia, q.y - ib);
 }

@@ -28,7 +28,7 @@ int grid_for(int64_t items, int threads, int per_sm) {
 
 // One thread per 16 consecutive elements of a row (16 | K, and every scale block is a
 // whole number of 16-element chunks).  `cps` = chunks per scale (1, 8 or K / 16).
-template <int FMT>
+template <int QK>
 __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict__ w, const float* __restrict__ s,
                                                         uint4* __restrict__ out, uint64_t nchunks, uint32_t cps) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -42,12 +42,12 @@ __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict_
     float v[16];
     unpack8(u0, v);
     unpack8(u1, v + 8);
-    fakequant_inplace<FMT, 16>(v, sc);
+    fakequant_inplace<QK, 16>(v, sc);
     st_stream(out + 2 * c, pack8(v));
     st_stream(out + 2 * c + 1, pack8(v + 8));
     unpack8(u2, v);
     unpack8(u3, v + 8);
-    fakequant_inplace<FMT, 16>(v, sc2);
+    fakequant_inplace<QK, 16>(v, sc2);
     st_stream(out + 2 * c2, pack8(v));
     st_stream(out + 2 * c2 + 1, pack8(v + 8));
   }
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict_
     float v[16];
     unpack8(u0, v);
     unpack8(u1, v + 8);
-    fakequant_inplace<FMT, 16>(v, sc);
+    fakequant_inplace<QK, 16>(v, sc);
     st_stream(out + 2 * c, pack8(v));
     st_stream(out + 2 * c + 1, pack8(v + 8));
   }
@@ -218,14 +218,15 @@ __global__ void __launch_bounds__(256) act_quant_nvfp4_kernel(const uint4* __res
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    fakequant_act_inplace<kFmtNvfp4, 16>(v, __fdiv_rn(amax, 6.0f));
+    fakequant_act_inplace<kQE2M1, 16>(v, __fdiv_rn(amax, 6.0f));
     out[2 * b] = pack8(v);
     out[2 * b + 1] = pack8(v + 8);
   }
 }
 
-// fp8: one warp per row, scale fp32(row amax / 448)
-__global__ void __launch_bounds__(256) act_quant_fp8_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+// E4M3 / INT8: one warp per row, scale fp32(row amax / 448) or fp32(row amax / 127)
+template <int QK>
+__global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
                                                             int64_t rows, int64_t cols, const int32_t* dev_rows) {
   const int64_t nrows = dev_rows ? (int64_t)*dev_rows : rows;
   const int lane = threadIdx.x & 31;
@@ -241,11 +242,11 @@ __global__ void __launch_bounds__(256) act_quant_fp8_kernel(const uint4* __restr
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
     }
     amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 448.0f);
+    const float s = __fdiv_rn(amax, QK == kQE4M3 ? 448.0f : 127.0f);
     for (int64_t c = lane; c < c8; c += 32) {
       float v[8];
       unpack8(src[c], v);
-      fakequant_act_inplace<kFmtFp8, 8>(v, s);
+      fakequant_act_inplace<QK, 8>(v, s);
       out[r * c8 + c] = pack8(v);
     }
   }
@@ -429,12 +430,11 @@ cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, 
   const uint4* wi = static_cast<const uint4*>(w);
   uint4* o = static_cast<uint4*>(out);
   prof_begin(QAD_K_FAKEQUANT, st);
-  if (fmt == kFmtNvfp4) {
-    fakequant_kernel<kFmtNvfp4><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 1u);
-  } else if (fmt == kFmtInt4) {
-    fakequant_kernel<kFmtInt4><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 8u);
-  } else {
-    fakequant_kernel<kFmtFp8><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16));
+  switch (weight_kind(fmt)) {
+    case kQE2M1: fakequant_kernel<kQE2M1><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 1u); break;
+    case kQInt4: fakequant_kernel<kQInt4><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 8u); break;
+    case kQE4M3: fakequant_kernel<kQE4M3><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16)); break;
+    default: fakequant_kernel<kQInt8><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16)); break;
   }
   prof_end(QAD_K_FAKEQUANT, st);
   return cudaGetLastError();
@@ -482,15 +482,18 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_act_quant_rows(int fmt, const void* in, void* out, int64_t rows, int64_t cols,
+cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   prof_begin(QAD_K_ACT_QUANT, st);
-  if (fmt == kFmtNvfp4) {
+  if (kind == kQE2M1) {
     act_quant_nvfp4_kernel<<<grid_for(rows * (cols / 16), 256, 8), 256, 0, st>>>(
         static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
+  } else if (kind == kQE4M3) {
+    act_quant_row_kernel<kQE4M3><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
   } else {
-    act_quant_fp8_kernel<<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
+    act_quant_row_kernel<kQInt8><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
         static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
   }
   prof_end(QAD_K_ACT_QUANT, st);

@@ -62,7 +62,7 @@ struct Params {
   int num_kb;                   // rows mode: K / 64
   int b_rows;                   // rows of the B tensor map per expert
   int F;                        // expert FFN width (fc1 / SwiGLU epilogues)
-  int fmt, flags;
+  int wq, aq, flags;  // weight grid (LSQ), activation grid of the fc1 epilogue (kQNone: none)
   __nv_bfloat16* out;  int64_t ld_out;   // STORE: out; FC1: Z1; SWIGLU_BWD: dZ1
   __nv_bfloat16* out2; int64_t ld_out2;  // FC1: H_hat
   __nv_bfloat16* out3;                   // FC1: H (same leading dimension as out2)
@@ -277,16 +277,17 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t, uint32_t rank) {
 // ---------------------------------------------------------------------------------- epilogues
 
 // Z1 (bf16) and H = bf16(silu(gate) * up) for 64 of the tile's 128 FFN columns (this warp's
-// half), 16 at a time (one activation-quant block); H_hat = AQ(H) for nvfp4, = H for
-// w4a16; fp8 needs the row amax over all F columns, so H goes to the H buffer and a
-// separate pass quantizes it.
+// half), 16 at a time (one activation-quant block); H_hat = AQ(H) for the E2M1 (per 16)
+// activation grid, = H without activation quant; the per-row grids (E4M3, INT8) need the
+// row amax over all F columns, so H goes to the H buffer and a separate pass quantizes it.
 template <int BN>
 __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
   const int64_t row = ti.row_base + row_in_tile;
   __nv_bfloat16* z1 = p.out + row * p.ld_out;
   __nv_bfloat16* hrow = p.out3 + row * p.ld_out2;
   __nv_bfloat16* hhrow = p.out2 + row * p.ld_out2;
-  const bool stash_h = (p.flags & QAD_FLAG_STASH_H) || p.fmt == kFmtFp8;
+  const bool row_aq = row_scaled(p.aq);
+  const bool stash_h = (p.flags & QAD_FLAG_STASH_H) || row_aq;
   const int c0 = 64 * half;  // first of this warp's 64 columns within the tile's 128
   uint32_t g[16], u[16], gn[16], un[16];
   tmem_ld16_issue(tbase + c0, g);
@@ -318,12 +319,12 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_
       hs[0] = pack8(h);
       hs[1] = pack8(h + 8);
     }
-    if (p.fmt != kFmtFp8) {
-      if (p.fmt == kFmtNvfp4) {
+    if (!row_aq) {
+      if (p.aq == kQE2M1) {
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[i]));
-        fakequant_act_inplace<kFmtNvfp4, 16>(h, __fdiv_rn(amax, 6.0f));
+        fakequant_act_inplace<kQE2M1, 16>(h, __fdiv_rn(amax, 6.0f));
       }
       uint4* hh = reinterpret_cast<uint4*>(hhrow + f0);
       hh[0] = pack8(h);
@@ -427,7 +428,7 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, 
 // tiles) each column half writes its partial sum to
 // part[ds_index * parts + (tile in block) * 2 + half] and a reduction kernel adds the
 // parts in a fixed order.
-template <int FMT>
+template <int QK>
 __device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const uint4 (&wraw)[2], float sc) {
   float wv[16], x[16];
   unpack8(wraw[0], wv);
@@ -437,7 +438,7 @@ __device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const 
     quotients_unguarded<16>(wv, sc, x);
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      const float2 ph = lsq_pair<FMT>(x[i], x[i + 1]);
+      const float2 ph = lsq_pair<QK>(x[i], x[i + 1]);
       t = fmaf(__uint_as_float(acc[i]), ph.x, t);
       t = fmaf(__uint_as_float(acc[i + 1]), ph.y, t);
     }
@@ -447,7 +448,7 @@ __device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const 
     t = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      const float2 ph = lsq_pair<FMT>(x[i], x[i + 1]);
+      const float2 ph = lsq_pair<QK>(x[i], x[i + 1]);
       t = fmaf(__uint_as_float(acc[i]), ph.x, t);
       t = fmaf(__uint_as_float(acc[i + 1]), ph.y, t);
     }
@@ -455,7 +456,7 @@ __device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const 
   return t;
 }
 
-template <int BN, int FMT>
+template <int BN, int QK>
 __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                                   int half) {
   constexpr int STEPS = BN / 32;  // 16-column steps per half (= nvfp4 scales per half)
@@ -464,13 +465,13 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
   const int col0 = half * (BN / 2);
   const int64_t k_first = (int64_t)ti.nb * BN + col0;
   const __nv_bfloat16* wr = p.w + wrow * p.w_cols + k_first;
-  constexpr bool kDirectGroups = (FMT == kFmtInt4) && (BN == 256);
+  constexpr bool kDirectGroups = (QK == kQInt4) && (BN == 256);
   const bool have_acc = ti.nkb > 0;
 
   // scales of this half row
   float sv[STEPS];
   float* ds_vec = nullptr;
-  if constexpr (FMT == kFmtNvfp4) {
+  if constexpr (QK == kQE2M1) {
     const int64_t sidx = wrow * (p.w_cols / 16) + k_first / 16;  // a multiple of 4
     const float4* sp = reinterpret_cast<const float4*>(p.s + sidx);
 #pragma unroll
@@ -480,7 +481,7 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
     }
     ds_vec = p.ds + sidx;
   } else {
-    const float sc = (FMT == kFmtInt4) ? __ldg(p.s + wrow * (p.w_cols / 128) + k_first / 128) : __ldg(p.s + wrow);
+    const float sc = (QK == kQInt4) ? __ldg(p.s + wrow * (p.w_cols / 128) + k_first / 128) : __ldg(p.s + wrow);
 #pragma unroll
     for (int i = 0; i < STEPS; ++i) sv[i] = sc;
   }
@@ -508,7 +509,7 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
       wq[(j + 2) % 3][1] = __ldg(reinterpret_cast<const uint4*>(wr) + 2 * (j + 2) + 1);
     }
     if (have_acc && j + 1 < STEPS) tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
-    tsum[j] = lsq_block_sum<FMT>(r, wq[j % 3], sv[j]);
+    tsum[j] = lsq_block_sum<QK>(r, wq[j % 3], sv[j]);
     if (j + 1 < STEPS && have_acc) {
       tmem_wait16(rn);
 #pragma unroll
@@ -516,7 +517,7 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
     }
   }
 
-  if constexpr (FMT == kFmtNvfp4) {
+  if constexpr (QK == kQE2M1) {
     float4* dv = reinterpret_cast<float4*>(ds_vec);
 #pragma unroll
     for (int i = 0; i < STEPS / 4; ++i) {
@@ -535,7 +536,7 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
       float* dst = p.ds + wrow * (p.w_cols / 128) + k_first / 128;
       *dst = p.accumulate ? *dst + sum : sum;
     } else {
-      const int64_t B = (FMT == kFmtInt4) ? 128 : p.w_cols;  // elements per scale
+      const int64_t B = (QK == kQInt4) ? 128 : p.w_cols;  // elements per scale
       const int tiles_per_block = (int)(B / BN);
       const int64_t ds_index = wrow * (p.w_cols / B) + ((int64_t)ti.nb * BN) / B;
       p.part[ds_index * (2 * tiles_per_block) + (ti.nb % tiles_per_block) * 2 + half] = sum;
@@ -553,9 +554,10 @@ __device__ __forceinline__ void run_epilogue(const Params& p, const Tile& ti, ui
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
     epi_swiglu_bwd<BN>(p, ti, tbase, row_in_tile, half);
   } else {
-    if (p.fmt == kFmtNvfp4) epi_scalegrad_fmt<BN, kFmtNvfp4>(p, ti, tbase, row_in_tile, half);
-    else if (p.fmt == kFmtInt4) epi_scalegrad_fmt<BN, kFmtInt4>(p, ti, tbase, row_in_tile, half);
-    else epi_scalegrad_fmt<BN, kFmtFp8>(p, ti, tbase, row_in_tile, half);
+    if (p.wq == kQE2M1) epi_scalegrad_fmt<BN, kQE2M1>(p, ti, tbase, row_in_tile, half);
+    else if (p.wq == kQInt4) epi_scalegrad_fmt<BN, kQInt4>(p, ti, tbase, row_in_tile, half);
+    else if (p.wq == kQE4M3) epi_scalegrad_fmt<BN, kQE4M3>(p, ti, tbase, row_in_tile, half);
+    else epi_scalegrad_fmt<BN, kQInt8>(p, ti, tbase, row_in_tile, half);
   }
 }
 
@@ -861,7 +863,8 @@ Params base_params(const GemmCtx& c) {
   p.poff = at<int32_t>(c.ws, L.offs);
   p.E = (int)L.E;
   p.F = (int)L.F;
-  p.fmt = c.fmt;
+  p.wq = c.wq;
+  p.aq = c.aq;
   p.flags = c.flags;
   return p;
 }
@@ -974,8 +977,8 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   cudaError_t e = bn == 256 ? launch<256, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st)
                             : launch<128, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st);
   if (e != cudaSuccess) return e;
-  if (c.fmt == kFmtFp8 || (c.fmt == kFmtInt4 && bn == 128)) {
-    const int64_t B = c.fmt == kFmtInt4 ? 128 : k_w;  // elements per scale
+  if (row_scaled(c.wq) || (c.wq == kQInt4 && bn == 128)) {
+    const int64_t B = c.wq == kQInt4 ? 128 : k_w;  // elements per scale
     return launch_scale_reduce(p.part, ds, L.E * m_w * (k_w / B), (int)(2 * (B / bn)), accumulate, c.st);
   }
   return cudaSuccess;

@@ -43,8 +43,9 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
                               int32_t* chunk_counts, int32_t* chunk_base, int32_t* counts, int32_t* offs,
                               int32_t* mtile_expert, int32_t* row_token, int32_t* row_slot, int32_t* row_of,
                               cudaStream_t st);
-// out[r, :] = AQ(in[r, :]) for r < rows (or < *dev_rows when dev_rows != nullptr)
-cudaError_t launch_act_quant_rows(int fmt, const void* in, void* out, int64_t rows, int64_t cols,
+// out[r, :] = AQ(in[r, :]) with activation grid `kind` (kQE2M1: per 16, kQE4M3 / kQInt8: per
+// row) for r < rows (or < *dev_rows when dev_rows != nullptr)
+cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st);
 // dst[r, :] = src[row_token[r], :], zeros where row_token[r] < 0, for r < *dev_rows
 cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* row_token, int64_t rmax, int64_t cols,
@@ -69,7 +70,8 @@ cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, f
 struct GemmCtx {
   const Layout* L;
   uint8_t* ws;
-  int fmt, flags;  // fmt selects the activation quantizer of the fc1 epilogue and the LSQ grid
+  int wq, aq;  // weight grid (LSQ factor) and activation grid of the fc1 epilogue (kQNone: none)
+  int flags;
   cudaStream_t st;
   const void* w13h;  // the weights the GEMMs read: the fake-quantized copies in the workspace,
   const void* w2h;   // or the caller's raw weights for the unquantized teacher pass

@@ -13,6 +13,9 @@ Workloads, named by what they are:
   qwen3_30b_a3b_fp8     same shapes, fp8 W8A8 per-row, Zipf(1.2) expert popularity
   large_nvfp4           E=256, d=4096, F=1536, top-8, 32768 tokens, nvfp4, 0.1% outliers
 
+Any workload can be run in another format with workload(name, fmt=...): 3 nvfp4a16,
+4 w8a8, 5 w4afp8.
+
 The MoE-layer shapes follow the Qwen3-MoE model family that the pages support
 ("MCoreQAD Backend", Support Matrix) and its example run (seq_len 2048, micro-batch
 8); the hidden states are N(0, 1) stand-ins for the pages' random-token inputs.

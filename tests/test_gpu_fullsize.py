@@ -19,7 +19,9 @@ from gpu_util import Run, assert_close, assert_scale_grad, bits, host_inputs, un
 
 pytestmark = pytest.mark.gpu
 
-WORKLOADS = ["qwen3_30b_a3b_nvfp4", "qwen3_30b_a3b_w4a16", "qwen3_30b_a3b_fp8", "large_nvfp4"]
+WORKLOADS = ["qwen3_30b_a3b_nvfp4", "qwen3_30b_a3b_w4a16", "qwen3_30b_a3b_fp8", "large_nvfp4",
+             # the remaining formats of the support matrix on the same Qwen3-30B-A3B shapes
+             "qwen3_30b_a3b_nvfp4:3", "qwen3_30b_a3b_nvfp4:4", "qwen3_30b_a3b_nvfp4:5"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,7 +44,8 @@ def _expert_w(run, name, e, n, k):
 
 @pytest.mark.parametrize("name", WORKLOADS)
 def test_full_size_sampled(name):
-    cfg = synth.workload(name)
+    base, _, fmt_override = name.partition(":")
+    cfg = synth.workload(base, **({"fmt": int(fmt_override)} if fmt_override else {}))
     inp = synth.make_inputs(cfg, seed=0, device="cuda")
     fmt, T, d, F, E, k = inp["fmt"], inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"]
     run = Run(inp, flags=Q.QAD_FLAG_STASH_H)

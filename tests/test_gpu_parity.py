@@ -19,7 +19,8 @@ from gpu_util import Run, assert_close, assert_scale_grad, bits, host_inputs, un
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW]
+FMTS = [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8,
+        Q.QAD_FMT_W4AFP8]
 
 
 @pytest.fixture(scope="module", autouse=True)
