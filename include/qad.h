@@ -236,6 +236,16 @@ int qad_route_permute_noalloc(const int32_t* topk_idx, int64_t T, int32_t topk, 
                               int32_t* counts, int32_t* header, qad_stream_t stream);
 
 /*
+ * Self-check of the failure path (not an operation of the method).  Every pipeline wait of
+ * the GEMM kernels is bounded; when one expires the kernel sets QAD_DEV_TIMEOUT in the
+ * workspace error word, drains what it issued and returns instead of hanging.  This
+ * launches one warp that runs that same bounded-wait routine on a barrier nothing ever
+ * arrives on, with a budget of `budget_cycles` SM clock cycles (<= 2e9), and ORs
+ * QAD_DEV_TIMEOUT into *err_word (device int32) when it gives up.
+ */
+int qad_debug_wait_timeout(int32_t* err_word, int64_t budget_cycles, qad_stream_t stream);
+
+/*
  * Self-check of the division inside the quantizers (not an operation of the method).
  * The kernels compute x = fp32(w / s) from the correctly rounded reciprocal of s and one
  * FMA correction (Markstein's theorem) instead of a division per element.  For each i

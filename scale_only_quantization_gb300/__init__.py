@@ -27,7 +27,7 @@ KERNELS = 14
 EXPORTS = ["qad_fakequant_fwd", "qad_moe_workspace_bytes", "qad_moe_fwd", "qad_moe_bwd_dgrad",
            "qad_moe_bwd_scalegrad", "qad_check_device_error", "qad_status_string", "qad_moe_debug_view",
            "qad_profile_enable", "qad_profile_reset", "qad_profile_read", "qad_kernel_name", "qad_launch_count",
-           "qad_debug_quotient", "qad_route_permute_noalloc"]
+           "qad_debug_quotient", "qad_route_permute_noalloc", "qad_debug_wait_timeout"]
 
 
 class QADError(RuntimeError):
@@ -74,6 +74,7 @@ def lib():
             "qad_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
             "qad_launch_count": (ctypes.c_int64, []),
             "qad_debug_quotient": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int32, _P]),
+            "qad_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
             "qad_route_permute_noalloc": (ctypes.c_int, [_P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P,
                                                          _P, _P, _P]),
         }
@@ -190,6 +191,11 @@ def qad_route_permute_noalloc(topk_idx, T, topk, E, row_token, row_slot, row_of,
     return _check(lib().qad_route_permute_noalloc(_ptr(topk_idx), int(T), int(topk), int(E), _ptr(row_token),
                                                   _ptr(row_slot), _ptr(row_of), _ptr(offsets), _ptr(counts),
                                                   _ptr(header), _stream(stream)), "qad_route_permute_noalloc")
+
+
+def qad_debug_wait_timeout(err_word, budget_cycles, stream=None):
+    return _check(lib().qad_debug_wait_timeout(_ptr(err_word), int(budget_cycles), _stream(stream)),
+                  "qad_debug_wait_timeout")
 
 
 def workspace_view(ws, s, which, dtype):

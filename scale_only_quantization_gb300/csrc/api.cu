@@ -376,6 +376,11 @@ const char* qad_kernel_name(int id) {
 
 int64_t qad_launch_count(void) { return g_launch_total.load(); }
 
+int qad_debug_wait_timeout(int32_t* err_word, int64_t budget_cycles, qad_stream_t stream) {
+  if (!err_word || budget_cycles < 0 || budget_cycles > 2000000000LL) return QAD_ERR_INVALID_ARG;
+  return to_status(launch_wait_selftest(err_word, budget_cycles, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int qad_debug_quotient(const float* w, const float* s, float* x_fast, float* x_ieee, int64_t n, int32_t mode,
                        qad_stream_t stream) {
   if (n < 0 || mode < 0 || mode > 1) return QAD_ERR_INVALID_ARG;

@@ -66,6 +66,35 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
 }
 
+// ---------------------------------------------------------------------------------- f32x2
+// Blackwell's packed fp32 arithmetic: two independent lanes per instruction, each rounded
+// to nearest even exactly as the scalar instruction would.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return make_float2(a, b);
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // ---------------------------------------------------------------------------------- quantizers
 
 // E2M1 rounding of two values; returns the decoded grid values (exact in fp32).
@@ -162,11 +191,20 @@ __device__ __forceinline__ void quotients(const float* w, float s, float* x) {
 template <int N>
 __device__ __forceinline__ void quotients_unguarded(const float* w, float s, float* x) {
   const float r = __frcp_rn(s);
+  const uint64_t r2 = f2pack(r, r), ns2 = f2pack(-s, -s);
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const float q = __fmul_rn(w[i], r);
-    const float e = __fmaf_rn(-q, s, w[i]);
-    x[i] = __fmaf_rn(e, r, q);
+  for (int i = 0; i + 1 < N; i += 2) {  // q = w r, e = w - q s, x = q + e r, two lanes at a time
+    const uint64_t w2 = f2pack(w[i], w[i + 1]);
+    const uint64_t q2 = f2mul(w2, r2);
+    const uint64_t e2 = f2fma(q2, ns2, w2);
+    const float2 x2 = f2unpack(f2fma(e2, r2, q2));
+    x[i] = x2.x;
+    x[i + 1] = x2.y;
+  }
+  if constexpr (N & 1) {
+    const float q = __fmul_rn(w[N - 1], r);
+    const float e = __fmaf_rn(-q, s, w[N - 1]);
+    x[N - 1] = __fmaf_rn(e, r, q);
   }
 }
 __device__ __forceinline__ bool scale_in_fast_range(float s) { return s >= 0x1p-60f && s <= 0x1p60f; }

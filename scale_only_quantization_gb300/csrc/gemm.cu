@@ -100,8 +100,10 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with parity `parity` of barrier `bar`.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+// Bounded wait for the phase with parity `parity` of barrier `bar`: gives up after `budget`
+// clock cycles (or as soon as another role of the CTA gave up), raising QAD_DEV_TIMEOUT.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                      long long budget = kWaitCycles) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -109,12 +111,27 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     for (int i = 0; i < 64; ++i)
       if (mbar_try(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > budget) {
       *abort_flag = 1;
       atomicOr(err, QAD_DEV_TIMEOUT);
       return false;
     }
   }
+}
+
+// Self-check of the timeout path: one thread waits, with the GEMMs' own bounded-wait routine,
+// on a barrier that nothing ever arrives on.  It must give up after `budget` cycles and
+// raise QAD_DEV_TIMEOUT in *err; nothing faults or hangs.
+__global__ void wait_selftest_kernel(int32_t* err, long long budget) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err, budget);
 }
 
 // TMA tile load into this CTA's shared memory; the bytes complete on `bar`, a shared::cluster
@@ -436,12 +453,23 @@ __device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const 
   float t = 0.0f;
   if (scale_in_fast_range(sc)) {
     quotients_unguarded<16>(wv, sc, x);
+    uint64_t t2 = f2pack(0.0f, 0.0f);  // two partial sums, one per lane
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      const float2 ph = lsq_pair<QK>(x[i], x[i + 1]);
-      t = fmaf(__uint_as_float(acc[i]), ph.x, t);
-      t = fmaf(__uint_as_float(acc[i + 1]), ph.y, t);
+      const float2 q = q_pair_raw<QK>(x[i], x[i + 1]);
+      float ia, ib;  // x inside the closed clip range, else 0 (q is then the violated bound)
+      if constexpr (QK == kQInt4 || QK == kQInt8) {
+        ia = (x[i] >= Clip<QK>::lo && x[i] <= Clip<QK>::hi) ? x[i] : 0.0f;
+        ib = (x[i + 1] >= Clip<QK>::lo && x[i + 1] <= Clip<QK>::hi) ? x[i + 1] : 0.0f;
+      } else {
+        ia = fabsf(x[i]) <= Clip<QK>::hi ? x[i] : 0.0f;
+        ib = fabsf(x[i + 1]) <= Clip<QK>::hi ? x[i + 1] : 0.0f;
+      }
+      const uint64_t ph2 = f2sub(f2pack(q.x, q.y), f2pack(ia, ib));
+      t2 = f2fma(f2pack(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1])), ph2, t2);
     }
+    const float2 tt = f2unpack(t2);
+    t = tt.x + tt.y;
   }
   if (!scale_in_fast_range(sc) || !isfinite(t)) {  // rare: extreme scale or an overflowing quotient
     quotients<16>(wv, sc, x);
@@ -872,6 +900,11 @@ Params base_params(const GemmCtx& c) {
 inline int pick_bn(int64_t n) { return n % 256 == 0 ? 256 : 128; }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(int32_t* err, int64_t budget_cycles, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(err, (long long)budget_cycles);
+  return cudaGetLastError();
+}
 
 cudaError_t gemm_prepare(const GemmCtx& c) {
   const Layout& L = *c.L;

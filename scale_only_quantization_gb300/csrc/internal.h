@@ -67,6 +67,8 @@ cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, f
                                   cudaStream_t st);
 
 // ---- grouped GEMMs (gemm.cu) ----
+// the GEMMs' bounded mbarrier wait on a barrier nothing arrives on; sets QAD_DEV_TIMEOUT in *err
+cudaError_t launch_wait_selftest(int32_t* err, int64_t budget_cycles, cudaStream_t st);
 struct GemmCtx {
   const Layout* L;
   uint8_t* ws;

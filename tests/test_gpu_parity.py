@@ -394,3 +394,21 @@ def test_teacher_pass_without_quantizers(fmt):
     da1 = rows("DA1", d)
     assert_close(da1, OM.grouped_gemm_nn(dz1, w13, off), "teacher dA1")
     assert_close(vals(dx), OM.combine(da1, np.ones((T, k)), row_of), "teacher dx")
+
+
+# ------------------------------------------------------------------------------ failure path
+
+def test_bounded_wait_reports_timeout_and_leaves_the_context_usable():
+    """The GEMMs' bounded mbarrier wait, on a barrier nothing arrives on with a ~0.5 ms budget,
+    gives up and raises QAD_DEV_TIMEOUT; the device keeps working afterwards."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.qad_debug_wait_timeout(err, 1_000_000)
+    torch.cuda.synchronize()
+    assert int(err.item()) == Q.QAD_DEV_TIMEOUT
+    # the context is intact: a normal call still runs and is still bit exact
+    w, s = _special_weights(1, 8, 256, Q.QAD_FMT_NVFP4, seed=5)
+    out = torch.empty_like(w)
+    Q.qad_fakequant_fwd(Q.QAD_FMT_NVFP4, w, s, out, 1, 8, 256)
+    torch.cuda.synchronize()
+    want = OQ.f64_to_bf16_bits(OQ.fakequant_weight(Q.QAD_FMT_NVFP4, bits(w), synth.to_numpy(s)))
+    assert np.array_equal(bits(out), want)
