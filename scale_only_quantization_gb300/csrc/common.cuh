@@ -94,6 +94,11 @@ __device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // ---------------------------------------------------------------------------------- quantizers
 
@@ -287,6 +292,13 @@ __device__ __forceinline__ float rcp_approx(float v) {
 }
 __device__ __forceinline__ float sigmoid_f(float g) { return rcp_approx(1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return __fmul_rn(g, sigmoid_f(g)); }
+
+// sigmoid of two lanes: the exponentials by the intrinsic, the +1 in packed fp32.
+__device__ __forceinline__ uint64_t sigmoid2(uint64_t g2) {
+  const float2 g = f2unpack(g2);
+  const float2 d = f2unpack(f2add(f2pack(__expf(-g.x), __expf(-g.y)), f2pack(1.0f, 1.0f)));
+  return f2pack(rcp_approx(d.x), rcp_approx(d.y));
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -323,7 +323,13 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_
     for (int i = 0; i < 16; ++i) {
       gv[i] = round_bf16(__uint_as_float(g[i]));
       uv[i] = round_bf16(__uint_as_float(u[i]));
-      h[i] = round_bf16(__fmul_rn(silu_f(gv[i]), uv[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {  // H = silu(g) u, two lanes at a time
+      const uint64_t g2 = f2pack(gv[i], gv[i + 1]);
+      const float2 hv = f2unpack(f2mul(f2mul(g2, sigmoid2(g2)), f2pack(uv[i], uv[i + 1])));
+      h[i] = round_bf16(hv.x);
+      h[i + 1] = round_bf16(hv.y);
     }
     uint4* zg = reinterpret_cast<uint4*>(z1 + f0);
     uint4* zu = reinterpret_cast<uint4*>(z1 + p.F + f0);
@@ -419,13 +425,18 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, 
     unpack8(z[j % 3][2], u);
     unpack8(z[j % 3][3], u + 8);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float dh = __uint_as_float(r[i]);
-      const float sg = sigmoid_f(g[i]);
-      const float dgi = dh * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
-      const float dui = dh * g[i] * sg;
-      g[i] = dgi;
-      u[i] = dui;
+    for (int i = 0; i < 16; i += 2) {  // two lanes at a time
+      const uint64_t one2 = f2pack(1.0f, 1.0f);
+      const uint64_t g2 = f2pack(g[i], g[i + 1]);
+      const uint64_t sg2 = sigmoid2(g2);
+      const uint64_t t2 = f2mul(f2pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sg2);  // dh sig
+      const uint64_t inner2 = f2fma(g2, f2sub(one2, sg2), one2);                                   // 1 + g (1 - sig)
+      const float2 dgv = f2unpack(f2mul(f2mul(t2, f2pack(u[i], u[i + 1])), inner2));
+      const float2 duv = f2unpack(f2mul(t2, g2));
+      g[i] = dgv.x;
+      g[i + 1] = dgv.y;
+      u[i] = duv.x;
+      u[i + 1] = duv.y;
     }
     store16(dz1 + f0, g);
     store16(dz1 + p.F + f0, u);
