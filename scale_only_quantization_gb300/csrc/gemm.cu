@@ -63,9 +63,8 @@ struct Params {
   int b_rows;                   // rows of the B tensor map per expert
   int F;                        // expert FFN width (fc1 / SwiGLU epilogues)
   int wq, aq, flags;  // weight grid (LSQ), activation grid of the fc1 epilogue (kQNone: none)
-  __nv_bfloat16* out;  int64_t ld_out;   // STORE: out; FC1: Z1; SWIGLU_BWD: dZ1
-  __nv_bfloat16* out2; int64_t ld_out2;  // FC1: H_hat
-  __nv_bfloat16* out3;                   // FC1: H (same leading dimension as out2)
+  __nv_bfloat16* out3; int64_t ld_out2;  // FC1: H, kept besides H_hat with QAD_FLAG_STASH_H
+  // (the tiles the epilogues produce are written through the kernel's store tensor maps)
   const __nv_bfloat16* aux; int64_t ld_aux;  // SWIGLU_BWD: Z1
   const __nv_bfloat16* w;  const float* s;   // SCALEGRAD: raw weights [E, Mw, Kw] and scales
   int64_t w_rows, w_cols;
@@ -81,6 +80,17 @@ template <int BN> struct Cfg {
   static constexpr int SMEM = RING + 256 + 1024;  // + barriers, + alignment slack
   static constexpr int TMEM_COLS = 2 * BN;
 };
+
+// Shared memory that the epilogues stage their bf16 outputs in for TMA stores: 4 KB per
+// epilogue warp.  The plain store uses it as two 32-row x 32-column boxes (64-byte swizzle),
+// the fc1 and SwiGLU-backward epilogues as a ring of four 32-row x 16-column boxes
+// (32-byte swizzle).  The scale-gradient epilogue writes no tiles.
+constexpr int kStageBox = 32 * 32 * 2;
+constexpr int kStageWarp = 4096;
+template <int EPI> __host__ __device__ constexpr int staging_bytes() {
+  return EPI == EPI_SCALEGRAD ? 0 : (kEpiThreads / 32) * kStageWarp;
+}
+template <int BN, int EPI> __host__ __device__ constexpr int smem_bytes() { return Cfg<BN>::SMEM + staging_bytes<EPI>(); }
 
 // ---------------------------------------------------------------------------------- PTX
 
@@ -142,6 +152,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "%3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+// TMA tile store from this CTA's shared memory (bulk-group completion, tracked per thread)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's bulk groups still read shared memory
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until all of this thread's bulk groups have completed (writes done)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// make this thread's shared-memory writes visible to the TMA (async proxy)
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 // shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
@@ -243,16 +273,6 @@ __device__ __forceinline__ void tmem_wait16x2(uint32_t (&a)[16], uint32_t (&b)[1
   asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]) :: "memory");
 }
 
-__device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = pack8(v + 8 * i);
-}
-__device__ __forceinline__ void store16(__nv_bfloat16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = pack8(v);
-  d[1] = pack8(v + 8);
-}
 
 // ---------------------------------------------------------------------------------- tiles
 
@@ -293,18 +313,46 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t, uint32_t rank) {
 
 // ---------------------------------------------------------------------------------- epilogues
 
+// A warp's ring of four 1 KB staging boxes, each 32 rows x 16 bf16 columns in the 32-byte
+// swizzle (thread = row; its two 16-byte chunks c at c ^ ((row >> 2) & 1), which keeps the
+// shared-memory writes free of bank conflicts).  Every box is its own bulk group, so a slot
+// is rewritten once the store issued from it four boxes earlier has read it.
+struct BoxRing {
+  uint32_t base;  // this warp's 4 KB
+  uint32_t slot;
+};
+__device__ __forceinline__ void store_box16(BoxRing& ring, const CUtensorMap* tm, int lane, const float* v, int x,
+                                            int y) {
+  const uint32_t box = ring.base + ring.slot * 1024u;
+  if (lane == 0) bulk_wait_read<3>();
+  __syncwarp();
+  const uint32_t row = (uint32_t)lane * 32u, sw = ((uint32_t)lane >> 2) & 1u;
+  st_shared_v4(box + row + (sw << 4), pack8(v));
+  st_shared_v4(box + row + ((sw ^ 1u) << 4), pack8(v + 8));
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm, box, x, y);
+    bulk_commit();
+  }
+  ring.slot = (ring.slot + 1u) & 3u;
+}
+
 // Z1 (bf16) and H = bf16(silu(gate) * up) for 64 of the tile's 128 FFN columns (this warp's
 // half), 16 at a time (one activation-quant block); H_hat = AQ(H) for the E2M1 (per 16)
 // activation grid, = H without activation quant; the per-row grids (E4M3, INT8) need the
 // row amax over all F columns, so H goes to the H buffer and a separate pass quantizes it.
 template <int BN>
-__device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
+__device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z1, const CUtensorMap* tm_h,
+                                        const Tile& ti, uint32_t tbase, int q, int lane, int half, BoxRing& ring) {
+  const int row_in_tile = q * 32 + lane;
   const int64_t row = ti.row_base + row_in_tile;
-  __nv_bfloat16* z1 = p.out + row * p.ld_out;
+  const int y = (int)ti.row_base + 32 * q;
   __nv_bfloat16* hrow = p.out3 + row * p.ld_out2;
-  __nv_bfloat16* hhrow = p.out2 + row * p.ld_out2;
   const bool row_aq = row_scaled(p.aq);
-  const bool stash_h = (p.flags & QAD_FLAG_STASH_H) || row_aq;
+  // tm_h is the H_hat map, or the H map for the per-row activation grids (whose H_hat is
+  // made by a separate pass); with QAD_FLAG_STASH_H and a per-block grid H is also kept.
+  const bool extra_h = (p.flags & QAD_FLAG_STASH_H) && !row_aq;
   const int c0 = 64 * half;  // first of this warp's 64 columns within the tile's 128
   uint32_t g[16], u[16], gn[16], un[16];
   tmem_ld16_issue(tbase + c0, g);
@@ -331,28 +379,20 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_
       h[i] = round_bf16(hv.x);
       h[i + 1] = round_bf16(hv.y);
     }
-    uint4* zg = reinterpret_cast<uint4*>(z1 + f0);
-    uint4* zu = reinterpret_cast<uint4*>(z1 + p.F + f0);
-    zg[0] = pack8(gv);
-    zg[1] = pack8(gv + 8);
-    zu[0] = pack8(uv);
-    zu[1] = pack8(uv + 8);
-    if (stash_h) {
+    store_box16(ring, tm_z1, lane, gv, f0, y);
+    store_box16(ring, tm_z1, lane, uv, p.F + f0, y);
+    if (extra_h) {
       uint4* hs = reinterpret_cast<uint4*>(hrow + f0);
       hs[0] = pack8(h);
       hs[1] = pack8(h + 8);
     }
-    if (!row_aq) {
-      if (p.aq == kQE2M1) {
-        float amax = 0.0f;
+    if (p.aq == kQE2M1) {
+      float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[i]));
-        fakequant_act_inplace<kQE2M1, 16>(h, __fdiv_rn(amax, 6.0f));
-      }
-      uint4* hh = reinterpret_cast<uint4*>(hhrow + f0);
-      hh[0] = pack8(h);
-      hh[1] = pack8(h + 8);
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[i]));
+      fakequant_act_inplace<kQE2M1, 16>(h, __fdiv_rn(amax, 6.0f));
     }
+    store_box16(ring, tm_h, lane, h, f0, y);
     if (j < 3) {
       tmem_wait16x2(gn, un);
 #pragma unroll
@@ -364,36 +404,55 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const Tile& ti, uint32_
   }
 }
 
-// bf16 store of this warp's half of the tile: all its TMEM loads are issued at once, then
-// one wait (a single TMEM latency per tile instead of one per chunk).
+// bf16 store of this warp's 32 rows x BN/2 columns: all its TMEM loads are issued at once,
+// then one wait; each 32-column chunk is written into one of the warp's two staging boxes
+// (thread = row, 16-byte chunk c of the 64-byte row at position c ^ ((row >> 1) & 3), the
+// 64-byte swizzle, which also keeps the shared-memory writes free of bank conflicts) and
+// one lane stores the box with TMA.  A box is rewritten only after the TMA store issued
+// from it two chunks earlier has read it.
 template <int BN>
-__device__ __forceinline__ void epi_store(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile, int half) {
-  const int64_t row = ti.row_base + row_in_tile;
+__device__ __forceinline__ void epi_store(const CUtensorMap* tmC, const Tile& ti, uint32_t tbase, int q, int lane,
+                                          int half, uint32_t stage_base, uint32_t& buf) {
   constexpr int NH = BN / 64;  // 32-column chunks per half: 4 or 2
   const int c0 = half * NH;
-  __nv_bfloat16* dst = p.out + row * p.ld_out + (int64_t)ti.nb * BN + 32 * c0;
   uint32_t r[NH][32];
 #pragma unroll
   for (int c = 0; c < NH; ++c) tmem_ld32_issue(tbase + 32 * (c0 + c), r[c]);
 #pragma unroll
   for (int c = 0; c < NH; ++c) tmem_wait32(r[c]);
+  const int y = (int)ti.row_base + 32 * q;
+  const uint32_t row_addr = (uint32_t)lane * 64u;
+  const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
 #pragma unroll
   for (int c = 0; c < NH; ++c) {
-    float v[32];
+    const uint32_t box = stage_base + buf * kStageBox;
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c][i]);
-    store32(dst + 32 * c, v);
+    for (int ch = 0; ch < 4; ++ch) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[c][8 * ch + i]);
+      st_shared_v4(box + row_addr + ((((uint32_t)ch) ^ sw) << 4), pack8(v));
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, box, ti.nb * BN + 32 * (c0 + c), y);
+      bulk_commit();
+    }
+    buf ^= 1u;
   }
 }
 
 // dZ1 = [dH * up * sig(g) * (1 + g (1 - sig(g))), dH * g * sig(g)] from the stored bf16 Z1,
 // 16 columns at a time; the Z1 loads run two steps ahead, the TMEM loads one step ahead.
 template <int BN>
-__device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
-                                               int half) {
-  const int64_t row = ti.row_base + row_in_tile;
+__device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const CUtensorMap* tm_dz1, const Tile& ti,
+                                               uint32_t tbase, int q, int lane, int half, BoxRing& ring) {
+  const int64_t row = ti.row_base + q * 32 + lane;
+  const int y = (int)ti.row_base + 32 * q;
   const __nv_bfloat16* z1 = p.aux + row * p.ld_aux;
-  __nv_bfloat16* dz1 = p.out + row * p.ld_out;
   constexpr int STEPS = BN / 32;  // 16-column steps per half
   const int col0 = half * (BN / 2);
   const int f_first = ti.nb * BN + col0;
@@ -438,8 +497,8 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const Tile& ti, 
       u[i] = duv.x;
       u[i + 1] = duv.y;
     }
-    store16(dz1 + f0, g);
-    store16(dz1 + p.F + f0, u);
+    store_box16(ring, tm_dz1, lane, g, f0, y);
+    store_box16(ring, tm_dz1, lane, u, p.F + f0, y);
     if (j + 1 < STEPS) {
       tmem_wait16(rn);
 #pragma unroll
@@ -583,16 +642,10 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
   }
 }
 
-template <int BN, int EPI>
-__device__ __forceinline__ void run_epilogue(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
+template <int BN>
+__device__ __forceinline__ void run_scalegrad(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                              int half) {
-  if constexpr (EPI == EPI_FC1) {
-    epi_fc1<BN>(p, ti, tbase, row_in_tile, half);
-  } else if constexpr (EPI == EPI_STORE) {
-    epi_store<BN>(p, ti, tbase, row_in_tile, half);
-  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-    epi_swiglu_bwd<BN>(p, ti, tbase, row_in_tile, half);
-  } else {
+  {
     if (p.wq == kQE2M1) epi_scalegrad_fmt<BN, kQE2M1>(p, ti, tbase, row_in_tile, half);
     else if (p.wq == kQInt4) epi_scalegrad_fmt<BN, kQInt4>(p, ti, tbase, row_in_tile, half);
     else if (p.wq == kQE4M3) epi_scalegrad_fmt<BN, kQE4M3>(p, ti, tbase, row_in_tile, half);
@@ -605,6 +658,7 @@ __device__ __forceinline__ void run_epilogue(const Params& p, const Tile& ti, ui
 template <int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const Params p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
@@ -613,7 +667,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a_ring = smem_u32(smem);
   const uint32_t b_ring = a_ring + STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING);
+  const uint32_t stage_out = a_ring + C::RING;  // EPI_STORE: the epilogue warps' staging boxes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING + staging_bytes<EPI>());
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -762,18 +817,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t buf = 0;
+    const uint32_t my_stage = stage_out + (uint32_t)(warp - 2) * (uint32_t)kStageWarp;
+    BoxRing ring{my_stage, 0u};
+    if constexpr (EPI != EPI_SCALEGRAD) tma_prefetch_desc(&tmC);
+    if constexpr (EPI == EPI_FC1) tma_prefetch_desc(&tmD);
     for (int t = first; t < total; t += step) {
       const Tile ti = tile_of(p, t, rank);
       const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      if (ti.live) run_epilogue<BN, EPI>(p, ti, tbase, row_in_tile, half);
+      if (ti.live) {
+        if constexpr (EPI == EPI_STORE) epi_store<BN>(&tmC, ti, tbase, q, lane, half, my_stage, buf);
+        else if constexpr (EPI == EPI_FC1) epi_fc1<BN>(p, &tmC, &tmD, ti, tbase, q, lane, half, ring);
+        else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<BN>(p, &tmC, ti, tbase, q, lane, half, ring);
+        else run_scalegrad<BN>(p, ti, tbase, row_in_tile, half);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(peer_addr(tempty_bar(acc), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+    }
+    if constexpr (EPI != EPI_SCALEGRAD) {
+      if (lane == 0) bulk_wait_all();  // the staged tiles are in global memory before the CTA exits
     }
   }
 
@@ -819,13 +887,28 @@ bool make_tmap(CUtensorMap* tm, const void* base, int64_t inner, int64_t outer, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output map of a staged epilogue: [outer, inner] bf16, box {cols, 32} with cols = 32 (64-byte
+// swizzle) or 16 (32-byte swizzle)
+bool make_store_tmap(CUtensorMap* tm, void* base, int64_t inner, int64_t outer, int64_t ld, int cols = 32) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)cols, 32u};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, bool A_MN, bool B_MN, int EPI>
-cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int64_t max_tiles, int kid,
-                   cudaStream_t st) {
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& td,
+                   const Params& p, int64_t max_tiles, int kid, cudaStream_t st) {
   auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+  constexpr int SMEM = smem_bytes<BN, EPI>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  static int max_pairs[64] = {0};
+  static int max_pairs[64] = {0};  // per device (one instantiation of this function per kernel)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
@@ -834,7 +917,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.dynamicSmemBytes = SMEM;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
@@ -845,7 +928,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p
   int64_t pairs = max_tiles < max_pairs[dev] ? max_tiles : max_pairs[dev];
   if (pairs < 1) return cudaSuccess;
   prof_begin(kid, st);
-  kern<<<(unsigned)(2 * pairs), kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, p);
+  kern<<<(unsigned)(2 * pairs), kThreads, SMEM, st>>>(ta, tb, tc, td, p);
   prof_end(kid, st);
   return cudaGetLastError();
 }
@@ -934,12 +1017,13 @@ cudaError_t gemm_fc1(const GemmCtx& c) {
   p.n_ntiles = (int)(L.F / 128);
   p.num_kb = (int)(L.d / BK);
   p.b_rows = (int)(2 * L.F);
-  p.out = at<__nv_bfloat16>(c.ws, L.z1);
-  p.ld_out = 2 * L.F;
-  p.out2 = at<__nv_bfloat16>(c.ws, L.hh);
   p.ld_out2 = L.F;
   p.out3 = at<__nv_bfloat16>(c.ws, L.h);
-  return launch<256, false, false, EPI_FC1>(ta, tb, p, (L.Rmax / BM) * (int64_t)p.n_ntiles, QAD_K_GEMM_FC1, c.st);
+  CUtensorMap tz, th;
+  if (!make_store_tmap(&tz, c.ws + L.z1, 2 * L.F, L.Rmax, 2 * L.F, 16)) return cudaErrorInvalidValue;
+  if (!make_store_tmap(&th, c.ws + (row_scaled(c.aq) ? L.h : L.hh), L.F, L.Rmax, L.F, 16)) return cudaErrorInvalidValue;
+  return launch<256, false, false, EPI_FC1>(ta, tb, tz, th, p, (L.Rmax / BM) * (int64_t)p.n_ntiles, QAD_K_GEMM_FC1,
+                                            c.st);
 }
 
 cudaError_t gemm_fc2(const GemmCtx& c) {
@@ -952,11 +1036,11 @@ cudaError_t gemm_fc2(const GemmCtx& c) {
   p.n_ntiles = (int)(L.d / bn);
   p.num_kb = (int)(L.F / BK);
   p.b_rows = (int)L.d;
-  p.out = at<__nv_bfloat16>(c.ws, L.y);
-  p.ld_out = L.d;
+  CUtensorMap tc;
+  if (!make_store_tmap(&tc, c.ws + L.y, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
-  return bn == 256 ? launch<256, false, false, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_FC2, c.st)
-                   : launch<128, false, false, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_FC2, c.st);
+  return bn == 256 ? launch<256, false, false, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st)
+                   : launch<128, false, false, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
 }
 
 cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
@@ -970,13 +1054,13 @@ cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
   p.n_ntiles = (int)(L.F / bn);
   p.num_kb = (int)(L.d / BK);
   p.b_rows = (int)L.d;
-  p.out = at<__nv_bfloat16>(c.ws, L.dz1);
-  p.ld_out = 2 * L.F;
   p.aux = at<__nv_bfloat16>(c.ws, L.z1);
   p.ld_aux = 2 * L.F;
+  CUtensorMap tz;
+  if (!make_store_tmap(&tz, c.ws + L.dz1, 2 * L.F, L.Rmax, 2 * L.F, 16)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
-  return bn == 256 ? launch<256, false, true, EPI_SWIGLU_BWD>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st)
-                   : launch<128, false, true, EPI_SWIGLU_BWD>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st);
+  return bn == 256 ? launch<256, false, true, EPI_SWIGLU_BWD>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st)
+                   : launch<128, false, true, EPI_SWIGLU_BWD>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st);
 }
 
 cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
@@ -990,11 +1074,11 @@ cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
   p.n_ntiles = (int)(L.d / bn);
   p.num_kb = (int)(2 * L.F / BK);
   p.b_rows = (int)(2 * L.F);
-  p.out = at<__nv_bfloat16>(c.ws, L.da1);
-  p.ld_out = L.d;
+  CUtensorMap tc;
+  if (!make_store_tmap(&tc, c.ws + L.da1, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
-  return bn == 256 ? launch<256, false, true, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st)
-                   : launch<128, false, true, EPI_STORE>(ta, tb, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st);
+  return bn == 256 ? launch<256, false, true, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st)
+                   : launch<128, false, true, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st);
 }
 
 namespace {
@@ -1018,8 +1102,8 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   p.part = at<float>(c.ws, part_off);
   p.accumulate = accumulate;
   const int64_t tiles = L.E * p.n_mtiles_w * p.n_ntiles;
-  cudaError_t e = bn == 256 ? launch<256, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st)
-                            : launch<128, true, true, EPI_SCALEGRAD>(ta, tb, p, tiles, kid, c.st);
+  cudaError_t e = bn == 256 ? launch<256, true, true, EPI_SCALEGRAD>(ta, tb, ta, ta, p, tiles, kid, c.st)
+                            : launch<128, true, true, EPI_SCALEGRAD>(ta, tb, ta, ta, p, tiles, kid, c.st);
   if (e != cudaSuccess) return e;
   if (row_scaled(c.wq) || (c.wq == kQInt4 && bn == 128)) {
     const int64_t B = c.wq == kQInt4 ? 128 : k_w;  // elements per scale
