@@ -229,12 +229,8 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
   }
   const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
-  if (c.aq == kQNone) {
-    QAD_TRY(launch_gather_rows(x, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
-  } else {
-    QAD_TRY(launch_act_quant_rows(c.aq, x, wsb + L.xq, L.T, L.d, nullptr, st));
-    QAD_TRY(launch_gather_rows(wsb + L.xq, wsb + L.a1, row_token, L.Rmax, L.d, rpad, st));
-  }
+  QAD_TRY(launch_scatter_tokens(c.aq, x, wsb + L.xq, wsb + L.a1, reinterpret_cast<const int32_t*>(wsb + L.row_of),
+                                row_token, L.T, (int)L.k, L.d, rpad, st));
   QAD_TRY(gemm_prepare(c));
   QAD_TRY(gemm_fc1(c));
   if (row_scaled(c.aq)) QAD_TRY(launch_act_quant_rows(c.aq, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
@@ -257,10 +253,9 @@ int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* top
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   int32_t* hdr = reinterpret_cast<int32_t*>(wsb + L.header);
   const int32_t* rpad = hdr + HDR_RPAD;
-  if (dprobs && L.R > 0) QAD_TRY(cudaMemsetAsync(dprobs, 0, sizeof(float) * L.R, st));
-  QAD_TRY(launch_dy_gather(dout, topk_w, reinterpret_cast<const int32_t*>(wsb + L.row_token),
-                           reinterpret_cast<const int32_t*>(wsb + L.row_slot), wsb + L.y, wsb + L.dy, dprobs, L.Rmax,
-                           (int)L.k, L.d, rpad, st));
+  QAD_TRY(launch_dy_scatter(dout, topk_w, reinterpret_cast<const int32_t*>(wsb + L.row_of),
+                            reinterpret_cast<const int32_t*>(wsb + L.row_token), wsb + L.y, wsb + L.dy, dprobs, L.T,
+                            (int)L.k, L.d, rpad, st));
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
   QAD_TRY(gemm_dgrad_fc2(c));
   QAD_TRY(gemm_dgrad_fc1(c));

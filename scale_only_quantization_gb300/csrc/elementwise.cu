@@ -205,25 +205,6 @@ __global__ void __launch_bounds__(32) route_scatter_kernel(const int32_t* __rest
 
 // ------------------------------------------------------------------------- activations
 
-// nvfp4: one thread per 16-element block, scale fp32(amax / 6)
-__global__ void __launch_bounds__(256) act_quant_nvfp4_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                                                              int64_t rows, int64_t cols, const int32_t* dev_rows) {
-  const int64_t nrows = dev_rows ? (int64_t)*dev_rows : rows;
-  const int64_t nblk = nrows * (cols / 16);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride) {
-    float v[16];
-    unpack8(in[2 * b], v);
-    unpack8(in[2 * b + 1], v + 8);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    fakequant_act_inplace<kQE2M1, 16>(v, __fdiv_rn(amax, 6.0f));
-    out[2 * b] = pack8(v);
-    out[2 * b + 1] = pack8(v + 8);
-  }
-}
-
 // E4M3 / INT8: one warp per row, scale fp32(row amax / 448) or fp32(row amax / 127)
 template <int QK>
 __global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
@@ -252,31 +233,107 @@ __global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restr
   }
 }
 
-// one warp per destination row
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                          const int32_t* __restrict__ row_token, int64_t c8,
-                                                          const int32_t* dev_rows) {
-  const int64_t nrows = *dev_rows;
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows; r += warps) {
-    const int32_t t = row_token[r];
-    uint4* d = dst + r * c8;
-    if (t < 0) {
-      for (int64_t c = lane; c < c8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
-    } else {
-      const uint4* s = src + (int64_t)t * c8;
-      int64_t c = lane;
-      for (; c + 96 < c8; c += 128) {  // four 16-byte loads in flight per lane
-        const uint4 a0 = __ldg(s + c), a1 = __ldg(s + c + 32), a2 = __ldg(s + c + 64), a3 = __ldg(s + c + 96);
-        d[c] = a0;
-        d[c + 32] = a1;
-        d[c + 64] = a2;
-        d[c + 96] = a3;
-      }
-      for (; c < c8; c += 32) d[c] = __ldg(s + c);
+// Zero the padding rows (row_token < 0) of a routed-row buffer below *dev_rpad: each warp
+// tests 32 rows at a time and clears the padding ones (c16 16-byte chunks per row).
+__device__ __forceinline__ void zero_pad_rows(uint4* __restrict__ dst, const int32_t* __restrict__ row_token,
+                                              int64_t c16, const int32_t* dev_rpad, int64_t w0, int64_t warps,
+                                              int lane) {
+  const int64_t rpad = *dev_rpad;
+  for (int64_t g = w0; g * 32 < rpad; g += warps) {
+    const int64_t r = g * 32 + lane;
+    const bool pad = r < rpad && __ldg(row_token + r) < 0;
+    unsigned m = __ballot_sync(0xffffffffu, pad);
+    while (m) {
+      const int i = __ffs(m) - 1;
+      m &= m - 1;
+      uint4* d = dst + (g * 32 + i) * c16;
+      for (int64_t c = lane; c < c16; c += 32) d[c] = make_uint4(0, 0, 0, 0);
     }
   }
+}
+
+constexpr int kScatterNB = 4;  // 16-element blocks per lane per pass over a row chunk
+
+// Forward gather, one warp per token: the token's row of x is read once, fake-quantized on
+// the activation grid (E2M1 per 16-element block with scale fp32(block amax / 6); E4M3 /
+// INT8 per row with fp32(row amax / 448) / fp32(row amax / 127); or not at all), written to
+// xq (when the grid quantizes) and to each routed row of the token; then the padding rows
+// are zeroed.  Lane l holds the 16-element blocks l, l + 32, ... of a 128 x 16-element
+// chunk of the row.
+template <int AQ>
+__global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __restrict__ x, uint4* __restrict__ xq,
+                                                             uint4* __restrict__ a1, const int32_t* __restrict__ row_of,
+                                                             const int32_t* __restrict__ row_token, int64_t T, int k,
+                                                             int64_t nblk, const int32_t* dev_rpad) {
+  constexpr int NB = kScatterNB;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  for (int64_t t = w0; t < T; t += warps) {
+    const int32_t my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
+    const uint4* src = x + t * nblk * 2;
+    float s_row = 0.0f;
+    if constexpr (AQ == kQE4M3 || AQ == kQInt8) {
+      float amax = 0.0f;
+      for (int64_t b = lane; b < nblk; b += 32) {
+        float f[16];
+        unpack8(__ldg(src + 2 * b), f);
+        unpack8(__ldg(src + 2 * b + 1), f + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      }
+      s_row = __fdiv_rn(warp_max(amax), AQ == kQE4M3 ? 448.0f : 127.0f);
+    }
+    for (int64_t b0 = 0; b0 < nblk; b0 += 32 * NB) {
+      uint4 v[NB][2];
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        const int64_t b = b0 + 32 * i + lane;
+        if (b < nblk) {
+          v[i][0] = __ldg(src + 2 * b);
+          v[i][1] = __ldg(src + 2 * b + 1);
+        }
+      }
+      if constexpr (AQ != kQNone) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int64_t b = b0 + 32 * i + lane;
+          if (b < nblk) {
+            float f[16];
+            unpack8(v[i][0], f);
+            unpack8(v[i][1], f + 8);
+            float sc = s_row;
+            if constexpr (AQ == kQE2M1) {
+              float amax = 0.0f;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(f[e]));
+              sc = __fdiv_rn(amax, 6.0f);
+            }
+            fakequant_act_inplace<AQ, 16>(f, sc);
+            v[i][0] = pack8(f);
+            v[i][1] = pack8(f + 8);
+            uint4* o = xq + t * nblk * 2 + 2 * b;
+            o[0] = v[i][0];
+            o[1] = v[i][1];
+          }
+        }
+      }
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
+        if (r < 0) continue;
+        uint4* dst = a1 + (int64_t)r * nblk * 2;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int64_t b = b0 + 32 * i + lane;
+          if (b < nblk) {
+            dst[2 * b] = v[i][0];
+            dst[2 * b + 1] = v[i][1];
+          }
+        }
+      }
+    }
+  }
+  zero_pad_rows(a1, row_token, nblk * 2, dev_rpad, w0, warps, lane);
 }
 
 // ------------------------------------------------------------------------- combine
@@ -332,56 +389,74 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   }
 }
 
-// one warp per padded row: dy[r] = bf16(fp32(p * dout[t])), dprobs[t, j] = <dout[t], y[r]>
-__global__ void __launch_bounds__(256) dy_gather_kernel(const uint4* __restrict__ dout, const float* __restrict__ p,
-                                                        const int32_t* __restrict__ row_token,
-                                                        const int32_t* __restrict__ row_slot, const uint4* __restrict__ y,
-                                                        uint4* __restrict__ dy, float* __restrict__ dprobs, int k,
-                                                        int64_t c8, const int32_t* dev_rows) {
-  const int64_t nrows = *dev_rows;
+// Backward gather, one warp per token: for each routed row r of the token (slot j),
+// dy[r] = bf16(fp32(p[t, j] * dout[t])) and dprobs[t, j] = <dout[t], y[r]> (fp32, each lane
+// over its blocks in order, then a warp sum; 0 for a dropped pair); dout[t] is read from
+// memory once and from L1 for the later slots.  Then the padding rows of dy are zeroed.
+__global__ void __launch_bounds__(256) dy_scatter_kernel(const uint4* __restrict__ dout, const float* __restrict__ p,
+                                                         const int32_t* __restrict__ row_of,
+                                                         const int32_t* __restrict__ row_token,
+                                                         const uint4* __restrict__ y, uint4* __restrict__ dy,
+                                                         float* __restrict__ dprobs, int64_t T, int k, int64_t nblk,
+                                                         const int32_t* dev_rpad) {
+  constexpr int NB = kScatterNB;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows; r += warps) {
-    const int32_t t = row_token[r];
-    uint4* d = dy + r * c8;
-    if (t < 0) {
-      for (int64_t c = lane; c < c8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const int j = row_slot[r];
-    const float pj = __ldg(p + (int64_t)t * k + j);
-    const uint4* g = dout + (int64_t)t * c8;
-    const uint4* yr = y + r * c8;
-    float dot = 0.0f;
-    for (int64_t c0 = lane; c0 < c8; c0 += 64) {  // two 16-byte chunks per lane in flight
-      const bool two = c0 + 32 < c8;
-      const uint4 g0 = __ldg(g + c0);
-      const uint4 g1 = two ? __ldg(g + c0 + 32) : make_uint4(0, 0, 0, 0);
-      uint4 y0 = make_uint4(0, 0, 0, 0), y1 = make_uint4(0, 0, 0, 0);
-      if (dprobs) {
-        y0 = __ldg(yr + c0);
-        if (two) y1 = __ldg(yr + c0 + 32);
-      }
+  const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  for (int64_t t = w0; t < T; t += warps) {
+    const int32_t my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
+    const float my_p = lane < k ? __ldg(p + t * k + lane) : 0.0f;
+    const uint4* g = dout + t * nblk * 2;
+    for (int j = 0; j < k; ++j) {
+      const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
+      const float pj = __shfl_sync(0xffffffffu, my_p, j);
+      float dot = 0.0f;
+      if (r >= 0) {
+        const uint4* yr = y + (int64_t)r * nblk * 2;
+        uint4* dr = dy + (int64_t)r * nblk * 2;
+        for (int64_t b0 = 0; b0 < nblk; b0 += 32 * NB) {
+          uint4 gv[NB][2], yv[NB][2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (h == 1 && !two) break;
-        float v[8], yv[8];
-        unpack8(h ? g1 : g0, v);
-        if (dprobs) {
-          unpack8(h ? y1 : y0, yv);
+          for (int i = 0; i < NB; ++i) {
+            const int64_t b = b0 + 32 * i + lane;
+            if (b < nblk) {
+              gv[i][0] = __ldg(g + 2 * b);
+              gv[i][1] = __ldg(g + 2 * b + 1);
+              if (dprobs) {
+                yv[i][0] = __ldcs(yr + 2 * b);
+                yv[i][1] = __ldcs(yr + 2 * b + 1);
+              }
+            }
+          }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dot = fmaf(v[i], yv[i], dot);
+          for (int i = 0; i < NB; ++i) {
+            const int64_t b = b0 + 32 * i + lane;
+            if (b < nblk) {
+              float f[16];
+              unpack8(gv[i][0], f);
+              unpack8(gv[i][1], f + 8);
+              if (dprobs) {
+                float yf[16];
+                unpack8(yv[i][0], yf);
+                unpack8(yv[i][1], yf + 8);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dot = fmaf(f[e], yf[e], dot);
+              }
+#pragma unroll
+              for (int e = 0; e < 16; ++e) f[e] = __fmul_rn(pj, f[e]);
+              dr[2 * b] = pack8(f);
+              dr[2 * b + 1] = pack8(f + 8);
+            }
+          }
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(pj, v[i]);
-        d[c0 + 32 * h] = pack8(v);
       }
-    }
-    if (dprobs) {
-      dot = warp_sum(dot);
-      if (lane == 0) dprobs[(int64_t)t * k + j] = dot;
+      if (dprobs) {
+        dot = warp_sum(dot);
+        if (lane == 0) dprobs[t * k + j] = dot;
+      }
     }
   }
+  zero_pad_rows(dy, row_token, nblk * 2, dev_rpad, w0, warps, lane);
 }
 
 __global__ void __launch_bounds__(256) scale_reduce_kernel(const float* __restrict__ part, float* __restrict__ ds,
@@ -485,11 +560,9 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
 cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
+  if (kind != kQE4M3 && kind != kQInt8) return cudaErrorInvalidValue;
   prof_begin(QAD_K_ACT_QUANT, st);
-  if (kind == kQE2M1) {
-    act_quant_nvfp4_kernel<<<grid_for(rows * (cols / 16), 256, 8), 256, 0, st>>>(
-        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
-  } else if (kind == kQE4M3) {
+  if (kind == kQE4M3) {
     act_quant_row_kernel<kQE4M3><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
         static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
   } else {
@@ -500,12 +573,20 @@ cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t r
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* row_token, int64_t rmax, int64_t cols,
-                               const int32_t* dev_rows, cudaStream_t st) {
-  if (rmax == 0) return cudaSuccess;
+cudaError_t launch_scatter_tokens(int aq, const void* x, void* xq, void* a1, const int32_t* row_of,
+                                  const int32_t* row_token, int64_t T, int k, int64_t d, const int32_t* dev_rpad,
+                                  cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
   prof_begin(QAD_K_GATHER, st);
-  gather_rows_kernel<<<grid_for(rmax * 32, 256, 8), 256, 0, st>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), row_token, cols / 8, dev_rows);
+  const int grid = grid_for(T * 32, 256, 8);
+  const uint4* xs = static_cast<const uint4*>(x);
+  uint4* q = static_cast<uint4*>(xq);
+  uint4* a = static_cast<uint4*>(a1);
+  const int64_t nblk = d / 16;
+  if (aq == kQE2M1) scatter_tokens_kernel<kQE2M1><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
+  else if (aq == kQE4M3) scatter_tokens_kernel<kQE4M3><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
+  else if (aq == kQInt8) scatter_tokens_kernel<kQInt8><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
+  else scatter_tokens_kernel<kQNone><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
   prof_end(QAD_K_GATHER, st);
   return cudaGetLastError();
 }
@@ -526,14 +607,14 @@ cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* p,
   return cudaGetLastError();
 }
 
-cudaError_t launch_dy_gather(const void* dout, const float* p, const int32_t* row_token, const int32_t* row_slot,
-                             const void* y, void* dy, float* dprobs, int64_t rmax, int k, int64_t d,
-                             const int32_t* dev_rows, cudaStream_t st) {
-  if (rmax == 0) return cudaSuccess;
+cudaError_t launch_dy_scatter(const void* dout, const float* p, const int32_t* row_of, const int32_t* row_token,
+                              const void* y, void* dy, float* dprobs, int64_t T, int k, int64_t d,
+                              const int32_t* dev_rpad, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
   prof_begin(QAD_K_DY_GATHER, st);
-  dy_gather_kernel<<<grid_for(rmax * 32, 256, 8), 256, 0, st>>>(
-      static_cast<const uint4*>(dout), p, row_token, row_slot, static_cast<const uint4*>(y), static_cast<uint4*>(dy),
-      dprobs, k, d / 8, dev_rows);
+  dy_scatter_kernel<<<grid_for(T * 32, 256, 8), 256, 0, st>>>(
+      static_cast<const uint4*>(dout), p, row_of, row_token, static_cast<const uint4*>(y), static_cast<uint4*>(dy),
+      dprobs, T, k, d / 16, dev_rpad);
   prof_end(QAD_K_DY_GATHER, st);
   return cudaGetLastError();
 }

@@ -69,6 +69,7 @@ struct Params {
   const __nv_bfloat16* w;  const float* s;   // SCALEGRAD: raw weights [E, Mw, Kw] and scales
   int64_t w_rows, w_cols;
   float* ds; float* part; int accumulate;
+  int pf_dist;  // k-blocks between an L2 prefetch of a CTA's operand tiles and their load (0: none)
 };
 
 template <int BN> struct Cfg {
@@ -153,6 +154,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// L2 prefetch of the tile a TMA load with the same map and coordinates would fetch
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // TMA tile store from this CTA's shared memory (bulk-group completion, tracked per thread)
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -718,6 +726,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;  // stages with a load in flight, and its phase parity
     bool ok = true;
+    const int half_n = (int)rank * (BN / 2);
+    // this CTA's A tile and half of the B tile for k-block kb of tile ti: TMA loads into
+    // shared memory completing on `fb`, or (prefetch) L2 prefetches of the same boxes
+    auto operand_tiles = [&](const Tile& ti, int kb, uint32_t sa, uint32_t sb, uint32_t fb, bool prefetch) {
+      auto box = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
+        if (prefetch) tma_prefetch_2d(tm, x, y);
+        else tma_load_2d(dst, tm, x, y, fb);
+      };
+      if (!p.wgrad) {
+        box(sa, &tmA, kb * BK, ti.r0);
+        if constexpr (!B_MN) {
+          if constexpr (EPI == EPI_FC1) {
+            // leader: the 128 gate rows of the tile, peer: the matching 128 up rows
+            box(sb, &tmB, kb * BK, ti.e * p.b_rows + (int)rank * p.F + ti.nb * 128);
+          } else {
+            box(sb, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * BN + half_n);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i)
+            box(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, ti.e * p.b_rows + kb * BK);
+        }
+      } else {
+        const int y = ti.r0 + kb * BK;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) box(sa + i * 64 * 128, &tmA, ti.mb * 2 * BM + (int)rank * BM + i * 64, y);
+#pragma unroll
+        for (int i = 0; i < BN / 128; ++i) box(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, y);
+      }
+    };
     for (int t = first; ok && t < total; t += step) {
       const Tile ti = tile_of(p, t, rank);
       for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -727,30 +765,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (leader) mbar_expect_tx(full_bar(stage), 2 * C::STAGE);  // both CTAs' bytes
         const uint32_t fb = peer_addr(full_bar(stage), 0);          // the leader's barrier
-        const uint32_t sa = a_ring + stage * C::A_BYTES;
-        const uint32_t sb = b_ring + stage * C::B_BYTES;
-        const int half_n = (int)rank * (BN / 2);
-        if (!p.wgrad) {
-          tma_load_2d(sa, &tmA, kb * BK, ti.r0, fb);
-          if constexpr (!B_MN) {
-            if constexpr (EPI == EPI_FC1) {
-              // leader: the 128 gate rows of the tile, peer: the matching 128 up rows
-              tma_load_2d(sb, &tmB, kb * BK, ti.e * p.b_rows + (int)rank * p.F + ti.nb * 128, fb);
-            } else {
-              tma_load_2d(sb, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * BN + half_n, fb);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < BN / 128; ++i)
-              tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, ti.e * p.b_rows + kb * BK, fb);
+        operand_tiles(ti, kb, a_ring + stage * C::A_BYTES, b_ring + stage * C::B_BYTES, fb, false);
+        if (p.pf_dist > 0) {  // warm L2 with the tiles this CTA loads pf_dist k-blocks from now
+          const int kp = kb + p.pf_dist;
+          if (kp < ti.nkb) {
+            operand_tiles(ti, kp, 0, 0, 0, true);
+          } else if (t + step < total) {
+            const Tile tn = tile_of(p, t + step, rank);
+            if (kp - ti.nkb < tn.nkb) operand_tiles(tn, kp - ti.nkb, 0, 0, 0, true);
           }
-        } else {
-          const int y = ti.r0 + kb * BK;
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            tma_load_2d(sa + i * 64 * 128, &tmA, ti.mb * 2 * BM + (int)rank * BM + i * 64, y, fb);
-#pragma unroll
-          for (int i = 0; i < BN / 128; ++i) tma_load_2d(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, y, fb);
         }
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -988,6 +1011,7 @@ Params base_params(const GemmCtx& c) {
   p.wq = c.wq;
   p.aq = c.aq;
   p.flags = c.flags;
+  p.pf_dist = 0;  // L2 prefetch off: measured slower (each prefetch costs TMA requests like a load)
   return p;
 }
 

@@ -47,16 +47,19 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
 // row) for r < rows (or < *dev_rows when dev_rows != nullptr)
 cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st);
-// dst[r, :] = src[row_token[r], :], zeros where row_token[r] < 0, for r < *dev_rows
-cudaError_t launch_gather_rows(const void* src, void* dst, const int32_t* row_token, int64_t rmax, int64_t cols,
-                               const int32_t* dev_rows, cudaStream_t st);
+// Per token t: xq[t] = AQ(x[t]) (aq != kQNone) and a1[row_of[t, j]] = AQ(x[t]) for its routed
+// rows; the padding rows (row_token < 0) below *dev_rpad are zeroed
+cudaError_t launch_scatter_tokens(int aq, const void* x, void* xq, void* a1, const int32_t* row_of,
+                                  const int32_t* row_token, int64_t T, int k, int64_t d, const int32_t* dev_rpad,
+                                  cudaStream_t st);
 // out[t, :] = bf16(sum_j p[t, j] * y[row_of[t, j], :]) (p == nullptr: weight 1)
 cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* p, void* out, int64_t T, int k,
                            int64_t d, cudaStream_t st);
-// dy[r] = bf16(p[t, j] * dout[t]); dprobs[t, j] = <dout[t], y[r]> (dprobs may be null)
-cudaError_t launch_dy_gather(const void* dout, const float* p, const int32_t* row_token, const int32_t* row_slot,
-                             const void* y, void* dy, float* dprobs, int64_t rmax, int k, int64_t d,
-                             const int32_t* dev_rows, cudaStream_t st);
+// dy[row_of[t, j]] = bf16(p[t, j] * dout[t]); dprobs[t, j] = <dout[t], y[row_of[t, j]]> (0 for a
+// dropped pair; dprobs may be null); the padding rows of dy below *dev_rpad are zeroed
+cudaError_t launch_dy_scatter(const void* dout, const float* p, const int32_t* row_of, const int32_t* row_token,
+                              const void* y, void* dy, float* dprobs, int64_t T, int k, int64_t d,
+                              const int32_t* dev_rpad, cudaStream_t st);
 // ds[i] = (accumulate ? ds[i] : 0) + sum_j part[i * nparts + j]
 cudaError_t launch_scale_reduce(const float* part, float* ds, int64_t n, int nparts, int accumulate,
                                 cudaStream_t st);
