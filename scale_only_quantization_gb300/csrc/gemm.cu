@@ -69,7 +69,6 @@ struct Params {
   const __nv_bfloat16* w;  const float* s;   // SCALEGRAD: raw weights [E, Mw, Kw] and scales
   int64_t w_rows, w_cols;
   float* ds; float* part; int accumulate;
-  int pf_dist;  // k-blocks between an L2 prefetch of a CTA's operand tiles and their load (0: none)
 };
 
 template <int BN> struct Cfg {
@@ -113,9 +112,10 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with parity `parity` of barrier `bar`: gives up after `budget`
 // clock cycles (or as soon as another role of the CTA gave up), raising QAD_DEV_TIMEOUT.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                      long long budget = kWaitCycles) {
-  if (mbar_try(bar, parity)) return true;
+// The first tries are inline: the producer and MMA-issuer threads wait once per k-block, and
+// a function call there (with its stack frame) measurably slows every GEMM.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                           long long budget) {
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
@@ -128,6 +128,14 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                          long long budget = kWaitCycles) {
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i)
+    if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, budget);
 }
 
 // Self-check of the timeout path: one thread waits, with the GEMMs' own bounded-wait routine,
@@ -154,13 +162,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// L2 prefetch of the tile a TMA load with the same map and coordinates would fetch
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // TMA tile store from this CTA's shared memory (bulk-group completion, tracked per thread)
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -727,13 +728,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t armed = 0, armed_parity = 0;  // stages with a load in flight, and its phase parity
     bool ok = true;
     const int half_n = (int)rank * (BN / 2);
-    // this CTA's A tile and half of the B tile for k-block kb of tile ti: TMA loads into
-    // shared memory completing on `fb`, or (prefetch) L2 prefetches of the same boxes
-    auto operand_tiles = [&](const Tile& ti, int kb, uint32_t sa, uint32_t sb, uint32_t fb, bool prefetch) {
-      auto box = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
-        if (prefetch) tma_prefetch_2d(tm, x, y);
-        else tma_load_2d(dst, tm, x, y, fb);
-      };
+    // TMA loads of this CTA's A tile and half of the B tile for k-block kb of tile ti into
+    // shared memory, completing on `fb`
+    auto operand_tiles = [&](const Tile& ti, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
+      auto box = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) { tma_load_2d(dst, tm, x, y, fb); };
       if (!p.wgrad) {
         box(sa, &tmA, kb * BK, ti.r0);
         if constexpr (!B_MN) {
@@ -765,16 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (leader) mbar_expect_tx(full_bar(stage), 2 * C::STAGE);  // both CTAs' bytes
         const uint32_t fb = peer_addr(full_bar(stage), 0);          // the leader's barrier
-        operand_tiles(ti, kb, a_ring + stage * C::A_BYTES, b_ring + stage * C::B_BYTES, fb, false);
-        if (p.pf_dist > 0) {  // warm L2 with the tiles this CTA loads pf_dist k-blocks from now
-          const int kp = kb + p.pf_dist;
-          if (kp < ti.nkb) {
-            operand_tiles(ti, kp, 0, 0, 0, true);
-          } else if (t + step < total) {
-            const Tile tn = tile_of(p, t + step, rank);
-            if (kp - ti.nkb < tn.nkb) operand_tiles(tn, kp - ti.nkb, 0, 0, 0, true);
-          }
-        }
+        operand_tiles(ti, kb, a_ring + stage * C::A_BYTES, b_ring + stage * C::B_BYTES, fb);
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -1011,7 +1000,6 @@ Params base_params(const GemmCtx& c) {
   p.wq = c.wq;
   p.aq = c.aq;
   p.flags = c.flags;
-  p.pf_dist = 0;  // L2 prefetch off: measured slower (each prefetch costs TMA requests like a load)
   return p;
 }
 
