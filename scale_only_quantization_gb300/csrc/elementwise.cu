@@ -103,27 +103,43 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const int32_t* __restri
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
-// One block of 1024 threads, thread e owns expert e (E <= 1024).  Produces per-expert
-// counts, padded offsets (multiples of 128 rows), each chunk's first row per expert, the
-// expert of every 128-row tile, and marks padding rows with token -1.
+// One block of 1024 threads.  Each expert gets G = 1024 / (E rounded up to a power of two)
+// threads, each of which sums the expert's counts over a contiguous range of chunks; the
+// ranges' exclusive prefixes give each chunk's first row for the expert.  Produces per-expert
+// counts, padded offsets (multiples of 128 rows), the chunk bases, the expert of every
+// 128-row tile, and marks padding rows with token -1.
 __global__ void __launch_bounds__(1024) route_scan_kernel(int64_t nchunks, int E, const int32_t* __restrict__ chunk_counts,
                                                           int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offs, int32_t* __restrict__ mtile_expert,
                                                           int32_t* __restrict__ row_token, int32_t* __restrict__ row_slot,
                                                           int32_t* hdr) {
+  __shared__ int32_t part[1024];  // each thread's sum over its chunk range
+  __shared__ int32_t tot[1024];   // per-expert totals
+  __shared__ int32_t eoff[1024];  // per-expert padded offsets
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t valid_tot[32];
-  const int e = threadIdx.x, lane = e & 31, w = e >> 5;
-  int32_t total = 0;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int ep = 1;
+  while (ep < E) ep <<= 1;
+  const int G = 1024 / ep;
+  const int e = tid / G, g = tid - (tid / G) * G;
+  const int64_t per = (nchunks + G - 1) / G;
+  const int64_t c0 = min(nchunks, (int64_t)g * per), c1 = min(nchunks, c0 + per);
+  int32_t sum = 0;
   if (e < E) {
 #pragma unroll 8
-    for (int64_t c = 0; c < nchunks; ++c) {
-      const int32_t v = chunk_counts[c * E + e];
-      chunk_base[c * E + e] = total;
-      total += v;
-    }
-    counts[e] = total;
+    for (int64_t c = c0; c < c1; ++c) sum += chunk_counts[c * E + e];
   }
+  part[tid] = sum;
+  __syncthreads();
+  int32_t before = 0;  // the expert's rows in the chunks before this thread's range
+  if (e < E) {
+    for (int h = e * G; h < tid; ++h) before += part[h];
+    if (g == G - 1) tot[e] = before + sum;
+  }
+  __syncthreads();
+  // exclusive scan over experts of the padded totals (thread x: expert x)
+  const int32_t total = tid < E ? tot[tid] : 0;
   const int32_t padded = (total + kTileRows - 1) / kTileRows * kTileRows;
   int32_t v = padded, nv = total;
 #pragma unroll
@@ -137,68 +153,90 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int64_t nchunks, int E
   if (lane == 0) valid_tot[w] = nv;
   __syncthreads();
   if (w == 0) {
-    int32_t t = warp_tot[lane], s = valid_tot[lane];
+    int32_t t = warp_tot[lane], sv = valid_tot[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int32_t n = __shfl_up_sync(0xffffffffu, t, o);
       if (lane >= o) t += n;
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int o = 16; o; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
     warp_tot[lane] = t;
-    if (lane == 0) valid_tot[0] = s;
+    if (lane == 0) valid_tot[0] = sv;
   }
   __syncthreads();
-  const int32_t incl = v + (w > 0 ? warp_tot[w - 1] : 0);
-  const int32_t excl = incl - padded;
-  if (e < E) {
-    offs[e] = excl;
-    if (e == E - 1) {
+  if (tid < E) {
+    const int32_t incl = v + (w > 0 ? warp_tot[w - 1] : 0);
+    eoff[tid] = incl - padded;
+    counts[tid] = total;
+    offs[tid] = incl - padded;
+    if (tid == E - 1) {
       offs[E] = incl;
       hdr[HDR_NMTILES] = incl / kTileRows;
       hdr[HDR_RPAD] = incl;
       hdr[HDR_NVALID] = valid_tot[0];
     }
-    for (int64_t c = 0; c < nchunks; ++c) chunk_base[c * E + e] += excl;
-    for (int32_t r = excl + total; r < incl; ++r) {
+  }
+  __syncthreads();
+  if (e < E) {
+    int32_t run = eoff[e] + before;
+#pragma unroll 8
+    for (int64_t c = c0; c < c1; ++c) {
+      const int32_t n = chunk_counts[c * E + e];
+      chunk_base[c * E + e] = run;
+      run += n;
+    }
+    const int32_t ex = eoff[e], t = tot[e];
+    const int32_t end = ex + (t + kTileRows - 1) / kTileRows * kTileRows;
+    for (int32_t r = ex + t + g; r < end; r += G) {
       row_token[r] = -1;
       row_slot[r] = -1;
     }
-    for (int32_t mb = excl / kTileRows; mb < incl / kTileRows; ++mb) mtile_expert[mb] = e;
+    for (int32_t mb = ex / kTileRows + g; mb < end / kTileRows; mb += G) mtile_expert[mb] = e;
   }
 }
 
-// One warp per chunk of 1024 pairs, 32 at a time in order; a pair's row is its chunk's
-// first row for the expert plus the number of earlier pairs of the chunk with that expert.
-__global__ void __launch_bounds__(32) route_scatter_kernel(const int32_t* __restrict__ idx, int64_t R, int k, int E,
-                                                           const int32_t* __restrict__ chunk_base,
-                                                           int32_t* __restrict__ row_token, int32_t* __restrict__ row_slot,
-                                                           int32_t* __restrict__ row_of) {
-  extern __shared__ int32_t seen[];
-  const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) seen[e] = 0;
-  __syncwarp();
-  const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
-  const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
-  for (int step = 0; step < kRouteChunk / 32; ++step) {
-    const int64_t g = base + step * 32 + lane;
-    int err = 0;
-    const int e = g < R ? pair_expert(idx, g, k, E, &err) : -1;
-    const int key = e >= 0 ? e : -1 - lane;  // unmatched keys for dropped pairs
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int before = __popc(peers & ((1u << lane) - 1u));
-    int pos = -1;
-    if (e >= 0) pos = cb[e] + seen[e] + before;
-    __syncwarp();
-    if (e >= 0 && before == 0) seen[e] += __popc(peers);
-    __syncwarp();
-    if (g < R) {
-      row_of[g] = pos;
-      if (pos >= 0) {
-        const int64_t t = g / k;
-        row_token[pos] = (int32_t)t;
-        row_slot[pos] = (int32_t)(g - t * k);
-      }
+// One block of 1024 threads per chunk of 1024 pairs, one pair per thread.  A pair's row is its
+// chunk's first row for the expert plus the number of earlier pairs of the chunk with that
+// expert: the pairs' experts and their ranks within each warp (match_any) are found in
+// parallel, then the warps take their turns in order to add the earlier warps' counts.
+static_assert(kRouteChunk == 1024, "route_scatter_kernel maps one chunk to one 1024-thread block");
+__global__ void __launch_bounds__(1024) route_scatter_kernel(const int32_t* __restrict__ idx, int64_t R, int k, int E,
+                                                             const int32_t* __restrict__ chunk_base,
+                                                             int32_t* __restrict__ row_token,
+                                                             int32_t* __restrict__ row_slot,
+                                                             int32_t* __restrict__ row_of) {
+  extern __shared__ int32_t sm[];
+  int32_t* seen = sm;      // [E] pairs of the chunk placed so far, per expert
+  int32_t* base = sm + E;  // [E] the chunk's first row per expert
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int64_t chunk = blockIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) {
+    seen[e] = 0;
+    base[e] = chunk_base[chunk * E + e];
+  }
+  const int64_t gi = chunk * kRouteChunk + tid;
+  int err = 0;
+  const int e = gi < R ? pair_expert(idx, gi, k, E, &err) : -1;
+  const int key = e >= 0 ? e : -1 - lane;  // unmatched keys for dropped pairs
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const int before = __popc(peers & ((1u << lane) - 1u));
+  __syncthreads();
+  int pos = -1;
+  for (int turn = 0; turn < 32; ++turn) {
+    if (w == turn) {
+      if (e >= 0) pos = base[e] + seen[e] + before;
+      __syncwarp();
+      if (e >= 0 && before == 0) seen[e] += __popc(peers);
+    }
+    __syncthreads();
+  }
+  if (gi < R) {
+    row_of[gi] = pos;
+    if (pos >= 0) {
+      const int64_t t = gi / k;
+      row_token[pos] = (int32_t)t;
+      row_slot[pos] = (int32_t)(gi - t * k);
     }
   }
 }
@@ -516,26 +554,11 @@ cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, 
 }
 
 cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st) {
-  int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.header);
-  int32_t* cc = reinterpret_cast<int32_t*>(ws + L.chunk_counts);
-  int32_t* cb = reinterpret_cast<int32_t*>(ws + L.chunk_base);
-  int32_t* row_token = reinterpret_cast<int32_t*>(ws + L.row_token);
-  int32_t* row_slot = reinterpret_cast<int32_t*>(ws + L.row_slot);
-  const int E = (int)L.E, k = (int)L.k;
-  prof_begin(QAD_K_ROUTE, st);
-  if (L.nchunks > 0) {
-    route_hist_kernel<<<(unsigned)L.nchunks, 256, E * sizeof(int32_t), st>>>(idx, L.R, k, E, cc, hdr);
-  }
-  route_scan_kernel<<<1, 1024, 0, st>>>(L.nchunks, E, cc, cb, reinterpret_cast<int32_t*>(ws + L.counts),
-                                        reinterpret_cast<int32_t*>(ws + L.offs),
-                                        reinterpret_cast<int32_t*>(ws + L.mtile_expert), row_token, row_slot, hdr);
-  if (L.nchunks > 0) {
-    route_scatter_kernel<<<(unsigned)L.nchunks, 32, E * sizeof(int32_t), st>>>(
-        idx, L.R, k, E, cb, row_token, row_slot, reinterpret_cast<int32_t*>(ws + L.row_of));
-  }
-  prof_end(QAD_K_ROUTE, st);
-  if (L.nchunks > 0) note_launches(2);
-  return cudaGetLastError();
+  return launch_route_ptrs(idx, L.R, (int)L.k, (int)L.E, L.nchunks, reinterpret_cast<int32_t*>(ws + L.header),
+                           reinterpret_cast<int32_t*>(ws + L.chunk_counts), reinterpret_cast<int32_t*>(ws + L.chunk_base),
+                           reinterpret_cast<int32_t*>(ws + L.counts), reinterpret_cast<int32_t*>(ws + L.offs),
+                           reinterpret_cast<int32_t*>(ws + L.mtile_expert), reinterpret_cast<int32_t*>(ws + L.row_token),
+                           reinterpret_cast<int32_t*>(ws + L.row_slot), reinterpret_cast<int32_t*>(ws + L.row_of), st);
 }
 
 cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64_t nchunks, int32_t* hdr,
@@ -549,8 +572,8 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
   route_scan_kernel<<<1, 1024, 0, st>>>(nchunks, E, chunk_counts, chunk_base, counts, offs, mtile_expert, row_token,
                                         row_slot, hdr);
   if (nchunks > 0) {
-    route_scatter_kernel<<<(unsigned)nchunks, 32, E * sizeof(int32_t), st>>>(idx, R, k, E, chunk_base, row_token,
-                                                                            row_slot, row_of);
+    route_scatter_kernel<<<(unsigned)nchunks, kRouteChunk, 2 * E * sizeof(int32_t), st>>>(idx, R, k, E, chunk_base,
+                                                                                         row_token, row_slot, row_of);
   }
   prof_end(QAD_K_ROUTE, st);
   if (nchunks > 0) note_launches(2);
