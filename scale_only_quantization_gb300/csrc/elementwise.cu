@@ -291,20 +291,37 @@ __device__ __forceinline__ void zero_pad_rows(uint4* __restrict__ dst, const int
 }
 
 constexpr int kScatterNB = 4;  // 16-element blocks per lane per pass over a row chunk
+constexpr int kStageChunk = 32 * kScatterNB * 2;  // 16-byte units of one staged row chunk (4 KB)
+constexpr int kDyScatterSmem = 8 * 2 * kStageChunk * 16;  // two staged chunks per warp, 8 warps
+
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"((uint32_t)__cvta_generic_to_shared(src_smem)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_one() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_done() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Forward gather, one warp per token: the token's row of x is read once, fake-quantized on
 // the activation grid (E2M1 per 16-element block with scale fp32(block amax / 6); E4M3 /
 // INT8 per row with fp32(row amax / 448) / fp32(row amax / 127); or not at all), written to
 // xq (when the grid quantizes) and to each routed row of the token; then the padding rows
 // are zeroed.  Lane l holds the 16-element blocks l, l + 32, ... of a 128 x 16-element
-// chunk of the row.
+// chunk of the row.  The quantized chunk is staged in the warp's 4 KB of shared memory and
+// lane j < k copies it to routed row j with one bulk copy (plain per-thread stores of the
+// same rows ran at two thirds of the speed).
 template <int AQ>
 __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __restrict__ x, uint4* __restrict__ xq,
                                                              uint4* __restrict__ a1, const int32_t* __restrict__ row_of,
                                                              const int32_t* __restrict__ row_token, int64_t T, int k,
                                                              int64_t nblk, const int32_t* dev_rpad) {
   constexpr int NB = kScatterNB;
+  __shared__ __align__(128) uint4 stage_all[8][kStageChunk];
   const int lane = threadIdx.x & 31;
+  uint4* stage = stage_all[threadIdx.x / 32];
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   for (int64_t t = w0; t < T; t += warps) {
@@ -356,21 +373,26 @@ __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __rest
           }
         }
       }
-      for (int j = 0; j < k; ++j) {
-        const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
-        if (r < 0) continue;
-        uint4* dst = a1 + (int64_t)r * nblk * 2;
+      if (lane < k) bulk_wait_read_all();  // the previous chunk's copies have read the stage
+      __syncwarp();
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int64_t b = b0 + 32 * i + lane;
-          if (b < nblk) {
-            dst[2 * b] = v[i][0];
-            dst[2 * b + 1] = v[i][1];
-          }
+      for (int i = 0; i < NB; ++i) {
+        const int64_t b = b0 + 32 * i + lane;
+        if (b < nblk) {
+          stage[2 * (32 * i + lane)] = v[i][0];
+          stage[2 * (32 * i + lane) + 1] = v[i][1];
         }
+      }
+      fence_smem_to_async();
+      __syncwarp();
+      if (lane < k) {
+        const int64_t nb_here = nblk - b0 < 32 * NB ? nblk - b0 : 32 * NB;
+        if (my_row >= 0) bulk_store(a1 + (int64_t)my_row * nblk * 2 + 2 * b0, stage, (uint32_t)(nb_here * 32));
+        bulk_commit_group();
       }
     }
   }
+  if (lane < k) bulk_wait_done();
   zero_pad_rows(a1, row_token, nblk * 2, dev_rpad, w0, warps, lane);
 }
 
@@ -430,7 +452,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
 // Backward gather, one warp per token: for each routed row r of the token (slot j),
 // dy[r] = bf16(fp32(p[t, j] * dout[t])) and dprobs[t, j] = <dout[t], y[r]> (fp32, each lane
 // over its blocks in order, then a warp sum; 0 for a dropped pair); dout[t] is read from
-// memory once and from L1 for the later slots.  Then the padding rows of dy are zeroed.
+// memory once and from L1 for the later slots.  Each scaled row chunk is staged in one of
+// the warp's two 4 KB buffers (dynamic shared memory, kDyScatterSmem per block) and lane 0
+// writes it with one bulk copy.  Then the padding rows of dy are zeroed.
 __global__ void __launch_bounds__(256) dy_scatter_kernel(const uint4* __restrict__ dout, const float* __restrict__ p,
                                                          const int32_t* __restrict__ row_of,
                                                          const int32_t* __restrict__ row_token,
@@ -438,7 +462,10 @@ __global__ void __launch_bounds__(256) dy_scatter_kernel(const uint4* __restrict
                                                          float* __restrict__ dprobs, int64_t T, int k, int64_t nblk,
                                                          const int32_t* dev_rpad) {
   constexpr int NB = kScatterNB;
+  extern __shared__ __align__(128) uint4 dy_stage[];
   const int lane = threadIdx.x & 31;
+  uint4* stage0 = dy_stage + (threadIdx.x / 32) * 2 * kStageChunk;
+  uint32_t buf = 0;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   for (int64_t t = w0; t < T; t += warps) {
@@ -451,7 +478,6 @@ __global__ void __launch_bounds__(256) dy_scatter_kernel(const uint4* __restrict
       float dot = 0.0f;
       if (r >= 0) {
         const uint4* yr = y + (int64_t)r * nblk * 2;
-        uint4* dr = dy + (int64_t)r * nblk * 2;
         for (int64_t b0 = 0; b0 < nblk; b0 += 32 * NB) {
           uint4 gv[NB][2], yv[NB][2];
 #pragma unroll
@@ -466,6 +492,9 @@ __global__ void __launch_bounds__(256) dy_scatter_kernel(const uint4* __restrict
               }
             }
           }
+          uint4* stg = stage0 + buf * kStageChunk;
+          if (lane == 0) bulk_wait_read_one();  // the copy issued from this buffer last time has read it
+          __syncwarp();
 #pragma unroll
           for (int i = 0; i < NB; ++i) {
             const int64_t b = b0 + 32 * i + lane;
@@ -482,10 +511,18 @@ __global__ void __launch_bounds__(256) dy_scatter_kernel(const uint4* __restrict
               }
 #pragma unroll
               for (int e = 0; e < 16; ++e) f[e] = __fmul_rn(pj, f[e]);
-              dr[2 * b] = pack8(f);
-              dr[2 * b + 1] = pack8(f + 8);
+              stg[2 * (32 * i + lane)] = pack8(f);
+              stg[2 * (32 * i + lane) + 1] = pack8(f + 8);
             }
           }
+          fence_smem_to_async();
+          __syncwarp();
+          if (lane == 0) {
+            const int64_t nb_here = nblk - b0 < 32 * NB ? nblk - b0 : 32 * NB;
+            bulk_store(dy + (int64_t)r * nblk * 2 + 2 * b0, stg, (uint32_t)(nb_here * 32));
+            bulk_commit_group();
+          }
+          buf ^= 1u;
         }
       }
       if (dprobs) {
@@ -494,6 +531,7 @@ __global__ void __launch_bounds__(256) dy_scatter_kernel(const uint4* __restrict
       }
     }
   }
+  if (lane == 0) bulk_wait_done();
   zero_pad_rows(dy, row_token, nblk * 2, dev_rpad, w0, warps, lane);
 }
 
@@ -634,8 +672,17 @@ cudaError_t launch_dy_scatter(const void* dout, const float* p, const int32_t* r
                               const void* y, void* dy, float* dprobs, int64_t T, int k, int64_t d,
                               const int32_t* dev_rpad, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(dy_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kDyScatterSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
   prof_begin(QAD_K_DY_GATHER, st);
-  dy_scatter_kernel<<<grid_for(T * 32, 256, 8), 256, 0, st>>>(
+  dy_scatter_kernel<<<grid_for(T * 32, 256, 8), 256, kDyScatterSmem, st>>>(
       static_cast<const uint4*>(dout), p, row_of, row_token, static_cast<const uint4*>(y), static_cast<uint4*>(dy),
       dprobs, T, k, d / 16, dev_rpad);
   prof_end(QAD_K_DY_GATHER, st);
