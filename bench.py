@@ -167,7 +167,8 @@ def run_ours(args):
     cfg = synth.workload(args.workload, **over)
     inp = synth.make_inputs(cfg, seed=rank, device=dev)
     T, d, F, E, k, fmt = inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"]
-    s = Q.shape(T, d, F, E, k, fmt)
+    flags = Q.QAD_FLAG_RECOMPUTE if args.recompute else 0
+    s = Q.shape(T, d, F, E, k, fmt, flags)
     ws = torch.empty(Q.qad_moe_workspace_bytes(s), dtype=torch.uint8, device=dev)
     out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     dx = torch.empty_like(out)
@@ -314,6 +315,8 @@ def run_ours(args):
         "config": {"workload": args.workload + ("" if not over else "_T%d_E%d" % (T, E)),
                    "format": FMT_NAME[fmt], "E": E, "d": d, "F": F, "topk": k,
                    "tokens_per_gpu": T, "global_batch": T * world, "parallelism": "dp%d" % world,
+                   "activations": "recompute" if args.recompute else "stash",
+                   "workspace_gb": ws.numel() / 1e9,
                    "l2": "inputs larger than L2 (weights %.2f GB streamed per pass), no flush" %
                          (2 * 3 * E * F * d / 1e9)},
         "step_tflops": flops_step / (ms / 1e3) / 1e12,
@@ -421,6 +424,8 @@ def main():
                     help="override the workload's token count (small cases for profiler captures)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override the workload's expert count (small cases for profiler captures)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="QAD_FLAG_RECOMPUTE: recompute fc1's Z1 in the backward instead of stashing it")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -84,12 +84,20 @@ enum {
 /* qad_moe_shape.flags */
 enum {
   QAD_FLAG_STASH_H = 1,  /* also store the un-quantized SwiGLU output H in the workspace */
-  QAD_FLAG_NO_QUANT = 2  /* quantizers off: the self-distillation teacher pass ("MCoreQAD
+  QAD_FLAG_NO_QUANT = 2, /* quantizers off: the self-distillation teacher pass ("MCoreQAD
                             Backend", opening section: the same frozen model with quantization
                             disabled supplies the teacher logits).  qad_moe_fwd and
                             qad_moe_bwd_dgrad then use the raw bf16 weights and bf16
                             activations; the scales are not read (pass any valid pointer)
                             and qad_moe_bwd_scalegrad returns QAD_ERR_INVALID_ARG. */
+  QAD_FLAG_RECOMPUTE = 4 /* recompute instead of stash ("MCoreQAD Backend", performance notes:
+                            full activation recomputation for large models): qad_moe_fwd does
+                            not keep the fc1 output Z1, and qad_moe_bwd_dgrad recomputes it
+                            (one more fc1 GEMM, identical values) before its SwiGLU backward.
+                            When d >= 2F, Z1 then shares the workspace region of Y (Y is no
+                            longer needed once the dgrad call has used it for dprobs), so
+                            qad_moe_workspace_bytes is smaller by about 4·Rmax·F bytes.  The
+                            fwd, dgrad and scalegrad calls of one step must use the same flags. */
 };
 
 /* Shape of one MoE layer. T tokens, hidden d, expert FFN width F, E experts, top-k. */
@@ -196,7 +204,8 @@ enum {
   QAD_K_GEMM_FC1 = 4, QAD_K_GEMM_FC2 = 5, QAD_K_COMBINE = 6, QAD_K_DY_GATHER = 7,
   QAD_K_GEMM_DGRAD_FC2 = 8, QAD_K_GEMM_DGRAD_FC1 = 9, QAD_K_DX_COMBINE = 10,
   QAD_K_GEMM_WGRAD_FC2 = 11, QAD_K_GEMM_WGRAD_FC1 = 12, QAD_K_SCALE_REDUCE = 13,
-  QAD_K_COUNT = 14
+  QAD_K_GEMM_FC1_RECOMPUTE = 14, /* QAD_FLAG_RECOMPUTE: fc1 again in the dgrad call (Z1 only) */
+  QAD_K_COUNT = 15
 };
 int qad_profile_enable(int on);
 int qad_profile_reset(void);

@@ -18,11 +18,11 @@ QAD_ERR_SCRATCH_LIMIT = -6
 QAD_NOALLOC_MAX_EXPERTS, QAD_NOALLOC_MAX_PAIRS = 256, 262144
 QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW, QAD_FMT_NVFP4A16, QAD_FMT_W8A8, QAD_FMT_W4AFP8 = range(6)
 QAD_DEV_BAD_INDEX, QAD_DEV_DUP_INDEX, QAD_DEV_TIMEOUT = 1, 2, 4
-QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT = 1, 2
+QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT, QAD_FLAG_RECOMPUTE = 1, 2, 4
 VIEWS = ["HEADER", "OFFSETS", "COUNTS", "ROW_TOKEN", "ROW_SLOT", "ROW_OF", "W13_HAT", "W2_HAT", "A1", "Z1", "H",
          "H_HAT", "Y", "DY", "DZ1", "DA1", "XQ"]
 VIEW = {n: i for i, n in enumerate(VIEWS)}
-KERNELS = 14
+KERNELS = 15
 
 EXPORTS = ["qad_fakequant_fwd", "qad_moe_workspace_bytes", "qad_moe_fwd", "qad_moe_bwd_dgrad",
            "qad_moe_bwd_scalegrad", "qad_check_device_error", "qad_status_string", "qad_moe_debug_view",

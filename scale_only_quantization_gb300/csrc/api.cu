@@ -91,7 +91,8 @@ void prof_end(int id, cudaStream_t st) {
 int layout_of(const qad_moe_shape& s, Layout* L) {
   if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
   if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_W4AFP8) return QAD_ERR_INVALID_ARG;
-  if (s.reserved != 0 || (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT))) return QAD_ERR_INVALID_ARG;
+  if (s.reserved != 0 || (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT | QAD_FLAG_RECOMPUTE)))
+    return QAD_ERR_INVALID_ARG;
   if (s.d % 256 || s.F % 128) return QAD_ERR_UNSUPPORTED;
   if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
   const int64_t R = s.T * (int64_t)s.topk;
@@ -118,10 +119,14 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->w13h = take(2 * (size_t)(E * 2 * F * d));
   L->w2h = take(2 * (size_t)(E * d * F));
   L->a1 = take(2 * (size_t)(Rmax * d));
-  L->z1 = take(2 * (size_t)(Rmax * 2 * F));
+  // with QAD_FLAG_RECOMPUTE (and d >= 2F) Z1 lives in Y's region: it only exists between the
+  // dgrad call's recompute and its SwiGLU backward, after Y has been read for dprobs
+  const bool z1_in_y = (s.flags & QAD_FLAG_RECOMPUTE) && d >= 2 * F;
+  L->z1 = z1_in_y ? 0 : take(2 * (size_t)(Rmax * 2 * F));
   L->h = take(2 * (size_t)(Rmax * F));
   L->hh = take(2 * (size_t)(Rmax * F));
   L->y = take(2 * (size_t)(Rmax * d));
+  if (z1_in_y) L->z1 = L->y;
   L->dy = take(2 * (size_t)(Rmax * d));
   L->dz1 = take(2 * (size_t)(Rmax * 2 * F));
   L->da1 = take(2 * (size_t)(Rmax * d));
@@ -232,7 +237,7 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
   QAD_TRY(launch_scatter_tokens(c.aq, x, wsb + L.xq, wsb + L.a1, reinterpret_cast<const int32_t*>(wsb + L.row_of),
                                 row_token, L.T, (int)L.k, L.d, rpad, st));
   QAD_TRY(gemm_prepare(c));
-  QAD_TRY(gemm_fc1(c));
+  QAD_TRY(gemm_fc1(c, (s->flags & QAD_FLAG_RECOMPUTE) ? kFc1NoZ1 : kFc1Full));
   if (row_scaled(c.aq)) QAD_TRY(launch_act_quant_rows(c.aq, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
   QAD_TRY(gemm_fc2(c));
   QAD_TRY(launch_combine(wsb + L.y, reinterpret_cast<const int32_t*>(wsb + L.row_of), topk_w, out, L.T, (int)L.k,
@@ -257,6 +262,7 @@ int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* top
                             reinterpret_cast<const int32_t*>(wsb + L.row_token), wsb + L.y, wsb + L.dy, dprobs, L.T,
                             (int)L.k, L.d, rpad, st));
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
+  if (s->flags & QAD_FLAG_RECOMPUTE) QAD_TRY(gemm_fc1(c, kFc1Z1Only));  // Z1 again, after Y's last use
   QAD_TRY(gemm_dgrad_fc2(c));
   QAD_TRY(gemm_dgrad_fc1(c));
   QAD_TRY(launch_combine(wsb + L.da1, reinterpret_cast<const int32_t*>(wsb + L.row_of), nullptr, dx, L.T, (int)L.k,
@@ -365,7 +371,8 @@ const char* qad_kernel_name(int id) {
   static const char* names[QAD_K_COUNT] = {"fakequant_w", "route_permute", "act_quant", "gather_rows",
                                            "gemm_fc1_swiglu_aq", "gemm_fc2", "combine", "dy_gather",
                                            "gemm_dgrad_fc2_swiglu_bwd", "gemm_dgrad_fc1", "dx_combine",
-                                           "gemm_wgrad_fc2_scalegrad", "gemm_wgrad_fc1_scalegrad", "scale_reduce"};
+                                           "gemm_wgrad_fc2_scalegrad", "gemm_wgrad_fc1_scalegrad", "scale_reduce",
+                                           "gemm_fc1_recompute"};
   return (id >= 0 && id < QAD_K_COUNT) ? names[id] : "unknown";
 }
 

@@ -63,6 +63,7 @@ struct Params {
   int b_rows;                   // rows of the B tensor map per expert
   int F;                        // expert FFN width (fc1 / SwiGLU epilogues)
   int wq, aq, flags;  // weight grid (LSQ), activation grid of the fc1 epilogue (kQNone: none)
+  int fc1_mode;       // kFc1Full, kFc1NoZ1 or kFc1Z1Only
   __nv_bfloat16* out3; int64_t ld_out2;  // FC1: H, kept besides H_hat with QAD_FLAG_STASH_H
   // (the tiles the epilogues produce are written through the kernel's store tensor maps)
   const __nv_bfloat16* aux; int64_t ld_aux;  // SWIGLU_BWD: Z1
@@ -347,7 +348,7 @@ __device__ __forceinline__ void store_box16(BoxRing& ring, const CUtensorMap* tm
   ring.slot = (ring.slot + 1u) & 3u;
 }
 
-// Z1 (bf16) and H = bf16(silu(gate) * up) for 64 of the tile's 128 FFN columns (this warp's
+// Z1 (bf16; not with kFc1NoZ1) and H = bf16(silu(gate) * up) (not with kFc1Z1Only) for 64 of the tile's 128 FFN columns (this warp's
 // half), 16 at a time (one activation-quant block); H_hat = AQ(H) for the E2M1 (per 16)
 // activation grid, = H without activation quant; the per-row grids (E4M3, INT8) need the
 // row amax over all F columns, so H goes to the H buffer and a separate pass quantizes it.
@@ -381,6 +382,11 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
       gv[i] = round_bf16(__uint_as_float(g[i]));
       uv[i] = round_bf16(__uint_as_float(u[i]));
     }
+    if (p.fc1_mode != kFc1NoZ1) {
+      store_box16(ring, tm_z1, lane, gv, f0, y);
+      store_box16(ring, tm_z1, lane, uv, p.F + f0, y);
+    }
+    if (p.fc1_mode != kFc1Z1Only) {
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {  // H = silu(g) u, two lanes at a time
       const uint64_t g2 = f2pack(gv[i], gv[i + 1]);
@@ -388,8 +394,6 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
       h[i] = round_bf16(hv.x);
       h[i + 1] = round_bf16(hv.y);
     }
-    store_box16(ring, tm_z1, lane, gv, f0, y);
-    store_box16(ring, tm_z1, lane, uv, p.F + f0, y);
     if (extra_h) {
       uint4* hs = reinterpret_cast<uint4*>(hrow + f0);
       hs[0] = pack8(h);
@@ -402,6 +406,7 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
       fakequant_act_inplace<kQE2M1, 16>(h, __fdiv_rn(amax, 6.0f));
     }
     store_box16(ring, tm_h, lane, h, f0, y);
+    }
     if (j < 3) {
       tmem_wait16x2(gn, un);
 #pragma unroll
@@ -1020,9 +1025,10 @@ cudaError_t gemm_prepare(const GemmCtx& c) {
   return cudaGetLastError();
 }
 
-cudaError_t gemm_fc1(const GemmCtx& c) {
+cudaError_t gemm_fc1(const GemmCtx& c, int mode) {
   const Layout& L = *c.L;
   Params p = base_params(c);
+  p.fc1_mode = mode;
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.a1, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
   if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
@@ -1034,8 +1040,8 @@ cudaError_t gemm_fc1(const GemmCtx& c) {
   CUtensorMap tz, th;
   if (!make_store_tmap(&tz, c.ws + L.z1, 2 * L.F, L.Rmax, 2 * L.F, 16)) return cudaErrorInvalidValue;
   if (!make_store_tmap(&th, c.ws + (row_scaled(c.aq) ? L.h : L.hh), L.F, L.Rmax, L.F, 16)) return cudaErrorInvalidValue;
-  return launch<256, false, false, EPI_FC1>(ta, tb, tz, th, p, (L.Rmax / BM) * (int64_t)p.n_ntiles, QAD_K_GEMM_FC1,
-                                            c.st);
+  return launch<256, false, false, EPI_FC1>(ta, tb, tz, th, p, (L.Rmax / BM) * (int64_t)p.n_ntiles,
+                                            mode == kFc1Z1Only ? QAD_K_GEMM_FC1_RECOMPUTE : QAD_K_GEMM_FC1, c.st);
 }
 
 cudaError_t gemm_fc2(const GemmCtx& c) {

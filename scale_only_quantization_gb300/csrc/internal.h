@@ -82,7 +82,10 @@ struct GemmCtx {
   const void* w2h;   // or the caller's raw weights for the unquantized teacher pass
 };
 cudaError_t gemm_prepare(const GemmCtx& c);     // pair-tile table of the row-mode GEMMs (after routing)
-cudaError_t gemm_fc1(const GemmCtx& c);         // Z1, H, H_hat  <- A1 . W13_hat^T (+ SwiGLU, AQ)
+// fc1 epilogue modes: everything; everything but Z1 (recompute, forward); only Z1 (recompute,
+// backward: the same mainloop, so the same Z1 bits)
+enum { kFc1Full = 0, kFc1NoZ1 = 1, kFc1Z1Only = 2 };
+cudaError_t gemm_fc1(const GemmCtx& c, int mode);  // Z1, H, H_hat  <- A1 . W13_hat^T (+ SwiGLU, AQ)
 cudaError_t gemm_fc2(const GemmCtx& c);         // Y <- H_hat . W2_hat^T
 cudaError_t gemm_dgrad_fc2(const GemmCtx& c);   // dZ1 <- SwiGLU'(dY . W2_hat)
 cudaError_t gemm_dgrad_fc1(const GemmCtx& c);   // dA1 <- dZ1 . W13_hat

@@ -89,3 +89,20 @@ def test_status_strings(lib):
     for st in (0, -1, -2, -3, -4, -5):
         assert Q.status_string(st)
     assert Q.qad_kernel_name(4) == "gemm_fc1_swiglu_aq"
+
+
+def test_recompute_flag_shares_z1_with_y(lib):
+    """QAD_FLAG_RECOMPUTE: Z1 is not kept between the calls, so when d >= 2F it lives in Y's
+    region and the workspace is smaller by exactly that region; unknown flag bits are rejected."""
+    T, d, F, E, k = 512, 256, 128, 4, 2
+    Rmax = (T * k + 127 * E + 127) // 128 * 128
+    s0 = Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4)
+    s1 = Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4, Q.QAD_FLAG_RECOMPUTE)
+    assert Q.qad_moe_workspace_bytes(s0) - Q.qad_moe_workspace_bytes(s1) == 2 * Rmax * 2 * F
+    assert Q.qad_moe_debug_view(s1, "Z1")[0] == Q.qad_moe_debug_view(s1, "Y")[0]
+    assert Q.qad_moe_debug_view(s0, "Z1")[0] != Q.qad_moe_debug_view(s0, "Y")[0]
+    # d < 2F: Y is too small to hold Z1, nothing is shared
+    s2 = Q.shape(T, d, 256, E, k, Q.QAD_FMT_NVFP4, Q.QAD_FLAG_RECOMPUTE)
+    s3 = Q.shape(T, d, 256, E, k, Q.QAD_FMT_NVFP4)
+    assert Q.qad_moe_workspace_bytes(s2) == Q.qad_moe_workspace_bytes(s3)
+    assert Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4, 8)) == 0

@@ -129,3 +129,21 @@ def test_full_size_sampled(name):
     if pad.size:
         for nm, cols in (("A1", d), ("DY", d), ("H_HAT", F), ("DZ1", 2 * F)):
             assert np.all(_rows(run, nm, cols, pad) == 0), nm
+
+
+def test_recompute_matches_stash_at_full_size():
+    """qwen3_30b_a3b_nvfp4 with QAD_FLAG_RECOMPUTE: outputs and scale gradients equal the
+    stashing run's bit for bit, in a workspace smaller by the Z1 region."""
+    inp = synth.make_inputs(synth.workload("qwen3_30b_a3b_nvfp4"), seed=11, device="cuda")
+    a = Run(inp, flags=0)
+    out, dx, dprobs, ds13, ds2 = a.out.clone(), a.dx.clone(), a.dprobs.clone(), a.ds13.clone(), a.ds2.clone()
+    nb_a = a.ws.numel()
+    del a
+    torch.cuda.empty_cache()
+    b = Run(inp, flags=Q.QAD_FLAG_RECOMPUTE)
+    assert b.error == 0
+    assert b.ws.numel() < nb_a
+    assert torch.equal(out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(dx.view(torch.int16), b.dx.view(torch.int16))
+    assert torch.equal(dprobs, b.dprobs)
+    assert torch.equal(ds13, b.ds13) and torch.equal(ds2, b.ds2)

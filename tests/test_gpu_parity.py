@@ -189,6 +189,23 @@ def test_stash_h_flag_off_matches_on():
     assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
 
 
+@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_INT4_G128])
+def test_recompute_matches_stash_bit_for_bit(fmt):
+    """QAD_FLAG_RECOMPUTE drops the Z1 stash and reruns fc1 in the dgrad call: the same
+    mainloop over the same tiles, so every output and gradient is identical bit for bit."""
+    inp = _tiny(fmt)
+    a = Run(inp, flags=0)
+    b = Run(inp, flags=Q.QAD_FLAG_RECOMPUTE)
+    assert a.error == 0 and b.error == 0
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
+    assert torch.equal(a.dprobs, b.dprobs)
+    assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
+    F = inp["F"]
+    assert np.array_equal(a.rows_bits("Z1", 2 * F), b.rows_bits("Z1", 2 * F))
+    assert np.array_equal(a.rows_bits("DZ1", 2 * F), b.rows_bits("DZ1", 2 * F))
+
+
 def test_runs_are_deterministic():
     inp = _tiny(Q.QAD_FMT_NVFP4)
     a, b = Run(inp), Run(inp)
