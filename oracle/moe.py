@@ -170,8 +170,14 @@ def _values(a):
 
 
 def moe_forward(fmt, x_bits, topk_idx, topk_w, w13_bits, s13, w2_bits, s2,
-                quant=True, round_bf16=True):
-    """Forward of one MoE layer; returns out (fp64 on the bf16 grid) and the stash."""
+                quant=True, round_bf16=True, factored=False):
+    """Forward of one MoE layer; returns out (fp64 on the bf16 grid) and the stash.
+
+    factored=True (per-row scaled formats): the two forward GEMMs contract the quantization
+    codes and apply the per-row weight and activation scales to the sum, i.e. they use
+    q * s unrounded (the scales leave the contraction exactly in real arithmetic); the
+    Ŵ13, Ŵ2, Â1 and Ĥ kept for the backward are the rounded fake-quant values as usual.
+    """
     E = w13_bits.shape[0]
     rt = route(topk_idx, E)
     off = rt["offsets"]
@@ -184,10 +190,18 @@ def moe_forward(fmt, x_bits, topk_idx, topk_w, w13_bits, s13, w2_bits, s2,
     else:
         w13h, w2h = _values(w13_bits), _values(w2_bits)
         a1 = x[rt["row_token"]]
-    z1 = _maybe_round(grouped_gemm_nt(a1, w13h, off), round_bf16)
+    if quant and factored:
+        a1f = Q.fakequant_act_factored(fmt, x)[rt["row_token"]]
+        z1 = _maybe_round(grouped_gemm_nt(a1f, Q.fakequant_weight_factored(fmt, w13_bits, s13), off), round_bf16)
+    else:
+        z1 = _maybe_round(grouped_gemm_nt(a1, w13h, off), round_bf16)
     h = _maybe_round(swiglu(z1), round_bf16)
     hh = Q.fakequant_act(fmt, h) if quant else h
-    y = _maybe_round(grouped_gemm_nt(hh, w2h, off), round_bf16)
+    if quant and factored:
+        y = _maybe_round(grouped_gemm_nt(Q.fakequant_act_factored(fmt, h),
+                                         Q.fakequant_weight_factored(fmt, w2_bits, s2), off), round_bf16)
+    else:
+        y = _maybe_round(grouped_gemm_nt(hh, w2h, off), round_bf16)
     out = _maybe_round(combine(y, p, rt["row_of"]), round_bf16)
     return dict(out=out, route=rt, w13h=w13h, w2h=w2h, a1=a1, z1=z1, h=h, hh=hh, y=y)
 

@@ -205,6 +205,25 @@ def fakequant_weight(fmt, w_bits, scale):
     return _dequant(q_fmt(fmt, x), s)
 
 
+def fakequant_weight_factored(fmt, w_bits, scale):
+    """q(fp32(W / s)) * s in fp64, the product not rounded: the weight a GEMM applies when its
+    per-row scale is factored out of the contraction and multiplied into the accumulator
+    (native low-precision MMA on the codes q).  The codes are those of fakequant_weight, so
+    rounding this to fp32 and then bf16 gives fakequant_weight exactly."""
+    _, s, x = weight_quotient(fmt, w_bits, scale)
+    return q_fmt(fmt, x) * s
+
+
+def fakequant_act_factored(fmt, a):
+    """q(fp32(a / s_a)) * s_a in fp64, not rounded (see fakequant_weight_factored)."""
+    a = np.asarray(a, dtype=np.float64)
+    kind = ACT_Q[fmt]
+    if kind is None:
+        return a.copy()
+    s = act_scale(fmt, a)
+    return Q_FUNC[kind](_quotient(a, s)) * s
+
+
 def act_scale(fmt, a):
     """Dynamic activation scale per block along the last axis (detached, not learnable).
 

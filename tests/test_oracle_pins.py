@@ -440,3 +440,90 @@ def test_finite_differences_of_the_ste_free_layer():
             fd = (loss(plus["x"], plus["w13"], plus["w2"], plus["p"])
                   - loss(minus["x"], minus["w13"], minus["w2"], minus["p"])) / (2 * h)
             assert abs(fd - grad[i]) <= 1e-6 * max(1.0, abs(fd)), (name, i, fd, grad[i])
+
+
+# ---------------------------------------------------------------- scale-factored forward
+# Per-row scaled formats: the forward GEMMs may contract the codes and apply the weight-row
+# and activation-row scales to the sum (native low-precision MMA).  The pins tie that
+# reading to the rounded fake-quant one.
+
+def _bits(t):
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _row_layer(fmt, T=40, E=3, d=64, F=32, k=2, seed=21, pow2=False):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((T, d), generator=g).clamp(-1.7, 1.7)
+    w13 = torch.randn((E, 2 * F, d), generator=g) * 0.05
+    w2 = torch.randn((E, d, F), generator=g) * 0.05
+    qmax = Q.AMAX_DIV[fmt]
+    if pow2:
+        # every row's amax is qmax * 2^-8, so the dynamic scale fp32(amax / qmax) is 2^-8 exactly,
+        # and the weight scales are powers of two: q * s is then exact in bf16
+        x = x * (qmax / 448.0)
+        x[:, 0] = torch.where(torch.rand(T, generator=g) < 0.5, -1.0, 1.0) * qmax * 2.0 ** -8
+    def scales(w):
+        amax = w.to(torch.bfloat16).float().abs().amax(-1, keepdim=True)
+        s = amax / qmax
+        if pow2:
+            return torch.exp2(torch.round(torch.log2(s))).numpy()
+        return (s * (1 + (torch.rand(s.shape, generator=g) * 0.2 - 0.1))).numpy()
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).numpy()
+    p = torch.softmax(torch.randn((T, k), generator=g), 1).numpy()
+    return dict(x=_bits(x), w13=_bits(w13), w2=_bits(w2), s13=scales(w13), s2=scales(w2), idx=idx, p=p)
+
+
+@pytest.mark.parametrize("fmt", [Q.FMT_FP8_ROW, Q.FMT_W8A8])
+def test_factored_values_round_to_the_fake_quant_values(fmt):
+    L = _row_layer(fmt)
+    wf = Q.fakequant_weight_factored(fmt, L["w13"], L["s13"])
+    assert np.array_equal(Q.f64_to_bf16_bits(Q.round_bf16(Q.round_f32(wf))),
+                          Q.f64_to_bf16_bits(Q.fakequant_weight(fmt, L["w13"], L["s13"])))
+    x = Q.bf16_to_f64(L["x"])
+    af = Q.fakequant_act_factored(fmt, x)
+    assert np.array_equal(Q.round_bf16(Q.round_f32(af)), Q.fakequant_act(fmt, x))
+    # the unrounded product is within the fp32-then-bf16 rounding of the stored value
+    for f, r in ((wf, Q.fakequant_weight(fmt, L["w13"], L["s13"])), (af, Q.fakequant_act(fmt, x))):
+        assert np.all(np.abs(f - r) <= 2.0 ** -8 * np.abs(f) + 1e-300)
+
+
+@pytest.mark.parametrize("fmt", [Q.FMT_FP8_ROW, Q.FMT_W8A8])
+def test_factored_fc1_equals_rounded_fc1_for_power_of_two_scales(fmt):
+    L = _row_layer(fmt, pow2=True)
+    args = (fmt, L["x"], L["idx"], L["p"], L["w13"], L["s13"], L["w2"], L["s2"])
+    a = M.moe_forward(*args, factored=False)
+    b = M.moe_forward(*args, factored=True)
+    assert np.array_equal(a["z1"], b["z1"]) and np.array_equal(a["h"], b["h"])
+    assert np.array_equal(a["hh"], b["hh"])
+    # with random scales the two readings differ, by about the bf16 rounding of q * s
+    L = _row_layer(fmt)
+    args = (fmt, L["x"], L["idx"], L["p"], L["w13"], L["s13"], L["w2"], L["s2"])
+    a = M.moe_forward(*args, factored=False, round_bf16=False)
+    b = M.moe_forward(*args, factored=True, round_bf16=False)
+    rms = np.sqrt(np.mean(a["z1"] ** 2))
+    assert 0 < np.abs(a["z1"] - b["z1"]).max() < 2e-2 * rms
+
+
+def test_factored_fc1_is_the_scaled_integer_code_product():
+    """E4M3 values are multiples of 2^-9, so the code contraction is an exact integer dot
+    product; fc1's unrounded output must be s_a[row] * s_w[n] times it (rows in the oracle's
+    expert-grouped order, W13 rows as output columns)."""
+    fmt = Q.FMT_FP8_ROW
+    L = _row_layer(fmt)
+    out = M.moe_forward(fmt, L["x"], L["idx"], L["p"], L["w13"], L["s13"], L["w2"], L["s2"],
+                        factored=True, round_bf16=False)
+    rt = out["route"]
+    x = Q.bf16_to_f64(L["x"])
+    sa = Q.round_f32(np.abs(x).max(axis=1) / 448.0)                        # [T]
+    qa = np.rint(Q.q_e4m3(Q.round_f32(x / sa[:, None])) * 512).astype(np.int64)
+    w = Q.bf16_to_f64(L["w13"])
+    sw = L["s13"][..., 0].astype(np.float64)                               # [E, 2F]
+    qw = np.rint(Q.q_e4m3(Q.round_f32(w / sw[..., None])) * 512).astype(np.int64)
+    off = rt["offsets"]
+    for e in range(w.shape[0]):
+        rows = range(off[e], off[e + 1])
+        toks = rt["row_token"][off[e]:off[e + 1]]
+        want = (qa[toks] @ qw[e].T).astype(np.float64) / 2.0 ** 18 * sa[toks][:, None] * sw[e][None, :]
+        got = out["z1"][off[e]:off[e + 1]]
+        # fp64 rounding of the oracle's sum only (cancellation makes the error absolute)
+        assert np.abs(got - want).max() <= 1e-12 * np.abs(want).max(), e
