@@ -90,7 +90,7 @@ enum {
                             qad_moe_bwd_dgrad then use the raw bf16 weights and bf16
                             activations; the scales are not read (pass any valid pointer)
                             and qad_moe_bwd_scalegrad returns QAD_ERR_INVALID_ARG. */
-  QAD_FLAG_RECOMPUTE = 4 /* recompute instead of stash ("MCoreQAD Backend", performance notes:
+  QAD_FLAG_RECOMPUTE = 4, /* recompute instead of stash ("MCoreQAD Backend", performance notes:
                             full activation recomputation for large models): qad_moe_fwd does
                             not keep the fc1 output Z1, and qad_moe_bwd_dgrad recomputes it
                             (one more fc1 GEMM, identical values) before its SwiGLU backward.
@@ -98,6 +98,14 @@ enum {
                             longer needed once the dgrad call has used it for dprobs), so
                             qad_moe_workspace_bytes is smaller by about 4·Rmax·F bytes.  The
                             fwd, dgrad and scalegrad calls of one step must use the same flags. */
+  QAD_FLAG_NATIVE_FP8 = 8 /* fp8 format (QAD_FMT_FP8_ROW) only: the forward GEMMs contract the
+                            E4M3 codes on the fp8 tensor path (tcgen05 kind::f8f6f4) and apply
+                            the per-row weight and activation scales to the fp32 sums -- the
+                            scales leave the contraction exactly ("MCoreQAD Backend", Support
+                            Matrix: fp8 W8A8 per-channel/per-token), so q*s is not rounded to
+                            bf16 before the products.  Also writes the codes and row scales to
+                            the workspace; the backward is unchanged (bf16 fake-quant copies).
+                            Any other format, or QAD_FLAG_NO_QUANT, gives QAD_ERR_INVALID_ARG. */
 };
 
 /* Shape of one MoE layer. T tokens, hidden d, expert FFN width F, E experts, top-k. */
@@ -189,7 +197,14 @@ enum {
   QAD_VIEW_DZ1 = 14,       /* bf16 [Rmax, 2F] */
   QAD_VIEW_DA1 = 15,       /* bf16 [Rmax, d] */
   QAD_VIEW_XQ = 16,        /* bf16 [T, d]: AQ(x) per token */
-  QAD_VIEW_COUNT = 17
+  /* QAD_FLAG_NATIVE_FP8 only (count 0 otherwise): */
+  QAD_VIEW_W13_CODES = 17, /* uint8 [E, 2F, d]: E4M3 codes of W13 */
+  QAD_VIEW_W2_CODES = 18,  /* uint8 [E, d, F] */
+  QAD_VIEW_A1_CODES = 19,  /* uint8 [Rmax, d]: E4M3 codes of the routed activation rows */
+  QAD_VIEW_H_CODES = 20,   /* uint8 [Rmax, F] */
+  QAD_VIEW_A_SCALE = 21,   /* fp32 [T]: activation scale fp32(row amax / 448) of each token */
+  QAD_VIEW_H_SCALE = 22,   /* fp32 [Rmax]: the same for each row of H */
+  QAD_VIEW_COUNT = 23
 };
 int qad_moe_debug_view(const qad_moe_shape* s, int which, size_t* byte_offset, int64_t* numel);
 

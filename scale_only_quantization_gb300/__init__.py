@@ -18,9 +18,10 @@ QAD_ERR_SCRATCH_LIMIT = -6
 QAD_NOALLOC_MAX_EXPERTS, QAD_NOALLOC_MAX_PAIRS = 256, 262144
 QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW, QAD_FMT_NVFP4A16, QAD_FMT_W8A8, QAD_FMT_W4AFP8 = range(6)
 QAD_DEV_BAD_INDEX, QAD_DEV_DUP_INDEX, QAD_DEV_TIMEOUT = 1, 2, 4
-QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT, QAD_FLAG_RECOMPUTE = 1, 2, 4
+QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT, QAD_FLAG_RECOMPUTE, QAD_FLAG_NATIVE_FP8 = 1, 2, 4, 8
 VIEWS = ["HEADER", "OFFSETS", "COUNTS", "ROW_TOKEN", "ROW_SLOT", "ROW_OF", "W13_HAT", "W2_HAT", "A1", "Z1", "H",
-         "H_HAT", "Y", "DY", "DZ1", "DA1", "XQ"]
+         "H_HAT", "Y", "DY", "DZ1", "DA1", "XQ", "W13_CODES", "W2_CODES", "A1_CODES", "H_CODES", "A_SCALE",
+         "H_SCALE"]
 VIEW = {n: i for i, n in enumerate(VIEWS)}
 KERNELS = 15
 

@@ -91,7 +91,10 @@ void prof_end(int id, cudaStream_t st) {
 int layout_of(const qad_moe_shape& s, Layout* L) {
   if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
   if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_W4AFP8) return QAD_ERR_INVALID_ARG;
-  if (s.reserved != 0 || (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT | QAD_FLAG_RECOMPUTE)))
+  if (s.reserved != 0 ||
+      (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT | QAD_FLAG_RECOMPUTE | QAD_FLAG_NATIVE_FP8)))
+    return QAD_ERR_INVALID_ARG;
+  if ((s.flags & QAD_FLAG_NATIVE_FP8) && (s.fmt != QAD_FMT_FP8_ROW || (s.flags & QAD_FLAG_NO_QUANT)))
     return QAD_ERR_INVALID_ARG;
   if (s.d % 256 || s.F % 128) return QAD_ERR_UNSUPPORTED;
   if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
@@ -132,6 +135,16 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->da1 = take(2 * (size_t)(Rmax * d));
   L->part13 = take(4 * (size_t)(E * 2 * F * (d / 128) * 2));
   L->part2 = take(4 * (size_t)(E * d * (F / 128) * 2));
+  L->native_fp8 = (s.flags & QAD_FLAG_NATIVE_FP8) != 0;
+  L->w13q = L->w2q = L->a1q = L->hq = L->sa_tok = L->sh_row = 0;
+  if (L->native_fp8) {
+    L->w13q = take((size_t)(E * 2 * F * d));
+    L->w2q = take((size_t)(E * d * F));
+    L->a1q = take((size_t)(Rmax * d));
+    L->hq = take((size_t)(Rmax * F));
+    L->sa_tok = take(4 * (size_t)(s.T > 0 ? s.T : 1));
+    L->sh_row = take(4 * (size_t)Rmax);
+  }
   L->total = o;
   return QAD_OK;
 }
@@ -176,6 +189,8 @@ GemmCtx gemm_ctx(const Layout& L, uint8_t* wsb, const qad_moe_shape& s, const vo
   c.st = st;
   c.w13h = no_quant ? w13 : static_cast<const void*>(wsb + L.w13h);
   c.w2h = no_quant ? w2 : static_cast<const void*>(wsb + L.w2h);
+  c.s13 = nullptr;
+  c.s2 = nullptr;
   return c;
 }
 
@@ -228,17 +243,23 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
   const bool no_quant = (s->flags & QAD_FLAG_NO_QUANT) != 0;
   QAD_TRY(cudaMemsetAsync(hdr, 0, 256, st));
   QAD_TRY(launch_route(topk_idx, L, wsb, st));
+  const bool f8 = L.native_fp8;  // E4M3 codes for the fp8 tensor path as well
   if (!no_quant) {
-    QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st));
-    QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st));
+    QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
+    QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st, f8 ? wsb + L.w2q : nullptr));
   }
   const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
+  c.s13 = s13;
+  c.s2 = s2;
   QAD_TRY(launch_scatter_tokens(c.aq, x, wsb + L.xq, wsb + L.a1, reinterpret_cast<const int32_t*>(wsb + L.row_of),
-                                row_token, L.T, (int)L.k, L.d, rpad, st));
+                                row_token, L.T, (int)L.k, L.d, rpad, st, f8 ? wsb + L.a1q : nullptr,
+                                f8 ? reinterpret_cast<float*>(wsb + L.sa_tok) : nullptr));
   QAD_TRY(gemm_prepare(c));
   QAD_TRY(gemm_fc1(c, (s->flags & QAD_FLAG_RECOMPUTE) ? kFc1NoZ1 : kFc1Full));
-  if (row_scaled(c.aq)) QAD_TRY(launch_act_quant_rows(c.aq, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st));
+  if (row_scaled(c.aq))
+    QAD_TRY(launch_act_quant_rows(c.aq, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st, f8 ? wsb + L.hq : nullptr,
+                                  f8 ? reinterpret_cast<float*>(wsb + L.sh_row) : nullptr));
   QAD_TRY(gemm_fc2(c));
   QAD_TRY(launch_combine(wsb + L.y, reinterpret_cast<const int32_t*>(wsb + L.row_of), topk_w, out, L.T, (int)L.k,
                          L.d, st));
@@ -262,6 +283,8 @@ int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* top
                             reinterpret_cast<const int32_t*>(wsb + L.row_token), wsb + L.y, wsb + L.dy, dprobs, L.T,
                             (int)L.k, L.d, rpad, st));
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
+  c.s13 = s13;
+  c.s2 = s2;
   if (s->flags & QAD_FLAG_RECOMPUTE) QAD_TRY(gemm_fc1(c, kFc1Z1Only));  // Z1 again, after Y's last use
   QAD_TRY(gemm_dgrad_fc2(c));
   QAD_TRY(gemm_dgrad_fc1(c));
@@ -321,6 +344,12 @@ int qad_moe_debug_view(const qad_moe_shape* s, int which, size_t* byte_offset, i
     case QAD_VIEW_DZ1: off = L.dz1; n = Rm * 2 * F; break;
     case QAD_VIEW_DA1: off = L.da1; n = Rm * d; break;
     case QAD_VIEW_XQ: off = L.xq; n = L.T * d; break;
+    case QAD_VIEW_W13_CODES: off = L.w13q; n = L.native_fp8 ? E * 2 * F * d : 0; break;
+    case QAD_VIEW_W2_CODES: off = L.w2q; n = L.native_fp8 ? E * d * F : 0; break;
+    case QAD_VIEW_A1_CODES: off = L.a1q; n = L.native_fp8 ? Rm * d : 0; break;
+    case QAD_VIEW_H_CODES: off = L.hq; n = L.native_fp8 ? Rm * F : 0; break;
+    case QAD_VIEW_A_SCALE: off = L.sa_tok; n = L.native_fp8 ? L.T : 0; break;
+    case QAD_VIEW_H_SCALE: off = L.sh_row; n = L.native_fp8 ? Rm : 0; break;
     default: return QAD_ERR_INVALID_ARG;
   }
   *byte_offset = off;

@@ -214,11 +214,11 @@ __device__ __forceinline__ void quotients_unguarded(const float* w, float s, flo
 }
 __device__ __forceinline__ bool scale_in_fast_range(float s) { return s >= 0x1p-60f && s <= 0x1p60f; }
 
-// Activation fake-quant of n values sharing the dynamic scale s = fp32(amax / Qmax): |x| <=
-// amax / s stays near Qmax, so no overflow is possible; the sign of a zero result is w's.
-template <int QK, int N>
-__device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
-  float x[N];
+// Quotients x = fp32(v / s) of n activation values sharing the dynamic scale s = fp32(amax /
+// Qmax): |x| <= amax / s stays near Qmax, so no overflow is possible; the sign of a zero
+// result is v's.
+template <int N>
+__device__ __forceinline__ void act_quotients(const float* v, float s, float* x) {
   if (scale_in_fast_range(s)) {
     quotients_unguarded<N>(v, s, x);
 #pragma unroll
@@ -227,21 +227,14 @@ __device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
 #pragma unroll
     for (int i = 0; i < N; ++i) x[i] = quotient(v[i], s);
   }
-#pragma unroll
-  for (int i = 0; i < N; i += 2) {
-    const float2 q = q_pair<QK>(x[i], x[i + 1]);
-    v[i] = round_bf16(__fmul_rn(q.x, s));
-    v[i + 1] = round_bf16(__fmul_rn(q.y, s));
-  }
 }
 
-// Fake-quantize n (even) values that share scale s, in place: v <- bf16(fp32(q(v / s) * s)).
-// Weights are arbitrary, so besides the block's scale range the quotients are checked for
-// overflow through one NaN/inf-propagating sum (an overflowing fast quotient gives inf or
-// NaN); a block that fails is recomputed with the per-element guarded form.
-template <int QK, int N>
-__device__ __forceinline__ void fakequant_inplace(float* v, float s) {
-  float x[N];
+// Quotients of n weights sharing scale s.  Weights are arbitrary, so besides the block's
+// scale range the quotients are checked for overflow through one NaN/inf-propagating sum (an
+// overflowing fast quotient gives inf or NaN); a block that fails is recomputed with the
+// per-element guarded form.
+template <int N>
+__device__ __forceinline__ void weight_quotients(const float* v, float s, float* x) {
   bool fast = scale_in_fast_range(s);
   if (fast) {
     quotients_unguarded<N>(v, s, x);
@@ -254,11 +247,64 @@ __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
     fast = probe == 0.0f;
   }
   if (!fast) quotients<N>(v, s, x);
+}
+
+// Activation fake-quant of n values sharing the dynamic scale s, in place.
+template <int QK, int N>
+__device__ __forceinline__ void fakequant_act_inplace(float* v, float s) {
+  float x[N];
+  act_quotients<N>(v, s, x);
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
     const float2 q = q_pair<QK>(x[i], x[i + 1]);
     v[i] = round_bf16(__fmul_rn(q.x, s));
     v[i + 1] = round_bf16(__fmul_rn(q.y, s));
+  }
+}
+
+// Fake-quantize n (even) values that share scale s, in place: v <- bf16(fp32(q(v / s) * s)).
+template <int QK, int N>
+__device__ __forceinline__ void fakequant_inplace(float* v, float s) {
+  float x[N];
+  weight_quotients<N>(v, s, x);
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const float2 q = q_pair<QK>(x[i], x[i + 1]);
+    v[i] = round_bf16(__fmul_rn(q.x, s));
+    v[i + 1] = round_bf16(__fmul_rn(q.y, s));
+  }
+}
+
+// E4M3 codes of a pair (a in the low byte, b in the high byte) and their grid values, signed
+// as q_pair<kQE4M3> signs them.
+__device__ __forceinline__ uint16_t e4m3_codes2(float a, float b, float2* q) {
+  uint16_t p;
+  uint32_t h2;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p) : "f"(a), "f"(b));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(p));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  *q = make_float2(copysignf(__low2float(h), a), copysignf(__high2float(h), b));
+  return p;
+}
+
+// E4M3 fake-quant of N (a multiple of 4) values sharing scale s, in place, also returning
+// their codes (byte i of the N / 4 words = code of value i): the quotients and grid values
+// of fakequant_inplace (ACT = false) or fakequant_act_inplace (ACT = true).
+template <int N, bool ACT>
+__device__ __forceinline__ void fakequant_e4m3_codes(float* v, float s, uint32_t* codes) {
+  float x[N];
+  if constexpr (ACT) act_quotients<N>(v, s, x);
+  else weight_quotients<N>(v, s, x);
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    float2 q0, q1;
+    const uint32_t c0 = e4m3_codes2(x[i], x[i + 1], &q0);
+    const uint32_t c1 = e4m3_codes2(x[i + 2], x[i + 3], &q1);
+    codes[i / 4] = c0 | (c1 << 16);
+    v[i] = round_bf16(__fmul_rn(q0.x, s));
+    v[i + 1] = round_bf16(__fmul_rn(q0.y, s));
+    v[i + 2] = round_bf16(__fmul_rn(q1.x, s));
+    v[i + 3] = round_bf16(__fmul_rn(q1.y, s));
   }
 }
 

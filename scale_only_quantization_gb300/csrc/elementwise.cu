@@ -27,10 +27,23 @@ int grid_for(int64_t items, int threads, int per_sm) {
 // ------------------------------------------------------------------------- weight fake-quant
 
 // One thread per 16 consecutive elements of a row (16 | K, and every scale block is a
-// whole number of 16-element chunks).  `cps` = chunks per scale (1, 8 or K / 16).
-template <int QK>
+// whole number of 16-element chunks).  `cps` = chunks per scale (1, 8 or K / 16).  CODES
+// (E4M3 only): also write each element's E4M3 code byte to `codes` (same layout as w).
+template <int QK, bool CODES = false>
+__device__ __forceinline__ void fakequant_chunk(float* v, float sc, uint4* codes, uint64_t c) {
+  if constexpr (CODES) {
+    uint32_t cw[4];
+    fakequant_e4m3_codes<16, false>(v, sc, cw);
+    st_stream(codes + c, make_uint4(cw[0], cw[1], cw[2], cw[3]));
+  } else {
+    fakequant_inplace<QK, 16>(v, sc);
+  }
+}
+
+template <int QK, bool CODES = false>
 __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict__ w, const float* __restrict__ s,
-                                                        uint4* __restrict__ out, uint64_t nchunks, uint32_t cps) {
+                                                        uint4* __restrict__ out, uint64_t nchunks, uint32_t cps,
+                                                        uint4* __restrict__ codes = nullptr) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (; c + stride < nchunks; c += 2 * stride) {  // two chunks (64 bytes) per thread in flight
@@ -42,12 +55,12 @@ __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict_
     float v[16];
     unpack8(u0, v);
     unpack8(u1, v + 8);
-    fakequant_inplace<QK, 16>(v, sc);
+    fakequant_chunk<QK, CODES>(v, sc, codes, c);
     st_stream(out + 2 * c, pack8(v));
     st_stream(out + 2 * c + 1, pack8(v + 8));
     unpack8(u2, v);
     unpack8(u3, v + 8);
-    fakequant_inplace<QK, 16>(v, sc2);
+    fakequant_chunk<QK, CODES>(v, sc2, codes, c2);
     st_stream(out + 2 * c2, pack8(v));
     st_stream(out + 2 * c2 + 1, pack8(v + 8));
   }
@@ -58,7 +71,7 @@ __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict_
     float v[16];
     unpack8(u0, v);
     unpack8(u1, v + 8);
-    fakequant_inplace<QK, 16>(v, sc);
+    fakequant_chunk<QK, CODES>(v, sc, codes, c);
     st_stream(out + 2 * c, pack8(v));
     st_stream(out + 2 * c + 1, pack8(v + 8));
   }
@@ -243,10 +256,13 @@ __global__ void __launch_bounds__(1024) route_scatter_kernel(const int32_t* __re
 
 // ------------------------------------------------------------------------- activations
 
-// E4M3 / INT8: one warp per row, scale fp32(row amax / 448) or fp32(row amax / 127)
-template <int QK>
+// E4M3 / INT8: one warp per row, scale fp32(row amax / 448) or fp32(row amax / 127).  CODES
+// (E4M3): also the code bytes of the row (8 bytes per 8 elements) and the row's scale.
+template <int QK, bool CODES = false>
 __global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                                                            int64_t rows, int64_t cols, const int32_t* dev_rows) {
+                                                            int64_t rows, int64_t cols, const int32_t* dev_rows,
+                                                            uint2* __restrict__ codes = nullptr,
+                                                            float* __restrict__ row_scale = nullptr) {
   const int64_t nrows = dev_rows ? (int64_t)*dev_rows : rows;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
@@ -262,10 +278,19 @@ __global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restr
     }
     amax = warp_max(amax);
     const float s = __fdiv_rn(amax, QK == kQE4M3 ? 448.0f : 127.0f);
+    if constexpr (CODES) {
+      if (lane == 0) row_scale[r] = s;
+    }
     for (int64_t c = lane; c < c8; c += 32) {
       float v[8];
       unpack8(src[c], v);
-      fakequant_act_inplace<QK, 8>(v, s);
+      if constexpr (CODES) {
+        uint32_t cw[2];
+        fakequant_e4m3_codes<8, true>(v, s, cw);
+        codes[r * c8 + c] = make_uint2(cw[0], cw[1]);
+      } else {
+        fakequant_act_inplace<QK, 8>(v, s);
+      }
       out[r * c8 + c] = pack8(v);
     }
   }
@@ -312,16 +337,22 @@ __device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.prox
 // are zeroed.  Lane l holds the 16-element blocks l, l + 32, ... of a 128 x 16-element
 // chunk of the row.  The quantized chunk is staged in the warp's 4 KB of shared memory and
 // lane j < k copies it to routed row j with one bulk copy (plain per-thread stores of the
-// same rows ran at two thirds of the speed).
-template <int AQ>
+// same rows ran at two thirds of the speed).  CODES (E4M3): each routed row also gets the
+// E4M3 code bytes of its elements in a1q (16 bytes per block, staged and bulk-copied the same
+// way) and sa_tok[t] the token's scale.
+template <int AQ, bool CODES = false>
 __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __restrict__ x, uint4* __restrict__ xq,
                                                              uint4* __restrict__ a1, const int32_t* __restrict__ row_of,
                                                              const int32_t* __restrict__ row_token, int64_t T, int k,
-                                                             int64_t nblk, const int32_t* dev_rpad) {
+                                                             int64_t nblk, const int32_t* dev_rpad,
+                                                             uint4* __restrict__ a1q = nullptr,
+                                                             float* __restrict__ sa_tok = nullptr) {
   constexpr int NB = kScatterNB;
   __shared__ __align__(128) uint4 stage_all[8][kStageChunk];
+  __shared__ __align__(128) uint4 cstage_all[CODES ? 8 : 1][CODES ? kStageChunk / 2 : 1];
   const int lane = threadIdx.x & 31;
   uint4* stage = stage_all[threadIdx.x / 32];
+  uint4* cstage = cstage_all[CODES ? threadIdx.x / 32 : 0];
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   for (int64_t t = w0; t < T; t += warps) {
@@ -338,9 +369,13 @@ __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __rest
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
       }
       s_row = __fdiv_rn(warp_max(amax), AQ == kQE4M3 ? 448.0f : 127.0f);
+      if constexpr (CODES) {
+        if (lane == 0) sa_tok[t] = s_row;
+      }
     }
     for (int64_t b0 = 0; b0 < nblk; b0 += 32 * NB) {
       uint4 v[NB][2];
+      uint4 cd[CODES ? NB : 1];
 #pragma unroll
       for (int i = 0; i < NB; ++i) {
         const int64_t b = b0 + 32 * i + lane;
@@ -364,7 +399,13 @@ __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __rest
               for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(f[e]));
               sc = __fdiv_rn(amax, 6.0f);
             }
-            fakequant_act_inplace<AQ, 16>(f, sc);
+            if constexpr (CODES) {
+              uint32_t cw[4];
+              fakequant_e4m3_codes<16, true>(f, sc, cw);
+              cd[i] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            } else {
+              fakequant_act_inplace<AQ, 16>(f, sc);
+            }
             v[i][0] = pack8(f);
             v[i][1] = pack8(f + 8);
             uint4* o = xq + t * nblk * 2 + 2 * b;
@@ -381,19 +422,24 @@ __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __rest
         if (b < nblk) {
           stage[2 * (32 * i + lane)] = v[i][0];
           stage[2 * (32 * i + lane) + 1] = v[i][1];
+          if constexpr (CODES) cstage[32 * i + lane] = cd[i];
         }
       }
       fence_smem_to_async();
       __syncwarp();
       if (lane < k) {
         const int64_t nb_here = nblk - b0 < 32 * NB ? nblk - b0 : 32 * NB;
-        if (my_row >= 0) bulk_store(a1 + (int64_t)my_row * nblk * 2 + 2 * b0, stage, (uint32_t)(nb_here * 32));
+        if (my_row >= 0) {
+          bulk_store(a1 + (int64_t)my_row * nblk * 2 + 2 * b0, stage, (uint32_t)(nb_here * 32));
+          if constexpr (CODES) bulk_store(a1q + (int64_t)my_row * nblk + b0, cstage, (uint32_t)(nb_here * 16));
+        }
         bulk_commit_group();
       }
     }
   }
   if (lane < k) bulk_wait_done();
   zero_pad_rows(a1, row_token, nblk * 2, dev_rpad, w0, warps, lane);
+  if constexpr (CODES) zero_pad_rows(a1q, row_token, nblk, dev_rpad, w0, warps, lane);
 }
 
 // ------------------------------------------------------------------------- combine
@@ -574,7 +620,7 @@ cudaError_t launch_quotient_check(const float* w, const float* s, float* fast, f
 // ------------------------------------------------------------------------- launchers
 
 cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, int64_t rows, int64_t K,
-                             cudaStream_t st) {
+                             cudaStream_t st, void* codes) {
   const uint64_t nchunks = (uint64_t)rows * (uint64_t)(K / 16);
   if (nchunks == 0) return cudaSuccess;
   const int grid = grid_for((int64_t)nchunks, 256, 8);
@@ -584,7 +630,13 @@ cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, 
   switch (weight_kind(fmt)) {
     case kQE2M1: fakequant_kernel<kQE2M1><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 1u); break;
     case kQInt4: fakequant_kernel<kQInt4><<<grid, 256, 0, st>>>(wi, s, o, nchunks, 8u); break;
-    case kQE4M3: fakequant_kernel<kQE4M3><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16)); break;
+    case kQE4M3:
+      if (codes)
+        fakequant_kernel<kQE4M3, true><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16),
+                                                             static_cast<uint4*>(codes));
+      else
+        fakequant_kernel<kQE4M3><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16));
+      break;
     default: fakequant_kernel<kQInt8><<<grid, 256, 0, st>>>(wi, s, o, nchunks, (uint32_t)(K / 16)); break;
   }
   prof_end(QAD_K_FAKEQUANT, st);
@@ -619,11 +671,15 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
 }
 
 cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
-                                  const int32_t* dev_rows, cudaStream_t st) {
+                                  const int32_t* dev_rows, cudaStream_t st, void* codes, float* row_scale) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   if (kind != kQE4M3 && kind != kQInt8) return cudaErrorInvalidValue;
   prof_begin(QAD_K_ACT_QUANT, st);
-  if (kind == kQE4M3) {
+  if (kind == kQE4M3 && codes) {
+    act_quant_row_kernel<kQE4M3, true><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows, static_cast<uint2*>(codes),
+        row_scale);
+  } else if (kind == kQE4M3) {
     act_quant_row_kernel<kQE4M3><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
         static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
   } else {
@@ -636,7 +692,7 @@ cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t r
 
 cudaError_t launch_scatter_tokens(int aq, const void* x, void* xq, void* a1, const int32_t* row_of,
                                   const int32_t* row_token, int64_t T, int k, int64_t d, const int32_t* dev_rpad,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, void* a1q, float* sa_tok) {
   if (T == 0) return cudaSuccess;
   prof_begin(QAD_K_GATHER, st);
   const int grid = grid_for(T * 32, 256, 8);
@@ -645,6 +701,9 @@ cudaError_t launch_scatter_tokens(int aq, const void* x, void* xq, void* a1, con
   uint4* a = static_cast<uint4*>(a1);
   const int64_t nblk = d / 16;
   if (aq == kQE2M1) scatter_tokens_kernel<kQE2M1><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
+  else if (aq == kQE4M3 && a1q)
+    scatter_tokens_kernel<kQE4M3, true><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad,
+                                                              static_cast<uint4*>(a1q), sa_tok);
   else if (aq == kQE4M3) scatter_tokens_kernel<kQE4M3><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
   else if (aq == kQInt8) scatter_tokens_kernel<kQInt8><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
   else scatter_tokens_kernel<kQNone><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);

@@ -64,6 +64,11 @@ struct Params {
   int F;                        // expert FFN width (fc1 / SwiGLU epilogues)
   int wq, aq, flags;  // weight grid (LSQ), activation grid of the fc1 epilogue (kQNone: none)
   int fc1_mode;       // kFc1Full, kFc1NoZ1 or kFc1Z1Only
+  // E4M3 operands (native fp8): the epilogue multiplies the fp32 sum of row r, column n by
+  // row_scale[row_tok ? row_tok[r] : r] * col_scale[e * b_rows + weight row of n]
+  const float* row_scale;
+  const int32_t* row_tok;
+  const float* col_scale;
   __nv_bfloat16* out3; int64_t ld_out2;  // FC1: H, kept besides H_hat with QAD_FLAG_STASH_H
   // (the tiles the epilogues produce are written through the kernel's store tensor maps)
   const __nv_bfloat16* aux; int64_t ld_aux;  // SWIGLU_BWD: Z1
@@ -232,22 +237,33 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12
-// = 1), A/B major in bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 in [17,23),
-// M >> 4 in [24,29); M = 256 for the pair.
-template <int N, bool A_MN, bool B_MN>
+// Instruction descriptor: D fp32 (bits 4-5 = 1); A and B types in bits 7-9 and 10-12 (kind::f16:
+// bf16 = 1; kind::f8f6f4: E4M3 = 0); A/B major in bits 15/16 (0 = K-major, 1 = MN-major),
+// N >> 3 in [17,23), M >> 4 in [24,29); M = 256 for the pair.
+template <int N, bool A_MN, bool B_MN, bool F8 = false>
 __host__ __device__ constexpr uint32_t instr_desc() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+  return (1u << 4) | (F8 ? 0u : ((1u << 7) | (1u << 10))) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-          d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// One pair MMA, 256 x N x 16 (bf16) or 256 x N x 32 (E4M3: kind::f8f6f4); both read 32 bytes
+// of K per operand row.
+template <bool F8>
+__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if constexpr (F8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 // arrive on the barrier at offset `bar` in every CTA of `mask` once the MMAs issued so far are done
 __device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t mask) {
@@ -352,7 +368,7 @@ __device__ __forceinline__ void store_box16(BoxRing& ring, const CUtensorMap* tm
 // half), 16 at a time (one activation-quant block); H_hat = AQ(H) for the E2M1 (per 16)
 // activation grid, = H without activation quant; the per-row grids (E4M3, INT8) need the
 // row amax over all F columns, so H goes to the H buffer and a separate pass quantizes it.
-template <int BN>
+template <int BN, bool F8>
 __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z1, const CUtensorMap* tm_h,
                                         const Tile& ti, uint32_t tbase, int q, int lane, int half, BoxRing& ring) {
   const int row_in_tile = q * 32 + lane;
@@ -364,6 +380,11 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
   // made by a separate pass); with QAD_FLAG_STASH_H and a per-block grid H is also kept.
   const bool extra_h = (p.flags & QAD_FLAG_STASH_H) && !row_aq;
   const int c0 = 64 * half;  // first of this warp's 64 columns within the tile's 128
+  float rs = 1.0f;
+  if constexpr (F8) {
+    const int32_t tok = p.row_tok ? __ldg(p.row_tok + row) : (int32_t)row;
+    rs = tok >= 0 ? __ldg(p.row_scale + tok) : 0.0f;
+  }
   uint32_t g[16], u[16], gn[16], un[16];
   tmem_ld16_issue(tbase + c0, g);
   tmem_ld16_issue(tbase + 128 + c0, u);
@@ -377,10 +398,25 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
     }
     const int f0 = ti.nb * 128 + cc;
     float gv[16], uv[16], h[16];
+    if constexpr (F8) {
+      const float4* cg = reinterpret_cast<const float4*>(p.col_scale + (int64_t)ti.e * p.b_rows + f0);
+      const float4* cu = reinterpret_cast<const float4*>(p.col_scale + (int64_t)ti.e * p.b_rows + p.F + f0);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      gv[i] = round_bf16(__uint_as_float(g[i]));
-      uv[i] = round_bf16(__uint_as_float(u[i]));
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 a = __ldg(cg + i4), b = __ldg(cu + i4);
+        const float sa[4] = {a.x, a.y, a.z, a.w}, sb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          gv[4 * i4 + i] = round_bf16(__fmul_rn(__uint_as_float(g[4 * i4 + i]), __fmul_rn(rs, sa[i])));
+          uv[4 * i4 + i] = round_bf16(__fmul_rn(__uint_as_float(u[4 * i4 + i]), __fmul_rn(rs, sb[i])));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        gv[i] = round_bf16(__uint_as_float(g[i]));
+        uv[i] = round_bf16(__uint_as_float(u[i]));
+      }
     }
     if (p.fc1_mode != kFc1NoZ1) {
       store_box16(ring, tm_z1, lane, gv, f0, y);
@@ -424,9 +460,9 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
 // 64-byte swizzle, which also keeps the shared-memory writes free of bank conflicts) and
 // one lane stores the box with TMA.  A box is rewritten only after the TMA store issued
 // from it two chunks earlier has read it.
-template <int BN>
-__device__ __forceinline__ void epi_store(const CUtensorMap* tmC, const Tile& ti, uint32_t tbase, int q, int lane,
-                                          int half, uint32_t stage_base, uint32_t& buf) {
+template <int BN, bool F8>
+__device__ __forceinline__ void epi_store(const Params& p, const CUtensorMap* tmC, const Tile& ti, uint32_t tbase,
+                                          int q, int lane, int half, uint32_t stage_base, uint32_t& buf) {
   constexpr int NH = BN / 64;  // 32-column chunks per half: 4 or 2
   const int c0 = half * NH;
   uint32_t r[NH][32];
@@ -437,8 +473,26 @@ __device__ __forceinline__ void epi_store(const CUtensorMap* tmC, const Tile& ti
   const int y = (int)ti.row_base + 32 * q;
   const uint32_t row_addr = (uint32_t)lane * 64u;
   const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
+  float rs = 1.0f;
+  if constexpr (F8) {
+    const int64_t row = ti.row_base + 32 * q + lane;
+    const int32_t tok = p.row_tok ? __ldg(p.row_tok + row) : (int32_t)row;
+    rs = tok >= 0 ? __ldg(p.row_scale + tok) : 0.0f;
+  }
 #pragma unroll
   for (int c = 0; c < NH; ++c) {
+    if constexpr (F8) {
+      const float4* cs =
+          reinterpret_cast<const float4*>(p.col_scale + (int64_t)ti.e * p.b_rows + ti.nb * BN + 32 * (c0 + c));
+#pragma unroll
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 a = __ldg(cs + i4);
+        const float sc[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          r[c][4 * i4 + i] = __float_as_uint(__fmul_rn(__uint_as_float(r[c][4 * i4 + i]), __fmul_rn(rs, sc[i])));
+      }
+    }
     const uint32_t box = stage_base + buf * kStageBox;
     if (lane == 0) bulk_wait_read<1>();
     __syncwarp();
@@ -669,14 +723,16 @@ __device__ __forceinline__ void run_scalegrad(const Params& p, const Tile& ti, u
 
 // ---------------------------------------------------------------------------------- kernel
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const Params p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
-  constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN>();
+  static_assert(!F8 || (!A_MN && !B_MN), "E4M3 operands are K-major (forward GEMMs)");
+  constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN, F8>();
+  constexpr int BKE = F8 ? 128 : BK;  // K elements per 128-byte row of a stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a_ring = smem_u32(smem);
@@ -738,13 +794,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto operand_tiles = [&](const Tile& ti, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
       auto box = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) { tma_load_2d(dst, tm, x, y, fb); };
       if (!p.wgrad) {
-        box(sa, &tmA, kb * BK, ti.r0);
+        box(sa, &tmA, kb * BKE, ti.r0);
         if constexpr (!B_MN) {
           if constexpr (EPI == EPI_FC1) {
             // leader: the 128 gate rows of the tile, peer: the matching 128 up rows
-            box(sb, &tmB, kb * BK, ti.e * p.b_rows + (int)rank * p.F + ti.nb * 128);
+            box(sb, &tmB, kb * BKE, ti.e * p.b_rows + (int)rank * p.F + ti.nb * 128);
           } else {
-            box(sb, &tmB, kb * BK, ti.e * p.b_rows + ti.nb * BN + half_n);
+            box(sb, &tmB, kb * BKE, ti.e * p.b_rows + ti.nb * BN + half_n);
           }
         } else {
 #pragma unroll
@@ -809,7 +865,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k = 0; k < BK / 16; ++k) {
           const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, 64 * 128, 1024) : smem_desc(sa + k * 32, 16, 1024);
           const uint64_t bd = B_MN ? smem_desc(sb + k * 2048, 64 * 128, 1024) : smem_desc(sb + k * 32, 16, 1024);
-          mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          mma_issue<F8>(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
         mma_commit(empty_bar(stage), 3);  // frees the slot in both CTAs
         if (++stage == STAGES) {
@@ -846,8 +902,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       if (ti.live) {
-        if constexpr (EPI == EPI_STORE) epi_store<BN>(&tmC, ti, tbase, q, lane, half, my_stage, buf);
-        else if constexpr (EPI == EPI_FC1) epi_fc1<BN>(p, &tmC, &tmD, ti, tbase, q, lane, half, ring);
+        if constexpr (EPI == EPI_STORE) epi_store<BN, F8>(p, &tmC, ti, tbase, q, lane, half, my_stage, buf);
+        else if constexpr (EPI == EPI_FC1) epi_fc1<BN, F8>(p, &tmC, &tmD, ti, tbase, q, lane, half, ring);
         else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<BN>(p, &tmC, ti, tbase, q, lane, half, ring);
         else run_scalegrad<BN>(p, ti, tbase, row_in_tile, half);
       }
@@ -904,6 +960,19 @@ bool make_tmap(CUtensorMap* tm, const void* base, int64_t inner, int64_t outer, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D byte tensor [outer, inner] (E4M3 codes, `ld` bytes per row), box {128, box_rows}, 128B swizzle
+bool make_tmap_u8(CUtensorMap* tm, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Output map of a staged epilogue: [outer, inner] bf16, box {cols, 32} with cols = 32 (64-byte
 // swizzle) or 16 (32-byte swizzle)
 bool make_store_tmap(CUtensorMap* tm, void* base, int64_t inner, int64_t outer, int64_t ld, int cols = 32) {
@@ -918,10 +987,10 @@ bool make_store_tmap(CUtensorMap* tm, void* base, int64_t inner, int64_t outer, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& td,
                    const Params& p, int64_t max_tiles, int kid, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI>;
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, F8>;
   constexpr int SMEM = smem_bytes<BN, EPI>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
@@ -1029,34 +1098,56 @@ cudaError_t gemm_fc1(const GemmCtx& c, int mode) {
   const Layout& L = *c.L;
   Params p = base_params(c);
   p.fc1_mode = mode;
+  const bool f8 = L.native_fp8;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, c.ws + L.a1, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
+  if (f8) {
+    if (!make_tmap_u8(&ta, c.ws + L.a1q, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tb, c.ws + L.w13q, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
+    p.row_scale = at<float>(c.ws, L.sa_tok);
+    p.row_tok = at<int32_t>(c.ws, L.row_token);
+    p.col_scale = c.s13;
+  } else {
+    if (!make_tmap(&ta, c.ws + L.a1, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
+  }
   p.n_ntiles = (int)(L.F / 128);
-  p.num_kb = (int)(L.d / BK);
+  p.num_kb = (int)(L.d / (f8 ? 128 : BK));
   p.b_rows = (int)(2 * L.F);
   p.ld_out2 = L.F;
   p.out3 = at<__nv_bfloat16>(c.ws, L.h);
   CUtensorMap tz, th;
   if (!make_store_tmap(&tz, c.ws + L.z1, 2 * L.F, L.Rmax, 2 * L.F, 16)) return cudaErrorInvalidValue;
   if (!make_store_tmap(&th, c.ws + (row_scaled(c.aq) ? L.h : L.hh), L.F, L.Rmax, L.F, 16)) return cudaErrorInvalidValue;
-  return launch<256, false, false, EPI_FC1>(ta, tb, tz, th, p, (L.Rmax / BM) * (int64_t)p.n_ntiles,
-                                            mode == kFc1Z1Only ? QAD_K_GEMM_FC1_RECOMPUTE : QAD_K_GEMM_FC1, c.st);
+  const int kid = mode == kFc1Z1Only ? QAD_K_GEMM_FC1_RECOMPUTE : QAD_K_GEMM_FC1;
+  const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
+  return f8 ? launch<256, false, false, EPI_FC1, true>(ta, tb, tz, th, p, tiles, kid, c.st)
+            : launch<256, false, false, EPI_FC1>(ta, tb, tz, th, p, tiles, kid, c.st);
 }
 
 cudaError_t gemm_fc2(const GemmCtx& c) {
   const Layout& L = *c.L;
   Params p = base_params(c);
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, c.ws + L.hh, L.F, L.Rmax, L.F, 128)) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.d);
-  if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
+  const bool f8 = L.native_fp8 && bn == 256;
+  if (L.native_fp8 && !f8) return cudaErrorInvalidValue;  // d % 256 == 0 is a layout precondition
+  if (f8) {
+    if (!make_tmap_u8(&ta, c.ws + L.hq, L.F, L.Rmax, L.F, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tb, c.ws + L.w2q, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
+    p.row_scale = at<float>(c.ws, L.sh_row);
+    p.row_tok = nullptr;
+    p.col_scale = c.s2;
+  } else {
+    if (!make_tmap(&ta, c.ws + L.hh, L.F, L.Rmax, L.F, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
+  }
   p.n_ntiles = (int)(L.d / bn);
-  p.num_kb = (int)(L.F / BK);
+  p.num_kb = (int)(L.F / (f8 ? 128 : BK));
   p.b_rows = (int)L.d;
   CUtensorMap tc;
   if (!make_store_tmap(&tc, c.ws + L.y, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
+  if (f8) return launch<256, false, false, EPI_STORE, true>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
   return bn == 256 ? launch<256, false, false, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st)
                    : launch<128, false, false, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
 }

@@ -18,6 +18,10 @@ struct Layout {
   size_t header, counts, offs, chunk_counts, chunk_base, mtile_expert, ptile_row0, ptile_expert, row_token,
       row_slot, row_of;
   size_t xq, w13h, w2h, a1, z1, h, hh, y, dy, dz1, da1, part13, part2;
+  // QAD_FLAG_NATIVE_FP8: E4M3 codes of W13, W2, A1 and H, per-token activation scales and
+  // per-row H scales (all 0 otherwise)
+  bool native_fp8;
+  size_t w13q, w2q, a1q, hq, sa_tok, sh_row;
   size_t total;
 };
 
@@ -34,8 +38,9 @@ void note_launches(int n);  // extra kernels launched inside one profiled region
 int num_sms();
 
 // ---- kernels (each returns the launch's cudaError_t) ----
+// codes (E4M3 weights only, may be null): the E4M3 code byte of every element, [rows, K]
 cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, int64_t rows, int64_t K,
-                             cudaStream_t st);
+                             cudaStream_t st, void* codes = nullptr);
 cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st);
 // the same three routing kernels on explicit buffers (hdr: int32[64], zeroed by the caller;
 // chunk_counts / chunk_base: int32[nchunks * E]; mtile_expert: int32[Rmax / 128])
@@ -46,12 +51,13 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
 // out[r, :] = AQ(in[r, :]) with activation grid `kind` (kQE2M1: per 16, kQE4M3 / kQInt8: per
 // row) for r < rows (or < *dev_rows when dev_rows != nullptr)
 cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
-                                  const int32_t* dev_rows, cudaStream_t st);
+                                  const int32_t* dev_rows, cudaStream_t st, void* codes = nullptr,
+                                  float* row_scale = nullptr);
 // Per token t: xq[t] = AQ(x[t]) (aq != kQNone) and a1[row_of[t, j]] = AQ(x[t]) for its routed
 // rows; the padding rows (row_token < 0) below *dev_rpad are zeroed
 cudaError_t launch_scatter_tokens(int aq, const void* x, void* xq, void* a1, const int32_t* row_of,
                                   const int32_t* row_token, int64_t T, int k, int64_t d, const int32_t* dev_rpad,
-                                  cudaStream_t st);
+                                  cudaStream_t st, void* a1q = nullptr, float* sa_tok = nullptr);
 // out[t, :] = bf16(sum_j p[t, j] * y[row_of[t, j], :]) (p == nullptr: weight 1)
 cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* p, void* out, int64_t T, int k,
                            int64_t d, cudaStream_t st);
@@ -80,6 +86,8 @@ struct GemmCtx {
   cudaStream_t st;
   const void* w13h;  // the weights the GEMMs read: the fake-quantized copies in the workspace,
   const void* w2h;   // or the caller's raw weights for the unquantized teacher pass
+  const float* s13;  // the caller's weight scales (read by the native fp8 forward epilogues)
+  const float* s2;
 };
 cudaError_t gemm_prepare(const GemmCtx& c);     // pair-tile table of the row-mode GEMMs (after routing)
 // fc1 epilogue modes: everything; everything but Z1 (recompute, forward); only Z1 (recompute,

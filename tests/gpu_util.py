@@ -119,6 +119,12 @@ class Run:
         return bits(t)
 
 
+def e4m3_values(codes):
+    """E4M3 (fn) code bytes -> fp64 values (torch's float8_e4m3fn decoding)."""
+    t = torch.as_tensor(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
 def unpadded_row_of(rt):
     """Map padded row indices in row_of to the oracle's unpadded numbering."""
     real = rt["real"]

@@ -21,7 +21,9 @@ pytestmark = pytest.mark.gpu
 
 WORKLOADS = ["qwen3_30b_a3b_nvfp4", "qwen3_30b_a3b_w4a16", "qwen3_30b_a3b_fp8", "large_nvfp4",
              # the remaining formats of the support matrix on the same Qwen3-30B-A3B shapes
-             "qwen3_30b_a3b_nvfp4:3", "qwen3_30b_a3b_nvfp4:4", "qwen3_30b_a3b_nvfp4:5"]
+             "qwen3_30b_a3b_nvfp4:3", "qwen3_30b_a3b_nvfp4:4", "qwen3_30b_a3b_nvfp4:5",
+             # fp8 with the forward GEMMs on the fp8 tensor path (scales applied to the sums)
+             "qwen3_30b_a3b_fp8+native"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,11 +46,13 @@ def _expert_w(run, name, e, n, k):
 
 @pytest.mark.parametrize("name", WORKLOADS)
 def test_full_size_sampled(name):
+    name, _, native = name.partition("+")
     base, _, fmt_override = name.partition(":")
     cfg = synth.workload(base, **({"fmt": int(fmt_override)} if fmt_override else {}))
     inp = synth.make_inputs(cfg, seed=0, device="cuda")
     fmt, T, d, F, E, k = inp["fmt"], inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"]
-    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    factored = native == "native"
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H | (Q.QAD_FLAG_NATIVE_FP8 if factored else 0))
     assert run.error == 0
     rng = np.random.default_rng(0)
 
@@ -96,13 +100,21 @@ def test_full_size_sampled(name):
         a1 = _rows(run, "A1", d, pick)
         assert np.array_equal(OQ.f64_to_bf16_bits(a1), OQ.f64_to_bf16_bits(OQ.fakequant_act(fmt, x)))
         z1 = _rows(run, "Z1", 2 * F, pick)
-        assert_close(z1, a1 @ w13h.T, "Z1 rows e%d" % e)
+        if factored:
+            want_z1 = OQ.fakequant_act_factored(fmt, x) @ OQ.fakequant_weight_factored(fmt, w13_e, s13_e).T
+        else:
+            want_z1 = a1 @ w13h.T
+        assert_close(z1, want_z1, "Z1 rows e%d" % e)
         h = _rows(run, "H", F, pick)
         assert_close(h, OM.swiglu(z1), "H rows e%d" % e)
         hh = _rows(run, "H_HAT", F, pick)
         assert np.array_equal(OQ.f64_to_bf16_bits(hh), OQ.f64_to_bf16_bits(OQ.fakequant_act(fmt, h)))
         y = _rows(run, "Y", d, pick)
-        assert_close(y, hh @ w2h.T, "Y rows e%d" % e)
+        if factored:
+            want_y = OQ.fakequant_act_factored(fmt, h) @ OQ.fakequant_weight_factored(fmt, w2_e, s2_e).T
+        else:
+            want_y = hh @ w2h.T
+        assert_close(y, want_y, "Y rows e%d" % e)
         dy = _rows(run, "DY", d, pick)
         want_dy = OQ.round_bf16(OQ.round_f32(dout * p[toks, slots][:, None]))
         assert np.array_equal(OQ.f64_to_bf16_bits(dy), OQ.f64_to_bf16_bits(want_dy))

@@ -15,7 +15,7 @@ from oracle import moe as OM
 from oracle import quant as OQ
 import synth
 
-from gpu_util import Run, assert_close, assert_scale_grad, bits, host_inputs, unpadded_row_of, vals
+from gpu_util import Run, assert_close, assert_scale_grad, bits, e4m3_values, host_inputs, unpadded_row_of, vals
 
 pytestmark = pytest.mark.gpu
 
@@ -80,8 +80,16 @@ def _check_routing(run, host):
 
 # ------------------------------------------------------------------------------ the layer, stage by stage
 
-def _stagewise(run, host, check_h=True):
-    """Teacher-forced comparison of every stage; returns the GPU stages for further use."""
+def _codes(run, name, n_rows, cols, rows=None):
+    t = run.view(name, torch.uint8).cpu().numpy()[: n_rows * cols].reshape(n_rows, cols)
+    return e4m3_values(t if rows is None else t[rows])
+
+
+def _stagewise(run, host, check_h=True, factored=False):
+    """Teacher-forced comparison of every stage; returns the GPU stages for further use.
+
+    factored: the native fp8 forward (QAD_FLAG_NATIVE_FP8) -- the E4M3 codes and row scales
+    are checked bit for bit and fc1 / fc2 against the oracle's scale-factored GEMMs."""
     inp = run.inp
     fmt, T, d, F, E, k = inp["fmt"], inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"]
     rt, ref = _check_routing(run, host)
@@ -106,7 +114,25 @@ def _stagewise(run, host, check_h=True):
     # Z1 = A1 . W13_hat^T
     z1_all = run.rows("Z1", 2 * F)
     z1 = z1_all[real]
-    assert_close(z1, OM.grouped_gemm_nt(a1, w13h, off), "Z1")
+    x64 = OQ.bf16_to_f64(host["x"])
+    if factored:
+        qw13 = _codes(run, "W13_CODES", E * 2 * F, d).reshape(E, 2 * F, d)
+        s13 = host["s13"].astype(np.float64)
+        assert np.array_equal(qw13 * s13, OQ.fakequant_weight_factored(fmt, host["w13"], host["s13"]))
+        qw2 = _codes(run, "W2_CODES", E * d, F).reshape(E, d, F)
+        assert np.array_equal(qw2 * host["s2"].astype(np.float64),
+                              OQ.fakequant_weight_factored(fmt, host["w2"], host["s2"]))
+        sa = synth.to_numpy(run.view("A_SCALE", torch.float32)).astype(np.float64)
+        assert np.array_equal(sa, OQ.act_scale(fmt, x64)[:, 0])
+        qa = _codes(run, "A1_CODES", rt["rpad"], d)
+        assert np.array_equal(qa[real] * sa[ref["row_token"]][:, None],
+                              OQ.fakequant_act_factored(fmt, x64)[ref["row_token"]])
+        assert np.all(qa[~real] == 0)
+        want_z1 = OM.grouped_gemm_nt(OQ.fakequant_act_factored(fmt, x64)[ref["row_token"]],
+                                     OQ.fakequant_weight_factored(fmt, host["w13"], host["s13"]), off)
+    else:
+        want_z1 = OM.grouped_gemm_nt(a1, w13h, off)
+    assert_close(z1, want_z1, "Z1")
     assert np.all(z1_all[~real] == 0)
 
     # H and H_hat = AQ(H): bit exact given the GPU's H
@@ -118,7 +144,17 @@ def _stagewise(run, host, check_h=True):
 
     # Y = H_hat . W2_hat^T, out = sum_j p Y
     y = run.rows("Y", d)[real]
-    assert_close(y, OM.grouped_gemm_nt(hh, w2h, off), "Y")
+    if factored:
+        h = run.rows("H", F)[real]
+        sh = synth.to_numpy(run.view("H_SCALE", torch.float32)).astype(np.float64)[: rt["rpad"]][real]
+        assert np.array_equal(sh, OQ.act_scale(fmt, h)[:, 0])
+        qh = _codes(run, "H_CODES", rt["rpad"], F)[real]
+        assert np.array_equal(qh * sh[:, None], OQ.fakequant_act_factored(fmt, h))
+        want_y = OM.grouped_gemm_nt(OQ.fakequant_act_factored(fmt, h),
+                                    OQ.fakequant_weight_factored(fmt, host["w2"], host["s2"]), off)
+    else:
+        want_y = OM.grouped_gemm_nt(hh, w2h, off)
+    assert_close(y, want_y, "Y")
     out = vals(run.out)
     assert_close(out, OM.combine(y, p, row_of), "out")
 
@@ -184,6 +220,37 @@ def test_stash_h_flag_off_matches_on():
     inp = _tiny(Q.QAD_FMT_NVFP4)
     a = Run(inp, flags=Q.QAD_FLAG_STASH_H)
     b = Run(inp, flags=0)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
+    assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
+
+
+def test_native_fp8_forward_stagewise_tiny():
+    """QAD_FLAG_NATIVE_FP8: fc1 and fc2 contract E4M3 codes on the fp8 tensor path and apply the
+    row scales to the sums; every stage against the oracle's scale-factored forward."""
+    inp = _tiny(Q.QAD_FMT_FP8_ROW)
+    host = host_inputs(inp)
+    run = Run(inp, flags=Q.QAD_FLAG_NATIVE_FP8 | Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    _stagewise(run, host, factored=True)
+    # the end-to-end output stays close to the rounded reading's
+    fwd = OM.moe_forward(Q.QAD_FMT_FP8_ROW, host["x"], host["topk_idx"], host["topk_w"], host["w13"], host["s13"],
+                         host["w2"], host["s2"], factored=True)
+    rel = np.max(np.abs(vals(run.out) - fwd["out"])) / np.sqrt(np.mean(fwd["out"] ** 2))
+    assert rel < 0.5
+
+
+def test_native_fp8_flag_rejected_for_other_formats():
+    for fmt in (Q.QAD_FMT_NVFP4, Q.QAD_FMT_W8A8):
+        assert Q.qad_moe_workspace_bytes(Q.shape(512, 256, 128, 4, 2, fmt, Q.QAD_FLAG_NATIVE_FP8)) == 0
+    assert Q.qad_moe_workspace_bytes(
+        Q.shape(512, 256, 128, 4, 2, Q.QAD_FMT_FP8_ROW, Q.QAD_FLAG_NATIVE_FP8 | Q.QAD_FLAG_NO_QUANT)) == 0
+
+
+def test_native_fp8_recompute_is_bit_identical():
+    inp = _tiny(Q.QAD_FMT_FP8_ROW)
+    a = Run(inp, flags=Q.QAD_FLAG_NATIVE_FP8)
+    b = Run(inp, flags=Q.QAD_FLAG_NATIVE_FP8 | Q.QAD_FLAG_RECOMPUTE)
     assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
     assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
     assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
