@@ -288,6 +288,9 @@ def run_ours(args):
         if n == 0:
             continue
         entry = {"ms_per_launch": tot / n, "launches_per_step": n / args.steps, "share": None}
+        if name == "route_permute":
+            # on the library's side stream beside the weight fake-quant: wall time while sharing the GPU
+            entry["overlapped_with"] = "fakequant_w"
         if name in alg:
             bound, amount = alg[name]
             per_s = amount / (tot / n / 1e3)
@@ -297,9 +300,10 @@ def run_ours(args):
             else:
                 entry.update(achieved_gbs=per_s / 1e9, frac=per_s / 1e9 / hbm)
         kernels[name] = entry
-    total_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values())
+    total_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values() if "overlapped_with" not in v)
     for v in kernels.values():
-        v["share"] = v["ms_per_launch"] * v["launches_per_step"] / total_ms if total_ms else None
+        if "overlapped_with" not in v:
+            v["share"] = v["ms_per_launch"] * v["launches_per_step"] / total_ms if total_ms else None
     dom = max((nm for nm in kernels if nm in alg), key=lambda nm: kernels[nm]["share"])
     bound, amount = alg[dom]
     dur = kernels[dom]["ms_per_launch"] / 1e3

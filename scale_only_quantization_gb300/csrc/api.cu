@@ -227,6 +227,34 @@ size_t qad_moe_workspace_bytes(const qad_moe_shape* s) {
   return layout_of(*s, &L) == QAD_OK ? L.total : 0;
 }
 
+namespace qad {
+namespace {
+// Per-device side stream and events of the forward's fork / join: the routing kernels
+// (latency-bound, a few tens of microseconds) run beside the HBM-bound weight fake-quant.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+cudaError_t side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+}  // namespace
+}  // namespace qad
+
 int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, const float* topk_w,
                 const void* w13, const float* s13, const void* w2, const float* s2, void* out, void* ws,
                 size_t ws_bytes, qad_stream_t stream) {
@@ -242,11 +270,21 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
   const int fmt = s->fmt;
   const bool no_quant = (s->flags & QAD_FLAG_NO_QUANT) != 0;
   QAD_TRY(cudaMemsetAsync(hdr, 0, 256, st));
-  QAD_TRY(launch_route(topk_idx, L, wsb, st));
   const bool f8 = L.native_fp8;  // E4M3 codes for the fp8 tensor path as well
-  if (!no_quant) {
-    QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
-    QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st, f8 ? wsb + L.w2q : nullptr));
+  {
+    // routing on the side stream, the weight fake-quant on the caller's; joined before the gather
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    SideStream* ss = nullptr;
+    QAD_TRY(side_stream(&ss));
+    QAD_TRY(cudaEventRecord(ss->fork, st));
+    QAD_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+    QAD_TRY(launch_route(topk_idx, L, wsb, ss->s));
+    QAD_TRY(cudaEventRecord(ss->join, ss->s));
+    if (!no_quant) {
+      QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
+      QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st, f8 ? wsb + L.w2q : nullptr));
+    }
+    QAD_TRY(cudaStreamWaitEvent(st, ss->join, 0));
   }
   const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
