@@ -513,44 +513,62 @@ __device__ __forceinline__ void epi_store(const Params& p, const CUtensorMap* tm
   }
 }
 
+// This thread's Z1 row and first column in a tile of the SwiGLU-backward epilogue.
+struct Z1Cursor {
+  const __nv_bfloat16* row;
+  int f_first;
+};
+template <int BN>
+__device__ __forceinline__ Z1Cursor z1_cursor(const Params& p, const Tile& ti, int q, int lane, int half) {
+  const int64_t row = ti.row_base + q * 32 + lane;
+  return {p.aux + row * p.ld_aux, ti.nb * BN + half * (BN / 2)};
+}
+// Z1 of 16-column step `step`: gate 2 x 16 B, up 2 x 16 B
+__device__ __forceinline__ void z1_load(const Params& p, const Z1Cursor& c, int step, uint4 (&slot)[4]) {
+  const uint4* g = reinterpret_cast<const uint4*>(c.row + c.f_first + 16 * step);
+  const uint4* u = reinterpret_cast<const uint4*>(c.row + p.F + c.f_first + 16 * step);
+  slot[0] = __ldg(g);
+  slot[1] = __ldg(g + 1);
+  slot[2] = __ldg(u);
+  slot[3] = __ldg(u + 1);
+}
+
 // dZ1 = [dH * up * sig(g) * (1 + g (1 - sig(g))), dH * g * sig(g)] from the stored bf16 Z1,
-// 16 columns at a time; the Z1 loads run two steps ahead, the TMEM loads one step ahead.
+// 16 columns at a time.  The Z1 loads run three steps ahead in a 4-slot register ring that
+// carries over from tile to tile: the last steps of a tile load the first steps of the
+// thread's next tile (`next`, when `next_ok`), so a tile only waits for memory at the start
+// when nothing was prefetched for it (`prefetched` false: first tile, or after a dead one).
+// The TMEM loads run one step ahead.
 template <int BN>
 __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const CUtensorMap* tm_dz1, const Tile& ti,
-                                               uint32_t tbase, int q, int lane, int half, BoxRing& ring) {
-  const int64_t row = ti.row_base + q * 32 + lane;
+                                               uint32_t tbase, int q, int lane, int half, BoxRing& ring,
+                                               uint4 (&z)[4][4], bool prefetched, bool next_ok,
+                                               const Z1Cursor& next) {
   const int y = (int)ti.row_base + 32 * q;
-  const __nv_bfloat16* z1 = p.aux + row * p.ld_aux;
   constexpr int STEPS = BN / 32;  // 16-column steps per half
+  constexpr int AHEAD = 3;
+  static_assert(STEPS % 4 == 0, "the Z1 ring's slots must line up from tile to tile");
   const int col0 = half * (BN / 2);
-  const int f_first = ti.nb * BN + col0;
+  const Z1Cursor cur = z1_cursor<BN>(p, ti, q, lane, half);
+  const int f_first = cur.f_first;
   uint32_t r[16], rn[16];
-  uint4 z[3][4];  // ring of Z1 (gate 2 x 16 B, up 2 x 16 B) for three steps
-  {
-    const uint4* g0 = reinterpret_cast<const uint4*>(z1 + f_first);
-    const uint4* u0 = reinterpret_cast<const uint4*>(z1 + p.F + f_first);
-    z[0][0] = __ldg(g0); z[0][1] = __ldg(g0 + 1); z[0][2] = __ldg(u0); z[0][3] = __ldg(u0 + 1);
-    if (STEPS > 1) {
-      z[1][0] = __ldg(g0 + 2); z[1][1] = __ldg(g0 + 3); z[1][2] = __ldg(u0 + 2); z[1][3] = __ldg(u0 + 3);
-    }
+  if (!prefetched) {
+#pragma unroll
+    for (int s = 0; s < AHEAD && s < STEPS; ++s) z1_load(p, cur, s, z[s % 4]);
   }
   tmem_ld16_issue(tbase + col0, r);
   tmem_wait16(r);
 #pragma unroll
   for (int j = 0; j < STEPS; ++j) {
     const int f0 = f_first + 16 * j;
-    if (j + 2 < STEPS) {
-      const uint4* g2 = reinterpret_cast<const uint4*>(z1 + f0 + 32);
-      const uint4* u2 = reinterpret_cast<const uint4*>(z1 + p.F + f0 + 32);
-      z[(j + 2) % 3][0] = __ldg(g2); z[(j + 2) % 3][1] = __ldg(g2 + 1);
-      z[(j + 2) % 3][2] = __ldg(u2); z[(j + 2) % 3][3] = __ldg(u2 + 1);
-    }
+    if (j + AHEAD < STEPS) z1_load(p, cur, j + AHEAD, z[(j + AHEAD) % 4]);
+    else if (next_ok) z1_load(p, next, j + AHEAD - STEPS, z[(j + AHEAD) % 4]);
     if (j + 1 < STEPS) tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
     float g[16], u[16];
-    unpack8(z[j % 3][0], g);
-    unpack8(z[j % 3][1], g + 8);
-    unpack8(z[j % 3][2], u);
-    unpack8(z[j % 3][3], u + 8);
+    unpack8(z[j % 4][0], g);
+    unpack8(z[j % 4][1], g + 8);
+    unpack8(z[j % 4][2], u);
+    unpack8(z[j % 4][3], u + 8);
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {  // two lanes at a time
       const uint64_t one2 = f2pack(1.0f, 1.0f);
@@ -893,6 +911,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t buf = 0;
     const uint32_t my_stage = stage_out + (uint32_t)(warp - 2) * (uint32_t)kStageWarp;
     BoxRing ring{my_stage, 0u};
+    uint4 zr[4][4];          // SwiGLU backward: Z1 ring carried from tile to tile
+    bool prefetched = false;  // the ring holds the first steps of the current tile
     if constexpr (EPI != EPI_SCALEGRAD) tma_prefetch_desc(&tmC);
     if constexpr (EPI == EPI_FC1) tma_prefetch_desc(&tmD);
     for (int t = first; t < total; t += step) {
@@ -904,7 +924,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (ti.live) {
         if constexpr (EPI == EPI_STORE) epi_store<BN, F8>(p, &tmC, ti, tbase, q, lane, half, my_stage, buf);
         else if constexpr (EPI == EPI_FC1) epi_fc1<BN, F8>(p, &tmC, &tmD, ti, tbase, q, lane, half, ring);
-        else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<BN>(p, &tmC, ti, tbase, q, lane, half, ring);
+        else if constexpr (EPI == EPI_SWIGLU_BWD) {
+          bool next_ok = false;
+          Z1Cursor next{nullptr, 0};
+          if (t + step < total) {
+            const Tile tn = tile_of(p, t + step, rank);
+            next_ok = tn.live;
+            next = z1_cursor<BN>(p, tn, q, lane, half);
+          }
+          epi_swiglu_bwd<BN>(p, &tmC, ti, tbase, q, lane, half, ring, zr, prefetched, next_ok, next);
+          prefetched = next_ok;
+        }
         else run_scalegrad<BN>(p, ti, tbase, row_in_tile, half);
       }
       tc_fence_before();
