@@ -322,6 +322,18 @@ def test_empty_experts_single_row_expert_and_small_batch():
     assert np.count_nonzero(synth.to_numpy(run.ds13)[6]) > 0
 
 
+@pytest.mark.parametrize("E, topk, T", [
+    (1024, 32, 96),   # the largest expert count and top-k the layout accepts; most experts empty
+    (1, 1, 700),      # a dense layer: one expert, every token routed to it (ragged last tile)
+    (4, 1, 513),      # top-1 routing
+])
+def test_extreme_expert_counts_and_top_k(E, topk, T):
+    inp = synth.make_inputs(synth.workload("tiny_nvfp4", E=E, topk=topk, T=T), seed=4, device="cuda")
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    _stagewise(run, host_inputs(inp))
+
+
 def test_fewer_rows_than_one_tile():
     base = synth.make_inputs(synth.workload("tiny_nvfp4"), seed=2, device="cuda")
     idx = np.array([[1, 2], [2, 3], [0, 1], [3, 0], [1, 3]])
