@@ -288,7 +288,7 @@ def run_ours(args):
         if n == 0:
             continue
         entry = {"ms_per_launch": tot / n, "launches_per_step": n / args.steps, "share": None}
-        if name == "route_permute":
+        if name in ("route_permute", "gather_rows"):
             # on the library's side stream beside the weight fake-quant: wall time while sharing the GPU
             entry["overlapped_with"] = "fakequant_w"
         if name in alg:

@@ -271,14 +271,23 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
   const bool no_quant = (s->flags & QAD_FLAG_NO_QUANT) != 0;
   QAD_TRY(cudaMemsetAsync(hdr, 0, 256, st));
   const bool f8 = L.native_fp8;  // E4M3 codes for the fp8 tensor path as well
+  const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
+  GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
+  c.s13 = s13;
+  c.s2 = s2;
   {
-    // routing on the side stream, the weight fake-quant on the caller's; joined before the gather
+    // routing and the activation gather on the side stream, the weight fake-quant on the
+    // caller's: the latency-bound routing hides under the fake-quant, and the two HBM-bound
+    // passes share the memory system; joined before the GEMMs
     std::lock_guard<std::mutex> lk(g_side_mu);
     SideStream* ss = nullptr;
     QAD_TRY(side_stream(&ss));
     QAD_TRY(cudaEventRecord(ss->fork, st));
     QAD_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
     QAD_TRY(launch_route(topk_idx, L, wsb, ss->s));
+    QAD_TRY(launch_scatter_tokens(c.aq, x, wsb + L.xq, wsb + L.a1, reinterpret_cast<const int32_t*>(wsb + L.row_of),
+                                  row_token, L.T, (int)L.k, L.d, rpad, ss->s, f8 ? wsb + L.a1q : nullptr,
+                                  f8 ? reinterpret_cast<float*>(wsb + L.sa_tok) : nullptr));
     QAD_TRY(cudaEventRecord(ss->join, ss->s));
     if (!no_quant) {
       QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
@@ -286,13 +295,6 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
     }
     QAD_TRY(cudaStreamWaitEvent(st, ss->join, 0));
   }
-  const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
-  GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
-  c.s13 = s13;
-  c.s2 = s2;
-  QAD_TRY(launch_scatter_tokens(c.aq, x, wsb + L.xq, wsb + L.a1, reinterpret_cast<const int32_t*>(wsb + L.row_of),
-                                row_token, L.T, (int)L.k, L.d, rpad, st, f8 ? wsb + L.a1q : nullptr,
-                                f8 ? reinterpret_cast<float*>(wsb + L.sa_tok) : nullptr));
   QAD_TRY(gemm_prepare(c));
   QAD_TRY(gemm_fc1(c, (s->flags & QAD_FLAG_RECOMPUTE) ? kFc1NoZ1 : kFc1Full));
   if (row_scaled(c.aq))
