@@ -43,7 +43,13 @@ namespace qad {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;
+constexpr int BK = 64;  // bf16 K elements in one 128-byte swizzle atom row
+// Pipeline stages hold ATOMS 128-byte K atoms per operand row.  Two atoms (8 MMAs per stage)
+// halve the per-stage barrier and commit work of the single producer and MMA threads at the
+// same bytes of lookahead; measured per GEMM, two atoms help fc1 and the two wgrad GEMMs
+// (5-7%) and cost fc2 and the two dgrad GEMMs 1-3%, which keep one.
+__host__ __device__ constexpr int bke_of(bool f8, int atoms) { return atoms * (f8 ? 128 : BK); }  // K per stage
+constexpr int kAtomsFc1 = 2, kAtomsFc2 = 1, kAtomsDgrad = 1, kAtomsWgrad = 2;
 constexpr int kThreads = 320;       // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-9 epilogue
 constexpr int kEpiThreads = 256;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
@@ -77,11 +83,13 @@ struct Params {
   float* ds; float* part; int accumulate;
 };
 
-template <int BN> struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;        // this CTA's 128 rows of A
-  static constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's half of B
+template <int BN, int ATOMS> struct Cfg {
+  static constexpr int A_ATOM = BM * 128;                  // this CTA's 128 rows of A, one atom
+  static constexpr int B_ATOM = (BN / 2) * 128;            // this CTA's half of B, one atom
+  static constexpr int A_BYTES = ATOMS * A_ATOM;
+  static constexpr int B_BYTES = ATOMS * B_ATOM;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (192 * 1024) / STAGE;  // 6 (BN = 256) or 8 (BN = 128)
+  static constexpr int STAGES = (192 * 1024) / STAGE;  // BN = 256: 6 (one atom) or 3; BN = 128: 8 or 4
   static constexpr int RING = STAGES * STAGE;
   static constexpr int SMEM = RING + 256 + 1024;  // + barriers, + alignment slack
   static constexpr int TMEM_COLS = 2 * BN;
@@ -96,7 +104,9 @@ constexpr int kStageWarp = 4096;
 template <int EPI> __host__ __device__ constexpr int staging_bytes() {
   return EPI == EPI_SCALEGRAD ? 0 : (kEpiThreads / 32) * kStageWarp;
 }
-template <int BN, int EPI> __host__ __device__ constexpr int smem_bytes() { return Cfg<BN>::SMEM + staging_bytes<EPI>(); }
+template <int BN, int EPI, int ATOMS> __host__ __device__ constexpr int smem_bytes() {
+  return Cfg<BN, ATOMS>::SMEM + staging_bytes<EPI>();
+}
 
 // ---------------------------------------------------------------------------------- PTX
 
@@ -312,7 +322,7 @@ __device__ __forceinline__ int tile_count(const Params& p) {
   return p.wgrad ? p.E * p.n_mtiles_w * p.n_ntiles : p.hdr[HDR_NPTILES] * p.n_ntiles;
 }
 
-__device__ __forceinline__ Tile tile_of(const Params& p, int t, uint32_t rank) {
+__device__ __forceinline__ Tile tile_of(const Params& p, int t, uint32_t rank, int bke) {
   Tile ti;
   if (p.wgrad) {
     const int per_e = p.n_mtiles_w * p.n_ntiles;
@@ -321,7 +331,7 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t, uint32_t rank) {
     ti.mb = rem / p.n_ntiles;
     ti.nb = rem - ti.mb * p.n_ntiles;
     ti.r0 = __ldg(p.poff + ti.e);
-    ti.nkb = (__ldg(p.poff + ti.e + 1) - ti.r0) / BK;
+    ti.nkb = (__ldg(p.poff + ti.e + 1) - ti.r0) / bke;
     ti.row_base = (int64_t)ti.mb * (2 * BM) + (int64_t)rank * BM;
     ti.live = true;
   } else {
@@ -741,16 +751,17 @@ __device__ __forceinline__ void run_scalegrad(const Params& p, const Tile& ti, u
 
 // ---------------------------------------------------------------------------------- kernel
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool F8>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8, int ATOMS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const Params p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, ATOMS>;
   constexpr int STAGES = C::STAGES;
   static_assert(!F8 || (!A_MN && !B_MN), "E4M3 operands are K-major (forward GEMMs)");
   constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN, F8>();
-  constexpr int BKE = F8 ? 128 : BK;  // K elements per 128-byte row of a stage
+  constexpr int BKE = bke_of(F8, ATOMS);  // K elements per stage
+  constexpr int AKE = F8 ? 128 : BK;  // K elements per 128-byte atom row
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a_ring = smem_u32(smem);
@@ -811,30 +822,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // shared memory, completing on `fb`
     auto operand_tiles = [&](const Tile& ti, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
       auto box = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) { tma_load_2d(dst, tm, x, y, fb); };
+      // K-major operands: one box {64 bf16 | 128 E4M3, rows} per 128-byte K atom; MN-major
+      // operands: one box {64, BKE K rows} per 64 columns of M or N
       if (!p.wgrad) {
-        box(sa, &tmA, kb * BKE, ti.r0);
+#pragma unroll
+        for (int a = 0; a < ATOMS; ++a) box(sa + a * C::A_ATOM, &tmA, kb * BKE + a * AKE, ti.r0);
         if constexpr (!B_MN) {
-          if constexpr (EPI == EPI_FC1) {
-            // leader: the 128 gate rows of the tile, peer: the matching 128 up rows
-            box(sb, &tmB, kb * BKE, ti.e * p.b_rows + (int)rank * p.F + ti.nb * 128);
-          } else {
-            box(sb, &tmB, kb * BKE, ti.e * p.b_rows + ti.nb * BN + half_n);
+#pragma unroll
+          for (int a = 0; a < ATOMS; ++a) {
+            if constexpr (EPI == EPI_FC1) {
+              // leader: the 128 gate rows of the tile, peer: the matching 128 up rows
+              box(sb + a * C::B_ATOM, &tmB, kb * BKE + a * AKE, ti.e * p.b_rows + (int)rank * p.F + ti.nb * 128);
+            } else {
+              box(sb + a * C::B_ATOM, &tmB, kb * BKE + a * AKE, ti.e * p.b_rows + ti.nb * BN + half_n);
+            }
           }
         } else {
 #pragma unroll
           for (int i = 0; i < BN / 128; ++i)
-            box(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, ti.e * p.b_rows + kb * BK);
+            box(sb + i * BKE * 128, &tmB, ti.nb * BN + half_n + i * 64, ti.e * p.b_rows + kb * BKE);
         }
       } else {
-        const int y = ti.r0 + kb * BK;
+        const int y = ti.r0 + kb * BKE;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) box(sa + i * 64 * 128, &tmA, ti.mb * 2 * BM + (int)rank * BM + i * 64, y);
+        for (int i = 0; i < 2; ++i) box(sa + i * BKE * 128, &tmA, ti.mb * 2 * BM + (int)rank * BM + i * 64, y);
 #pragma unroll
-        for (int i = 0; i < BN / 128; ++i) box(sb + i * 64 * 128, &tmB, ti.nb * BN + half_n + i * 64, y);
+        for (int i = 0; i < BN / 128; ++i) box(sb + i * BKE * 128, &tmB, ti.nb * BN + half_n + i * 64, y);
       }
     };
     for (int t = first; ok && t < total; t += step) {
-      const Tile ti = tile_of(p, t, rank);
+      const Tile ti = tile_of(p, t, rank, BKE);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, err)) {
           ok = false;
@@ -867,7 +884,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     bool ok = true;
     for (int t = first; ok && t < total; t += step) {
-      const Tile ti = tile_of(p, t, rank);
+      const Tile ti = tile_of(p, t, rank, BKE);
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, err)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -880,9 +897,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t sa = a_ring + stage * C::A_BYTES;
         const uint32_t sb = b_ring + stage * C::B_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, 64 * 128, 1024) : smem_desc(sa + k * 32, 16, 1024);
-          const uint64_t bd = B_MN ? smem_desc(sb + k * 2048, 64 * 128, 1024) : smem_desc(sb + k * 32, 16, 1024);
+        for (int k = 0; k < ATOMS * 4; ++k) {  // each MMA reads 32 bytes of K per row
+          const uint64_t ad = A_MN ? smem_desc(sa + k * 2048, BKE * 128, 1024)
+                                   : smem_desc(sa + (k / 4) * C::A_ATOM + (k % 4) * 32, 16, 1024);
+          const uint64_t bd = B_MN ? smem_desc(sb + k * 2048, BKE * 128, 1024)
+                                   : smem_desc(sb + (k / 4) * C::B_ATOM + (k % 4) * 32, 16, 1024);
           mma_issue<F8>(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
         mma_commit(empty_bar(stage), 3);  // frees the slot in both CTAs
@@ -916,7 +935,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if constexpr (EPI != EPI_SCALEGRAD) tma_prefetch_desc(&tmC);
     if constexpr (EPI == EPI_FC1) tma_prefetch_desc(&tmD);
     for (int t = first; t < total; t += step) {
-      const Tile ti = tile_of(p, t, rank);
+      const Tile ti = tile_of(p, t, rank, BKE);
       const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
@@ -928,7 +947,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bool next_ok = false;
           Z1Cursor next{nullptr, 0};
           if (t + step < total) {
-            const Tile tn = tile_of(p, t + step, rank);
+            const Tile tn = tile_of(p, t + step, rank, BKE);
             next_ok = tn.live;
             next = z1_cursor<BN>(p, tn, q, lane, half);
           }
@@ -1017,11 +1036,11 @@ bool make_store_tmap(CUtensorMap* tm, void* base, int64_t inner, int64_t outer, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, int ATOMS, bool F8 = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& td,
                    const Params& p, int64_t max_tiles, int kid, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, F8>;
-  constexpr int SMEM = smem_bytes<BN, EPI>();
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, F8, ATOMS>;
+  constexpr int SMEM = smem_bytes<BN, EPI, ATOMS>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   static int max_pairs[64] = {0};  // per device (one instantiation of this function per kernel)
@@ -1141,7 +1160,7 @@ cudaError_t gemm_fc1(const GemmCtx& c, int mode) {
     if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
   }
   p.n_ntiles = (int)(L.F / 128);
-  p.num_kb = (int)(L.d / (f8 ? 128 : BK));
+  p.num_kb = (int)(L.d / bke_of(f8, f8 ? 1 : kAtomsFc1));
   p.b_rows = (int)(2 * L.F);
   p.ld_out2 = L.F;
   p.out3 = at<__nv_bfloat16>(c.ws, L.h);
@@ -1150,8 +1169,8 @@ cudaError_t gemm_fc1(const GemmCtx& c, int mode) {
   if (!make_store_tmap(&th, c.ws + (row_scaled(c.aq) ? L.h : L.hh), L.F, L.Rmax, L.F, 16)) return cudaErrorInvalidValue;
   const int kid = mode == kFc1Z1Only ? QAD_K_GEMM_FC1_RECOMPUTE : QAD_K_GEMM_FC1;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
-  return f8 ? launch<256, false, false, EPI_FC1, true>(ta, tb, tz, th, p, tiles, kid, c.st)
-            : launch<256, false, false, EPI_FC1>(ta, tb, tz, th, p, tiles, kid, c.st);
+  return f8 ? launch<256, false, false, EPI_FC1, 1, true>(ta, tb, tz, th, p, tiles, kid, c.st)
+            : launch<256, false, false, EPI_FC1, kAtomsFc1>(ta, tb, tz, th, p, tiles, kid, c.st);
 }
 
 cudaError_t gemm_fc2(const GemmCtx& c) {
@@ -1172,14 +1191,14 @@ cudaError_t gemm_fc2(const GemmCtx& c) {
     if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
   }
   p.n_ntiles = (int)(L.d / bn);
-  p.num_kb = (int)(L.F / (f8 ? 128 : BK));
+  p.num_kb = (int)(L.F / bke_of(f8, f8 ? 1 : kAtomsFc2));
   p.b_rows = (int)L.d;
   CUtensorMap tc;
   if (!make_store_tmap(&tc, c.ws + L.y, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
-  if (f8) return launch<256, false, false, EPI_STORE, true>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
-  return bn == 256 ? launch<256, false, false, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st)
-                   : launch<128, false, false, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
+  if (f8) return launch<256, false, false, EPI_STORE, 1, true>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
+  return bn == 256 ? launch<256, false, false, EPI_STORE, kAtomsFc2>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st)
+                   : launch<128, false, false, EPI_STORE, kAtomsFc2>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
 }
 
 cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
@@ -1188,18 +1207,19 @@ cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.dy, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
   // W2_hat viewed as [E * d (GEMM K), F (GEMM N)], N contiguous
-  if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, bke_of(false, kAtomsDgrad))) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.F);
   p.n_ntiles = (int)(L.F / bn);
-  p.num_kb = (int)(L.d / BK);
+  p.num_kb = (int)(L.d / bke_of(false, kAtomsDgrad));
   p.b_rows = (int)L.d;
   p.aux = at<__nv_bfloat16>(c.ws, L.z1);
   p.ld_aux = 2 * L.F;
   CUtensorMap tz;
   if (!make_store_tmap(&tz, c.ws + L.dz1, 2 * L.F, L.Rmax, 2 * L.F, 16)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
-  return bn == 256 ? launch<256, false, true, EPI_SWIGLU_BWD>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st)
-                   : launch<128, false, true, EPI_SWIGLU_BWD>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st);
+  return bn == 256
+             ? launch<256, false, true, EPI_SWIGLU_BWD, kAtomsDgrad>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st)
+             : launch<128, false, true, EPI_SWIGLU_BWD, kAtomsDgrad>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st);
 }
 
 cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
@@ -1208,16 +1228,17 @@ cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, c.ws + L.dz1, 2 * L.F, L.Rmax, 2 * L.F, 128)) return cudaErrorInvalidValue;
   // W13_hat viewed as [E * 2F (GEMM K), d (GEMM N)], N contiguous
-  if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, bke_of(false, kAtomsDgrad))) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.d);
   p.n_ntiles = (int)(L.d / bn);
-  p.num_kb = (int)(2 * L.F / BK);
+  p.num_kb = (int)(2 * L.F / bke_of(false, kAtomsDgrad));
   p.b_rows = (int)(2 * L.F);
   CUtensorMap tc;
   if (!make_store_tmap(&tc, c.ws + L.da1, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
-  return bn == 256 ? launch<256, false, true, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st)
-                   : launch<128, false, true, EPI_STORE>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st);
+  return bn == 256
+             ? launch<256, false, true, EPI_STORE, kAtomsDgrad>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st)
+             : launch<128, false, true, EPI_STORE, kAtomsDgrad>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st);
 }
 
 namespace {
@@ -1227,8 +1248,8 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   Params p = base_params(c);
   CUtensorMap ta, tb;
   // A = dZ [Rmax, Mw] (M contiguous), B = A_hat [Rmax, Kw] (N contiguous)
-  if (!make_tmap(&ta, c.ws + a_off, m_w, L.Rmax, m_w, 64)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tb, c.ws + b_off, k_w, L.Rmax, k_w, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap(&ta, c.ws + a_off, m_w, L.Rmax, m_w, bke_of(false, kAtomsWgrad))) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, c.ws + b_off, k_w, L.Rmax, k_w, bke_of(false, kAtomsWgrad))) return cudaErrorInvalidValue;
   const int bn = pick_bn(k_w);
   p.wgrad = 1;
   p.n_mtiles_w = (int)(m_w / (2 * BM));
@@ -1241,8 +1262,8 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   p.part = at<float>(c.ws, part_off);
   p.accumulate = accumulate;
   const int64_t tiles = L.E * p.n_mtiles_w * p.n_ntiles;
-  cudaError_t e = bn == 256 ? launch<256, true, true, EPI_SCALEGRAD>(ta, tb, ta, ta, p, tiles, kid, c.st)
-                            : launch<128, true, true, EPI_SCALEGRAD>(ta, tb, ta, ta, p, tiles, kid, c.st);
+  cudaError_t e = bn == 256 ? launch<256, true, true, EPI_SCALEGRAD, kAtomsWgrad>(ta, tb, ta, ta, p, tiles, kid, c.st)
+                            : launch<128, true, true, EPI_SCALEGRAD, kAtomsWgrad>(ta, tb, ta, ta, p, tiles, kid, c.st);
   if (e != cudaSuccess) return e;
   if (row_scaled(c.wq) || (c.wq == kQInt4 && bn == 128)) {
     const int64_t B = c.wq == kQInt4 ? 128 : k_w;  // elements per scale
