@@ -115,6 +115,7 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->mtile_expert = take(4 * (size_t)(Rmax / kTileRows));
   L->ptile_row0 = take(4 * (size_t)(Rmax / kTileRows));
   L->ptile_expert = take(4 * (size_t)(Rmax / kTileRows));
+  L->wg_order = take(4 * (size_t)E);
   L->row_token = take(4 * (size_t)Rmax);
   L->row_slot = take(4 * (size_t)Rmax);
   L->row_of = take(4 * (size_t)R);

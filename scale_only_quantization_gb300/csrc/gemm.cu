@@ -60,6 +60,7 @@ struct Params {
   int32_t* hdr;                 // workspace header ([HDR_ERR], [HDR_NPTILES])
   const int32_t* ptile_row0;    // first row of each row-mode pair tile
   const int32_t* ptile_expert;  // expert of each row-mode pair tile
+  const int32_t* wg_order;      // wgrad: experts by decreasing padded row count (tile order)
   const int32_t* poff;          // padded expert offsets [E + 1]
   int E;
   int wgrad;                    // 0: output rows grouped by expert; 1: contraction over an expert's rows
@@ -326,8 +327,9 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t, uint32_t rank, i
   Tile ti;
   if (p.wgrad) {
     const int per_e = p.n_mtiles_w * p.n_ntiles;
-    ti.e = t / per_e;
-    const int rem = t - ti.e * per_e;
+    const int k = t / per_e;
+    ti.e = __ldg(p.wg_order + k);
+    const int rem = t - k * per_e;
     ti.mb = rem / p.n_ntiles;
     ti.nb = rem - ti.mb * p.n_ntiles;
     ti.r0 = __ldg(p.poff + ti.e);
@@ -1070,15 +1072,20 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
 
 // Row-mode pair tiles: expert e with m_e padded 128-row blocks gets ceil(m_e / 2) tiles of two
 // consecutive blocks starting at row offs[e] + 256 i.  One block of 1024 threads, one
-// expert per thread (E <= 1024), exclusive scan of the tile counts.
+// expert per thread (E <= 1024), exclusive scan of the tile counts.  Also the order in which
+// the wgrad GEMMs visit the experts: by decreasing padded row count (ties by index), so that
+// the persistent CTAs, which take tiles round-robin, start with the longest ones (with skewed
+// routing the index order left the busiest CTA with ~1.8x the mean work).
 __global__ void __launch_bounds__(1024) pair_tiles_kernel(const int32_t* __restrict__ offs, int E,
                                                           int32_t* __restrict__ row0, int32_t* __restrict__ expert,
-                                                          int32_t* hdr) {
+                                                          int32_t* __restrict__ wg_order, int32_t* hdr) {
   __shared__ int32_t warp_tot[32];
+  __shared__ int32_t rows_of[1024];
   const int e = threadIdx.x, lane = e & 31, w = e >> 5;
   const int32_t start = e < E ? offs[e] : 0;
   const int32_t blocks = e < E ? (offs[e + 1] - start) / BM : 0;
   const int32_t n = (blocks + 1) / 2;
+  if (e < E) rows_of[e] = blocks;
   int32_t v = n;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -1104,6 +1111,15 @@ __global__ void __launch_bounds__(1024) pair_tiles_kernel(const int32_t* __restr
     expert[excl + i] = e;
   }
   if (e == E - 1) hdr[HDR_NPTILES] = incl;
+  __syncthreads();
+  if (e < E) {  // rank of expert e in decreasing row count, ties by index
+    int32_t rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const int32_t bf = rows_of[f];
+      rank += (bf > blocks || (bf == blocks && f < e)) ? 1 : 0;
+    }
+    wg_order[rank] = e;
+  }
 }
 
 template <typename T>
@@ -1117,6 +1133,7 @@ Params base_params(const GemmCtx& c) {
   p.hdr = at<int32_t>(c.ws, L.header);
   p.ptile_row0 = at<int32_t>(c.ws, L.ptile_row0);
   p.ptile_expert = at<int32_t>(c.ws, L.ptile_expert);
+  p.wg_order = at<int32_t>(c.ws, L.wg_order);
   p.poff = at<int32_t>(c.ws, L.offs);
   p.E = (int)L.E;
   p.F = (int)L.F;
@@ -1138,7 +1155,8 @@ cudaError_t launch_wait_selftest(int32_t* err, int64_t budget_cycles, cudaStream
 cudaError_t gemm_prepare(const GemmCtx& c) {
   const Layout& L = *c.L;
   pair_tiles_kernel<<<1, 1024, 0, c.st>>>(at<int32_t>(c.ws, L.offs), (int)L.E, at<int32_t>(c.ws, L.ptile_row0),
-                                          at<int32_t>(c.ws, L.ptile_expert), at<int32_t>(c.ws, L.header));
+                                          at<int32_t>(c.ws, L.ptile_expert), at<int32_t>(c.ws, L.wg_order),
+                                          at<int32_t>(c.ws, L.header));
   note_launches(1);
   return cudaGetLastError();
 }

@@ -15,7 +15,7 @@ constexpr int kRouteChunk = 1024;  // (token, slot) pairs per routing chunk
 // Byte offsets of the workspace regions (each 1024-byte aligned).
 struct Layout {
   int64_t T, d, F, E, k, R, Rmax, nchunks;
-  size_t header, counts, offs, chunk_counts, chunk_base, mtile_expert, ptile_row0, ptile_expert, row_token,
+  size_t header, counts, offs, chunk_counts, chunk_base, mtile_expert, ptile_row0, ptile_expert, wg_order, row_token,
       row_slot, row_of;
   size_t xq, w13h, w2h, a1, z1, h, hh, y, dy, dz1, da1, part13, part2;
   // QAD_FLAG_NATIVE_FP8: E4M3 codes of W13, W2, A1 and H, per-token activation scales and
