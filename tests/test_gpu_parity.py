@@ -334,6 +334,18 @@ def test_extreme_expert_counts_and_top_k(E, topk, T):
     _stagewise(run, host_inputs(inp))
 
 
+@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW])
+def test_layer_stagewise_uneven_shapes(fmt):
+    """d = 768 (not a multiple of 512: a partial row chunk in the token scatters, six 128-wide
+    K stages in fc1), F = 384 (128-column tiles for the F-sized GEMMs, 2F = 768), top-3,
+    T = 333 (ragged), E = 6."""
+    inp = synth.make_inputs(synth.workload("tiny_nvfp4", fmt=fmt, E=6, d=768, F=384, topk=3, T=333), seed=9,
+                            device="cuda")
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    _stagewise(run, host_inputs(inp))
+
+
 def test_fewer_rows_than_one_tile():
     base = synth.make_inputs(synth.workload("tiny_nvfp4"), seed=2, device="cuda")
     idx = np.array([[1, 2], [2, 3], [0, 1], [3, 0], [1, 3]])
