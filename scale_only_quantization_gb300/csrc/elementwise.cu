@@ -1,5 +1,7 @@
-// Memory-bound kernels of the scale-only QAD MoE path: weight fake-quant, routing
-// permutation, activation fake-quant, row gather, combine, dY gather, scale reduce.
+// Memory-bound kernels of the scale-only QAD MoE path: weight fake-quant (optionally with
+// E4M3 codes), routing permutation, the per-token activation fake-quant and scatter to the
+// routed rows, the per-row activation fake-quant of H, combine, the per-token dY scatter,
+// the scale-gradient reduction, and the quotient self-check.
 //
 // Weight fake-quant: the whole stacked expert weight is fake-quantized in one vectorised
 // pass (AngelSlim mcore_qad walkthrough, nxmr.cn/news/131691, section 二.4); the weight a

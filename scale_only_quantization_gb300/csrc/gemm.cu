@@ -11,6 +11,9 @@
 //   wgrad  dW2 = dY_e^T . H_hat_e    epilogue: x LSQ factor, per-block sums -> ds2 (dW never stored)
 //   wgrad  dW13 = dZ1_e^T . A1_e     epilogue: same -> ds13
 //
+// With E4M3 operands (F8) the forward GEMMs run tcgen05 kind::f8f6f4 on the quantization
+// codes and the epilogues multiply each fp32 sum by its activation-row and weight-row scale.
+//
 // Rows of each expert are padded to a multiple of 128 (zero rows), so a 128-row half tile
 // never straddles two experts and a wgrad contraction runs over whole 64-row blocks.
 //
@@ -25,8 +28,8 @@
 // not stored).
 //
 // Per CTA (persistent over the pair's tiles): warp 0 issues TMA loads (128B-swizzled
-// tiles) into a STAGES-deep ring; the pair's TMA bytes complete on the leader's "full"
-// barrier; warp 1 of each CTA owns the pair's tensor memory allocation and, in the
+// tiles) into a ring of stages holding one or two 128-byte K atoms per operand row (ATOMS);
+// the pair's TMA bytes complete on the leader's "full" barrier; warp 1 of each CTA owns the pair's tensor memory allocation and, in the
 // leader, one thread issues the MMAs and commits to both CTAs' "empty" (ring slot free)
 // and "full accumulator" barriers at once (multicast); warps 2-9 read their CTA's
 // accumulator (two TMEM buffers, so the next tile's MMAs overlap this epilogue) with
