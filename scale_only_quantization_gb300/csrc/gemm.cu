@@ -15,7 +15,7 @@
 // codes and the epilogues multiply each fp32 sum by its activation-row and weight-row scale.
 //
 // Rows of each expert are padded to a multiple of 128 (zero rows), so a 128-row half tile
-// never straddles two experts and a wgrad contraction runs over whole 64-row blocks.
+// never straddles two experts and a wgrad contraction runs over whole 128-row blocks.
 //
 // The MMAs run on SM pairs (a cluster of two CTAs, tcgen05 cta_group::2): one
 // 256 x BN x 16 MMA issued by the pair's leader reads the 256 rows of A from the two CTAs'
