@@ -106,3 +106,41 @@ def test_recompute_flag_shares_z1_with_y(lib):
     s3 = Q.shape(T, d, 256, E, k, Q.QAD_FMT_NVFP4)
     assert Q.qad_moe_workspace_bytes(s2) == Q.qad_moe_workspace_bytes(s3)
     assert Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4, 8)) == 0
+
+
+def test_native_fp8_flag_adds_codes_and_row_scales(lib):
+    T, d, F, E, k = 512, 256, 128, 4, 2
+    Rmax = (T * k + 127 * E + 127) // 128 * 128
+    base = Q.shape(T, d, F, E, k, Q.QAD_FMT_FP8_ROW)
+    nat = Q.shape(T, d, F, E, k, Q.QAD_FMT_FP8_ROW, Q.QAD_FLAG_NATIVE_FP8)
+    up = lambda n: (n + 1023) // 1024 * 1024
+    extra = up(E * 2 * F * d) + up(E * d * F) + up(Rmax * d) + up(Rmax * F) + up(4 * T) + up(4 * Rmax)
+    assert Q.qad_moe_workspace_bytes(nat) - Q.qad_moe_workspace_bytes(base) == extra
+    for name, n in (("W13_CODES", E * 2 * F * d), ("W2_CODES", E * d * F), ("A1_CODES", Rmax * d),
+                    ("H_CODES", Rmax * F), ("A_SCALE", T), ("H_SCALE", Rmax)):
+        assert Q.qad_moe_debug_view(nat, name)[1] == n
+        assert Q.qad_moe_debug_view(base, name)[1] == 0
+    for fmt in (Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_W8A8, Q.QAD_FMT_W4AFP8):
+        assert Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, fmt, Q.QAD_FLAG_NATIVE_FP8)) == 0
+
+
+def _enum(prefix):
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "qad.h")).read(), flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(%s[A-Z0-9_]+)\s*=\s*(-?\d+)" % prefix, text)}
+
+
+def test_binding_constants_match_the_header(lib):
+    views = _enum("QAD_VIEW_")
+    count = views.pop("QAD_VIEW_COUNT")
+    assert count == len(Q.VIEWS)
+    assert {"QAD_VIEW_" + n: i for i, n in enumerate(Q.VIEWS)} == views
+    kernels = _enum("QAD_K_")
+    assert kernels.pop("QAD_K_COUNT") == Q.KERNELS
+    assert sorted(kernels.values()) == list(range(Q.KERNELS))
+    assert len({Q.qad_kernel_name(i) for i in range(Q.KERNELS)}) == Q.KERNELS
+    flags = _enum("QAD_FLAG_")
+    assert flags == {"QAD_FLAG_STASH_H": Q.QAD_FLAG_STASH_H, "QAD_FLAG_NO_QUANT": Q.QAD_FLAG_NO_QUANT,
+                     "QAD_FLAG_RECOMPUTE": Q.QAD_FLAG_RECOMPUTE, "QAD_FLAG_NATIVE_FP8": Q.QAD_FLAG_NATIVE_FP8}
+    fmts = _enum("QAD_FMT_")
+    assert fmts == {"QAD_FMT_NVFP4": 0, "QAD_FMT_INT4_G128": 1, "QAD_FMT_FP8_ROW": 2, "QAD_FMT_NVFP4A16": 3,
+                    "QAD_FMT_W8A8": 4, "QAD_FMT_W4AFP8": 5}
