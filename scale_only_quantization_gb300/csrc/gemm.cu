@@ -84,6 +84,7 @@ struct Params {
   const __nv_bfloat16* aux; int64_t ld_aux;  // SWIGLU_BWD: Z1
   const __nv_bfloat16* w;  const float* s;   // SCALEGRAD: raw weights [E, Mw, Kw] and scales
   int64_t w_rows, w_cols;
+  int w_vec32;  // w is 32-byte aligned: its sectors are read with 256-bit loads
   float* ds; float* part; int accumulate;
 };
 
@@ -538,14 +539,20 @@ __device__ __forceinline__ Z1Cursor z1_cursor(const Params& p, const Tile& ti, i
   const int64_t row = ti.row_base + q * 32 + lane;
   return {p.aux + row * p.ld_aux, ti.nb * BN + half * (BN / 2)};
 }
-// Z1 of 16-column step `step`: gate 2 x 16 B, up 2 x 16 B
+// Z1 of 16-column step `step`: the 32-byte gate sector and the 32-byte up sector of this
+// thread's row, each with one 256-bit load that allocates no L1 line.  A warp's load touches
+// 32 rows, i.e. 32 lines, and L1 shares the SM with the 225 KB of shared memory this kernel
+// takes: with 16-byte loads through L1 the line allocations throttled the loads and the
+// kernel ran ~11% slower.  Alignment: Z1 rows are 4F bytes apart (F % 128 == 0) from a
+// 256-byte aligned region, and the columns start at multiples of 16 elements.
+__device__ __forceinline__ void ld_nc_256(const void* ptr, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+               : "l"(ptr));
+}
 __device__ __forceinline__ void z1_load(const Params& p, const Z1Cursor& c, int step, uint4 (&slot)[4]) {
-  const uint4* g = reinterpret_cast<const uint4*>(c.row + c.f_first + 16 * step);
-  const uint4* u = reinterpret_cast<const uint4*>(c.row + p.F + c.f_first + 16 * step);
-  slot[0] = __ldg(g);
-  slot[1] = __ldg(g + 1);
-  slot[2] = __ldg(u);
-  slot[3] = __ldg(u + 1);
+  ld_nc_256(c.row + c.f_first + 16 * step, slot[0], slot[1]);
+  ld_nc_256(c.row + p.F + c.f_first + 16 * step, slot[2], slot[3]);
 }
 
 // dZ1 = [dH * up * sig(g) * (1 + g (1 - sig(g))), dH * g * sig(g)] from the stored bf16 Z1,
@@ -616,6 +623,19 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const CUtensorMa
 // tiles) each column half writes its partial sum to
 // part[ds_index * parts + (tile in block) * 2 + half] and a reduction kernel adds the
 // parts in a fixed order.
+// 16 weights (one 32-byte sector of a W row): one 256-bit load that allocates no L1 line
+// when W is 32-byte aligned (rows are multiples of 32 bytes apart and the columns start at
+// multiples of 16), else two 16-byte loads.  A warp's load touches 32 rows of W; the wide
+// form made the two scale-gradient GEMMs 2-3% faster.
+__device__ __forceinline__ void w_load(const __nv_bfloat16* ptr, bool vec32, uint4 (&v)[2]) {
+  if (vec32) {
+    ld_nc_256(ptr, v[0], v[1]);
+  } else {
+    v[0] = __ldg(reinterpret_cast<const uint4*>(ptr));
+    v[1] = __ldg(reinterpret_cast<const uint4*>(ptr) + 1);
+  }
+}
+
 template <int QK>
 __device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const uint4 (&wraw)[2], float sc) {
   float wv[16], x[16];
@@ -687,12 +707,9 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
 
   uint32_t r[16], rn[16];
   uint4 wq[3][2];
-  wq[0][0] = __ldg(reinterpret_cast<const uint4*>(wr));
-  wq[0][1] = __ldg(reinterpret_cast<const uint4*>(wr) + 1);
-  if (STEPS > 1) {
-    wq[1][0] = __ldg(reinterpret_cast<const uint4*>(wr) + 2);
-    wq[1][1] = __ldg(reinterpret_cast<const uint4*>(wr) + 3);
-  }
+  const bool vec32 = p.w_vec32 != 0;
+  w_load(wr, vec32, wq[0]);
+  if (STEPS > 1) w_load(wr + 16, vec32, wq[1]);
   if (have_acc) {
     tmem_ld16_issue(tbase + col0, r);
     tmem_wait16(r);
@@ -703,10 +720,7 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
   float tsum[STEPS];
 #pragma unroll
   for (int j = 0; j < STEPS; ++j) {
-    if (j + 2 < STEPS) {
-      wq[(j + 2) % 3][0] = __ldg(reinterpret_cast<const uint4*>(wr) + 2 * (j + 2));
-      wq[(j + 2) % 3][1] = __ldg(reinterpret_cast<const uint4*>(wr) + 2 * (j + 2) + 1);
-    }
+    if (j + 2 < STEPS) w_load(wr + 16 * (j + 2), vec32, wq[(j + 2) % 3]);
     if (have_acc && j + 1 < STEPS) tmem_ld16_issue(tbase + col0 + 16 * (j + 1), rn);
     tsum[j] = lsq_block_sum<QK>(r, wq[j % 3], sv[j]);
     if (j + 1 < STEPS && have_acc) {
@@ -1276,6 +1290,7 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   p.n_mtiles_w = (int)(m_w / (2 * BM));
   p.n_ntiles = (int)(k_w / bn);
   p.w = static_cast<const __nv_bfloat16*>(w);
+  p.w_vec32 = (reinterpret_cast<uintptr_t>(w) & 31u) == 0;
   p.s = s;
   p.w_rows = m_w;
   p.w_cols = k_w;

@@ -282,6 +282,27 @@ def test_runs_are_deterministic():
     assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
 
 
+@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW])
+def test_weights_only_16_byte_aligned_give_identical_results(fmt):
+    """The scale-gradient epilogue reads W with 256-bit loads when W is 32-byte aligned and
+    with 16-byte loads otherwise (the ABI asks for 16): both give the same bits."""
+    inp = _tiny(fmt)
+    a = Run(inp)
+    moved = dict(inp)
+    for name in ("w13", "w2"):
+        buf = torch.empty(inp[name].numel() + 8, dtype=torch.bfloat16, device="cuda")
+        assert buf.data_ptr() % 32 == 0
+        v = buf[8:].view(inp[name].shape)  # 16 bytes past a 32-byte boundary
+        v.copy_(inp[name])
+        assert v.data_ptr() % 32 == 16
+        moved[name] = v
+    b = Run(moved)
+    assert a.error == 0 and b.error == 0
+    assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_scalegrad_accumulate_adds(fmt):
     inp = _tiny(fmt)
