@@ -50,6 +50,57 @@ def test_workspace_size_and_views(lib):
         assert o + k <= ws
 
 
+_ELEM = dict(HEADER=4, OFFSETS=4, COUNTS=4, ROW_TOKEN=4, ROW_SLOT=4, ROW_OF=4, W13_HAT=2, W2_HAT=2, A1=2, Z1=2,
+             H=2, H_HAT=2, Y=2, DY=2, DZ1=2, DA1=2, XQ=2, W13_CODES=1, W2_CODES=1, A1_CODES=1, H_CODES=1,
+             A_SCALE=4, H_SCALE=4)
+_ALL_FMTS = [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8,
+             Q.QAD_FMT_W4AFP8]
+
+
+def _layouts():
+    for T, d, F, E, k in [(0, 256, 128, 4, 2), (1, 256, 128, 1, 1), (7, 512, 384, 3, 3), (512, 256, 128, 4, 2),
+                          (4096, 2048, 768, 32, 8), (16384, 2048, 768, 128, 8), (1000, 256, 1024, 16, 4)]:
+        for fmt in _ALL_FMTS:
+            flag_sets = [0, Q.QAD_FLAG_STASH_H, Q.QAD_FLAG_RECOMPUTE, Q.QAD_FLAG_NO_QUANT]
+            if fmt == Q.QAD_FMT_FP8_ROW:
+                flag_sets += [Q.QAD_FLAG_NATIVE_FP8, Q.QAD_FLAG_NATIVE_FP8 | Q.QAD_FLAG_RECOMPUTE]
+            for flags in flag_sets:
+                yield T, d, F, E, k, fmt, flags
+
+
+def test_workspace_views_lie_inside_and_do_not_overlap(lib):
+    """Every stage view is 1 KB aligned, lies inside the workspace in bytes, and no two views share
+    bytes except Z1 and Y under QAD_FLAG_RECOMPUTE when Y's rows hold Z1's (d >= 2F)."""
+    n_cases = 0
+    for T, d, F, E, k, fmt, flags in _layouts():
+        s = Q.shape(T, d, F, E, k, fmt, flags)
+        ws = Q.qad_moe_workspace_bytes(s)
+        assert ws > 0 and ws % 1024 == 0
+        spans = []
+        for name in Q.VIEWS:
+            off, n = Q.qad_moe_debug_view(s, name)
+            assert n >= 0
+            if n == 0:
+                continue
+            assert off % 1024 == 0, (name, off)
+            end = off + n * _ELEM[name]
+            assert end <= ws, (name, off, n, ws)
+            spans.append((off, end, name))
+        spans.sort()
+        aliased = (flags & Q.QAD_FLAG_RECOMPUTE) and d >= 2 * F
+        for (a0, a1, an), (b0, b1, bn) in zip(spans, spans[1:]):
+            if b0 < a1:
+                assert aliased and {an, bn} == {"Z1", "Y"}, (an, bn, T, d, F, E, k, fmt, flags)
+        names = [n for _, _, n in spans]
+        if flags & Q.QAD_FLAG_NATIVE_FP8:
+            per_token = {"A_SCALE"} if T > 0 else set()  # one activation scale per token
+            assert {"W13_CODES", "W2_CODES", "A1_CODES", "H_CODES", "H_SCALE"} | per_token <= set(names)
+        else:
+            assert not {"W13_CODES", "W2_CODES", "A1_CODES", "H_CODES", "A_SCALE", "H_SCALE"} & set(names)
+        n_cases += 1
+    assert n_cases > 150
+
+
 @pytest.mark.parametrize("bad, status", [
     (dict(d=200), Q.QAD_ERR_UNSUPPORTED),
     (dict(d=384), Q.QAD_ERR_UNSUPPORTED),
