@@ -165,6 +165,9 @@ int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* top
  *   accumulate != 0.
  * The weight gradient is reduced into the scale gradient inside the GEMM epilogue and
  * never stored.  Must follow qad_moe_bwd_dgrad on the same workspace and stream.
+ * The epilogue reads w13 / w2 row by row: with 32-byte aligned weights (as PyTorch's
+ * allocations are) one 256-bit load per 16 weights, with 16-byte aligned ones two 16-byte
+ * loads; the results are the same bits.
  */
 int qad_moe_bwd_scalegrad(const qad_moe_shape* s, const void* w13, const float* s13,
                           const void* w2, const float* s2, float* ds13, float* ds2,
