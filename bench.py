@@ -5,13 +5,19 @@
 A step is one pass of the whole path over one batch: qad_moe_fwd, qad_moe_bwd_dgrad and
 qad_moe_bwd_scalegrad through the C ABI.  `value` is tokens/s with inputs resident in HBM;
 `e2e` adds, every step, the host->device copy of the step's activations and routing from
-pinned memory and the device->host read of out, dx and the scale gradients, double-buffered
-on a copy stream as an input pipeline would run them.  Every step
-streams far more than the 129 MB L2 (weights alone are 1.2 GB at the default workload),
-so no explicit flush is used.  Under torchrun each rank runs its own replica on its own
-batch (weak scaling) and the scale gradients are averaged over ranks, as data-parallel
-training does.  `--impl reference` times the fp64 CPU oracle on a bounded sample of the
-same workload.
+pinned memory and the device->host read of out, dx, dprobs and the scale gradients,
+double-buffered as an input pipeline would run them (inputs up on one copy stream, results
+down on another, both beside the compute).  Every step streams far more than the 129 MB L2
+(weights alone are 1.2 GB at the default workload), so no explicit flush is used.
+
+Roofline fractions of the GEMMs are taken against the measured bf16 peak of the clock
+regime the timed region ran in: the burst figure when the sampled median SM clock sat at
+its maximum with no power cap, the sustained one otherwise; both fractions are printed.
+`configs` holds a short timed run of every other workload on the same box.
+
+Under torchrun each rank runs its own replica on its own batch (weak scaling) and the
+scale gradients are averaged over ranks, as data-parallel training does.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
 """
 import argparse
 import json
@@ -66,7 +72,7 @@ class Clocks:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -86,10 +92,15 @@ class Clocks:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, *others):
+        """Median SM clock, maximum and active throttle reasons over this sampler's lines and
+        those of `others` (the other timed regions of the same run)."""
         sm, mx, reasons = [], None, set()
+        lines = list(self.lines)
+        for o in others:
+            lines += o.lines
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -149,6 +160,194 @@ def _traffic(kernel, workload):
     return None
 
 
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s the fake-quant target is stated against (nominal HBM3e)
+
+
+def tensor_peak(clocks, tf_burst, tf_sust):
+    """The measured bf16 peak that matches the run's clock regime: the burst figure when the
+    median SM clock under load sat at the maximum and no power cap was active (or when no
+    clock was sampled: the larger peak, so no fraction is overstated), else the sustained one."""
+    sm, mx, reasons = clocks.get("sm_mhz"), clocks.get("sm_max_mhz"), clocks.get("reasons") or []
+    if sm is None or not mx:
+        return tf_burst, "bf16_tflops (burst; clocks not sampled)"
+    if sm >= 0.97 * mx and "sw_power_cap" not in reasons:
+        return tf_burst, "bf16_tflops (burst: median SM clock %.0f of %.0f MHz, no power cap)" % (sm, mx)
+    return tf_sust, "bf16_tflops_sustained (median SM clock %.0f of %.0f MHz, reasons %s)" % (
+        sm, mx, ",".join(reasons) or "none")
+
+
+def kernel_table(prof, steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels=()):
+    """Per kernel: time per launch, launches per step, share of the step's serial kernel time,
+    and for the GEMMs and the weight fake-quant the achieved rate against the peaks."""
+    kernels = {}
+    for name, (tot, n) in prof.items():
+        if n == 0:
+            continue
+        entry = {"ms_per_launch": tot / n, "launches_per_step": n / steps, "share": None}
+        if name in ("route_permute", "gather_rows"):
+            # on the library's side stream beside the weight fake-quant: wall time while sharing the GPU
+            entry["overlapped_with"] = "fakequant_w"
+        if name in alg:
+            bound, amount = alg[name]
+            per_s = amount / (tot / n / 1e3)
+            if bound == "tensor":
+                m = 2 if name in f8_kernels else 1  # E4M3 x E4M3: nominal fp8 / bf16 ratio
+                entry.update(achieved_tflops=per_s / 1e12, frac=per_s / 1e12 / (m * peak),
+                             frac_of_burst=per_s / 1e12 / (m * tf_burst),
+                             frac_of_sustained=per_s / 1e12 / (m * tf_sust))
+            else:
+                entry.update(achieved_gbs=per_s / 1e9, frac=per_s / 1e9 / hbm,
+                             frac_of_nominal_8tbs=per_s / 1e9 / NOMINAL_HBM_GBS)
+        kernels[name] = entry
+    total_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values() if "overlapped_with" not in v)
+    for v in kernels.values():
+        if "overlapped_with" not in v:
+            v["share"] = v["ms_per_launch"] * v["launches_per_step"] / total_ms if total_ms else None
+    return kernels
+
+
+class Layer:
+    """One MoE layer's buffers on the device and its fwd + dgrad + scalegrad step (C ABI)."""
+
+    def __init__(self, Q, inp, flags, dev):
+        self.Q, self.inp = Q, inp
+        T, d, F, E, k, fmt = inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"]
+        self.s = Q.shape(T, d, F, E, k, fmt, flags)
+        nb = Q.qad_moe_workspace_bytes(self.s)
+        if nb == 0:
+            raise RuntimeError("shape not supported: %r" % ((T, d, F, E, k, fmt, flags),))
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        self.outs = self.new_outputs()
+
+    def new_outputs(self):
+        inp = self.inp
+        out = torch.empty((inp["T"], inp["d"]), dtype=torch.bfloat16, device=self.ws.device)
+        return (out, torch.empty_like(out), torch.empty((inp["T"], inp["topk"]), dtype=torch.float32,
+                                                         device=self.ws.device),
+                torch.empty_like(inp["s13"]), torch.empty_like(inp["s2"]))
+
+    def step(self, stream, x, idx, p, dout, outs=None, average=None):
+        Q, inp = self.Q, self.inp
+        out, dx, dprobs, ds13, ds2 = outs if outs is not None else self.outs
+        Q.qad_moe_fwd(self.s, x, idx, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], out, self.ws, stream)
+        Q.qad_moe_bwd_dgrad(self.s, dout, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], dx, dprobs, self.ws,
+                            stream)
+        Q.qad_moe_bwd_scalegrad(self.s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], ds13, ds2, 0, self.ws, stream)
+        if average is not None:
+            average([ds13, ds2])
+
+
+def timed_steps(Q, layer, stream, dev, steps, warmup, barrier, local, average=None):
+    """Warm-up, then `steps` device-resident steps timed with CUDA events on the launching
+    stream, the library's per-kernel events on, clocks sampled.  Returns (ms per step, kernel
+    profile, library launches in the timed region, clock sampler)."""
+    inp = layer.inp
+    args_dev = (inp["x"], inp["topk_idx"], inp["topk_w"], inp["dout"])
+    for _ in range(warmup):
+        layer.step(stream, *args_dev, average=average)
+    err = Q.qad_check_device_error(layer.ws, stream)
+    if err:
+        raise RuntimeError("device error word %d after warm-up" % err)
+    barrier()
+    Q.qad_profile_reset()
+    Q.qad_profile_enable(True)
+    n0 = Q.qad_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(steps):
+            layer.step(stream, *args_dev, average=average)
+        e1.record(stream)
+        barrier()
+    launches = Q.qad_launch_count() - n0
+    ms = e0.elapsed_time(e1) / steps
+    prof = Q.qad_profile_read()
+    Q.qad_profile_enable(False)
+    return ms, prof, launches, clk
+
+
+def e2e_steps(layer, stream, dev, steps, warmup, barrier, local, average=None):
+    """The same step end to end through the public calls: every step copies its inputs (x,
+    topk_idx, topk_w, dout) from pinned host memory and reads its results (out, dx, dprobs,
+    ds13, ds2) back to pinned host memory.  Double-buffered as an input pipeline runs it:
+    one copy stream moves step i+1's inputs to the device while the compute stream runs step
+    i, and a second copy stream moves step i's results to the host, so the two directions of
+    the host link run at the same time.  Returns (ms per step, H2D bytes, D2H bytes, clocks)."""
+    inp = layer.inp
+    args_dev = (inp["x"], inp["topk_idx"], inp["topk_w"], inp["dout"])
+    host_in = [[a.cpu().pin_memory() for a in args_dev] for _ in range(2)]
+    dev_in = [[torch.empty_like(a) for a in args_dev] for _ in range(2)]
+    dev_out = [layer.new_outputs() for _ in range(2)]
+    host_out = [[torch.empty(a.shape, dtype=a.dtype, pin_memory=True) for a in dev_out[0]] for _ in range(2)]
+    h2d = sum(a.numel() * a.element_size() for a in host_in[0])
+    d2h = sum(a.numel() * a.element_size() for a in host_out[0])
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        with torch.cuda.stream(up):
+            for dst, src in zip(dev_in[0], host_in[0]):
+                dst.copy_(src, non_blocking=True)
+            ev_in[0].record(up)
+        for i in range(n):
+            b = i % 2
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_read[b])  # step i-2's results have left dev_out[b]
+            layer.step(stream, *dev_in[b], outs=dev_out[b], average=average)
+            ev_done[b].record(stream)
+            if i + 1 < n:
+                nb = (i + 1) % 2
+                with torch.cuda.stream(up):
+                    if i >= 1:
+                        up.wait_event(ev_done[nb])  # step i-1 has finished reading dev_in[nb]
+                    for dst, src in zip(dev_in[nb], host_in[nb]):
+                        dst.copy_(src, non_blocking=True)
+                    ev_in[nb].record(up)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done[b])
+                for dst, src in zip(host_out[b], dev_out[b]):
+                    dst.copy_(src, non_blocking=True)
+                ev_read[b].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+
+    run(max(3, warmup))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        e0.record(stream)
+        run(steps)
+        e1.record(stream)
+        barrier()
+    return e0.elapsed_time(e1) / steps, h2d, d2h, clk
+
+
+def dominant_roofline(kernels, alg, peak, peak_name, hbm, peak_src, f8_kernels, workload):
+    dom = max((nm for nm in kernels if nm in alg), key=lambda nm: kernels[nm]["share"])
+    bound, amount = alg[dom]
+    dur = kernels[dom]["ms_per_launch"] / 1e3
+    if bound == "tensor":
+        m = 2 if dom in f8_kernels else 1
+        roof = {"bound": "tensor", "kernel": dom, "achieved": amount / dur / 1e12, "peak": m * peak,
+                "unit": "TFLOP/s",
+                "peak_source": peak_src + " " + peak_name + (" x 2 (nominal fp8 / bf16)" if m == 2 else ""),
+                "frac_of_burst": kernels[dom]["frac_of_burst"],
+                "frac_of_sustained": kernels[dom]["frac_of_sustained"]}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": amount / dur / 1e9, "peak": hbm, "unit": "GB/s",
+                "peak_source": peak_src + " hbm_gbs", "frac_of_nominal_8tbs": amount / dur / 1e9 / NOMINAL_HBM_GBS}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = _traffic(dom, workload)
+    return roof
+
+
 def run_ours(args):
     import scale_only_quantization_gb300 as Q
     from scale_only_quantization_gb300 import build as B
@@ -170,21 +369,8 @@ def run_ours(args):
     inp = synth.make_inputs(cfg, seed=rank, device=dev)
     T, d, F, E, k, fmt = inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"]
     flags = (Q.QAD_FLAG_RECOMPUTE if args.recompute else 0) | (Q.QAD_FLAG_NATIVE_FP8 if args.native_fp8 else 0)
-    s = Q.shape(T, d, F, E, k, fmt, flags)
-    ws = torch.empty(Q.qad_moe_workspace_bytes(s), dtype=torch.uint8, device=dev)
-    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-    dx = torch.empty_like(out)
-    dprobs = torch.empty((T, k), dtype=torch.float32, device=dev)
-    ds13 = torch.empty_like(inp["s13"])
-    ds2 = torch.empty_like(inp["s2"])
     stream = torch.cuda.current_stream(dev)
-
-    def step(x, idx, p, dout):
-        Q.qad_moe_fwd(s, x, idx, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], out, ws, stream)
-        Q.qad_moe_bwd_dgrad(s, dout, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], dx, dprobs, ws, stream)
-        Q.qad_moe_bwd_scalegrad(s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], ds13, ds2, 0, ws, stream)
-        if world > 1:
-            dp.average_scale_grads([ds13, ds2])
+    average = dp.average_scale_grads if world > 1 else None
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -193,132 +379,27 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    args_dev = (inp["x"], inp["topk_idx"], inp["topk_w"], inp["dout"])
-    for _ in range(args.warmup):
-        step(*args_dev)
-    err = Q.qad_check_device_error(ws, stream)
-    if err:
-        raise RuntimeError("device error word %d after warm-up" % err)
-    barrier()
+    layer = Layer(Q, inp, flags, dev)
 
     # ---- device-resident timed region (kernel timing on, clocks sampled)
-    Q.qad_profile_reset()
-    Q.qad_profile_enable(True)
-    n0 = Q.qad_launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
-        barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
-            step(*args_dev)
-        e1.record(stream)
-        barrier()
-    launches = Q.qad_launch_count() - n0
-    ms = e0.elapsed_time(e1) / args.steps
-    prof = Q.qad_profile_read()
-    Q.qad_profile_enable(False)
+    ms, prof, launches, clk = timed_steps(Q, layer, stream, dev, args.steps, args.warmup, barrier, local, average)
     ms = dp.max_over_ranks(ms, device=dev)
 
-    # ---- end to end through the public API with pinned host buffers.  Every step copies its
-    # inputs (x, topk_idx, topk_w, dout) from pinned host memory and reads its results (out,
-    # dx, ds13, ds2) back, as a double-buffered input pipeline does: a copy stream moves step
-    # i+1's inputs and step i's results while the compute stream runs step i+1.
-    host_in = [[a.cpu().pin_memory() for a in args_dev] for _ in range(2)]
-    dev_in = [[torch.empty_like(a) for a in args_dev] for _ in range(2)]
-    dev_out = [[torch.empty_like(a) for a in (out, dx, ds13, ds2)] for _ in range(2)]
-    host_out = [[torch.empty(a.shape, dtype=a.dtype, pin_memory=True) for a in (out, dx, ds13, ds2)]
-                for _ in range(2)]
-    h2d = sum(a.numel() * a.element_size() for a in host_in[0])
-    d2h = sum(a.numel() * a.element_size() for a in host_out[0])
-    copy = torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_read = [torch.cuda.Event() for _ in range(2)]
-
-    def step_into(b, x, idx, p, dout):
-        o, g, d13, d2 = dev_out[b]
-        Q.qad_moe_fwd(s, x, idx, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], o, ws, stream)
-        Q.qad_moe_bwd_dgrad(s, dout, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], g, dprobs, ws, stream)
-        Q.qad_moe_bwd_scalegrad(s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], d13, d2, 0, ws, stream)
-        if world > 1:
-            dp.average_scale_grads([d13, d2])
-
-    def e2e_run(n):
-        with torch.cuda.stream(copy):
-            for dst, src in zip(dev_in[0], host_in[0]):
-                dst.copy_(src, non_blocking=True)
-            ev_in[0].record(copy)
-        for i in range(n):
-            b = i % 2
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_read[b])  # step i-2's results have left dev_out[b]
-            step_into(b, *dev_in[b])
-            ev_done[b].record(stream)
-            with torch.cuda.stream(copy):
-                if i + 1 < n:
-                    nb = (i + 1) % 2
-                    if i >= 1:
-                        copy.wait_event(ev_done[nb])  # step i-1 has finished reading dev_in[nb]
-                    for dst, src in zip(dev_in[nb], host_in[nb]):
-                        dst.copy_(src, non_blocking=True)
-                    ev_in[nb].record(copy)
-                copy.wait_event(ev_done[b])
-                for dst, src in zip(host_out[b], dev_out[b]):
-                    dst.copy_(src, non_blocking=True)
-                ev_read[b].record(copy)
-        stream.wait_stream(copy)
-
-    e2e_run(max(3, args.warmup))
-    barrier()
-    e0.record(stream)
-    e2e_run(args.steps)
-    e1.record(stream)
-    barrier()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
+    # ---- end to end through the public API with pinned host buffers
+    ms_e2e, h2d, d2h, clk_e2e = e2e_steps(layer, stream, dev, args.steps, args.warmup, barrier, local, average)
     ms_e2e = dp.max_over_ranks(ms_e2e, device=dev)
 
-    # ---- roofline of the dominant kernel (largest share of the timed region)
+    # ---- roofline of the dominant kernel (largest share of the timed region), against the
+    # measured peak of the clock regime the timed region ran in
     hbm, tf_burst, tf_sust, peak_src = _peaks()
+    clocks = clk.summary()
+    peak, peak_name = tensor_peak(clocks, tf_burst, tf_sust)
     alg = algorithmic_per_launch(cfg, native_fp8=args.native_fp8)
-    # E4M3 x E4M3 GEMMs take the fp8 peak: the measured bf16 one x the nominal fp8 / bf16 ratio (2)
     f8_kernels = ("gemm_fc1_swiglu_aq", "gemm_fc2") if args.native_fp8 else ()
-    kernels = {}
-    for name, (tot, n) in prof.items():
-        if n == 0:
-            continue
-        entry = {"ms_per_launch": tot / n, "launches_per_step": n / args.steps, "share": None}
-        if name in ("route_permute", "gather_rows"):
-            # on the library's side stream beside the weight fake-quant: wall time while sharing the GPU
-            entry["overlapped_with"] = "fakequant_w"
-        if name in alg:
-            bound, amount = alg[name]
-            per_s = amount / (tot / n / 1e3)
-            if bound == "tensor":
-                peak = tf_sust * (2 if name in f8_kernels else 1)
-                entry.update(achieved_tflops=per_s / 1e12, frac=per_s / 1e12 / peak)
-            else:
-                entry.update(achieved_gbs=per_s / 1e9, frac=per_s / 1e9 / hbm)
-        kernels[name] = entry
-    total_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values() if "overlapped_with" not in v)
-    for v in kernels.values():
-        if "overlapped_with" not in v:
-            v["share"] = v["ms_per_launch"] * v["launches_per_step"] / total_ms if total_ms else None
-    dom = max((nm for nm in kernels if nm in alg), key=lambda nm: kernels[nm]["share"])
-    bound, amount = alg[dom]
-    dur = kernels[dom]["ms_per_launch"] / 1e3
-    if bound == "tensor" and dom in f8_kernels:
-        roof = {"bound": "tensor", "kernel": dom, "achieved": amount / dur / 1e12, "peak": 2 * tf_sust,
-                "unit": "TFLOP/s", "peak_source": peak_src + " bf16_tflops_sustained x 2 (nominal fp8 / bf16)"}
-    elif bound == "tensor":
-        roof = {"bound": "tensor", "kernel": dom, "achieved": amount / dur / 1e12, "peak": tf_sust,
-                "unit": "TFLOP/s", "peak_source": peak_src + " bf16_tflops_sustained"}
-    else:
-        roof = {"bound": "hbm", "kernel": dom, "achieved": amount / dur / 1e9, "peak": hbm, "unit": "GB/s",
-                "peak_source": peak_src + " hbm_gbs"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = _traffic(dom, args.workload)
+    kernels = kernel_table(prof, args.steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels)
+    roof = dominant_roofline(kernels, alg, peak, peak_name, hbm, peak_src, f8_kernels, args.workload)
     flops_step = synth.tokens_to_flops(cfg)
+    step_tf = flops_step / (ms / 1e3) / 1e12
 
     line = {
         "metric": METRIC, "value": T * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
@@ -330,19 +411,27 @@ def run_ours(args):
                    "tokens_per_gpu": T, "global_batch": T * world, "parallelism": "dp%d" % world,
                    "activations": "recompute" if args.recompute else "stash",
                    "forward_gemms": "e4m3 codes, scales on the sums" if args.native_fp8 else "bf16 fake-quant",
-                   "workspace_gb": ws.numel() / 1e9,
+                   "workspace_gb": layer.ws.numel() / 1e9,
                    "l2": "inputs larger than L2 (weights %.2f GB streamed per pass), no flush" %
                          (2 * 3 * E * F * d / 1e9)},
-        "step_tflops": flops_step / (ms / 1e3) / 1e12,
-        "step_tensor_frac_of_sustained": flops_step / (ms / 1e3) / 1e12 / tf_sust,
+        "step_tflops": step_tf,
+        "step_tensor_frac": step_tf / peak,
+        "step_tensor_frac_of_burst": step_tf / tf_burst,
+        "step_tensor_frac_of_sustained": step_tf / tf_sust,
         "roofline": roof,
         "kernels": kernels,
         "gpu_launches": int(launches),
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": {"value": T * world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "note": "pinned host buffers; copies of step i+1 inputs and step i results overlap compute"},
+                "link_gbs": (h2d + d2h) / (ms_e2e / 1e3) / 1e9, "clocks": clk_e2e.summary(),
+                "note": "pinned host buffers; step i+1's inputs go up on one copy stream and step i's results "
+                        "come down on another while step i+1 computes"},
     }
+    del layer
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_configs and not over:
+        line["configs"] = other_configs(Q, args, dev, stream, barrier, local, tf_burst, tf_sust, hbm, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
     if rank == 0:
@@ -350,6 +439,35 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def other_configs(Q, args, dev, stream, barrier, local, tf_burst, tf_sust, hbm, peak_src):
+    """A short timed run of every other workload (same step, default flags): tokens/s, ms per
+    step, and the dominant kernel against the peak of that run's own clock regime."""
+    res = {}
+    for name in sorted(synth.WORKLOADS):
+        if name == args.workload:
+            continue
+        cfg = synth.workload(name)
+        inp = synth.make_inputs(cfg, seed=0, device=dev)
+        layer = Layer(Q, inp, 0, dev)
+        ms, prof, launches, clk = timed_steps(Q, layer, stream, dev, args.config_steps, 3, barrier, local)
+        clocks = clk.summary()
+        peak, peak_name = tensor_peak(clocks, tf_burst, tf_sust)
+        alg = algorithmic_per_launch(cfg)
+        kernels = kernel_table(prof, args.config_steps, alg, peak, tf_burst, tf_sust, hbm)
+        roof = dominant_roofline(kernels, alg, peak, peak_name, hbm, peak_src, (), name)
+        step_tf = synth.tokens_to_flops(cfg) / (ms / 1e3) / 1e12
+        res[name] = {"value": cfg["T"] / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+                     "steps": args.config_steps, "format": FMT_NAME[cfg["fmt"]],
+                     "routing": cfg.get("routing", "uniform"), "step_tflops": step_tf,
+                     "step_tensor_frac": step_tf / peak, "gpu_launches": int(launches),
+                     "roofline": {kk: roof[kk] for kk in ("kernel", "bound", "achieved", "unit", "frac",
+                                                          "peak_source")},
+                     "clocks": clocks}
+        del layer, inp
+        torch.cuda.empty_cache()
+    return res
 
 
 def _oracle_sample(cfg, host, n_experts):
@@ -433,6 +551,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the short timed runs of the other workloads (the `configs` key)")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps of each other workload")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")

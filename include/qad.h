@@ -248,14 +248,19 @@ int64_t qad_launch_count(void);
  *   counts    int32 [E]                               routed rows per expert
  *   header    int32 [4]                               device error word (QAD_DEV_*), 128-row
  *                                                     tiles, padded rows, routed rows
- * All pointers are device pointers; nothing is allocated.  The library's own scratch for
- * this call is a file-scope device array of 534 KB per GPU (held until the process
- * exits), sized for E <= QAD_NOALLOC_MAX_EXPERTS and T * topk <= QAD_NOALLOC_MAX_PAIRS;
- * larger problems return QAD_ERR_SCRATCH_LIMIT before anything is launched.  The first
- * call on a device looks up the scratch's device address (cudaGetSymbolAddress), so make
- * that first call before any stream capture.  Every call shares the one scratch array:
- * calls whose execution overlaps on the GPU (different streams, or different host threads)
- * race and give undefined results; the header is cleared at the start of each call.
+ * All pointers are device pointers to int32 data and need only 4-byte alignment (unlike the
+ * layer calls' 16 bytes: these kernels read and write single int32 values); nothing is
+ * allocated.  The library's own scratch for this call is a file-scope device array of
+ * 534 KB per GPU (held until the process exits), sized for E <= QAD_NOALLOC_MAX_EXPERTS and
+ * T * topk <= QAD_NOALLOC_MAX_PAIRS; larger problems return QAD_ERR_SCRATCH_LIMIT before
+ * anything is launched.  The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress) and keeps it for the life of the process, so make that first call
+ * before any stream capture, and do not call cudaDeviceReset on a device between calls (a
+ * reset unloads the library's device code with the array; its address may change).  Every
+ * call shares the one scratch array: calls whose execution overlaps on the GPU (different
+ * streams, or different host threads) race and give undefined results; the header is
+ * cleared at the start of each call.  Null pointers and sizes outside the limits return
+ * QAD_ERR_INVALID_ARG / QAD_ERR_SCRATCH_LIMIT.
  */
 enum { QAD_NOALLOC_MAX_EXPERTS = 256, QAD_NOALLOC_MAX_PAIRS = 262144 };
 int qad_route_permute_noalloc(const int32_t* topk_idx, int64_t T, int32_t topk, int32_t E,

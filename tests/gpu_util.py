@@ -35,6 +35,16 @@ def vals(t):
     return OQ.bf16_to_f64(bits(t))
 
 
+E2E_REL_L2 = 1e-3  # end-to-end (oracle from the raw inputs) relative L2 bound of out and dx
+
+
+def rel_l2(gpu, ref):
+    """||gpu - ref||_2 / ||ref||_2 over all elements."""
+    gpu = np.asarray(gpu, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    return float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
 def assert_close(gpu, ref, what):
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

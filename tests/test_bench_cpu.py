@@ -32,3 +32,37 @@ def test_reference_arm_prints_the_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    m = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(m)
+    return m
+
+
+def test_tensor_peak_follows_the_clock_regime():
+    """Burst peak when the median SM clock sat at its maximum with no power cap, sustained peak
+    under the power cap or a lower clock, and the larger (burst) peak when nothing was sampled."""
+    b = _bench_module()
+    assert b.tensor_peak({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}, 1890.0, 1710.0)[0] == 1890.0
+    assert b.tensor_peak({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}, 1890.0,
+                         1710.0)[0] == 1710.0
+    assert b.tensor_peak({"sm_mhz": 1700.0, "sm_max_mhz": 2070.0, "reasons": []}, 1890.0, 1710.0)[0] == 1710.0
+    assert b.tensor_peak({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}, 1890.0, 1710.0)[0] == 1890.0
+
+
+def test_kernel_table_fractions_and_shares():
+    b = _bench_module()
+    alg = {"gemm_fc1_swiglu_aq": ("tensor", 1e12), "fakequant_w": ("hbm", 1e9)}
+    prof = {"gemm_fc1_swiglu_aq": (2.0, 2), "fakequant_w": (1.0, 4), "route_permute": (0.5, 2), "combine": (0.0, 0)}
+    k = b.kernel_table(prof, 2, alg, 2000.0, 2000.0, 1000.0, 5000.0)
+    g = k["gemm_fc1_swiglu_aq"]
+    assert abs(g["achieved_tflops"] - 1000.0) < 1e-9 and abs(g["frac"] - 0.5) < 1e-12
+    assert abs(g["frac_of_sustained"] - 1.0) < 1e-12 and abs(g["frac_of_burst"] - 0.5) < 1e-12
+    f = k["fakequant_w"]
+    assert abs(f["achieved_gbs"] - 4000.0) < 1e-9 and abs(f["frac"] - 0.8) < 1e-12
+    assert abs(f["frac_of_nominal_8tbs"] - 0.5) < 1e-12
+    assert "combine" not in k and k["route_permute"]["share"] is None
+    assert abs(g["share"] - 2.0 / 3.0) < 1e-12 and abs(f["share"] - 1.0 / 3.0) < 1e-12

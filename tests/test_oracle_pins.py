@@ -527,3 +527,108 @@ def test_factored_fc1_is_the_scaled_integer_code_product():
         got = out["z1"][off[e]:off[e + 1]]
         # fp64 rounding of the oracle's sum only (cancellation makes the error absolute)
         assert np.abs(got - want).max() <= 1e-12 * np.abs(want).max(), e
+
+
+# ------------------------------------------------------------------------------ quantizer placement (hand-worked)
+
+def _bf16_bits_of(values):
+    return Q.f64_to_bf16_bits(np.asarray(values, dtype=np.float64))
+
+
+def test_quantizer_placement_hand_worked_case():
+    """nvfp4, one expert, one token, d = F = 16, p = 0.5: every stage worked out by hand.
+
+    x = [6, 1.25, 0...]: block amax 6, s_a = 1, and 1.25 is a tie that rounds to the even
+    code 1, so A1 = [6, 1, 0...] (the activation quantizer sits on fc1's input).
+    Gate rows are [12, 0...] with s = 2 (12 / 2 = 6 on the grid): every gate is 6 * 12 = 72,
+    and silu(72) = 72 exactly in fp64 (exp(-72) vanishes beside 1).  Up row i is [w_i, c_i, 0...]
+    with a power-of-two scale that keeps it on the grid, so u_i = 6 w_i + c_i and H_i = 72 u_i.
+    H's block amax is 72 * 36 = 2592, s_H = 432, and H_i / s_H = u_i / 6:
+      u:      36   18   9    4.5   2.25   1.125  30   15   10.5  -18   0...
+      H/s_H:  6    3    1.5  0.75  0.375  0.1875 5    2.5  1.75  -3    0
+      code:   6    3    1.5  1     0.5    0      4    2    2     -3    0   (0.75, 5, 2.5, 1.75: ties to even)
+      H_hat:  2592 1296 648  432   216    0      1728 864  864   -1296 0
+    W2 is the identity (s = 1/4: 1 / 0.25 = 4 on the grid), so Y = H_hat and out = 0.5 H_hat.
+    Had fc2 read H instead of H_hat, out[3] would be 162, not 216; had the activation
+    quantizer been skipped on x, u_6 = 24 + 7.5 and H_hat_6 = 2592, not 1728."""
+    d = F = 16
+    x = np.zeros((1, d))
+    x[0, :2] = [6.0, 1.25]
+    w_up = [6, 3, 1.5, 0.75, 0.375, 0.1875, 4, 2, 1.5, -3] + [0] * 6
+    c_up = [0, 0, 0, 0, 0, 0, 6, 3, 1.5, 0] + [0] * 6
+    s_up = [1, 1, 1, 0.5, 0.25, 0.125, 1, 1, 1, 1] + [1] * 6
+    w13 = np.zeros((1, 2 * F, d))
+    s13 = np.ones((1, 2 * F, 1))
+    w13[0, :F, 0] = 12.0
+    s13[0, :F, 0] = 2.0
+    w13[0, F:, 0] = w_up
+    w13[0, F:, 1] = c_up
+    s13[0, F:, 0] = s_up
+    w2 = np.eye(d, F)[None]
+    s2 = np.full((1, d, 1), 0.25)
+    fwd = M.moe_forward(Q.FMT_NVFP4, _bf16_bits_of(x), np.zeros((1, 1), np.int64), np.array([[0.5]]),
+                        _bf16_bits_of(w13), s13.astype(np.float32), _bf16_bits_of(w2), s2.astype(np.float32))
+    a1 = np.zeros(d)
+    a1[:2] = [6.0, 1.0]
+    assert np.array_equal(fwd["a1"][0], a1)
+    assert np.array_equal(fwd["w13h"], w13) and np.array_equal(fwd["w2h"], w2)
+    u = np.array([36, 18, 9, 4.5, 2.25, 1.125, 30, 15, 10.5, -18] + [0] * 6)
+    assert np.array_equal(fwd["z1"][0], np.concatenate([np.full(F, 72.0), u]))
+    assert np.array_equal(fwd["h"][0], 72.0 * u)
+    hh = np.array([2592, 1296, 648, 432, 216, 0, 1728, 864, 864, -1296] + [0] * 6, dtype=np.float64)
+    assert np.array_equal(fwd["hh"][0], hh)
+    assert np.array_equal(fwd["y"][0], hh)
+    assert np.array_equal(fwd["out"][0], 0.5 * hh)
+
+    # backward, straight through the activation quantizer: dout = 2 everywhere, so dY = 1 and dH = 1
+    # (identity W2); at g = 72, sigmoid = 1 exactly, so dgate = dH * u and dup = dH * 72
+    bwd = M.moe_dgrad(_bf16_bits_of(np.full((1, d), 2.0)), np.array([[0.5]]), fwd)
+    assert np.array_equal(bwd["dy"][0], np.ones(d))
+    assert np.array_equal(bwd["dz1"][0], np.concatenate([u, np.full(F, 72.0)]))
+    # dA1[0] = 12 * sum(u) + 72 * sum(w_up) = 1300.5 + 1174.5 = 2475 -> bf16 (spacing 16) 2480;
+    # dA1[1] = 72 * sum(c_up) = 756
+    da1 = np.zeros(d)
+    da1[:2] = [2480.0, 756.0]
+    assert np.array_equal(bwd["da1"][0], da1) and np.array_equal(bwd["dx"][0], da1)
+
+
+# ------------------------------------------------------------------------------ the fp32 quotient, bit by bit
+
+def test_quotient_is_the_correctly_rounded_fp32_value():
+    """oracle.quant._quotient(w, s) against exact rational arithmetic: the result is the fp32
+    value nearest to w / s (ties to the even significand), on random pairs and on hard cases
+    (scales with all-ones significands, powers of two, quotients at fp32 midpoints, results in
+    fp32's subnormal range)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(7)
+    w = Q.bf16_to_f64(rng.integers(0, 1 << 16, 3000, dtype=np.uint32).astype(np.uint16))
+    w = w[np.isfinite(w) & (np.abs(w) < 2.0 ** 100)]                                 # quotients stay finite
+    s = rng.uniform(2.0 ** -20, 2.0 ** 4, 3000).astype(np.float32).astype(np.float64)
+    ones = np.float32(np.nextafter(np.float32(2.0), np.float32(0.0)))          # 2 - 2^-23
+    hard_s = [float(ones) * 2.0 ** e for e in range(-30, 10, 3)] + [2.0 ** e for e in range(-40, 20, 7)]
+    hard_w = [1.0, 3.0, -5.0, 0.0078125, 1.5, 65280.0, -0.0]
+    mid = []
+    for k in range(40):  # w = s * (a fp32 midpoint): s = 2^-k exact, w/s has 25 significant bits
+        m = (np.float64(np.float32(1.0 + k / 64.0)) + 2.0 ** -24) * 2.0 ** (k % 5)
+        mid.append((m * 2.0 ** -k, 2.0 ** -k))
+    pairs = list(zip(w, s)) + [(a, b) for a in hard_w for b in hard_s] + mid
+    pairs += [(1.0, 2.0 ** 100), (-3.0, 2.0 ** 120), (2.0 ** -120, 3.0)]                  # subnormal results
+    ws = np.array([p[0] for p in pairs])
+    ss = np.array([p[1] for p in pairs])
+    got = Q._quotient(ws, ss)
+    for a, b, x in zip(ws, ss, got):
+        if b == 0:
+            continue
+        q = Fraction(float(a)) / Fraction(float(b))
+        x32 = np.float32(x)
+        assert float(x32) == x, (a, b, x)                                            # lies on the fp32 grid
+        err = abs(Fraction(float(x)) - q)
+        for nb in (np.nextafter(x32, np.float32(np.inf)), np.nextafter(x32, np.float32(-np.inf))):
+            if not np.isfinite(nb):
+                continue
+            e2 = abs(Fraction(float(nb)) - q)
+            assert err <= e2, (a, b, x)                                              # nearest
+            if err == e2:                                                            # a tie: even significand
+                assert int(x32.view(np.uint32)) % 2 == 0, (a, b, x)
+        if q == 0:
+            assert np.signbit(x) == np.signbit(a)
