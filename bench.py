@@ -368,7 +368,8 @@ def run_ours(args):
     cfg = synth.workload(args.workload, **over)
     inp = synth.make_inputs(cfg, seed=rank, device=dev)
     T, d, F, E, k, fmt = inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"]
-    flags = (Q.QAD_FLAG_RECOMPUTE if args.recompute else 0) | (Q.QAD_FLAG_NATIVE_FP8 if args.native_fp8 else 0)
+    flags = ((Q.QAD_FLAG_RECOMPUTE if args.recompute else 0) | (Q.QAD_FLAG_NATIVE_FP8 if args.native_fp8 else 0) |
+             (Q.QAD_FLAG_SMEM_DEQUANT if args.smem_dequant else 0))
     stream = torch.cuda.current_stream(dev)
     average = dp.average_scale_grads if world > 1 else None
 
@@ -411,6 +412,8 @@ def run_ours(args):
                    "tokens_per_gpu": T, "global_batch": T * world, "parallelism": "dp%d" % world,
                    "activations": "recompute" if args.recompute else "stash",
                    "forward_gemms": "e4m3 codes, scales on the sums" if args.native_fp8 else "bf16 fake-quant",
+                   "weight_fake_quant": ("in the GEMMs' shared memory" if args.smem_dequant
+                                         else "one pass into a bf16 copy"),
                    "workspace_gb": layer.ws.numel() / 1e9,
                    "l2": "inputs larger than L2 (weights %.2f GB streamed per pass), no flush" %
                          (2 * 3 * E * F * d / 1e9)},
@@ -430,6 +433,21 @@ def run_ours(args):
     }
     del layer
     torch.cuda.empty_cache()
+    if not args.no_ab and not args.native_fp8:
+        # the other way of fake-quantizing the weights, same workload, same box
+        ab_flags = flags ^ Q.QAD_FLAG_SMEM_DEQUANT
+        lab = Layer(Q, inp, ab_flags, dev)
+        ms_ab, prof_ab, _, clk_ab = timed_steps(Q, lab, stream, dev, args.steps, args.warmup, barrier, local, average)
+        ms_ab = dp.max_over_ranks(ms_ab, device=dev)
+        k_ab = kernel_table(prof_ab, args.steps, alg, peak, tf_burst, tf_sust, hbm)
+        line["ab_weight_fake_quant"] = {
+            "mode": "in the GEMMs' shared memory" if ab_flags & Q.QAD_FLAG_SMEM_DEQUANT else "one pass into a bf16 copy",
+            "value": T * world / (ms_ab / 1e3), "unit": "tokens/s", "ms_per_step": ms_ab,
+            "workspace_gb": lab.ws.numel() / 1e9, "clocks": clk_ab.summary(),
+            "kernels": {nm: {kk: v[kk] for kk in ("ms_per_launch", "launches_per_step", "frac") if kk in v}
+                        for nm, v in k_ab.items()}}
+        del lab
+        torch.cuda.empty_cache()
     if world == 1 and not args.no_configs and not over:
         line["configs"] = other_configs(Q, args, dev, stream, barrier, local, tf_burst, tf_sust, hbm, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -561,6 +579,10 @@ def main():
                     help="override the workload's expert count (small cases for profiler captures)")
     ap.add_argument("--recompute", action="store_true",
                     help="QAD_FLAG_RECOMPUTE: recompute fc1's Z1 in the backward instead of stashing it")
+    ap.add_argument("--smem-dequant", action="store_true",
+                    help="QAD_FLAG_SMEM_DEQUANT: the GEMMs fake-quantize weight tiles in shared memory")
+    ap.add_argument("--no-ab", action="store_true",
+                    help="skip timing the other weight fake-quant mode (the `ab_weight_fake_quant` key)")
     ap.add_argument("--native-fp8", action="store_true",
                     help="QAD_FLAG_NATIVE_FP8 (fp8 workloads): forward GEMMs on the E4M3 tensor path")
     args = ap.parse_args()

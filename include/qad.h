@@ -98,7 +98,7 @@ enum {
                             longer needed once the dgrad call has used it for dprobs), so
                             qad_moe_workspace_bytes is smaller by about 4·Rmax·F bytes.  The
                             fwd, dgrad and scalegrad calls of one step must use the same flags. */
-  QAD_FLAG_NATIVE_FP8 = 8 /* fp8 format (QAD_FMT_FP8_ROW) only: the forward GEMMs contract the
+  QAD_FLAG_NATIVE_FP8 = 8, /* fp8 format (QAD_FMT_FP8_ROW) only: the forward GEMMs contract the
                             E4M3 codes on the fp8 tensor path (tcgen05 kind::f8f6f4) and apply
                             the per-row weight and activation scales to the fp32 sums -- the
                             scales leave the contraction exactly ("MCoreQAD Backend", Support
@@ -106,6 +106,21 @@ enum {
                             bf16 before the products.  Also writes the codes and row scales to
                             the workspace; the backward is unchanged (bf16 fake-quant copies).
                             Any other format, or QAD_FLAG_NO_QUANT, gives QAD_ERR_INVALID_ARG. */
+  QAD_FLAG_SMEM_DEQUANT = 16, /* the fake-quantized weights are never materialised (AngelSlim
+                            mcore_qad walkthrough, section 二.4: the stacked experts are
+                            fake-quantized and consumed by one grouped GEMM): instead of one
+                            fake-quant pass writing W13_hat and W2_hat to the workspace, the four
+                            GEMMs that read them (fc1, fc2 and the two input-gradient GEMMs) load
+                            tiles of the raw bf16 weights and fake-quantize each tile in shared
+                            memory before the tensor cores read it, with the same arithmetic and
+                            hence the same bits.  The workspace loses the two weight copies
+                            (E * 3 * F * d * 2 bytes).  Not with QAD_FLAG_NO_QUANT or
+                            QAD_FLAG_NATIVE_FP8 (QAD_ERR_INVALID_ARG).  All three calls of a step
+                            must pass it. */
+  QAD_FLAG_DEQUANT_DUMP = 32 /* testing aid for QAD_FLAG_SMEM_DEQUANT (required with it): the
+                            workspace keeps the W13_hat / W2_hat regions and every GEMM that
+                            dequantizes a weight tile in shared memory also writes the values it
+                            converted there, so they can be compared with qad_fakequant_fwd. */
 };
 
 /* Shape of one MoE layer. T tokens, hidden d, expert FFN width F, E experts, top-k. */

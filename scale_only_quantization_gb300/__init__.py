@@ -19,6 +19,7 @@ QAD_NOALLOC_MAX_EXPERTS, QAD_NOALLOC_MAX_PAIRS = 256, 262144
 QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW, QAD_FMT_NVFP4A16, QAD_FMT_W8A8, QAD_FMT_W4AFP8 = range(6)
 QAD_DEV_BAD_INDEX, QAD_DEV_DUP_INDEX, QAD_DEV_TIMEOUT = 1, 2, 4
 QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT, QAD_FLAG_RECOMPUTE, QAD_FLAG_NATIVE_FP8 = 1, 2, 4, 8
+QAD_FLAG_SMEM_DEQUANT, QAD_FLAG_DEQUANT_DUMP = 16, 32
 VIEWS = ["HEADER", "OFFSETS", "COUNTS", "ROW_TOKEN", "ROW_SLOT", "ROW_OF", "W13_HAT", "W2_HAT", "A1", "Z1", "H",
          "H_HAT", "Y", "DY", "DZ1", "DA1", "XQ", "W13_CODES", "W2_CODES", "A1_CODES", "H_CODES", "A_SCALE",
          "H_SCALE"]

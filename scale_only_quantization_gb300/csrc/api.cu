@@ -91,11 +91,14 @@ void prof_end(int id, cudaStream_t st) {
 int layout_of(const qad_moe_shape& s, Layout* L) {
   if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
   if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_W4AFP8) return QAD_ERR_INVALID_ARG;
-  if (s.reserved != 0 ||
-      (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT | QAD_FLAG_RECOMPUTE | QAD_FLAG_NATIVE_FP8)))
+  if (s.reserved != 0 || (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT | QAD_FLAG_RECOMPUTE |
+                                       QAD_FLAG_NATIVE_FP8 | QAD_FLAG_SMEM_DEQUANT | QAD_FLAG_DEQUANT_DUMP)))
     return QAD_ERR_INVALID_ARG;
   if ((s.flags & QAD_FLAG_NATIVE_FP8) && (s.fmt != QAD_FMT_FP8_ROW || (s.flags & QAD_FLAG_NO_QUANT)))
     return QAD_ERR_INVALID_ARG;
+  const bool dq = (s.flags & QAD_FLAG_SMEM_DEQUANT) != 0;
+  if (dq && (s.flags & (QAD_FLAG_NO_QUANT | QAD_FLAG_NATIVE_FP8))) return QAD_ERR_INVALID_ARG;
+  if ((s.flags & QAD_FLAG_DEQUANT_DUMP) && !dq) return QAD_ERR_INVALID_ARG;
   if (s.d % 256 || s.F % 128) return QAD_ERR_UNSUPPORTED;
   if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
   const int64_t R = s.T * (int64_t)s.topk;
@@ -120,8 +123,11 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->row_slot = take(4 * (size_t)Rmax);
   L->row_of = take(4 * (size_t)R);
   L->xq = take(2 * (size_t)(s.T * d));
-  L->w13h = take(2 * (size_t)(E * 2 * F * d));
-  L->w2h = take(2 * (size_t)(E * d * F));
+  // the fake-quantized weight copies (not with QAD_FLAG_SMEM_DEQUANT, unless dumped)
+  const bool copies = !dq || (s.flags & QAD_FLAG_DEQUANT_DUMP);
+  L->w13h = take(copies ? 2 * (size_t)(E * 2 * F * d) : 0);
+  L->w2h = take(copies ? 2 * (size_t)(E * d * F) : 0);
+  L->w_copies = copies;
   L->a1 = take(2 * (size_t)(Rmax * d));
   // with QAD_FLAG_RECOMPUTE (and d >= 2F) Z1 lives in Y's region: it only exists between the
   // dgrad call's recompute and its SwiGLU backward, after Y has been read for dprobs
@@ -181,6 +187,8 @@ bool ok_ptr(const void* p) { return p && aligned16(p); }
 GemmCtx gemm_ctx(const Layout& L, uint8_t* wsb, const qad_moe_shape& s, const void* w13, const void* w2,
                  cudaStream_t st) {
   const bool no_quant = (s.flags & QAD_FLAG_NO_QUANT) != 0;
+  const bool dq = (s.flags & QAD_FLAG_SMEM_DEQUANT) != 0;
+  const bool dump = (s.flags & QAD_FLAG_DEQUANT_DUMP) != 0;
   GemmCtx c;
   c.L = &L;
   c.ws = wsb;
@@ -188,10 +196,13 @@ GemmCtx gemm_ctx(const Layout& L, uint8_t* wsb, const qad_moe_shape& s, const vo
   c.aq = no_quant ? kQNone : act_kind(s.fmt);
   c.flags = s.flags;
   c.st = st;
-  c.w13h = no_quant ? w13 : static_cast<const void*>(wsb + L.w13h);
-  c.w2h = no_quant ? w2 : static_cast<const void*>(wsb + L.w2h);
+  c.w13h = (no_quant || dq) ? w13 : static_cast<const void*>(wsb + L.w13h);
+  c.w2h = (no_quant || dq) ? w2 : static_cast<const void*>(wsb + L.w2h);
   c.s13 = nullptr;
   c.s2 = nullptr;
+  c.dq = dq;
+  c.dump13 = dump ? static_cast<void*>(wsb + L.w13h) : nullptr;
+  c.dump2 = dump ? static_cast<void*>(wsb + L.w2h) : nullptr;
   return c;
 }
 
@@ -290,7 +301,7 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
                                   row_token, L.T, (int)L.k, L.d, rpad, ss->s, f8 ? wsb + L.a1q : nullptr,
                                   f8 ? reinterpret_cast<float*>(wsb + L.sa_tok) : nullptr));
     QAD_TRY(cudaEventRecord(ss->join, ss->s));
-    if (!no_quant) {
+    if (!no_quant && !c.dq) {  // with QAD_FLAG_SMEM_DEQUANT the GEMMs fake-quantize the weights themselves
       QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
       QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st, f8 ? wsb + L.w2q : nullptr));
     }
@@ -374,8 +385,8 @@ int qad_moe_debug_view(const qad_moe_shape* s, int which, size_t* byte_offset, i
     case QAD_VIEW_ROW_TOKEN: off = L.row_token; n = Rm; break;
     case QAD_VIEW_ROW_SLOT: off = L.row_slot; n = Rm; break;
     case QAD_VIEW_ROW_OF: off = L.row_of; n = L.R; break;
-    case QAD_VIEW_W13_HAT: off = L.w13h; n = E * 2 * F * d; break;
-    case QAD_VIEW_W2_HAT: off = L.w2h; n = E * d * F; break;
+    case QAD_VIEW_W13_HAT: off = L.w13h; n = L.w_copies ? E * 2 * F * d : 0; break;
+    case QAD_VIEW_W2_HAT: off = L.w2h; n = L.w_copies ? E * d * F : 0; break;
     case QAD_VIEW_A1: off = L.a1; n = Rm * d; break;
     case QAD_VIEW_Z1: off = L.z1; n = Rm * 2 * F; break;
     case QAD_VIEW_H: off = L.h; n = Rm * F; break;

@@ -275,6 +275,77 @@ __device__ __forceinline__ void fakequant_inplace(float* v, float s) {
   }
 }
 
+// Weight fake-quant of 16 weights packed as bf16 pairs (w[i]: element 2i in the low half,
+// 2i + 1 in the high half) sharing scale s, returning packed bf16 results: the same bits as
+// unpack8 -> fakequant_inplace<QK, 16> -> pack8, with fewer conversion instructions (they
+// issue at a fraction of the fp32 rate).  For a scale in [2^-60, 2^16) and finite quotients:
+//  - x = fp32(w / s) from the reciprocal and one FMA correction, as quotients_unguarded;
+//  - E2M1 / E4M3: the saturating conversion to the 4- / 8-bit code and back to f16 (two
+//    instructions per pair); an f16 magnitude shifted left by 13 bits is the fp32 bit pattern
+//    of |q| * 2^-112 (every grid value is a normal f16 or zero), and s * 2^112 is exact, so
+//    their fp32 product is RN(|q| s), the same rounding of the same real number;
+//  - INT4 / INT8: clamp to the clip range, then round to the nearest integer (ties to even) by
+//    adding and subtracting 1.5 * 2^23 (exact for |x| <= 2^22), equal to clamping rint(x);
+//  - one bf16x2 conversion of the products; the sign is w's (a zero result keeps w's sign,
+//    as fakequant_inplace's copysign does).
+// Other scales, or a non-finite quotient, take fakequant_inplace itself.
+template <int QK>
+__device__ __forceinline__ void fakequant16_packed(const uint32_t (&w)[8], float s, uint32_t (&out)[8]) {
+  if (s >= 0x1p-60f && s < 0x1p16f) {
+    const float r = __frcp_rn(s);
+    const uint64_t r2 = f2pack(r, r), ns2 = f2pack(-s, -s), zero2 = f2pack(0.0f, 0.0f);
+    const float sc = (QK == kQE2M1 || QK == kQE4M3) ? s * 0x1p112f : s;
+    const uint64_t sc2 = f2pack(sc, sc);
+    uint64_t probe = zero2;
+    uint32_t res[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t w2 = f2pack(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+      const uint64_t q2 = f2mul(w2, r2);
+      const uint64_t e2 = f2fma(q2, ns2, w2);
+      const uint64_t x2 = f2fma(e2, r2, q2);
+      probe = f2fma(x2, zero2, probe);  // stays 0 unless a quotient is inf or NaN
+      const float2 x = f2unpack(x2);
+      uint64_t m2;
+      if constexpr (QK == kQE2M1 || QK == kQE4M3) {
+        uint32_t h2;
+        if constexpr (QK == kQE2M1) {
+          asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+              : "=r"(h2) : "f"(x.x), "f"(x.y));
+        } else {
+          uint16_t c;
+          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(c) : "f"(x.x), "f"(x.y));
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+        }
+        const uint32_t la = (h2 << 13) & 0x0FFFE000u, lb = (h2 >> 3) & 0x0FFFE000u;
+        m2 = f2mul(f2pack(__uint_as_float(la), __uint_as_float(lb)), sc2);
+      } else {
+        const uint64_t big2 = f2pack(12582912.0f, 12582912.0f);  // 1.5 * 2^23
+        const float ta = fminf(fmaxf(x.x, Clip<QK>::lo), Clip<QK>::hi);
+        const float tb = fminf(fmaxf(x.y, Clip<QK>::lo), Clip<QK>::hi);
+        const uint64_t q = f2sub(f2add(f2pack(ta, tb), big2), big2);
+        m2 = f2mul(q, sc2);
+      }
+      const float2 m = f2unpack(m2);
+      res[i] = pack_bf16(m.x, m.y) | (w[i] & 0x80008000u);
+    }
+    if (f2unpack(probe).x == 0.0f && f2unpack(probe).y == 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = res[i];
+      return;
+    }
+  }
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16lo(w[i]);
+    v[2 * i + 1] = bf16hi(w[i]);
+  }
+  fakequant_inplace<QK, 16>(v, s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+}
+
 // E4M3 codes of a pair (a in the low byte, b in the high byte) and their grid values, signed
 // as q_pair<kQE4M3> signs them.
 __device__ __forceinline__ uint16_t e4m3_codes2(float a, float b, float2* q) {

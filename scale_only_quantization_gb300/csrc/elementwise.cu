@@ -32,13 +32,23 @@ int grid_for(int64_t items, int threads, int per_sm) {
 // whole number of 16-element chunks).  `cps` = chunks per scale (1, 8 or K / 16).  CODES
 // (E4M3 only): also write each element's E4M3 code byte to `codes` (same layout as w).
 template <int QK, bool CODES = false>
-__device__ __forceinline__ void fakequant_chunk(float* v, float sc, uint4* codes, uint64_t c) {
+__device__ __forceinline__ void fakequant_chunk(const uint4& u0, const uint4& u1, float sc, uint4* out, uint4* codes,
+                                                uint64_t c) {
   if constexpr (CODES) {
+    float v[16];
+    unpack8(u0, v);
+    unpack8(u1, v + 8);
     uint32_t cw[4];
     fakequant_e4m3_codes<16, false>(v, sc, cw);
     st_stream(codes + c, make_uint4(cw[0], cw[1], cw[2], cw[3]));
+    st_stream(out + 2 * c, pack8(v));
+    st_stream(out + 2 * c + 1, pack8(v + 8));
   } else {
-    fakequant_inplace<QK, 16>(v, sc);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint32_t o[8];
+    fakequant16_packed<QK>(w, sc, o);
+    st_stream(out + 2 * c, make_uint4(o[0], o[1], o[2], o[3]));
+    st_stream(out + 2 * c + 1, make_uint4(o[4], o[5], o[6], o[7]));
   }
 }
 
@@ -54,28 +64,14 @@ __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict_
     const uint4 u2 = ld_stream(w + 2 * c2), u3 = ld_stream(w + 2 * c2 + 1);
     const float sc = __ldg(s + (cps == 1 ? c : c / cps));
     const float sc2 = __ldg(s + (cps == 1 ? c2 : c2 / cps));
-    float v[16];
-    unpack8(u0, v);
-    unpack8(u1, v + 8);
-    fakequant_chunk<QK, CODES>(v, sc, codes, c);
-    st_stream(out + 2 * c, pack8(v));
-    st_stream(out + 2 * c + 1, pack8(v + 8));
-    unpack8(u2, v);
-    unpack8(u3, v + 8);
-    fakequant_chunk<QK, CODES>(v, sc2, codes, c2);
-    st_stream(out + 2 * c2, pack8(v));
-    st_stream(out + 2 * c2 + 1, pack8(v + 8));
+    fakequant_chunk<QK, CODES>(u0, u1, sc, out, codes, c);
+    fakequant_chunk<QK, CODES>(u2, u3, sc2, out, codes, c2);
   }
   for (; c < nchunks; c += stride) {
     const uint4 u0 = ld_stream(w + 2 * c);
     const uint4 u1 = ld_stream(w + 2 * c + 1);
     const float sc = __ldg(s + (cps == 1 ? c : c / cps));
-    float v[16];
-    unpack8(u0, v);
-    unpack8(u1, v + 8);
-    fakequant_chunk<QK, CODES>(v, sc, codes, c);
-    st_stream(out + 2 * c, pack8(v));
-    st_stream(out + 2 * c + 1, pack8(v + 8));
+    fakequant_chunk<QK, CODES>(u0, u1, sc, out, codes, c);
   }
 }
 

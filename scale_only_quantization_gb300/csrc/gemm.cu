@@ -55,6 +55,11 @@ __host__ __device__ constexpr int bke_of(bool f8, int atoms) { return atoms * (f
 constexpr int kAtomsFc1 = 2, kAtomsFc2 = 1, kAtomsDgrad = 1, kAtomsWgrad = 2;
 constexpr int kThreads = 320;       // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-9 epilogue
 constexpr int kEpiThreads = 256;
+// With the weight operand dequantized in shared memory (DQ), warps 10-13 are converters: they
+// fake-quantize each B stage in place after its TMA load and before the MMAs read it.
+constexpr int kConvWarps = 4;
+constexpr int kConvThreads = 32 * kConvWarps;
+__host__ __device__ constexpr int threads_of(bool dq) { return kThreads + (dq ? kConvThreads : 0); }
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 enum { EPI_FC1 = 0, EPI_STORE = 1, EPI_SWIGLU_BWD = 2, EPI_SCALEGRAD = 3 };
@@ -86,6 +91,13 @@ struct Params {
   int64_t w_rows, w_cols;
   int w_vec32;  // w is 32-byte aligned: its sectors are read with 256-bit loads
   float* ds; float* part; int accumulate;
+  // DQ: the B operand is the raw bf16 weight [E, dq_rows, dq_cols] with scales dq_s; the
+  // converters apply bf16(fp32(q(fp32(w / s)) * s)) (grid p.wq) to each B stage in shared
+  // memory.  dq_dump (debug, may be null): the converted values are also written there, laid
+  // out like the weight.
+  const float* dq_s;
+  int64_t dq_rows, dq_cols;
+  __nv_bfloat16* dq_dump;
 };
 
 template <int BN, int ATOMS> struct Cfg {
@@ -96,7 +108,7 @@ template <int BN, int ATOMS> struct Cfg {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE;  // BN = 256: 6 (one atom) or 3; BN = 128: 8 or 4
   static constexpr int RING = STAGES * STAGE;
-  static constexpr int SMEM = RING + 256 + 1024;  // + barriers, + alignment slack
+  static constexpr int SMEM = RING + 512 + 1024;  // + barriers, + alignment slack
   static constexpr int TMEM_COLS = 2 * BN;
 };
 
@@ -130,6 +142,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
+// The same test with acquire semantics at cluster scope: the phase was completed by release
+// arrivals from threads of both CTAs of the pair whose shared-memory writes must be visible.
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, "
+      "1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
 
 // Bounded wait for the phase with parity `parity` of barrier `bar`: gives up after `budget`
 // clock cycles (or as soon as another role of the CTA gave up), raising QAD_DEV_TIMEOUT.
@@ -159,6 +181,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return mbar_wait_slow(bar, parity, abort_flag, err, budget);
 }
 
+// Bounded wait with cluster-scope acquire (see mbar_try_cluster); the slow path ends with one
+// more acquiring test, so a phase it saw complete is also acquired.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i)
+    if (mbar_try_cluster(bar, parity)) return true;
+  if (!mbar_wait_slow(bar, parity, abort_flag, err, kWaitCycles)) return false;
+  return mbar_try_cluster(bar, parity);
+}
+
 // Self-check of the timeout path: one thread waits, with the GEMMs' own bounded-wait routine,
 // on a barrier that nothing ever arrives on.  It must give up after `budget` cycles and
 // raise QAD_DEV_TIMEOUT in *err; nothing faults or hangs.
@@ -180,6 +212,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
       "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// TMA tile load into this CTA's shared memory completing on one of its own barriers
+__device__ __forceinline__ void tma_load_2d_local(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
@@ -214,6 +254,12 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
 // wait for the epilogue's global stores to become visible, which release semantics would.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Arrive with release semantics at cluster scope: the arriving warp's shared-memory writes
+// (already ordered before the tensor cores' reads by fence.proxy.async) become visible to
+// the thread that acquires the phase.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
@@ -470,23 +516,23 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
   }
 }
 
-// bf16 store of this warp's 32 rows x BN/2 columns: all its TMEM loads are issued at once,
-// then one wait; each 32-column chunk is written into one of the warp's two staging boxes
+// bf16 store of this warp's 32 rows x BN/2 columns: its TMEM loads are issued in batches of
+// BATCH 32-column chunks (all at once unless the register budget is tight), one wait per batch;
+// each 32-column chunk is written into one of the warp's two staging boxes
 // (thread = row, 16-byte chunk c of the 64-byte row at position c ^ ((row >> 1) & 3), the
 // 64-byte swizzle, which also keeps the shared-memory writes free of bank conflicts) and
 // one lane stores the box with TMA.  A box is rewritten only after the TMA store issued
 // from it two chunks earlier has read it.
-template <int BN, bool F8>
-__device__ __forceinline__ void epi_store(const Params& p, const CUtensorMap* tmC, const Tile& ti, uint32_t tbase,
-                                          int q, int lane, int half, uint32_t stage_base, uint32_t& buf) {
-  constexpr int NH = BN / 64;  // 32-column chunks per half: 4 or 2
-  const int c0 = half * NH;
+template <int BN, bool F8, int BATCH>
+__device__ __forceinline__ void epi_store_batch(const Params& p, const CUtensorMap* tmC, const Tile& ti,
+                                                uint32_t tbase, int q, int lane, int c0, int y,
+                                                uint32_t stage_base, uint32_t& buf) {
+  constexpr int NH = BATCH;
   uint32_t r[NH][32];
 #pragma unroll
   for (int c = 0; c < NH; ++c) tmem_ld32_issue(tbase + 32 * (c0 + c), r[c]);
 #pragma unroll
   for (int c = 0; c < NH; ++c) tmem_wait32(r[c]);
-  const int y = (int)ti.row_base + 32 * q;
   const uint32_t row_addr = (uint32_t)lane * 64u;
   const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
   float rs = 1.0f;
@@ -528,6 +574,19 @@ __device__ __forceinline__ void epi_store(const Params& p, const CUtensorMap* tm
     buf ^= 1u;
   }
 }
+
+template <int BN, bool F8, int BATCH = BN / 64>
+__device__ __forceinline__ void epi_store(const Params& p, const CUtensorMap* tmC, const Tile& ti, uint32_t tbase,
+                                          int q, int lane, int half, uint32_t stage_base, uint32_t& buf) {
+  constexpr int NH = BN / 64;  // 32-column chunks per half: 4 or 2
+  static_assert(NH % BATCH == 0, "batches of whole chunks");
+  const int c0 = half * NH;
+  const int y = (int)ti.row_base + 32 * q;
+#pragma unroll
+  for (int b0 = 0; b0 < NH; b0 += BATCH)
+    epi_store_batch<BN, F8, BATCH>(p, tmC, ti, tbase, q, lane, c0 + b0, y, stage_base, buf);
+}
+
 
 // This thread's Z1 row and first column in a tile of the SwiGLU-backward epilogue.
 struct Z1Cursor {
@@ -768,16 +827,106 @@ __device__ __forceinline__ void run_scalegrad(const Params& p, const Tile& ti, u
   }
 }
 
+// ---------------------------------------------------------------------------------- B-operand dequant
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Elements sharing one weight scale along a weight row: 16 (E2M1), 128 (INT4), the whole row.
+__device__ __forceinline__ int64_t dq_block(int wq, int64_t cols) {
+  return wq == kQE2M1 ? 16 : wq == kQInt4 ? 128 : cols;
+}
+
+// Fake-quantizes, in place, the 16 consecutive weights of one row that sit in the 16-byte chunks
+// at shared addresses a0 and a1, with the routine of the standalone fake-quant pass
+// (fakequant16_packed), so the MMA reads exactly the values qad_fakequant_fwd writes.
+template <int QK>
+__device__ __forceinline__ void dq_convert16(uint32_t a0, uint32_t a1, float s, __nv_bfloat16* dump) {
+  const uint4 l0 = ld_shared_v4(a0), h0 = ld_shared_v4(a1);
+  const uint32_t w[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
+  uint32_t o[8];
+  fakequant16_packed<QK>(w, s, o);
+  const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
+  st_shared_v4(a0, lo);
+  st_shared_v4(a1, hi);
+  if (dump) {
+    reinterpret_cast<uint4*>(dump)[0] = lo;
+    reinterpret_cast<uint4*>(dump)[1] = hi;
+  }
+}
+
+// One B stage of this CTA, converted by the 128 converter threads.  The stage holds NB boxes of
+// R rows x 64 bf16 (128-byte rows, 128-byte swizzle: 16-byte chunk c of row r sits at chunk
+// position c ^ (r & 7)).  K-major B (forward GEMMs): box = 128-byte K atom, row = weight row
+// b_row0 + r, columns k0 + 64 box + [0, 64).  MN-major B (input-gradient GEMMs): box = 64
+// weight columns n0 + 64 box + [0, 64), row = weight row k0 + r.  A unit is 16 elements (chunks
+// 2m and 2m + 1 of a row, one E2M1 scale block); consecutive threads take consecutive rows of
+// the same m, so every quarter-warp's 16-byte accesses fall in distinct bank groups.
+template <int NB, int R, bool B_MN>
+struct DqStage {
+  static constexpr int UNITS = NB * R * 4;
+  static constexpr int PER = UNITS / kConvThreads;
+  static_assert(PER * kConvThreads == UNITS, "units per stage must split evenly over the converters");
+  struct Unit {
+    int box, r, m;
+    int64_t wrow, wcol;
+  };
+  __device__ __forceinline__ static Unit unit(int tid, int i, int64_t b_row0, int64_t k0, int64_t n0) {
+    Unit x;
+    const int u = tid + i * kConvThreads;
+    x.m = u / (NB * R);
+    const int rid = u - x.m * (NB * R);
+    x.box = rid / R;
+    x.r = rid - x.box * R;
+    if constexpr (B_MN) {
+      x.wrow = k0 + x.r;
+      x.wcol = n0 + 64 * x.box + 16 * x.m;
+    } else {
+      x.wrow = b_row0 + x.r;
+      x.wcol = k0 + 64 * x.box + 16 * x.m;
+    }
+    return x;
+  }
+  // the scales of this thread's units (issued early: their latency hides behind the previous stage)
+  __device__ __forceinline__ static void scales(const Params& p, int tid, int e, int64_t b_row0, int64_t k0,
+                                                int64_t n0, float (&sc)[PER]) {
+    const int64_t blk = dq_block(p.wq, p.dq_cols);
+    const int64_t s_pitch = p.dq_cols / blk;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const Unit x = unit(tid, i, b_row0, k0, n0);
+      sc[i] = __ldg(p.dq_s + ((int64_t)e * p.dq_rows + x.wrow) * s_pitch + x.wcol / blk);
+    }
+  }
+  template <int QK, int BOX_BYTES>
+  __device__ __forceinline__ static void convert(const Params& p, uint32_t sb, int tid, int e, int64_t b_row0,
+                                                 int64_t k0, int64_t n0, const float (&sc)[PER]) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const Unit x = unit(tid, i, b_row0, k0, n0);
+      const uint32_t row_addr = sb + (uint32_t)(x.box * BOX_BYTES + x.r * 128);
+      dq_convert16<QK>(row_addr + ((uint32_t)((2 * x.m) ^ (x.r & 7)) << 4),
+                       row_addr + ((uint32_t)((2 * x.m + 1) ^ (x.r & 7)) << 4), sc[i],
+                       p.dq_dump ? p.dq_dump + ((int64_t)e * p.dq_rows + x.wrow) * p.dq_cols + x.wcol : nullptr);
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------------- kernel
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool F8, int ATOMS>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8, int ATOMS, bool DQ>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(DQ), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const Params p) {
   using C = Cfg<BN, ATOMS>;
   constexpr int STAGES = C::STAGES;
   static_assert(!F8 || (!A_MN && !B_MN), "E4M3 operands are K-major (forward GEMMs)");
+  static_assert(!DQ || (!F8 && !A_MN), "the dequantized weight is the bf16 B operand of a row-mode GEMM");
   constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN, F8>();
   constexpr int BKE = bke_of(F8, ATOMS);  // K elements per stage
   constexpr int AKE = F8 ? 128 : BK;  // K elements per 128-byte atom row
@@ -795,6 +944,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // DQ: this CTA's raw B bytes of a stage have landed (local) / both CTAs' B halves of the stage
+  // are converted (the leader's, one arrival per converter warp of either CTA)
+  auto bfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 6 + s); };
+  auto bconv_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 6 + s); };
   int32_t* err = p.hdr + HDR_ERR;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -810,6 +963,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), 2 * (kEpiThreads / 32));  // one arrival per epilogue warp of either CTA
     }
     mbar_init(drain_bar, 1);
+    if constexpr (DQ) {
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(bfull_bar(s), 1);
+        mbar_init(bconv_bar(s), 2 * kConvWarps);
+      }
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -838,9 +997,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     const int half_n = (int)rank * (BN / 2);
     // TMA loads of this CTA's A tile and half of the B tile for k-block kb of tile ti into
-    // shared memory, completing on `fb`
-    auto operand_tiles = [&](const Tile& ti, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
-      auto box = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) { tma_load_2d(dst, tm, x, y, fb); };
+    // shared memory, completing on `fb` (DQ: the B half on this CTA's own barrier `bb`)
+    auto operand_tiles = [&](const Tile& ti, int kb, uint32_t sa, uint32_t sb, uint32_t fb, uint32_t bb) {
+      auto box = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
+        if (DQ && tm == &tmB) tma_load_2d_local(dst, tm, x, y, bb);
+        else tma_load_2d(dst, tm, x, y, fb);
+      };
       // K-major operands: one box {64 bf16 | 128 E4M3, rows} per 128-byte K atom; MN-major
       // operands: one box {64, BKE K rows} per 64 columns of M or N
       if (!p.wgrad) {
@@ -876,9 +1038,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (leader) mbar_expect_tx(full_bar(stage), 2 * C::STAGE);  // both CTAs' bytes
+        if constexpr (DQ) {
+          if (leader) mbar_expect_tx(full_bar(stage), 2 * C::A_BYTES);  // both CTAs' A bytes
+          mbar_expect_tx(bfull_bar(stage), C::B_BYTES);                 // this CTA's raw B bytes
+        } else {
+          if (leader) mbar_expect_tx(full_bar(stage), 2 * C::STAGE);  // both CTAs' bytes
+        }
         const uint32_t fb = peer_addr(full_bar(stage), 0);          // the leader's barrier
-        operand_tiles(ti, kb, a_ring + stage * C::A_BYTES, b_ring + stage * C::B_BYTES, fb);
+        operand_tiles(ti, kb, a_ring + stage * C::A_BYTES, b_ring + stage * C::B_BYTES, fb, bfull_bar(stage));
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -887,13 +1054,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (*abort_flag && leader) {
-      // let every load of the pair land before the CTA releases its shared memory
+    if (*abort_flag) {
+      // let every load of the pair land before the CTA releases its shared memory (the B halves
+      // of DQ stages land on each CTA's own barrier)
       int32_t dummy = 0;
       for (int s = 0; s < STAGES; ++s)
         if (armed & (1u << s)) {
           volatile int zero = 0;
-          mbar_wait(full_bar(s), (armed_parity >> s) & 1u, &zero, &dummy);
+          if (leader) mbar_wait(full_bar(s), (armed_parity >> s) & 1u, &zero, &dummy);
+          if (DQ) mbar_wait(bfull_bar(s), (armed_parity >> s) & 1u, &zero, &dummy);
         }
     }
   } else if (warp == 1 && lane == 0 && leader) {
@@ -909,6 +1078,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        if (DQ && !mbar_wait_cluster(bconv_bar(stage), phase, abort_flag, err)) {
           ok = false;
           break;
         }
@@ -939,7 +1112,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile int zero = 0;
     int32_t dummy = 0;
     mbar_wait(drain_bar, 0, &zero, &dummy);
-  } else if (warp >= 2) {
+  } else if (DQ && warp >= 2 + kEpiThreads / 32) {
+    // ------------------------------------------------------------------ B converters (DQ, both CTAs)
+    // Each stage's raw weight half is fake-quantized in place once this CTA's TMA bytes have
+    // landed; then every converter warp of both CTAs arrives on the leader's bconv barrier,
+    // which the MMA issuer waits on besides the A bytes.  The scales of the next stage are
+    // loaded while the current one is converted.
+    constexpr int NB = B_MN ? BN / 128 : ATOMS;
+    constexpr int R = B_MN ? BKE : BN / 2;
+    constexpr int BOX_BYTES = B_MN ? BKE * 128 : C::B_ATOM;
+    using S = DqStage<NB, R, B_MN>;
+    const int tid = threadIdx.x - kThreads;
+    const int half_n = (int)rank * (BN / 2);
+    auto b_row0 = [&](const Tile& ti) -> int64_t {
+      return EPI == EPI_FC1 ? (int64_t)rank * p.F + (int64_t)ti.nb * 128 : (int64_t)ti.nb * BN + half_n;
+    };
+    auto n0_of = [&](const Tile& ti) -> int64_t { return (int64_t)ti.nb * BN + half_n; };
+    int stage = 0;
+    uint32_t phase = 0;
+    int t = first;
+    if (t < total) {
+      Tile ti = tile_of(p, t, rank, BKE);
+      int kb = 0;
+      float sc[S::PER];
+      S::scales(p, tid, ti.e, b_row0(ti), (int64_t)kb * BKE, n0_of(ti), sc);
+      while (true) {
+        int t2 = t, kb2 = kb + 1;
+        Tile ti2 = ti;
+        if (kb2 == ti.nkb) {
+          t2 = t + step;
+          kb2 = 0;
+          if (t2 < total) ti2 = tile_of(p, t2, rank, BKE);
+        }
+        const bool more = t2 < total;
+        float sc2[S::PER];
+        if (more) S::scales(p, tid, ti2.e, b_row0(ti2), (int64_t)kb2 * BKE, n0_of(ti2), sc2);
+        const bool got = mbar_wait(bfull_bar(stage), phase, abort_flag, err);
+        if (!__all_sync(0xffffffffu, got)) break;
+        const uint32_t sb = b_ring + stage * C::B_BYTES;
+        const int64_t k0 = (int64_t)kb * BKE, br = b_row0(ti), n0 = n0_of(ti);
+        if (p.wq == kQE2M1) S::template convert<kQE2M1, BOX_BYTES>(p, sb, tid, ti.e, br, k0, n0, sc);
+        else if (p.wq == kQInt4) S::template convert<kQInt4, BOX_BYTES>(p, sb, tid, ti.e, br, k0, n0, sc);
+        else if (p.wq == kQE4M3) S::template convert<kQE4M3, BOX_BYTES>(p, sb, tid, ti.e, br, k0, n0, sc);
+        else S::template convert<kQInt8, BOX_BYTES>(p, sb, tid, ti.e, br, k0, n0, sc);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive_release_cluster(peer_addr(bconv_bar(stage), 0));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (!more) break;
+        t = t2;
+        kb = kb2;
+        ti = ti2;
+#pragma unroll
+        for (int i = 0; i < S::PER; ++i) sc[i] = sc2[i];
+      }
+    }
+  } else if (warp >= 2 && warp < 2 + kEpiThreads / 32) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // which half of the tile's columns it handles
@@ -960,7 +1191,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       if (ti.live) {
-        if constexpr (EPI == EPI_STORE) epi_store<BN, F8>(p, &tmC, ti, tbase, q, lane, half, my_stage, buf);
+        if constexpr (EPI == EPI_STORE)  // DQ: the converters' warps leave 128 registers: half the chunks at a time
+          epi_store<BN, F8, (DQ ? BN / 128 : BN / 64)>(p, &tmC, ti, tbase, q, lane, half, my_stage, buf);
         else if constexpr (EPI == EPI_FC1) epi_fc1<BN, F8>(p, &tmC, &tmD, ti, tbase, q, lane, half, ring);
         else if constexpr (EPI == EPI_SWIGLU_BWD) {
           bool next_ok = false;
@@ -1055,10 +1287,11 @@ bool make_store_tmap(CUtensorMap* tm, void* base, int64_t inner, int64_t outer, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, int ATOMS, bool F8 = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, int ATOMS, bool F8 = false, bool DQ = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& td,
                    const Params& p, int64_t max_tiles, int kid, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, F8, ATOMS>;
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, F8, ATOMS, DQ>;
+  constexpr int kThreadsK = threads_of(DQ);
   constexpr int SMEM = smem_bytes<BN, EPI, ATOMS>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
@@ -1070,7 +1303,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     // SM pairs that can hold one CTA each at the same time (persistent grid)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kThreadsK, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
@@ -1082,7 +1315,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
   int64_t pairs = max_tiles < max_pairs[dev] ? max_tiles : max_pairs[dev];
   if (pairs < 1) return cudaSuccess;
   prof_begin(kid, st);
-  kern<<<(unsigned)(2 * pairs), kThreads, SMEM, st>>>(ta, tb, tc, td, p);
+  kern<<<(unsigned)(2 * pairs), kThreadsK, SMEM, st>>>(ta, tb, tc, td, p);
   prof_end(kid, st);
   return cudaGetLastError();
 }
@@ -1162,6 +1395,15 @@ Params base_params(const GemmCtx& c) {
 
 inline int pick_bn(int64_t n) { return n % 256 == 0 ? 256 : 128; }
 
+// The weight operand of this GEMM is dequantized in shared memory: raw weight [E, rows, cols]
+// with scales s (grid p.wq)
+void set_dq(Params& p, const float* s, int64_t rows, int64_t cols, void* dump) {
+  p.dq_s = s;
+  p.dq_rows = rows;
+  p.dq_cols = cols;
+  p.dq_dump = static_cast<__nv_bfloat16*>(dump);
+}
+
 }  // namespace
 
 cudaError_t launch_wait_selftest(int32_t* err, int64_t budget_cycles, cudaStream_t st) {
@@ -1204,6 +1446,10 @@ cudaError_t gemm_fc1(const GemmCtx& c, int mode) {
   if (!make_store_tmap(&th, c.ws + (row_scaled(c.aq) ? L.h : L.hh), L.F, L.Rmax, L.F, 16)) return cudaErrorInvalidValue;
   const int kid = mode == kFc1Z1Only ? QAD_K_GEMM_FC1_RECOMPUTE : QAD_K_GEMM_FC1;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
+  if (c.dq) {
+    set_dq(p, c.s13, 2 * L.F, L.d, c.dump13);
+    return launch<256, false, false, EPI_FC1, kAtomsFc1, false, true>(ta, tb, tz, th, p, tiles, kid, c.st);
+  }
   return f8 ? launch<256, false, false, EPI_FC1, 1, true>(ta, tb, tz, th, p, tiles, kid, c.st)
             : launch<256, false, false, EPI_FC1, kAtomsFc1>(ta, tb, tz, th, p, tiles, kid, c.st);
 }
@@ -1232,6 +1478,14 @@ cudaError_t gemm_fc2(const GemmCtx& c) {
   if (!make_store_tmap(&tc, c.ws + L.y, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
   if (f8) return launch<256, false, false, EPI_STORE, 1, true>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
+  if (c.dq) {
+    set_dq(p, c.s2, L.d, L.F, c.dump2);
+    return bn == 256
+               ? launch<256, false, false, EPI_STORE, kAtomsFc2, false, true>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2,
+                                                                             c.st)
+               : launch<128, false, false, EPI_STORE, kAtomsFc2, false, true>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2,
+                                                                             c.st);
+  }
   return bn == 256 ? launch<256, false, false, EPI_STORE, kAtomsFc2>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st)
                    : launch<128, false, false, EPI_STORE, kAtomsFc2>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_FC2, c.st);
 }
@@ -1252,6 +1506,13 @@ cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
   CUtensorMap tz;
   if (!make_store_tmap(&tz, c.ws + L.dz1, 2 * L.F, L.Rmax, 2 * L.F, 16)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
+  if (c.dq) {
+    set_dq(p, c.s2, L.d, L.F, c.dump2);
+    return bn == 256 ? launch<256, false, true, EPI_SWIGLU_BWD, kAtomsDgrad, false, true>(ta, tb, tz, tz, p, tiles,
+                                                                                         QAD_K_GEMM_DGRAD_FC2, c.st)
+                     : launch<128, false, true, EPI_SWIGLU_BWD, kAtomsDgrad, false, true>(ta, tb, tz, tz, p, tiles,
+                                                                                         QAD_K_GEMM_DGRAD_FC2, c.st);
+  }
   return bn == 256
              ? launch<256, false, true, EPI_SWIGLU_BWD, kAtomsDgrad>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st)
              : launch<128, false, true, EPI_SWIGLU_BWD, kAtomsDgrad>(ta, tb, tz, tz, p, tiles, QAD_K_GEMM_DGRAD_FC2, c.st);
@@ -1271,6 +1532,13 @@ cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
   CUtensorMap tc;
   if (!make_store_tmap(&tc, c.ws + L.da1, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
+  if (c.dq) {
+    set_dq(p, c.s13, 2 * L.F, L.d, c.dump13);
+    return bn == 256 ? launch<256, false, true, EPI_STORE, kAtomsDgrad, false, true>(ta, tb, tc, tc, p, tiles,
+                                                                                    QAD_K_GEMM_DGRAD_FC1, c.st)
+                     : launch<128, false, true, EPI_STORE, kAtomsDgrad, false, true>(ta, tb, tc, tc, p, tiles,
+                                                                                    QAD_K_GEMM_DGRAD_FC1, c.st);
+  }
   return bn == 256
              ? launch<256, false, true, EPI_STORE, kAtomsDgrad>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st)
              : launch<128, false, true, EPI_STORE, kAtomsDgrad>(ta, tb, tc, tc, p, tiles, QAD_K_GEMM_DGRAD_FC1, c.st);

@@ -21,6 +21,7 @@ struct Layout {
   // QAD_FLAG_NATIVE_FP8: E4M3 codes of W13, W2, A1 and H, per-token activation scales and
   // per-row H scales (all 0 otherwise)
   bool native_fp8;
+  bool w_copies;  // the W13_hat / W2_hat regions exist (not with QAD_FLAG_SMEM_DEQUANT unless dumped)
   size_t w13q, w2q, a1q, hq, sa_tok, sh_row;
   size_t total;
 };
@@ -86,8 +87,14 @@ struct GemmCtx {
   cudaStream_t st;
   const void* w13h;  // the weights the GEMMs read: the fake-quantized copies in the workspace,
   const void* w2h;   // or the caller's raw weights for the unquantized teacher pass
-  const float* s13;  // the caller's weight scales (read by the native fp8 forward epilogues)
-  const float* s2;
+  const float* s13;  // the caller's weight scales (read by the native fp8 forward epilogues and,
+  const float* s2;   // with dq, by the GEMMs' shared-memory dequant)
+  // QAD_FLAG_SMEM_DEQUANT: w13h / w2h are the caller's raw weights and the row-mode GEMMs
+  // fake-quantize each weight tile in shared memory; dump13 / dump2 (QAD_FLAG_DEQUANT_DUMP,
+  // else null) receive the converted values, laid out like the weights
+  bool dq;
+  void* dump13;
+  void* dump2;
 };
 cudaError_t gemm_prepare(const GemmCtx& c);     // pair-tile table of the row-mode GEMMs (after routing)
 // fc1 epilogue modes: everything; everything but Z1 (recompute, forward); only Z1 (recompute,

@@ -76,13 +76,13 @@ def assert_scale_grad(gpu, ref, what):
 class Run:
     """One fwd + dgrad + scalegrad of the layer through the C ABI, on `inp` (synth dict)."""
 
-    def __init__(self, inp, flags=0, accumulate=0, ds_init=None, dprobs=True):
+    def __init__(self, inp, flags=0, accumulate=0, ds_init=None, dprobs=True, zero_ws=False):
         self.inp = inp
         dev = inp["x"].device
         self.s = Q.shape(inp["T"], inp["d"], inp["F"], inp["E"], inp["topk"], inp["fmt"], flags)
         nb = Q.qad_moe_workspace_bytes(self.s)
         assert nb > 0
-        self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        self.ws = (torch.zeros if zero_ws else torch.empty)(nb, dtype=torch.uint8, device=dev)
         T, d, k = inp["T"], inp["d"], inp["topk"]
         self.out = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device=dev)
         self.dx = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device=dev)

@@ -61,7 +61,9 @@ def _layouts():
     for T, d, F, E, k in [(0, 256, 128, 4, 2), (1, 256, 128, 1, 1), (7, 512, 384, 3, 3), (512, 256, 128, 4, 2),
                           (4096, 2048, 768, 32, 8), (16384, 2048, 768, 128, 8), (1000, 256, 1024, 16, 4)]:
         for fmt in _ALL_FMTS:
-            flag_sets = [0, Q.QAD_FLAG_STASH_H, Q.QAD_FLAG_RECOMPUTE, Q.QAD_FLAG_NO_QUANT]
+            flag_sets = [0, Q.QAD_FLAG_STASH_H, Q.QAD_FLAG_RECOMPUTE, Q.QAD_FLAG_NO_QUANT, Q.QAD_FLAG_SMEM_DEQUANT,
+                         Q.QAD_FLAG_SMEM_DEQUANT | Q.QAD_FLAG_DEQUANT_DUMP,
+                         Q.QAD_FLAG_SMEM_DEQUANT | Q.QAD_FLAG_RECOMPUTE]
             if fmt == Q.QAD_FMT_FP8_ROW:
                 flag_sets += [Q.QAD_FLAG_NATIVE_FP8, Q.QAD_FLAG_NATIVE_FP8 | Q.QAD_FLAG_RECOMPUTE]
             for flags in flag_sets:
@@ -191,7 +193,27 @@ def test_binding_constants_match_the_header(lib):
     assert len({Q.qad_kernel_name(i) for i in range(Q.KERNELS)}) == Q.KERNELS
     flags = _enum("QAD_FLAG_")
     assert flags == {"QAD_FLAG_STASH_H": Q.QAD_FLAG_STASH_H, "QAD_FLAG_NO_QUANT": Q.QAD_FLAG_NO_QUANT,
-                     "QAD_FLAG_RECOMPUTE": Q.QAD_FLAG_RECOMPUTE, "QAD_FLAG_NATIVE_FP8": Q.QAD_FLAG_NATIVE_FP8}
+                     "QAD_FLAG_RECOMPUTE": Q.QAD_FLAG_RECOMPUTE, "QAD_FLAG_NATIVE_FP8": Q.QAD_FLAG_NATIVE_FP8,
+                     "QAD_FLAG_SMEM_DEQUANT": Q.QAD_FLAG_SMEM_DEQUANT,
+                     "QAD_FLAG_DEQUANT_DUMP": Q.QAD_FLAG_DEQUANT_DUMP}
     fmts = _enum("QAD_FMT_")
     assert fmts == {"QAD_FMT_NVFP4": 0, "QAD_FMT_INT4_G128": 1, "QAD_FMT_FP8_ROW": 2, "QAD_FMT_NVFP4A16": 3,
                     "QAD_FMT_W8A8": 4, "QAD_FMT_W4AFP8": 5}
+
+
+def test_smem_dequant_flag_drops_the_weight_copies(lib):
+    """QAD_FLAG_SMEM_DEQUANT: no W13_hat / W2_hat regions (E * 3F * d bf16 less), unless
+    QAD_FLAG_DEQUANT_DUMP keeps them for testing; invalid with the teacher pass, the native fp8
+    path, or the dump flag alone."""
+    T, d, F, E, k = 16384, 2048, 768, 128, 8
+    for fmt in _ALL_FMTS:
+        base = Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, fmt))
+        dq = Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, fmt, Q.QAD_FLAG_SMEM_DEQUANT))
+        dump = Q.qad_moe_workspace_bytes(
+            Q.shape(T, d, F, E, k, fmt, Q.QAD_FLAG_SMEM_DEQUANT | Q.QAD_FLAG_DEQUANT_DUMP))
+        assert base - dq >= 2 * E * 3 * F * d and dump == base
+        s = Q.shape(T, d, F, E, k, fmt, Q.QAD_FLAG_SMEM_DEQUANT)
+        assert Q.qad_moe_debug_view(s, "W13_HAT")[1] == 0 and Q.qad_moe_debug_view(s, "W2_HAT")[1] == 0
+    for flags in (Q.QAD_FLAG_SMEM_DEQUANT | Q.QAD_FLAG_NO_QUANT, Q.QAD_FLAG_DEQUANT_DUMP,
+                  Q.QAD_FLAG_SMEM_DEQUANT | Q.QAD_FLAG_NATIVE_FP8):
+        assert Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, Q.QAD_FMT_FP8_ROW, flags)) == 0
