@@ -299,6 +299,7 @@ __global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restr
 __device__ __forceinline__ void zero_pad_rows(uint4* __restrict__ dst, const int32_t* __restrict__ row_token,
                                               int64_t c16, const int32_t* dev_rpad, int64_t w0, int64_t warps,
                                               int lane) {
+  if (!dev_rpad) return;  // rows without padding (the exchange pieces of an expert-parallel split)
   const int64_t rpad = *dev_rpad;
   for (int64_t g = w0; g * 32 < rpad; g += warps) {
     const int64_t r = g * 32 + lane;

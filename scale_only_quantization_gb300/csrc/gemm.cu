@@ -829,48 +829,26 @@ __device__ __forceinline__ void run_scalegrad(const Params& p, const Tile& ti, u
 
 // ---------------------------------------------------------------------------------- B-operand dequant
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
-}
-
 // Elements sharing one weight scale along a weight row: 16 (E2M1), 128 (INT4), the whole row.
 __device__ __forceinline__ int64_t dq_block(int wq, int64_t cols) {
   return wq == kQE2M1 ? 16 : wq == kQInt4 ? 128 : cols;
 }
 
-// Fake-quantizes, in place, the 16 consecutive weights of one row that sit in the 16-byte chunks
-// at shared addresses a0 and a1, with the routine of the standalone fake-quant pass
-// (fakequant16_packed), so the MMA reads exactly the values qad_fakequant_fwd writes.
-template <int QK>
-__device__ __forceinline__ void dq_convert16(uint32_t a0, uint32_t a1, float s, __nv_bfloat16* dump) {
-  const uint4 l0 = ld_shared_v4(a0), h0 = ld_shared_v4(a1);
-  const uint32_t w[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
-  uint32_t o[8];
-  fakequant16_packed<QK>(w, s, o);
-  const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
-  st_shared_v4(a0, lo);
-  st_shared_v4(a1, hi);
-  if (dump) {
-    reinterpret_cast<uint4*>(dump)[0] = lo;
-    reinterpret_cast<uint4*>(dump)[1] = hi;
-  }
-}
-
-// One B stage of this CTA, converted by the 128 converter threads.  The stage holds NB boxes of
-// R rows x 64 bf16 (128-byte rows, 128-byte swizzle: 16-byte chunk c of row r sits at chunk
-// position c ^ (r & 7)).  K-major B (forward GEMMs): box = 128-byte K atom, row = weight row
-// b_row0 + r, columns k0 + 64 box + [0, 64).  MN-major B (input-gradient GEMMs): box = 64
+// One B stage of this CTA, converted in place by the 128 converter threads.  The stage holds NB
+// boxes of R rows x 64 bf16 (128-byte rows, 128-byte swizzle: 16-byte chunk c of row r sits at
+// chunk position c ^ (r & 7)).  K-major B (forward GEMMs): box = 128-byte K atom, row = weight
+// row b_row0 + r, columns k0 + 64 box + [0, 64).  MN-major B (input-gradient GEMMs): box = 64
 // weight columns n0 + 64 box + [0, 64), row = weight row k0 + r.  A unit is 16 elements (chunks
 // 2m and 2m + 1 of a row, one E2M1 scale block); consecutive threads take consecutive rows of
-// the same m, so every quarter-warp's 16-byte accesses fall in distinct bank groups.
+// the same m, so every quarter-warp's 16-byte accesses fall in distinct bank groups.  Each unit
+// is fake-quantized with the routine of the standalone pass (fakequant16_packed), so the MMA
+// reads exactly the values qad_fakequant_fwd writes.
 template <int NB, int R, bool B_MN>
 struct DqStage {
   static constexpr int UNITS = NB * R * 4;
   static constexpr int PER = UNITS / kConvThreads;
-  static_assert(PER * kConvThreads == UNITS, "units per stage must split evenly over the converters");
+  static constexpr int BATCH = PER < 4 ? PER : 4;  // units whose loads are issued together
+  static_assert(PER * kConvThreads == UNITS && PER % BATCH == 0, "units per stage must split evenly");
   struct Unit {
     int box, r, m;
     int64_t wrow, wcol;
@@ -902,16 +880,40 @@ struct DqStage {
       sc[i] = __ldg(p.dq_s + ((int64_t)e * p.dq_rows + x.wrow) * s_pitch + x.wcol / blk);
     }
   }
+  // sb: the stage's B half in shared memory (generic pointer: ordinary accesses, ordered after the
+  // barrier wait and before the proxy fence that follows)
   template <int QK, int BOX_BYTES>
-  __device__ __forceinline__ static void convert(const Params& p, uint32_t sb, int tid, int e, int64_t b_row0,
+  __device__ __forceinline__ static void convert(const Params& p, uint8_t* sb, int tid, int e, int64_t b_row0,
                                                  int64_t k0, int64_t n0, const float (&sc)[PER]) {
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const Unit x = unit(tid, i, b_row0, k0, n0);
-      const uint32_t row_addr = sb + (uint32_t)(x.box * BOX_BYTES + x.r * 128);
-      dq_convert16<QK>(row_addr + ((uint32_t)((2 * x.m) ^ (x.r & 7)) << 4),
-                       row_addr + ((uint32_t)((2 * x.m + 1) ^ (x.r & 7)) << 4), sc[i],
-                       p.dq_dump ? p.dq_dump + ((int64_t)e * p.dq_rows + x.wrow) * p.dq_cols + x.wcol : nullptr);
+    for (int i0 = 0; i0 < PER; i0 += BATCH) {
+      uint4* c0[BATCH];
+      uint4* c1[BATCH];
+      uint32_t w[BATCH][8];
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j) {
+        const Unit x = unit(tid, i0 + j, b_row0, k0, n0);
+        uint8_t* row = sb + x.box * BOX_BYTES + x.r * 128;
+        c0[j] = reinterpret_cast<uint4*>(row + (((2 * x.m) ^ (x.r & 7)) << 4));
+        c1[j] = reinterpret_cast<uint4*>(row + (((2 * x.m + 1) ^ (x.r & 7)) << 4));
+        const uint4 lo = *c0[j], hi = *c1[j];
+        w[j][0] = lo.x; w[j][1] = lo.y; w[j][2] = lo.z; w[j][3] = lo.w;
+        w[j][4] = hi.x; w[j][5] = hi.y; w[j][6] = hi.z; w[j][7] = hi.w;
+      }
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j) {
+        uint32_t o[8];
+        fakequant16_packed<QK>(w[j], sc[i0 + j], o);
+        const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
+        *c0[j] = lo;
+        *c1[j] = hi;
+        if (p.dq_dump) {
+          const Unit x = unit(tid, i0 + j, b_row0, k0, n0);
+          uint4* d = reinterpret_cast<uint4*>(p.dq_dump + ((int64_t)e * p.dq_rows + x.wrow) * p.dq_cols + x.wcol);
+          d[0] = lo;
+          d[1] = hi;
+        }
+      }
     }
   }
 };
@@ -1149,7 +1151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(DQ), 1)
         if (more) S::scales(p, tid, ti2.e, b_row0(ti2), (int64_t)kb2 * BKE, n0_of(ti2), sc2);
         const bool got = mbar_wait(bfull_bar(stage), phase, abort_flag, err);
         if (!__all_sync(0xffffffffu, got)) break;
-        const uint32_t sb = b_ring + stage * C::B_BYTES;
+        uint8_t* sb = smem + (b_ring - a_ring) + stage * C::B_BYTES;
         const int64_t k0 = (int64_t)kb * BKE, br = b_row0(ti), n0 = n0_of(ti);
         if (p.wq == kQE2M1) S::template convert<kQE2M1, BOX_BYTES>(p, sb, tid, ti.e, br, k0, n0, sc);
         else if (p.wq == kQInt4) S::template convert<kQInt4, BOX_BYTES>(p, sb, tid, ti.e, br, k0, n0, sc);
