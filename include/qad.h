@@ -189,30 +189,21 @@ int qad_moe_bwd_scalegrad(const qad_moe_shape* s, const void* w13, const float* 
                           int accumulate, void* ws, size_t ws_bytes, qad_stream_t stream);
 
 /*
- * The layer's two per-token steps around the expert computation, on rows the caller holds.  They
- * serve an expert-parallel split (AngelSlim mcore_qad walkthrough, section 二.4: experts are split
- * across ranks only by expert parallelism, ETP = 1): a rank sends each routed (token, slot) pair
- * to the rank that owns its expert, that rank runs the layer on the received rows with top-1
- * routing and weight 1 (so its output rows are the expert outputs Y and its input-gradient rows
- * are dA1), and the rows come back in pair order, where these calls finish the layer exactly as
- * qad_moe_fwd / qad_moe_bwd_dgrad would on one GPU.
- *
- * qad_moe_combine:    out[t] = bf16(sum_{j = 0..topk-1} p[t, j] * rows[row_of[t, j]]), fp32 sums in
- *                     slot order; p NULL means weight 1 (the input gradient dx); a pair with
- *                     row_of < 0 is skipped.
+ * The layer's combine step on rows the caller holds: out[t] = bf16(sum_{j = 0..topk-1} p[t, j] *
+ * rows[row_of[t, j]]), fp32 sums in slot order; p NULL means weight 1; a pair with row_of < 0 is
+ * skipped.  It serves an expert-parallel split (AngelSlim mcore_qad walkthrough, section 二.4:
+ * experts are split across ranks only by expert parallelism, ETP = 1): a rank sends each routed
+ * (token, slot) pair to the rank that owns its expert, that rank runs the layer on the received
+ * rows with top-1 routing (weight 1 in the forward, the pair's weight in the input-gradient call),
+ * so its output rows are the expert outputs Y and its input-gradient rows are dA1; the rows come
+ * back in pair order and this call forms out (with p) and dx (weight 1) exactly as qad_moe_fwd /
+ * qad_moe_bwd_dgrad would on one GPU.
  *   rows bf16 [n_rows, d]; row_of int32 [T, topk]; p fp32 [T, topk] or NULL; out bf16 [T, d]
- * qad_moe_scale_dout: dy[row_of[t, j]] = bf16(fp32(p[t, j] * dout[t])) and
- *                     dprobs[t, j] = <dout[t], y[row_of[t, j]]> (fp32; 0 for row_of < 0).
- *   dout bf16 [T, d]; p fp32 [T, topk]; row_of int32 [T, topk]; y bf16 [n_rows, d] (the expert
- *   outputs of the forward); dy bf16 [n_rows, d] (written); dprobs fp32 [T, topk] or NULL.
  * Requires d % 16 == 0, 1 <= topk <= 32, 16-byte aligned pointers, and every row_of entry -1 or
- * in [0, n_rows) (the caller builds row_of; it is not checked on the device).  Rows of dy that no
- * pair names are left as they are.
+ * in [0, n_rows) (the caller builds row_of; it is not checked on the device).
  */
 int qad_moe_combine(const void* rows, const int32_t* row_of, const float* p, void* out, int64_t T, int32_t topk,
                     int64_t d, qad_stream_t stream);
-int qad_moe_scale_dout(const void* dout, const float* p, const int32_t* row_of, const void* y, void* dy,
-                       float* dprobs, int64_t T, int32_t topk, int64_t d, qad_stream_t stream);
 
 /* Synchronises `stream`, copies the device error word of `ws` into *code (host
  * pointer, may be NULL) and returns QAD_OK if it is zero, QAD_ERR_DEVICE otherwise. */

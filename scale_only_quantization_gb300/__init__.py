@@ -29,8 +29,7 @@ KERNELS = 15
 EXPORTS = ["qad_fakequant_fwd", "qad_moe_workspace_bytes", "qad_moe_fwd", "qad_moe_bwd_dgrad",
            "qad_moe_bwd_scalegrad", "qad_check_device_error", "qad_status_string", "qad_moe_debug_view",
            "qad_profile_enable", "qad_profile_reset", "qad_profile_read", "qad_kernel_name", "qad_launch_count",
-           "qad_debug_quotient", "qad_route_permute_noalloc", "qad_debug_wait_timeout", "qad_moe_combine",
-           "qad_moe_scale_dout"]
+           "qad_debug_quotient", "qad_route_permute_noalloc", "qad_debug_wait_timeout", "qad_moe_combine"]
 
 
 class QADError(RuntimeError):
@@ -81,7 +80,6 @@ def lib():
             "qad_route_permute_noalloc": (ctypes.c_int, [_P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P,
                                                          _P, _P, _P]),
             "qad_moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int32, _I64, _P]),
-            "qad_moe_scale_dout": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int32, _I64, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -201,11 +199,6 @@ def qad_route_permute_noalloc(topk_idx, T, topk, E, row_token, row_slot, row_of,
 def qad_moe_combine(rows, row_of, p, out, T, topk, d, stream=None):
     return _check(lib().qad_moe_combine(_ptr(rows), _ptr(row_of), _ptr(p), _ptr(out), int(T), int(topk), int(d),
                                         _stream(stream)), "qad_moe_combine")
-
-
-def qad_moe_scale_dout(dout, p, row_of, y, dy, dprobs, T, topk, d, stream=None):
-    return _check(lib().qad_moe_scale_dout(_ptr(dout), _ptr(p), _ptr(row_of), _ptr(y), _ptr(dy), _ptr(dprobs),
-                                           int(T), int(topk), int(d), _stream(stream)), "qad_moe_scale_dout")
 
 
 def qad_debug_wait_timeout(err_word, budget_cycles, stream=None):

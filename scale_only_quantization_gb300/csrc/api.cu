@@ -368,16 +368,6 @@ int qad_moe_combine(const void* rows, const int32_t* row_of, const float* p, voi
   return to_status(launch_combine(rows, row_of, p, out, T, topk, d, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int qad_moe_scale_dout(const void* dout, const float* p, const int32_t* row_of, const void* y, void* dy,
-                       float* dprobs, int64_t T, int32_t topk, int64_t d, qad_stream_t stream) {
-  if (T < 0 || d <= 0 || d % 16 || topk < 1 || topk > 32) return QAD_ERR_INVALID_ARG;
-  if (T == 0) return QAD_OK;
-  if (!ok_ptr(dout) || !ok_ptr(p) || !ok_ptr(row_of) || !ok_ptr(y) || !ok_ptr(dy) || (dprobs && !ok_ptr(dprobs)))
-    return QAD_ERR_INVALID_ARG;
-  return to_status(launch_dy_scatter(dout, p, row_of, nullptr, y, dy, dprobs, T, topk, d, nullptr,
-                                     reinterpret_cast<cudaStream_t>(stream)));
-}
-
 int qad_check_device_error(void* ws, qad_stream_t stream, int32_t* code) {
   if (!ws) return QAD_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

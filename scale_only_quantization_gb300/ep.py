@@ -19,9 +19,10 @@ One step, each rank holding its own tokens:
                (source rank, token, slot) order: the order a single process would give the
                ranks' tokens concatenated);
             4. all-to-all back; out[t] = bf16(sum_j p[t, j] Y[t, j]) on the sending rank.
-  backward  5. dY rows = bf16(p dout) and dprobs on the sending rank, all-to-all to the owners;
-            6. the owners' input-gradient call gives the dA1 rows, all-to-all back, and
-               dx[t] = bf16(sum_j dA1[t, j]);
+  backward  5. all-to-all of the pairs' dout rows and routing weights to the owners;
+            6. the owners' input-gradient call with those weights (the layer's own dY =
+               bf16(p dout), dprobs = <dout, Y> and dA1 rows), all-to-all of dA1 and dprobs
+               back, and dx[t] = bf16(sum_j dA1[t, j]) on the sending rank;
             7. the owners' scale-gradient call (their experts only), averaged over the
                expert-data-parallel group.
 
@@ -129,21 +130,25 @@ class ExpertParallelMoE:
         y_pairs[plan["order"]] = y_back
         out = self.backend.combine(y_pairs, plan["row_of"], topk_w)
         plan["recv_counts"] = recv_counts
-        self.plan, self.topk_w, self.y_pairs = plan, topk_w, y_pairs
+        self.plan, self.topk_w = plan, topk_w
         return out
 
     def backward(self, dout):
         """dx [T, d] and dprobs [T, k] for the tokens of the last forward."""
         plan = self.plan
         T, k = plan["row_of"].shape
-        dy_pairs, dprobs = self.backend.scale_dout(dout, self.topk_w, plan["row_of"], self.y_pairs)
-        dy_rows = exchange(dy_pairs[plan["order"]], plan["send_counts"], plan["recv_counts"], self.group)
-        da_rows = self.backend.dgrad(dy_rows)
-        da_back = exchange(da_rows, plan["recv_counts"], plan["send_counts"], self.group)
+        send, recv = plan["send_counts"], plan["recv_counts"]
+        g_rows = exchange(dout[plan["order"] // k], send, recv, self.group)
+        p_rows = exchange(self.topk_w.reshape(-1)[plan["order"]].contiguous(), send, recv, self.group)
+        da_rows, dp_rows = self.backend.dgrad(g_rows, p_rows)
+        da_back = exchange(da_rows, recv, send, self.group)
+        dp_back = exchange(dp_rows, recv, send, self.group)
         da_pairs = da_back.new_zeros((T * k,) + tuple(da_back.shape[1:]))
         da_pairs[plan["order"]] = da_back
+        dprobs = dp_back.new_zeros(T * k)
+        dprobs[plan["order"]] = dp_back
         dx = self.backend.combine(da_pairs, plan["row_of"], None)
-        return dx, dprobs
+        return dx, dprobs.reshape(T, k)
 
     def scale_grads(self):
         """ds13 [E / EP, 2F, d / B], ds2 [E / EP, d, F / B] of this rank's experts, averaged over
@@ -180,11 +185,15 @@ class CudaExperts:
         Q.qad_moe_fwd(self.s, x_rows.contiguous(), self.idx, self.p, self.w13, self.s13, self.w2, self.s2, y, self.ws)
         return y
 
-    def dgrad(self, dy_rows):
-        da = torch.empty_like(dy_rows)
-        self.Q.qad_moe_bwd_dgrad(self.s, dy_rows.contiguous(), self.p, self.w13, self.s13, self.w2, self.s2, da, None,
-                                 self.ws)
-        return da
+    def dgrad(self, dout_rows, p_rows):
+        """dA1 rows and dprobs of the received pairs: the layer's input-gradient call on the rows'
+        output gradients with the pairs' routing weights."""
+        n = dout_rows.shape[0]
+        da = torch.empty_like(dout_rows)
+        dp = torch.empty((n, 1), dtype=torch.float32, device=dout_rows.device)
+        self.Q.qad_moe_bwd_dgrad(self.s, dout_rows.contiguous(), p_rows.reshape(n, 1).contiguous(), self.w13,
+                                 self.s13, self.w2, self.s2, da, dp, self.ws)
+        return da, dp.reshape(n)
 
     def scalegrad(self):
         ds13, ds2 = torch.empty_like(self.s13), torch.empty_like(self.s2)
@@ -196,10 +205,3 @@ class CudaExperts:
         out = torch.empty((T, rows.shape[1]), dtype=torch.bfloat16, device=rows.device)
         self.Q.qad_moe_combine(rows.contiguous(), row_of, p, out, T, k, rows.shape[1])
         return out
-
-    def scale_dout(self, dout, p, row_of, y_pairs):
-        T, k = row_of.shape
-        dy = torch.zeros_like(y_pairs)
-        dprobs = torch.empty((T, k), dtype=torch.float32, device=dout.device)
-        self.Q.qad_moe_scale_dout(dout.contiguous(), p, row_of, y_pairs, dy, dprobs, T, k, dout.shape[1])
-        return dy, dprobs

@@ -219,15 +219,13 @@ def test_smem_dequant_flag_drops_the_weight_copies(lib):
         assert Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, Q.QAD_FMT_FP8_ROW, flags)) == 0
 
 
-def test_exchange_pieces_reject_bad_arguments_before_launch(lib):
-    """qad_moe_combine / qad_moe_scale_dout: d % 16, 1 <= topk <= 32 and 16-byte aligned pointers
-    are checked on the host (no GPU is touched); T = 0 is a no-op."""
+def test_combine_rejects_bad_arguments_before_launch(lib):
+    """qad_moe_combine: d % 16, 1 <= topk <= 32, T >= 0 and 16-byte aligned pointers are checked on
+    the host (no GPU is touched); T = 0 is a no-op."""
     P = 1 << 20  # a 16-byte aligned stand-in address; nothing is launched for invalid arguments
     assert lib.qad_moe_combine(P, P, P, P, 4, 2, 24, None) == Q.QAD_ERR_INVALID_ARG      # d % 16
     assert lib.qad_moe_combine(P, P, P, P, 4, 33, 32, None) == Q.QAD_ERR_INVALID_ARG     # topk > 32
     assert lib.qad_moe_combine(P + 4, P, P, P, 4, 2, 32, None) == Q.QAD_ERR_INVALID_ARG  # misaligned
     assert lib.qad_moe_combine(None, P, P, P, 4, 2, 32, None) == Q.QAD_ERR_INVALID_ARG
     assert lib.qad_moe_combine(None, None, None, None, 0, 2, 32, None) == Q.QAD_OK
-    assert lib.qad_moe_scale_dout(P, None, P, P, P, None, 4, 2, 32, None) == Q.QAD_ERR_INVALID_ARG  # p needed
-    assert lib.qad_moe_scale_dout(P, P, P, P, P, P + 8, 4, 2, 32, None) == Q.QAD_ERR_INVALID_ARG
-    assert lib.qad_moe_scale_dout(P, P, P, P, P, None, -1, 2, 32, None) == Q.QAD_ERR_INVALID_ARG
+    assert lib.qad_moe_combine(P, P, P, P, -1, 2, 32, None) == Q.QAD_ERR_INVALID_ARG

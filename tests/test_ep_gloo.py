@@ -67,10 +67,10 @@ class OracleExperts:
                                   self.ones, self.w13, self.s13, self.w2, self.s2)
         return self._bf16(self.fwd["out"])
 
-    def dgrad(self, dy_rows):
+    def dgrad(self, dout_rows, p_rows):
         from oracle import moe as OM
-        self.bwd = OM.moe_dgrad(self._bits(dy_rows), self.ones, self.fwd)
-        return self._bf16(self.bwd["dx"])
+        self.bwd = OM.moe_dgrad(self._bits(dout_rows), p_rows.numpy().astype(np.float64).reshape(-1, 1), self.fwd)
+        return self._bf16(self.bwd["dx"]), torch.from_numpy(self.bwd["dprobs"].reshape(-1).copy())
 
     def scalegrad(self):
         from oracle import moe as OM
@@ -83,20 +83,6 @@ class OracleExperts:
         ro = row_of.numpy().astype(np.int64)
         pw = np.ones(ro.shape) if p is None else p.numpy().astype(np.float64)
         return self._bf16(OM.combine(OQ.bf16_to_f64(self._bits(rows)), pw, ro))
-
-    def scale_dout(self, dout, p, row_of, y_pairs):
-        from oracle import quant as OQ
-        ro = row_of.numpy().astype(np.int64)
-        g = OQ.bf16_to_f64(self._bits(dout))
-        y = OQ.bf16_to_f64(self._bits(y_pairs))
-        pw = p.numpy().astype(np.float64)
-        dy = np.zeros_like(y)
-        dprobs = np.zeros(ro.shape)
-        for j in range(ro.shape[1]):
-            ok = ro[:, j] >= 0
-            dy[ro[ok, j]] = OQ.round_bf16(OQ.round_f32(g[ok] * pw[ok, j][:, None]))
-            dprobs[ok, j] = np.einsum("td,td->t", g[ok], y[ro[ok, j]])
-        return self._bf16(dy), torch.from_numpy(dprobs)
 
 
 def _rank_main(rank, world, ep, port, out):

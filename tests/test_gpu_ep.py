@@ -1,7 +1,7 @@
-"""The expert-parallel pieces on one GPU: the two per-token steps the C ABI exposes for the
-exchange (qad_moe_combine, qad_moe_scale_dout) against the oracle, and the expert-parallel layer
-with the CUDA backend on one rank (the exchange is then the identity) against the layer's own
-calls, bit for bit: the owner sees the same rows per expert in the same order."""
+"""The expert-parallel pieces on one GPU: the combine step the C ABI exposes for the exchange
+(qad_moe_combine) against the oracle, and the expert-parallel layer with the CUDA backend on one
+rank (the exchange is then the identity) against the layer's own calls, bit for bit: the owner
+sees the same rows per expert in the same order."""
 import numpy as np
 import pytest
 import torch
@@ -9,10 +9,9 @@ import torch
 import scale_only_quantization_gb300 as Q
 from scale_only_quantization_gb300 import ep as EP
 from oracle import moe as OM
-from oracle import quant as OQ
 import synth
 
-from gpu_util import Run, assert_close, bits, vals
+from gpu_util import Run, assert_close, vals
 
 pytestmark = pytest.mark.gpu
 
@@ -25,36 +24,22 @@ def _built():
 
 
 @pytest.mark.parametrize("T, k, d", [(300, 8, 2048), (77, 3, 784), (5, 1, 16)])
-def test_combine_and_scale_dout_against_the_oracle(T, k, d):
+def test_combine_against_the_oracle(T, k, d):
     g = torch.Generator(device="cuda").manual_seed(T + k)
     n_rows = T * k + 13
     rows = (torch.randn((n_rows, d), generator=g, device="cuda")).to(torch.bfloat16)
     perm = torch.randperm(n_rows, generator=g, device="cuda")[: T * k].to(torch.int32).view(T, k)
     row_of = torch.where(torch.rand((T, k), generator=g, device="cuda") < 0.1, -1, perm).to(torch.int32).contiguous()
     p = torch.softmax(torch.randn((T, k), generator=g, device="cuda"), 1).contiguous()
-    dout = torch.randn((T, d), generator=g, device="cuda").to(torch.bfloat16)
     out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
     dx = torch.empty_like(out)
     Q.qad_moe_combine(rows, row_of, p, out, T, k, d)
     Q.qad_moe_combine(rows, row_of, None, dx, T, k, d)
-    dy = torch.zeros_like(rows)
-    dprobs = torch.empty((T, k), dtype=torch.float32, device="cuda")
-    Q.qad_moe_scale_dout(dout, p, row_of, rows, dy, dprobs, T, k, d)
     torch.cuda.synchronize()
     ro = synth.to_numpy(row_of).astype(np.int64)
-    pw = synth.to_numpy(p).astype(np.float64)
     r64 = vals(rows)
-    assert_close(vals(out), OM.combine(r64, pw, ro), "combine")
+    assert_close(vals(out), OM.combine(r64, synth.to_numpy(p).astype(np.float64), ro), "combine")
     assert_close(vals(dx), OM.combine(r64, np.ones((T, k)), ro), "combine (weight 1)")
-    g64 = vals(dout)
-    want = np.zeros_like(r64)
-    dp = np.zeros((T, k))
-    for j in range(k):
-        ok = ro[:, j] >= 0
-        want[ro[ok, j]] = OQ.round_bf16(OQ.round_f32(g64[ok] * pw[ok, j][:, None]))
-        dp[ok, j] = np.einsum("td,td->t", g64[ok], r64[ro[ok, j]])
-    assert np.array_equal(bits(dy), OQ.f64_to_bf16_bits(want))     # untouched rows stay zero
-    assert_close(synth.to_numpy(dprobs).astype(np.float64), dp, "dprobs")
 
 
 @pytest.mark.parametrize("fmt, name", [(Q.QAD_FMT_NVFP4, "tiny_nvfp4"), (Q.QAD_FMT_FP8_ROW, "tiny_nvfp4"),
