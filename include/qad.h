@@ -156,8 +156,11 @@ size_t qad_moe_workspace_bytes(const qad_moe_shape* s);
  *   out      bf16 [T, d] (written)
  *   ws       workspace (256-byte aligned) of ws_bytes >= qad_moe_workspace_bytes(s); it keeps what the
  *            backward calls need (routing maps, fake-quantized weights, activations).
- * Supported: d % 256 == 0, F % 128 == 0, 1 <= topk <= min(E, 32), 1 <= E <= 1024,
- * T * topk < 2^31.  The error word is cleared at the start of this call.
+ * Supported: d and F multiples of 16 (multiples of 128 for the INT4 formats, whose group-128
+ * scales run along both; d % 256 == 0 and F % 128 == 0 with QAD_FLAG_NATIVE_FP8 or
+ * QAD_FLAG_SMEM_DEQUANT), 1 <= topk <= min(E, 32), 1 <= E <= 1024, T * topk < 2^31; other shapes
+ * return QAD_ERR_UNSUPPORTED before any launch.  The error word is cleared at the start of this
+ * call.
  */
 int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, const float* topk_w,
                 const void* w13, const float* s13, const void* w2, const float* s2,

@@ -99,7 +99,12 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   const bool dq = (s.flags & QAD_FLAG_SMEM_DEQUANT) != 0;
   if (dq && (s.flags & (QAD_FLAG_NO_QUANT | QAD_FLAG_NATIVE_FP8))) return QAD_ERR_INVALID_ARG;
   if ((s.flags & QAD_FLAG_DEQUANT_DUMP) && !dq) return QAD_ERR_INVALID_ARG;
-  if (s.d % 256 || s.F % 128) return QAD_ERR_UNSUPPORTED;
+  // d and F: multiples of 16 (the scale blocks, activation blocks and 32-byte row sectors), of 128
+  // for the INT4 formats (their group-128 scales run along both d and F); the E4M3 tensor path and
+  // the in-GEMM dequant take only whole 256 x 128 tiles (d % 256 == 0, F % 128 == 0)
+  const int64_t mult = weight_kind(s.fmt) == kQInt4 ? 128 : 16;
+  if (s.d % mult || s.F % mult) return QAD_ERR_UNSUPPORTED;
+  if ((s.flags & (QAD_FLAG_NATIVE_FP8 | QAD_FLAG_SMEM_DEQUANT)) && (s.d % 256 || s.F % 128)) return QAD_ERR_UNSUPPORTED;
   if (s.E > 1024 || s.topk > 32 || s.topk > s.E) return QAD_ERR_UNSUPPORTED;
   const int64_t R = s.T * (int64_t)s.topk;
   const int64_t Rmax = (R + (int64_t)(kTileRows - 1) * s.E + kTileRows - 1) / kTileRows * kTileRows;
@@ -140,8 +145,8 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->dy = take(2 * (size_t)(Rmax * d));
   L->dz1 = take(2 * (size_t)(Rmax * 2 * F));
   L->da1 = take(2 * (size_t)(Rmax * d));
-  L->part13 = take(4 * (size_t)(E * 2 * F * (d / 128) * 2));
-  L->part2 = take(4 * (size_t)(E * d * (F / 128) * 2));
+  L->part13 = take(4 * (size_t)(E * 2 * F * ((d + 127) / 128) * 2));
+  L->part2 = take(4 * (size_t)(E * d * ((F + 127) / 128) * 2));
   L->native_fp8 = (s.flags & QAD_FLAG_NATIVE_FP8) != 0;
   L->w13q = L->w2q = L->a1q = L->hq = L->sa_tok = L->sh_row = 0;
   if (L->native_fp8) {
@@ -214,7 +219,9 @@ const char* qad_status_string(int status) {
   switch (status) {
     case QAD_OK: return "ok";
     case QAD_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size or flag)";
-    case QAD_ERR_UNSUPPORTED: return "unsupported shape (needs d % 256 == 0, F % 128 == 0, topk <= min(E, 32), E <= 1024)";
+    case QAD_ERR_UNSUPPORTED:
+      return "unsupported shape (needs d, F multiples of 16 -- of 128 for INT4 weights, d % 256 == 0 and F % 128 == 0 "
+             "with the E4M3 tensor path or the in-GEMM dequant --, topk <= min(E, 32), E <= 1024)";
     case QAD_ERR_WORKSPACE: return "workspace smaller than qad_moe_workspace_bytes()";
     case QAD_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case QAD_ERR_DEVICE: return "device error word set (bad or repeated routing index, or a pipeline timeout)";

@@ -79,6 +79,7 @@ struct Params {
   int F;                        // expert FFN width (fc1 / SwiGLU epilogues)
   int wq, aq, flags;  // weight grid (LSQ), activation grid of the fc1 epilogue (kQNone: none)
   int fc1_mode;       // kFc1Full, kFc1NoZ1 or kFc1Z1Only
+  int n_total;        // the GEMM's N (output columns): store tiles past it are skipped
   // E4M3 operands (native fp8): the epilogue multiplies the fp32 sum of row r, column n by
   // row_scale[row_tok ? row_tok[r] : r] * col_scale[e * b_rows + weight row of n]
   const float* row_scale;
@@ -90,6 +91,7 @@ struct Params {
   const __nv_bfloat16* w;  const float* s;   // SCALEGRAD: raw weights [E, Mw, Kw] and scales
   int64_t w_rows, w_cols;
   int w_vec32;  // w is 32-byte aligned: its sectors are read with 256-bit loads
+  int s_vec4;   // E2M1 scale rows are 16-byte aligned (w_cols % 64 == 0): 4 scales per vector access
   float* ds; float* part; int accumulate;
   // DQ: the B operand is the raw bf16 weight [E, dq_rows, dq_cols] with scales dq_s; the
   // converters apply bf16(fp32(q(fp32(w / s)) * s)) (grid p.wq) to each B stage in shared
@@ -447,14 +449,19 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
     const int32_t tok = p.row_tok ? __ldg(p.row_tok + row) : (int32_t)row;
     rs = tok >= 0 ? __ldg(p.row_scale + tok) : 0.0f;
   }
+  // 16-column steps of this warp that lie inside F (all 4 unless F % 128 != 0 in the last tile);
+  // the same for the whole warp, so the warp-wide TMEM loads stay uniform
+  int nsteps = (p.F - (ti.nb * 128 + c0)) / 16;
+  nsteps = nsteps < 0 ? 0 : (nsteps > 4 ? 4 : nsteps);
+  if (nsteps == 0) return;
   uint32_t g[16], u[16], gn[16], un[16];
   tmem_ld16_issue(tbase + c0, g);
   tmem_ld16_issue(tbase + 128 + c0, u);
   tmem_wait16x2(g, u);
 #pragma unroll 1
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < nsteps; ++j) {
     const int cc = c0 + 16 * j;
-    if (j < 3) {
+    if (j + 1 < nsteps) {
       tmem_ld16_issue(tbase + cc + 16, gn);
       tmem_ld16_issue(tbase + 128 + cc + 16, un);
     }
@@ -505,7 +512,7 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
     }
     store_box16(ring, tm_h, lane, h, f0, y);
     }
-    if (j < 3) {
+    if (j + 1 < nsteps) {
       tmem_wait16x2(gn, un);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -543,6 +550,9 @@ __device__ __forceinline__ void epi_store_batch(const Params& p, const CUtensorM
   }
 #pragma unroll
   for (int c = 0; c < NH; ++c) {
+    // a 32-column box that starts past N is not stored (one that straddles it is cut by the
+    // tensor map's extent)
+    if (ti.nb * BN + 32 * (c0 + c) >= p.n_total) continue;
     if constexpr (F8) {
       const float4* cs =
           reinterpret_cast<const float4*>(p.col_scale + (int64_t)ti.e * p.b_rows + ti.nb * BN + 32 * (c0 + c));
@@ -664,8 +674,10 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, const CUtensorMa
       u[i] = duv.x;
       u[i + 1] = duv.y;
     }
-    store_box16(ring, tm_dz1, lane, g, f0, y);
-    store_box16(ring, tm_dz1, lane, u, p.F + f0, y);
+    if (f0 < p.F) {  // steps past F (the last tile when F % BN != 0) read and compute, but store nothing
+      store_box16(ring, tm_dz1, lane, g, f0, y);
+      store_box16(ring, tm_dz1, lane, u, p.F + f0, y);
+    }
     if (j + 1 < STEPS) {
       tmem_wait16(rn);
 #pragma unroll
@@ -734,6 +746,66 @@ __device__ __forceinline__ float lsq_block_sum(const uint32_t (&acc)[16], const 
   return t;
 }
 
+// A tile that reaches past the weight (rows % 256 or cols % BN != 0, or nvfp4 scale rows that
+// are not 16-byte aligned) takes this plain loop instead: every accumulator column is still read
+// (the TMEM loads are warp-wide), but W, the scales and ds are touched only inside the weight, one
+// 16-column step at a time -- few registers, no software pipelining; only edge tiles run it.
+template <int BN, int QK>
+__device__ __forceinline__ void epi_scalegrad_edge(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
+                                                   int half) {
+  constexpr int STEPS = BN / 32;
+  const int64_t n = ti.row_base + row_in_tile;
+  const int64_t wrow = (int64_t)ti.e * p.w_rows + n;
+  const int col0 = half * (BN / 2);
+  const int64_t k_first = (int64_t)ti.nb * BN + col0;
+  int nvalid = n < p.w_rows ? (int)((p.w_cols - k_first) / 16) : 0;
+  nvalid = nvalid < 0 ? 0 : (nvalid > STEPS ? STEPS : nvalid);
+  const bool have_acc = ti.nkb > 0;
+  const bool vec32 = p.w_vec32 != 0;
+  float sum = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < STEPS; ++j) {
+    uint32_t r[16];
+    if (have_acc) {
+      tmem_ld16_issue(tbase + col0 + 16 * j, r);
+      tmem_wait16(r);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = 0u;
+    }
+    if (j >= nvalid) continue;
+    uint4 wq[2];
+    w_load(p.w + wrow * p.w_cols + k_first + 16 * j, vec32, wq);
+    const int64_t k = k_first + 16 * j;
+    float sc;
+    if constexpr (QK == kQE2M1) sc = __ldg(p.s + wrow * (p.w_cols / 16) + k / 16);
+    else if constexpr (QK == kQInt4) sc = __ldg(p.s + wrow * (p.w_cols / 128) + k / 128);
+    else sc = __ldg(p.s + wrow);
+    const float t = lsq_block_sum<QK>(r, wq, sc);
+    if constexpr (QK == kQE2M1) {
+      float* dst = p.ds + wrow * (p.w_cols / 16) + k / 16;
+      *dst = p.accumulate ? *dst + t : t;
+    } else {
+      sum += t;
+    }
+  }
+  if constexpr (QK != kQE2M1) {
+    if (n >= p.w_rows) return;
+    if constexpr ((QK == kQInt4) && (BN == 256)) {
+      if (nvalid == 0) return;  // a half past the weight's last 128-column group
+      float* dst = p.ds + wrow * (p.w_cols / 128) + k_first / 128;
+      *dst = p.accumulate ? *dst + sum : sum;
+    } else {
+      // every part of a scale block is written (0 for a half past the weight), so the reduction
+      // adds a fixed number of parts in a fixed order
+      const int64_t B = (QK == kQInt4) ? 128 : p.w_cols;
+      const int tiles_per_block = (int)((B + BN - 1) / BN);
+      const int64_t ds_index = wrow * (p.w_cols / B) + ((int64_t)ti.nb * BN) / B;
+      p.part[ds_index * (2 * tiles_per_block) + (ti.nb % tiles_per_block) * 2 + half] = sum;
+    }
+  }
+}
+
 template <int BN, int QK>
 __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                                   int half) {
@@ -748,16 +820,16 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
 
   // scales of this half row
   float sv[STEPS];
-  float* ds_vec = nullptr;
+  float* ds_row = nullptr;
   if constexpr (QK == kQE2M1) {
     const int64_t sidx = wrow * (p.w_cols / 16) + k_first / 16;  // a multiple of 4
+    ds_row = p.ds + sidx;
     const float4* sp = reinterpret_cast<const float4*>(p.s + sidx);
 #pragma unroll
     for (int i = 0; i < STEPS / 4; ++i) {
       const float4 v4 = __ldg(sp + i);
       sv[4 * i] = v4.x; sv[4 * i + 1] = v4.y; sv[4 * i + 2] = v4.z; sv[4 * i + 3] = v4.w;
     }
-    ds_vec = p.ds + sidx;
   } else {
     const float sc = (QK == kQInt4) ? __ldg(p.s + wrow * (p.w_cols / 128) + k_first / 128) : __ldg(p.s + wrow);
 #pragma unroll
@@ -790,7 +862,7 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
   }
 
   if constexpr (QK == kQE2M1) {
-    float4* dv = reinterpret_cast<float4*>(ds_vec);
+    float4* dv = reinterpret_cast<float4*>(ds_row);
 #pragma unroll
     for (int i = 0; i < STEPS / 4; ++i) {
       float4 o = make_float4(tsum[4 * i], tsum[4 * i + 1], tsum[4 * i + 2], tsum[4 * i + 3]);
@@ -808,23 +880,32 @@ __device__ __forceinline__ void epi_scalegrad_fmt(const Params& p, const Tile& t
       float* dst = p.ds + wrow * (p.w_cols / 128) + k_first / 128;
       *dst = p.accumulate ? *dst + sum : sum;
     } else {
+      // every part of a scale block is written (0 for a half past the weight), so the reduction
+      // adds a fixed number of parts in a fixed order
       const int64_t B = (QK == kQInt4) ? 128 : p.w_cols;  // elements per scale
-      const int tiles_per_block = (int)(B / BN);
+      const int tiles_per_block = (int)((B + BN - 1) / BN);
       const int64_t ds_index = wrow * (p.w_cols / B) + ((int64_t)ti.nb * BN) / B;
       p.part[ds_index * (2 * tiles_per_block) + (ti.nb % tiles_per_block) * 2 + half] = sum;
     }
   }
 }
 
+template <int BN, int QK>
+__device__ __forceinline__ void scalegrad_tile(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
+                                               int half) {
+  const bool inside = p.s_vec4 && (int64_t)(ti.mb + 1) * (2 * BM) <= p.w_rows &&
+                      (int64_t)(ti.nb + 1) * BN <= p.w_cols;  // the same for every thread of the tile
+  if (inside) epi_scalegrad_fmt<BN, QK>(p, ti, tbase, row_in_tile, half);
+  else epi_scalegrad_edge<BN, QK>(p, ti, tbase, row_in_tile, half);
+}
+
 template <int BN>
 __device__ __forceinline__ void run_scalegrad(const Params& p, const Tile& ti, uint32_t tbase, int row_in_tile,
                                              int half) {
-  {
-    if (p.wq == kQE2M1) epi_scalegrad_fmt<BN, kQE2M1>(p, ti, tbase, row_in_tile, half);
-    else if (p.wq == kQInt4) epi_scalegrad_fmt<BN, kQInt4>(p, ti, tbase, row_in_tile, half);
-    else if (p.wq == kQE4M3) epi_scalegrad_fmt<BN, kQE4M3>(p, ti, tbase, row_in_tile, half);
-    else epi_scalegrad_fmt<BN, kQInt8>(p, ti, tbase, row_in_tile, half);
-  }
+  if (p.wq == kQE2M1) scalegrad_tile<BN, kQE2M1>(p, ti, tbase, row_in_tile, half);
+  else if (p.wq == kQInt4) scalegrad_tile<BN, kQInt4>(p, ti, tbase, row_in_tile, half);
+  else if (p.wq == kQE4M3) scalegrad_tile<BN, kQE4M3>(p, ti, tbase, row_in_tile, half);
+  else scalegrad_tile<BN, kQInt8>(p, ti, tbase, row_in_tile, half);
 }
 
 // ---------------------------------------------------------------------------------- B-operand dequant
@@ -1396,6 +1477,7 @@ Params base_params(const GemmCtx& c) {
 }
 
 inline int pick_bn(int64_t n) { return n % 256 == 0 ? 256 : 128; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // The weight operand of this GEMM is dequantized in shared memory: raw weight [E, rows, cols]
 // with scales s (grid p.wq)
@@ -1438,8 +1520,8 @@ cudaError_t gemm_fc1(const GemmCtx& c, int mode) {
     if (!make_tmap(&ta, c.ws + L.a1, L.d, L.Rmax, L.d, 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, 128)) return cudaErrorInvalidValue;
   }
-  p.n_ntiles = (int)(L.F / 128);
-  p.num_kb = (int)(L.d / bke_of(f8, f8 ? 1 : kAtomsFc1));
+  p.n_ntiles = (int)cdiv(L.F, 128);
+  p.num_kb = (int)cdiv(L.d, bke_of(f8, f8 ? 1 : kAtomsFc1));
   p.b_rows = (int)(2 * L.F);
   p.ld_out2 = L.F;
   p.out3 = at<__nv_bfloat16>(c.ws, L.h);
@@ -1473,8 +1555,9 @@ cudaError_t gemm_fc2(const GemmCtx& c) {
     if (!make_tmap(&ta, c.ws + L.hh, L.F, L.Rmax, L.F, 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, bn / 2)) return cudaErrorInvalidValue;
   }
-  p.n_ntiles = (int)(L.d / bn);
-  p.num_kb = (int)(L.F / bke_of(f8, f8 ? 1 : kAtomsFc2));
+  p.n_ntiles = (int)cdiv(L.d, bn);
+  p.num_kb = (int)cdiv(L.F, bke_of(f8, f8 ? 1 : kAtomsFc2));
+  p.n_total = (int)L.d;
   p.b_rows = (int)L.d;
   CUtensorMap tc;
   if (!make_store_tmap(&tc, c.ws + L.y, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
@@ -1500,8 +1583,9 @@ cudaError_t gemm_dgrad_fc2(const GemmCtx& c) {
   // W2_hat viewed as [E * d (GEMM K), F (GEMM N)], N contiguous
   if (!make_tmap(&tb, c.w2h, L.F, L.E * L.d, L.F, bke_of(false, kAtomsDgrad))) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.F);
-  p.n_ntiles = (int)(L.F / bn);
-  p.num_kb = (int)(L.d / bke_of(false, kAtomsDgrad));
+  p.n_ntiles = (int)cdiv(L.F, bn);
+  p.num_kb = (int)cdiv(L.d, bke_of(false, kAtomsDgrad));
+  p.n_total = (int)L.F;
   p.b_rows = (int)L.d;
   p.aux = at<__nv_bfloat16>(c.ws, L.z1);
   p.ld_aux = 2 * L.F;
@@ -1528,8 +1612,9 @@ cudaError_t gemm_dgrad_fc1(const GemmCtx& c) {
   // W13_hat viewed as [E * 2F (GEMM K), d (GEMM N)], N contiguous
   if (!make_tmap(&tb, c.w13h, L.d, L.E * 2 * L.F, L.d, bke_of(false, kAtomsDgrad))) return cudaErrorInvalidValue;
   const int bn = pick_bn(L.d);
-  p.n_ntiles = (int)(L.d / bn);
-  p.num_kb = (int)(2 * L.F / bke_of(false, kAtomsDgrad));
+  p.n_ntiles = (int)cdiv(L.d, bn);
+  p.num_kb = (int)cdiv(2 * L.F, bke_of(false, kAtomsDgrad));
+  p.n_total = (int)L.d;
   p.b_rows = (int)(2 * L.F);
   CUtensorMap tc;
   if (!make_store_tmap(&tc, c.ws + L.da1, L.d, L.Rmax, L.d)) return cudaErrorInvalidValue;
@@ -1557,8 +1642,9 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   if (!make_tmap(&tb, c.ws + b_off, k_w, L.Rmax, k_w, bke_of(false, kAtomsWgrad))) return cudaErrorInvalidValue;
   const int bn = pick_bn(k_w);
   p.wgrad = 1;
-  p.n_mtiles_w = (int)(m_w / (2 * BM));
-  p.n_ntiles = (int)(k_w / bn);
+  p.n_mtiles_w = (int)cdiv(m_w, 2 * BM);
+  p.n_ntiles = (int)cdiv(k_w, bn);
+  p.s_vec4 = (k_w % 64) == 0;
   p.w = static_cast<const __nv_bfloat16*>(w);
   p.w_vec32 = (reinterpret_cast<uintptr_t>(w) & 31u) == 0;
   p.s = s;
@@ -1573,7 +1659,7 @@ cudaError_t wgrad(const GemmCtx& c, size_t a_off, int64_t m_w, size_t b_off, int
   if (e != cudaSuccess) return e;
   if (row_scaled(c.wq) || (c.wq == kQInt4 && bn == 128)) {
     const int64_t B = c.wq == kQInt4 ? 128 : k_w;  // elements per scale
-    return launch_scale_reduce(p.part, ds, L.E * m_w * (k_w / B), (int)(2 * (B / bn)), accumulate, c.st);
+    return launch_scale_reduce(p.part, ds, L.E * m_w * (k_w / B), (int)(2 * cdiv(B, bn)), accumulate, c.st);
   }
   return cudaSuccess;
 }

@@ -104,9 +104,9 @@ def test_workspace_views_lie_inside_and_do_not_overlap(lib):
 
 
 @pytest.mark.parametrize("bad, status", [
-    (dict(d=200), Q.QAD_ERR_UNSUPPORTED),
-    (dict(d=384), Q.QAD_ERR_UNSUPPORTED),
-    (dict(F=96), Q.QAD_ERR_UNSUPPORTED),
+    (dict(d=200), Q.QAD_ERR_UNSUPPORTED),          # not a multiple of 16
+    (dict(d=272, fmt=1), Q.QAD_ERR_UNSUPPORTED),   # INT4 weights: multiples of 128
+    (dict(F=104), Q.QAD_ERR_UNSUPPORTED),
     (dict(topk=5, E=4), Q.QAD_ERR_UNSUPPORTED),
     (dict(E=2000), Q.QAD_ERR_UNSUPPORTED),
     (dict(fmt=7), Q.QAD_ERR_INVALID_ARG),
@@ -229,3 +229,22 @@ def test_combine_rejects_bad_arguments_before_launch(lib):
     assert lib.qad_moe_combine(None, P, P, P, 4, 2, 32, None) == Q.QAD_ERR_INVALID_ARG
     assert lib.qad_moe_combine(None, None, None, None, 0, 2, 32, None) == Q.QAD_OK
     assert lib.qad_moe_combine(P, P, P, P, -1, 2, 32, None) == Q.QAD_ERR_INVALID_ARG
+
+
+def test_shape_contract(lib):
+    """d and F: multiples of 16, of 128 for the INT4 formats; the E4M3 tensor path and the in-GEMM
+    dequant keep whole tiles (d % 256, F % 128).  Others are refused on the host."""
+    ok = lambda T, d, F, fmt, flags=0: Q.qad_moe_workspace_bytes(Q.shape(T, d, F, 4, 2, fmt, flags)) > 0  # noqa
+    for fmt in (Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8):
+        assert ok(64, 272, 144, fmt) and ok(64, 2880, 2880, fmt) and ok(64, 16, 16, fmt)
+        assert not ok(64, 264, 144, fmt) and not ok(64, 272, 136, fmt)
+    for fmt in (Q.QAD_FMT_INT4_G128, Q.QAD_FMT_W4AFP8):
+        assert ok(64, 384, 384, fmt) and ok(64, 128, 128, fmt)
+        assert not ok(64, 272, 384, fmt) and not ok(64, 384, 144, fmt)
+    assert not ok(64, 272, 144, Q.QAD_FMT_FP8_ROW, Q.QAD_FLAG_NATIVE_FP8)
+    assert ok(64, 512, 256, Q.QAD_FMT_FP8_ROW, Q.QAD_FLAG_NATIVE_FP8)
+    assert not ok(64, 2880, 2880, Q.QAD_FMT_NVFP4, Q.QAD_FLAG_SMEM_DEQUANT)
+    s = Q.shape(64, 264, 144, 4, 2, Q.QAD_FMT_NVFP4)
+    ws = ctypes.c_void_p(1 << 20)
+    assert lib.qad_moe_fwd(ctypes.byref(s), None, None, None, None, None, None, None, None, ws, 1 << 30,
+                           None) == Q.QAD_ERR_UNSUPPORTED

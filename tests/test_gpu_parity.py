@@ -543,3 +543,32 @@ def test_bounded_wait_reports_timeout_and_leaves_the_context_usable():
     torch.cuda.synchronize()
     want = OQ.f64_to_bf16_bits(OQ.fakequant_weight(Q.QAD_FMT_NVFP4, bits(w), synth.to_numpy(s)))
     assert np.array_equal(bits(out), want)
+
+
+# ------------------------------------------------------------------------------ shapes that are not whole tiles
+
+@pytest.mark.parametrize("fmt, d, F", [
+    (Q.QAD_FMT_NVFP4, 272, 144), (Q.QAD_FMT_FP8_ROW, 272, 144), (Q.QAD_FMT_NVFP4A16, 272, 144),
+    (Q.QAD_FMT_W8A8, 272, 144),
+    # INT4 weights need multiples of 128 (group-128 scales along d and F): 384 is not a whole 256 tile
+    (Q.QAD_FMT_INT4_G128, 384, 384), (Q.QAD_FMT_W4AFP8, 384, 384)])
+def test_layer_stagewise_partial_tiles(fmt, d, F):
+    """d and F that are multiples of 16 but not of the GEMM tiles: the last N tiles of fc1
+    (2 x 128 gate/up rows), fc2, both input-gradient GEMMs and the scale-gradient GEMMs are
+    partial, the last K blocks are partial (zero-filled by the tensor maps), the scale-gradient
+    tiles past the weight's rows or columns take the masked path, and nvfp4 scale rows are not
+    16-byte aligned (F / 16 = 9).  Every stage against the oracle, as for whole tiles."""
+    inp = synth.make_inputs(synth.workload("tiny_nvfp4", fmt=fmt, E=5, d=d, F=F, topk=3, T=301), seed=12,
+                            device="cuda")
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    _stagewise(run, host_inputs(inp))
+
+
+def test_layer_stagewise_gpt_oss_like_width():
+    """A layer as wide as GPT-OSS's experts (d = F = 2880: 11.25 tiles of 256 columns), nvfp4."""
+    inp = synth.make_inputs(synth.workload("tiny_nvfp4", E=16, d=2880, F=2880, topk=4, T=1024), seed=13,
+                            device="cuda")
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    _stagewise(run, host_inputs(inp))
