@@ -72,10 +72,16 @@ class Clocks:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # the sampler is running (its first line is in) before the timed region starts, so a
+            # region of a few tens of milliseconds still gets several samples
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 2.0 and self.proc.poll() is None:
+                time.sleep(0.005)
+            self.lines.clear()
         except Exception:
             self.proc = None
         return self
