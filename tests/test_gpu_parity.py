@@ -572,3 +572,40 @@ def test_layer_stagewise_gpt_oss_like_width():
     run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
     assert run.error == 0
     _stagewise(run, host_inputs(inp))
+
+
+# ------------------------------------------------------------------------------ a seeded sweep of small shapes
+
+def _sweep_cases(n=16, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        fmt = int(rng.choice(FMTS))
+        mult = 128 if fmt in (Q.QAD_FMT_INT4_G128, Q.QAD_FMT_W4AFP8) else 16
+        d = int(mult * rng.integers(1, 1024 // mult + 1))
+        F = int(mult * rng.integers(1, 640 // mult + 1))
+        E = int(rng.integers(1, 12))
+        k = int(rng.integers(1, min(E, 6) + 1))
+        T = int(rng.integers(1, 400))
+        flags = int(rng.choice([0, Q.QAD_FLAG_RECOMPUTE]))
+        cases.append((i, fmt, d, F, E, k, T, flags))
+    return cases
+
+
+@pytest.mark.parametrize("case", _sweep_cases(), ids=lambda c: "case%d" % c[0])
+def test_layer_stagewise_random_shapes(case):
+    """Random small layers (seeded): any format, d and F any multiple of 16 (128 for INT4 weights)
+    up to 1024 / 640, 1-11 experts, top-1..6, 1-399 tokens, with and without recompute -- every
+    stage against the oracle."""
+    _, fmt, d, F, E, k, T, flags = case
+    inp = synth.make_inputs(synth.workload("tiny_nvfp4", fmt=fmt, E=E, d=d, F=F, topk=k, T=T), seed=case[0],
+                            device="cuda")
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    _stagewise(run, host_inputs(inp))
+    if flags & Q.QAD_FLAG_RECOMPUTE:  # recompute reuses Y's region for Z1: compare with the stashing run
+        b = Run(inp, flags=Q.QAD_FLAG_RECOMPUTE)
+        assert b.error == 0
+        assert torch.equal(run.out.view(torch.int16), b.out.view(torch.int16))
+        assert torch.equal(run.dx.view(torch.int16), b.dx.view(torch.int16))
+        assert torch.equal(run.ds13, b.ds13) and torch.equal(run.ds2, b.ds2)
