@@ -83,7 +83,9 @@ def exchange(t, send_counts, recv_counts, group):
     if _world(group) == 1:
         return t
     out = t.new_empty((sum(recv_counts),) + tuple(t.shape[1:]))
-    send, recv = t.contiguous(), out
+    # an empty tensor may carry any strides (a zero-row view, or one made from an empty array):
+    # give it a fresh buffer so that the byte view below is valid
+    send, recv = (t.contiguous() if t.shape[0] else t.new_empty(t.shape)), out
     if t.dtype == torch.bfloat16:  # moved as raw bytes (not every backend has bf16 or int16)
         send, recv = send.view(torch.uint8), out.view(torch.uint8)
     dist.all_to_all_single(recv, send, output_split_sizes=list(recv_counts), input_split_sizes=list(send_counts),

@@ -34,11 +34,15 @@ def _weights():
     return synth.make_inputs(cfg, seed=0, device="cpu")
 
 
-def _tokens(rank):
+def _tokens(rank, skew=False):
     import synth
     cfg = synth.workload("tiny_nvfp4", E=E, d=D, F=F, topk=K, T=T)
     inp = synth.make_inputs(cfg, seed=100 + rank, device="cpu", with_weights=False)
-    if rank % 2 == 1:  # an invalid index and a repeated expert: both pairs are dropped
+    if skew:  # every pair to experts 0..E/2-1 (rank 0's with EP = 2): rank 1 receives nothing
+        idx = inp["topk_idx"] % (E // 2)
+        idx[:, 1] = torch.where(idx[:, 1] == idx[:, 0], (idx[:, 0] + 1) % (E // 2), idx[:, 1])
+        inp["topk_idx"] = idx.contiguous()
+    elif rank % 2 == 1:  # an invalid index and a repeated expert: both pairs are dropped
         inp["topk_idx"][3, 1] = E + 5
         inp["topk_idx"][5, 1] = inp["topk_idx"][5, 0]
     return inp
@@ -85,7 +89,7 @@ class OracleExperts:
         return self._bf16(OM.combine(OQ.bf16_to_f64(self._bits(rows)), pw, ro))
 
 
-def _rank_main(rank, world, ep, port, out):
+def _rank_main(rank, world, ep, port, out, skew=False):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -102,7 +106,7 @@ def _rank_main(rank, world, ep, port, out):
                             bits(w["w2"])[lo:lo + e_loc], w["s2"].numpy()[lo:lo + e_loc])
     layer = EP.ExpertParallelMoE(backend, E, group=ep_groups[my_ep],
                                  expert_dp_group=edp_groups[my_pos] if edp > 1 else None)
-    tok = _tokens(rank)
+    tok = _tokens(rank, skew)
     o = layer.forward(tok["x"], tok["topk_idx"], tok["topk_w"])
     dx, dprobs = layer.backward(tok["dout"])
     ds13, ds2 = layer.scale_grads()
@@ -119,12 +123,12 @@ def _rank_main(rank, world, ep, port, out):
     dist.destroy_process_group()
 
 
-def _single_process(ranks):
+def _single_process(ranks, skew=False):
     """The oracle layer on the tokens of `ranks` concatenated, with every expert."""
     from oracle import moe as OM
     w = _weights()
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-    toks = [_tokens(r) for r in ranks]
+    toks = [_tokens(r, skew) for r in ranks]
     x = np.concatenate([bits(t["x"]) for t in toks])
     idx = np.concatenate([t["topk_idx"].numpy() for t in toks]).astype(np.int64)
     p = np.concatenate([t["topk_w"].numpy() for t in toks]).astype(np.float64)
@@ -141,15 +145,18 @@ def _bf16_bits(v):
     return OQ.f64_to_bf16_bits(v)
 
 
-@pytest.mark.parametrize("world, ep", [(2, 2), (4, 4), (4, 2)])
-def test_expert_parallel_exchange_matches_one_process(world, ep):
+@pytest.mark.parametrize("world, ep, skew", [(2, 2, False), (4, 4, False), (4, 2, False), (2, 2, True)],
+                         ids=["ep2", "ep4", "ep2-edp2", "ep2-owner-without-rows"])
+def test_expert_parallel_exchange_matches_one_process(world, ep, skew):
     port = _free_port()
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
-    mp.start_processes(_rank_main, args=(world, ep, port, out), nprocs=world, start_method="spawn", join=True)
+    mp.start_processes(_rank_main, args=(world, ep, port, out, skew), nprocs=world, start_method="spawn", join=True)
     edp = world // ep
     e_loc = E // ep
-    refs = [_single_process(list(range(i * ep, (i + 1) * ep))) for i in range(edp)]
+    refs = [_single_process(list(range(i * ep, (i + 1) * ep)), skew) for i in range(edp)]
+    if skew:
+        assert int(np.sum(out[1]["counts"])) == 0  # rank 1 owned experts nobody was routed to
     for rank in range(world):
         r = out[rank]
         my_ep, my_pos = rank // ep, rank % ep

@@ -58,3 +58,19 @@ def test_single_rank_expert_parallel_layer_equals_the_layer(fmt, name):
     assert torch.equal(dx.view(torch.int16), ref.dx.view(torch.int16))
     assert torch.equal(dprobs, ref.dprobs)
     assert torch.equal(ds13, ref.ds13) and torch.equal(ds2, ref.ds2)
+
+
+def test_cuda_experts_with_no_received_rows():
+    """An owner that receives no pairs (every token routed elsewhere) runs the layer calls on zero
+    rows: empty outputs, and scale gradients of exactly zero for its experts."""
+    inp = synth.make_inputs(synth.workload("tiny_nvfp4"), seed=5, device="cuda")
+    be = EP.CudaExperts(inp["w13"], inp["s13"], inp["w2"], inp["s2"], inp["fmt"])
+    d = inp["d"]
+    y = be.forward(torch.empty((0, d), dtype=torch.bfloat16, device="cuda"),
+                   torch.empty((0,), dtype=torch.int32, device="cuda"))
+    da, dp = be.dgrad(torch.empty((0, d), dtype=torch.bfloat16, device="cuda"),
+                      torch.empty((0,), dtype=torch.float32, device="cuda"))
+    ds13, ds2 = be.scalegrad()
+    torch.cuda.synchronize()
+    assert y.shape == (0, d) and da.shape == (0, d) and dp.shape == (0,)
+    assert torch.count_nonzero(ds13) == 0 and torch.count_nonzero(ds2) == 0
