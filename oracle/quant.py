@@ -20,13 +20,22 @@ The pages never write the quantizer formulas down.  The readings used here:
 * INT8 (w8a8) grid {-128, ..., 127}: round half to even, then clamp; scales amax/127.
 * The weight scale is one fp32 number per block of B consecutive elements along K
   (B = 16 for nvfp4, 128 for INT4 group-128, B = K for fp8 per output row), not
-  itself rounded to a narrower format.
+  itself rounded to a narrower format (formats 0-5; format 6 below rounds it).
 * x = fp32(w / s) is an IEEE fp32 division; the dequantized product q(x)*s is
   rounded to fp32 and then to bf16.  Division of two fp32 values done in fp64 and
   rounded once to fp32 equals the IEEE fp32 quotient (53 >= 2*24 + 2), so these
   steps are bit-exact while everything else runs in fp64.
 * s == 0 (an all-zero block) gives x = +-0 (the sign of w), output +-0 and a zero
   LSQ factor.
+* nvfp4 with deployed scales (format 6): the compressed-tensors NVFP4 layout that the
+  format names map to (walkthrough, section 三) keeps each 16-element block's scale as an E4M3
+  number times an fp32 scale of the whole tensor.  Weights: the learnable fp32 block scale s is
+  used as s_q = fp32(e4m3(fp32(s / g)) * g), with g = fp32(max s / 448) over each expert matrix
+  (the largest block scale becomes E4M3's 448; gate and up share one g, as the fused gate-up
+  matrix of a deployed expert stores one); activations: the dynamic block scale
+  fp32(amax / 6) is rounded the same way under g = fp32(max of the row's block scales / 448).
+  g = 0 (an all-zero matrix or row) gives s_q = 0.  The gradient reaches s straight through the
+  E4M3 rounding; g is treated as a constant.
 * The LSQ straight-through factor (Esser et al., "Learned Step Size
   Quantization", 2019) is phi = q(x) - x inside the CLOSED clip range and the
   violated bound outside it.  No 1/sqrt(N*Qp) gradient scale is applied.
@@ -41,19 +50,23 @@ FMT_FP8_ROW = 2     # fp8 W8A8: E4M3, one scale per output row, activations per-
 FMT_NVFP4A16 = 3    # nvfp4a16: E2M1 weights as nvfp4, activations left in bf16
 FMT_W8A8 = 4        # w8a8: INT8 weights, one scale per output row, activations per-row amax/127
 FMT_W4AFP8 = 5      # w4afp8: INT4 weights as w4a16, activations E4M3 per-row amax/448
-FORMATS = (FMT_NVFP4, FMT_INT4_G128, FMT_FP8_ROW, FMT_NVFP4A16, FMT_W8A8, FMT_W4AFP8)
+FMT_NVFP4_E4M3 = 6  # nvfp4 with deployed scales: E4M3 block scales under an fp32 per-matrix / per-row scale
+FORMATS = (FMT_NVFP4, FMT_INT4_G128, FMT_FP8_ROW, FMT_NVFP4A16, FMT_W8A8, FMT_W4AFP8, FMT_NVFP4_E4M3)
 
 # element grids ("quantizer kinds") and what each format uses for weights / activations
 Q_E2M1, Q_INT4, Q_E4M3, Q_INT8 = "e2m1", "int4", "e4m3", "int8"
+Q_E2M1G = "e2m1g"  # E2M1 elements, E4M3 block scales under an fp32 scale of the row (activations)
 WEIGHT_Q = {FMT_NVFP4: Q_E2M1, FMT_INT4_G128: Q_INT4, FMT_FP8_ROW: Q_E4M3, FMT_NVFP4A16: Q_E2M1,
-            FMT_W8A8: Q_INT8, FMT_W4AFP8: Q_INT4}
+            FMT_W8A8: Q_INT8, FMT_W4AFP8: Q_INT4, FMT_NVFP4_E4M3: Q_E2M1}
 ACT_Q = {FMT_NVFP4: Q_E2M1, FMT_INT4_G128: None, FMT_FP8_ROW: Q_E4M3, FMT_NVFP4A16: None,
-         FMT_W8A8: Q_INT8, FMT_W4AFP8: Q_E4M3}
+         FMT_W8A8: Q_INT8, FMT_W4AFP8: Q_E4M3, FMT_NVFP4_E4M3: Q_E2M1G}
 # per quantizer kind: (lower clip bound, upper clip bound), the divisor that turns an amax
 # into a scale, and the block of consecutive K elements sharing a scale (None = a whole row)
-Q_CLIP = {Q_E2M1: (-6.0, 6.0), Q_INT4: (-8.0, 7.0), Q_E4M3: (-448.0, 448.0), Q_INT8: (-128.0, 127.0)}
-Q_AMAX_DIV = {Q_E2M1: 6.0, Q_INT4: 7.0, Q_E4M3: 448.0, Q_INT8: 127.0}
-Q_BLOCK = {Q_E2M1: 16, Q_INT4: 128, Q_E4M3: None, Q_INT8: None}
+Q_CLIP = {Q_E2M1: (-6.0, 6.0), Q_INT4: (-8.0, 7.0), Q_E4M3: (-448.0, 448.0), Q_INT8: (-128.0, 127.0),
+          Q_E2M1G: (-6.0, 6.0)}
+Q_AMAX_DIV = {Q_E2M1: 6.0, Q_INT4: 7.0, Q_E4M3: 448.0, Q_INT8: 127.0, Q_E2M1G: 6.0}
+Q_BLOCK = {Q_E2M1: 16, Q_INT4: 128, Q_E4M3: None, Q_INT8: None, Q_E2M1G: 16}
+E4M3_MAX = 448.0
 
 CLIP = {f: Q_CLIP[WEIGHT_Q[f]] for f in FORMATS}
 AMAX_DIV = {f: Q_AMAX_DIV[WEIGHT_Q[f]] for f in FORMATS}
@@ -163,7 +176,7 @@ def q_int8(x):
     return np.clip(np.rint(x), -128.0, 127.0)
 
 
-Q_FUNC = {Q_E2M1: q_e2m1, Q_INT4: q_int4, Q_E4M3: q_e4m3, Q_INT8: q_int8}
+Q_FUNC = {Q_E2M1: q_e2m1, Q_INT4: q_int4, Q_E4M3: q_e4m3, Q_INT8: q_int8, Q_E2M1G: q_e2m1}
 
 
 def q_fmt(fmt, x):
@@ -187,11 +200,28 @@ def _dequant(qx, s):
     return round_bf16(round_f32(qx * s))
 
 
+def deploy_scales(scale, axes):
+    """Block scales as deployed NVFP4 holds them: s_q = fp32(e4m3(fp32(s / g)) * g) with
+    g = fp32(max s / 448) over `axes` (a matrix, or a row); g = 0 gives s_q = 0."""
+    s = np.asarray(scale, dtype=np.float64)
+    g = round_f32(s.max(axis=axes, keepdims=True) / E4M3_MAX)
+    safe = np.where(g == 0, 1.0, g)
+    sq = round_f32(q_e4m3(round_f32(s / safe)) * g)
+    return np.where(g == 0, 0.0, sq)
+
+
+def effective_weight_scales(fmt, scale):
+    """The scales the weight quantizer uses: the learnable ones, or their deployed rounding
+    (format 6, one fp32 g per matrix: the last two axes)."""
+    s = np.asarray(scale, dtype=np.float64)
+    return deploy_scales(s, axes=(-2, -1)) if fmt == FMT_NVFP4_E4M3 else s
+
+
 def weight_quotient(fmt, w_bits, scale):
     """x = fp32(W / s) for stacked weights [..., N, K] and scales [..., N, K / B]."""
     w = bf16_to_f64(w_bits)
     K = w.shape[-1]
-    s = np.repeat(np.asarray(scale, dtype=np.float64), weight_block(fmt, K), axis=-1)
+    s = np.repeat(effective_weight_scales(fmt, scale), weight_block(fmt, K), axis=-1)
     return w, s, _quotient(w, s)
 
 
@@ -227,9 +257,10 @@ def fakequant_act_factored(fmt, a):
 def act_scale(fmt, a):
     """Dynamic activation scale per block along the last axis (detached, not learnable).
 
-    E2M1 (nvfp4): one scale per 16 elements, fp32(amax / 6).  E4M3 (fp8, w4afp8): one per
-    row, fp32(amax / 448).  INT8 (w8a8): one per row, fp32(amax / 127).  Returns the scale
-    broadcast to a's shape.
+    E2M1 (nvfp4): one scale per 16 elements, fp32(amax / 6); with deployed scales (format 6)
+    those block scales are then rounded as deploy_scales does, under one g per row.  E4M3 (fp8,
+    w4afp8): one per row, fp32(amax / 448).  INT8 (w8a8): one per row, fp32(amax / 127).
+    Returns the scale broadcast to a's shape.
     """
     a = np.asarray(a, dtype=np.float64)
     kind = ACT_Q[fmt]
@@ -239,7 +270,10 @@ def act_scale(fmt, a):
     if Q_BLOCK[kind] == 16:
         blocks = a.reshape(a.shape[:-1] + (a.shape[-1] // 16, 16))
         amax = np.abs(blocks).max(axis=-1)
-        return np.repeat(round_f32(amax / div), 16, axis=-1)
+        sb = round_f32(amax / div)
+        if kind == Q_E2M1G:
+            sb = deploy_scales(sb, axes=-1)
+        return np.repeat(sb, 16, axis=-1)
     amax = np.abs(a).max(axis=-1, keepdims=True)
     return np.broadcast_to(round_f32(amax / div), a.shape)
 

@@ -14,7 +14,7 @@ Workloads, named by what they are:
   large_nvfp4           E=256, d=4096, F=1536, top-8, 32768 tokens, nvfp4, 0.1% outliers
 
 Any workload can be run in another format with workload(name, fmt=...): 3 nvfp4a16,
-4 w8a8, 5 w4afp8.
+4 w8a8, 5 w4afp8, 6 nvfp4 with deployed (E4M3-rounded) block scales.
 
 The MoE-layer shapes follow the Qwen3-MoE model family that the pages support
 ("MCoreQAD Backend", Support Matrix) and its example run (seq_len 2048, micro-batch
@@ -24,7 +24,7 @@ import math
 
 import torch
 
-FMT_NVFP4, FMT_INT4_G128, FMT_FP8_ROW, FMT_NVFP4A16, FMT_W8A8, FMT_W4AFP8 = 0, 1, 2, 3, 4, 5
+FMT_NVFP4, FMT_INT4_G128, FMT_FP8_ROW, FMT_NVFP4A16, FMT_W8A8, FMT_W4AFP8, FMT_NVFP4_E4M3 = 0, 1, 2, 3, 4, 5, 6
 
 WORKLOADS = {
     "tiny_nvfp4": dict(E=4, d=256, F=128, topk=2, T=512, fmt=FMT_NVFP4, routing="uniform", outliers=0.0),
@@ -40,9 +40,9 @@ WORKLOADS = {
 
 # elements per weight scale along K (absent: one per row), and the divisor that turns a
 # block amax into a scale
-_BLOCK = {FMT_NVFP4: 16, FMT_INT4_G128: 128, FMT_NVFP4A16: 16, FMT_W4AFP8: 128}
+_BLOCK = {FMT_NVFP4: 16, FMT_INT4_G128: 128, FMT_NVFP4A16: 16, FMT_W4AFP8: 128, FMT_NVFP4_E4M3: 16}
 _QMAX = {FMT_NVFP4: 6.0, FMT_INT4_G128: 7.0, FMT_FP8_ROW: 448.0, FMT_NVFP4A16: 6.0, FMT_W8A8: 127.0,
-         FMT_W4AFP8: 7.0}
+         FMT_W4AFP8: 7.0, FMT_NVFP4_E4M3: 6.0}
 
 
 def workload(name, **override):

@@ -205,7 +205,8 @@ def test_fakequant_outputs_lie_on_scaled_grid(fmt):
     bits, s = _weights(fmt, N=4, K=128)
     what = Q.fakequant_weight(fmt, bits, s)
     K = bits.shape[-1]
-    sf = np.repeat(s.astype(np.float64), Q.weight_block(fmt, K), axis=-1)
+    # the scales the quantizer uses (format 6: the deployed E4M3 rounding of s)
+    sf = np.repeat(Q.effective_weight_scales(fmt, s), Q.weight_block(fmt, K), axis=-1)
     grid = _grid(fmt)
     # every output equals bf16(fp32(g * s)) for some g of the grid (enumerated, not computed by q)
     cand = Q.round_bf16(Q.round_f32(grid[None, :] * sf.reshape(-1)[:, None]))
@@ -263,6 +264,13 @@ def test_scale_grad_zero_for_weights_on_grid_points(fmt):
     rng = np.random.default_rng(10)
     grid = _grid(fmt)
     s = 2.0 ** rng.integers(-8, -2, (E, N, K // B))        # powers of two: g * s exact in bf16
+    if fmt == Q.FMT_NVFP4_E4M3:
+        # deployed scales: with each matrix's largest scale 448 * 2^-12 the per-matrix fp32
+        # scale is 2^-12 exactly and every power of two in [2^-8, 2^-4] is an E4M3 number
+        # times it, so the deployed rounding leaves s unchanged (448 * 2^-12 * grid is exact in bf16)
+        s = 2.0 ** rng.integers(-8, -3, (E, N, K // B))
+        s[:, 0, 0] = 448.0 * 2.0 ** -12
+        assert np.array_equal(Q.effective_weight_scales(fmt, s), s)
     g = rng.choice(grid, (E, N, K))
     lo, hi = Q.CLIP[fmt]
     g[0, 0, 0], g[0, 0, 1] = lo, hi                         # the clip bounds themselves (closed range)
@@ -326,7 +334,16 @@ def test_scale_grad_matches_autograd_of_ste_definition(fmt):
     dw = rng.standard_normal(bits.shape)
     w_t = torch.from_numpy(Q.bf16_to_f64(bits))
     s_t = torch.from_numpy(s.astype(np.float64)).requires_grad_(True)
-    s_full = s_t.repeat_interleave(B, dim=-1)
+    s_used = s_t
+    if fmt == Q.FMT_NVFP4_E4M3:
+        # the deployed rounding of the scale, passed straight through: the forward sees
+        # s_q = fp32(e4m3(fp32(s / g)) * g), computed here with torch's float8_e4m3fn cast, and
+        # the gradient reaches s unchanged (g a constant)
+        s32 = torch.from_numpy(s.astype(np.float32))
+        g = (s32.amax(dim=(-2, -1), keepdim=True) / 448.0)
+        sq = ((s32 / g).to(torch.float8_e4m3fn).float() * g).double()
+        s_used = s_t + (sq - s_t).detach()
+    s_full = s_used.repeat_interleave(B, dim=-1)
     safe = torch.where(s_full == 0, torch.ones_like(s_full), s_full)
     what = _ste_fakequant_torch(fmt, w_t, safe)
     what = torch.where(s_full == 0, torch.zeros_like(what), what)
@@ -632,3 +649,96 @@ def test_quotient_is_the_correctly_rounded_fp32_value():
                 assert int(x32.view(np.uint32)) % 2 == 0, (a, b, x)
         if q == 0:
             assert np.signbit(x) == np.signbit(a)
+
+
+# ------------------------------------------------------------------------------ deployed nvfp4 scales
+
+def _deployed_rows():
+    rows = _rows("nvfp4_deployed_scales.txt")
+    return [tuple(float.fromhex(c) for c in r) for r in rows]
+
+
+def test_deployed_scales_golden_weights():
+    rows = _deployed_rows()
+    v = np.array([r[0] for r in rows])
+    want = np.array([r[1] for r in rows]) * 2.0 ** -10
+    # one matrix [2, n] holding the blocks' scales (the 448 row fixes g = 2^-10), and the same
+    # blocks split over two matrices of one stack: each matrix gets its own g
+    s = np.stack([v, v[::-1]]) * 2.0 ** -10
+    assert np.array_equal(Q.deploy_scales(s, axes=(-2, -1)), np.stack([want, want[::-1]]))
+    stack = np.stack([s, 2.0 * s])[:, :, :]
+    got = Q.effective_weight_scales(Q.FMT_NVFP4_E4M3, stack)
+    assert np.array_equal(got[0], np.stack([want, want[::-1]]))
+    assert np.array_equal(got[1], 2.0 * np.stack([want, want[::-1]]))
+    # other formats use the learnable scales as they are
+    assert np.array_equal(Q.effective_weight_scales(Q.FMT_NVFP4, stack), stack)
+
+
+def test_deployed_scales_golden_activations():
+    rows = _deployed_rows()
+    n = len(rows)
+    rng = np.random.default_rng(30)
+    a = np.zeros((2, 16 * n))
+    for b, (v, _, _) in enumerate(rows):
+        amax = 6.0 * v * 2.0 ** -10
+        blk = rng.uniform(-1, 1, 16) * amax * 0.9
+        blk[(5 * b) % 16] = amax if b % 2 == 0 else -amax
+        a[0, 16 * b:16 * b + 16] = blk
+    a = Q.round_bf16(a)
+    a[1] = a[0, ::-1]                                   # the same blocks, reversed: same scales
+    assert np.array_equal(np.abs(a[0]).reshape(n, 16).max(-1), np.array([6.0 * r[0] * 2.0 ** -10 for r in rows]))
+    s_a = Q.act_scale(Q.FMT_NVFP4_E4M3, a)
+    want = np.repeat(np.array([r[1] for r in rows]) * 2.0 ** -10, 16)
+    assert np.array_equal(s_a[0], want)
+    assert np.array_equal(s_a[1], want[::-1])
+    ah = Q.fakequant_act(Q.FMT_NVFP4_E4M3, a)
+    top = np.abs(ah[0]).reshape(n, 16).max(-1)
+    assert np.array_equal(top, np.array([r[2] for r in rows]) * 2.0 ** -10)
+    # a block whose scale underflows E4M3 comes back as zeros
+    for b, (v, e, _) in enumerate(rows):
+        if e == 0:
+            assert np.all(ah[0, 16 * b:16 * b + 16] == 0)
+
+
+def test_deploy_scales_bruteforce_and_torch_cast():
+    rng = np.random.default_rng(31)
+    E, N, nb = 3, 24, 8
+    s = (rng.lognormal(-5, 1.5, (E, N, nb))).astype(np.float32)
+    s[0, 0, :3] = 0.0                                   # zero blocks
+    s[1] = s[1] * np.float32(1e-30)                     # tiny scales: g far below 1
+    s[2, 5, 2] = s[2].max() * np.float32(3.0)           # one outlier block: most others go subnormal
+    got = Q.deploy_scales(s.astype(np.float64), axes=(-2, -1))
+    # torch: the same two fp32 steps with the float8_e4m3fn cast
+    st = torch.from_numpy(s)
+    g = st.amax(dim=(-2, -1), keepdim=True) / 448.0
+    want_t = ((st / g).to(torch.float8_e4m3fn).float() * g).double().numpy()
+    assert np.array_equal(got, want_t)
+    # brute force: s_q / g is the E4M3 value nearest fp32(s / g), ties to the even mantissa
+    g64 = g.double().numpy()
+    ratio = (st / g).double().numpy()
+    grid, even = _e4m3_positive_grid()
+    near = _brute_nearest(ratio.reshape(-1), grid, even).reshape(ratio.shape)
+    assert np.array_equal(got, Q.round_f32(near * g64))
+    # the largest scale of each matrix is kept to fp32 accuracy; zeros stay zero
+    for e in range(E):
+        i = np.unravel_index(np.argmax(s[e]), s[e].shape)
+        assert abs(got[e][i] - s[e][i]) <= 2.0 ** -22 * s[e][i]
+    assert np.all(got[0, 0, :3] == 0)
+    # rounding is monotone in s within a matrix
+    for e in range(E):
+        o = np.argsort(s[e].reshape(-1), kind="stable")
+        assert np.all(np.diff(got[e].reshape(-1)[o]) >= 0)
+
+
+def test_deploy_scales_all_zero_matrix_and_row():
+    z = np.zeros((2, 4, 3))
+    z[1, 2, 1] = 0.25
+    got = Q.deploy_scales(z, axes=(-2, -1))
+    assert np.all(got[0] == 0)
+    assert got[1, 2, 1] == 0.25 and np.count_nonzero(got[1]) == 1
+    a = np.zeros((2, 32))
+    a[1, 3] = 1.5
+    s_a = Q.act_scale(Q.FMT_NVFP4_E4M3, a)
+    assert np.all(s_a[0] == 0) and np.all(s_a[1, 16:] == 0)
+    assert np.all(s_a[1, :16] == Q.round_f32(Q.round_f32(Q.round_f32(1.5 / 6.0) / 448.0) * 448.0))
+    assert np.array_equal(Q.fakequant_act(Q.FMT_NVFP4_E4M3, a)[1, 3], 1.5)
