@@ -30,7 +30,7 @@ The pages never write the quantizer formulas down.  The readings used here:
 * nvfp4 with deployed scales (format 6): the compressed-tensors NVFP4 layout that the
   format names map to (walkthrough, section 三) keeps each 16-element block's scale as an E4M3
   number times an fp32 scale of the whole tensor.  Weights: the learnable fp32 block scale s is
-  used as s_q = fp32(e4m3(fp32(s / g)) * g), with g = fp32(max s / 448) over each expert matrix
+  used as s_q = fp32(e4m3(fp32(s / g)) * g), with g = fp32(max |s| / 448) over each expert matrix
   (the largest block scale becomes E4M3's 448; gate and up share one g, as the fused gate-up
   matrix of a deployed expert stores one); activations: the dynamic block scale
   fp32(amax / 6) is rounded the same way under g = fp32(max of the row's block scales / 448).
@@ -202,9 +202,11 @@ def _dequant(qx, s):
 
 def deploy_scales(scale, axes):
     """Block scales as deployed NVFP4 holds them: s_q = fp32(e4m3(fp32(s / g)) * g) with
-    g = fp32(max s / 448) over `axes` (a matrix, or a row); g = 0 gives s_q = 0."""
+    g = fp32(max |s| / 448) over `axes` (a matrix, or a row); g = 0 gives s_q = 0.  (The
+    magnitude: a learnable scale is not constrained to stay positive, and a negative one is
+    rounded as its magnitude with the sign kept.)"""
     s = np.asarray(scale, dtype=np.float64)
-    g = round_f32(s.max(axis=axes, keepdims=True) / E4M3_MAX)
+    g = round_f32(np.abs(s).max(axis=axes, keepdims=True) / E4M3_MAX)
     safe = np.where(g == 0, 1.0, g)
     sq = round_f32(q_e4m3(round_f32(s / safe)) * g)
     return np.where(g == 0, 0.0, sq)

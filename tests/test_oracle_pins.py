@@ -340,7 +340,7 @@ def test_scale_grad_matches_autograd_of_ste_definition(fmt):
         # s_q = fp32(e4m3(fp32(s / g)) * g), computed here with torch's float8_e4m3fn cast, and
         # the gradient reaches s unchanged (g a constant)
         s32 = torch.from_numpy(s.astype(np.float32))
-        g = (s32.amax(dim=(-2, -1), keepdim=True) / 448.0)
+        g = (s32.abs().amax(dim=(-2, -1), keepdim=True) / 448.0)
         sq = ((s32 / g).to(torch.float8_e4m3fn).float() * g).double()
         s_used = s_t + (sq - s_t).detach()
     s_full = s_used.repeat_interleave(B, dim=-1)
@@ -707,23 +707,26 @@ def test_deploy_scales_bruteforce_and_torch_cast():
     s[0, 0, :3] = 0.0                                   # zero blocks
     s[1] = s[1] * np.float32(1e-30)                     # tiny scales: g far below 1
     s[2, 5, 2] = s[2].max() * np.float32(3.0)           # one outlier block: most others go subnormal
+    s[2, 7, :4] *= np.float32(-1.0)                     # negative scales: rounded as their magnitude
     got = Q.deploy_scales(s.astype(np.float64), axes=(-2, -1))
     # torch: the same two fp32 steps with the float8_e4m3fn cast
     st = torch.from_numpy(s)
-    g = st.amax(dim=(-2, -1), keepdim=True) / 448.0
+    g = st.abs().amax(dim=(-2, -1), keepdim=True) / 448.0
     want_t = ((st / g).to(torch.float8_e4m3fn).float() * g).double().numpy()
     assert np.array_equal(got, want_t)
     # brute force: s_q / g is the E4M3 value nearest fp32(s / g), ties to the even mantissa
     g64 = g.double().numpy()
     ratio = (st / g).double().numpy()
     grid, even = _e4m3_positive_grid()
-    near = _brute_nearest(ratio.reshape(-1), grid, even).reshape(ratio.shape)
+    near = _brute_nearest(np.abs(ratio).reshape(-1), grid, even).reshape(ratio.shape) * np.sign(ratio)
     assert np.array_equal(got, Q.round_f32(near * g64))
     # the largest scale of each matrix is kept to fp32 accuracy; zeros stay zero
     for e in range(E):
-        i = np.unravel_index(np.argmax(s[e]), s[e].shape)
+        i = np.unravel_index(np.argmax(np.abs(s[e])), s[e].shape)
         assert abs(got[e][i] - s[e][i]) <= 2.0 ** -22 * s[e][i]
     assert np.all(got[0, 0, :3] == 0)
+    # the negative ones are the magnitude's rounding, negated
+    assert np.all(got[2, 7, :4] < 0)
     # rounding is monotone in s within a matrix
     for e in range(E):
         o = np.argsort(s[e].reshape(-1), kind="stable")
