@@ -38,7 +38,7 @@ import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "qwen3_30b_a3b_nvfp4"
 METRIC = "MoE-layer fwd+bwd tokens/s (nvfp4, 1 GB300); % HBM / tensor-core roofline"
-FMT_NAME = {0: "nvfp4", 1: "w4a16", 2: "fp8", 3: "nvfp4a16", 4: "w8a8", 5: "w4afp8"}
+FMT_NAME = {0: "nvfp4", 1: "w4a16", 2: "fp8", 3: "nvfp4a16", 4: "w8a8", 5: "w4afp8", 6: "nvfp4_e4m3_scales"}
 
 
 def _dist():

@@ -71,7 +71,18 @@ typedef enum {
   QAD_FMT_NVFP4A16 = 3,  /* nvfp4a16: E2M1 weights as nvfp4; activations stay bf16 */
   QAD_FMT_W8A8 = 4,      /* w8a8: INT8 {-128..127} weights, one fp32 scale per output row;
                             activations INT8 with dynamic per-row scale amax/127 */
-  QAD_FMT_W4AFP8 = 5     /* w4afp8: INT4 weights as w4a16; activations E4M3 per row, amax/448 */
+  QAD_FMT_W4AFP8 = 5,    /* w4afp8: INT4 weights as w4a16; activations E4M3 per row, amax/448 */
+  QAD_FMT_NVFP4_E4M3 = 6 /* nvfp4 with deployed block scales: as nvfp4, but every block scale is
+                            used as the compressed-tensors NVFP4 layout stores it (AngelSlim
+                            mcore_qad walkthrough, section 三: the format names map to the
+                            deployment side's layout), an E4M3 number times one fp32 scale g of
+                            the tensor: s_q = fp32(e4m3(fp32(s / g)) * g) (round to nearest even,
+                            saturating).  Weights: g = fp32(max |s| / 448) over each expert's w13
+                            (gate and up share it) and each expert's w2, see
+                            qad_nvfp4_deploy_scales; the scale gradient reaches s straight through
+                            the rounding.  Activations: the dynamic per-16 scale fp32(amax / 6) is
+                            rounded the same way with g = fp32(max over the row's blocks / 448)
+                            per row.  A block whose s_q is 0 comes out as signed zeros. */
 } qad_fmt;
 
 /* Bits of the device error word */
@@ -140,9 +151,22 @@ typedef struct {
  *   w_hat  bf16 [E, N, K] (written; may not overlap w)
  * Requires K % 16 == 0 (K % 128 == 0 for the INT4 formats), scales >= 0 and finite.
  * Output is bit-exact: w_hat = bf16(fp32(q(fp32(w / s)) * s)).
+ * QAD_FMT_NVFP4_E4M3 returns QAD_ERR_UNSUPPORTED: round the scales with
+ * qad_nvfp4_deploy_scales and call this with QAD_FMT_NVFP4 and the rounded scales (the same
+ * arithmetic, which is what the layer calls do).
  */
 int qad_fakequant_fwd(int fmt, const void* w, const float* scale, void* w_hat,
                       int64_t E, int64_t N, int64_t K, qad_stream_t stream);
+
+/*
+ * The block scales of QAD_FMT_NVFP4_E4M3 weights as deployed NVFP4 stores them (AngelSlim
+ * mcore_qad walkthrough, section 三): for each of the n_mat matrices of per_mat consecutive
+ * scales, g = fp32(max |s| / 448) and s_q[i] = fp32(e4m3(fp32(s[i] / g)) * g) (E4M3 "fn":
+ * round to nearest even, saturating at 448); g = 0 (an all-zero matrix) gives s_q = 0.
+ *   s    fp32 [n_mat, per_mat] (read)          s_q fp32 [n_mat, per_mat] (written; may be s)
+ * Requires per_mat % 4 == 0 and 16-byte aligned pointers; n_mat == 0 does nothing.
+ */
+int qad_nvfp4_deploy_scales(const float* s, float* s_q, int64_t n_mat, int64_t per_mat, qad_stream_t stream);
 
 /* Bytes of workspace the three layer calls need for this shape; 0 if the shape is
  * not supported.  Host-only, no CUDA call. */
@@ -155,7 +179,9 @@ size_t qad_moe_workspace_bytes(const qad_moe_shape* s);
  *   w2       bf16 [E, d, F]     s2  fp32 [E, d, F / B]
  *   out      bf16 [T, d] (written)
  *   ws       workspace (256-byte aligned) of ws_bytes >= qad_moe_workspace_bytes(s); it keeps what the
- *            backward calls need (routing maps, fake-quantized weights, activations).
+ *            backward calls need (routing maps, fake-quantized weights, activations, and for
+ *            QAD_FMT_NVFP4_E4M3 the deployed weight scales, which the backward calls use in place
+ *            of s13 / s2 -- they must still be passed).
  * Supported: d and F multiples of 16 (multiples of 128 for the INT4 formats, whose group-128
  * scales run along both; d % 256 == 0 and F % 128 == 0 with QAD_FLAG_NATIVE_FP8 or
  * QAD_FLAG_SMEM_DEQUANT), 1 <= topk <= min(E, 32), 1 <= E <= 1024, T * topk < 2^31; other shapes
@@ -242,7 +268,10 @@ enum {
   QAD_VIEW_H_CODES = 20,   /* uint8 [Rmax, F] */
   QAD_VIEW_A_SCALE = 21,   /* fp32 [T]: activation scale fp32(row amax / 448) of each token */
   QAD_VIEW_H_SCALE = 22,   /* fp32 [Rmax]: the same for each row of H */
-  QAD_VIEW_COUNT = 23
+  /* QAD_FMT_NVFP4_E4M3 only (count 0 otherwise): the deployed weight scales the forward made */
+  QAD_VIEW_S13_DEPLOYED = 23, /* fp32 [E, 2F, d / 16] */
+  QAD_VIEW_S2_DEPLOYED = 24,  /* fp32 [E, d, F / 16] */
+  QAD_VIEW_COUNT = 25
 };
 int qad_moe_debug_view(const qad_moe_shape* s, int which, size_t* byte_offset, int64_t* numel);
 
@@ -258,7 +287,8 @@ enum {
   QAD_K_GEMM_DGRAD_FC2 = 8, QAD_K_GEMM_DGRAD_FC1 = 9, QAD_K_DX_COMBINE = 10,
   QAD_K_GEMM_WGRAD_FC2 = 11, QAD_K_GEMM_WGRAD_FC1 = 12, QAD_K_SCALE_REDUCE = 13,
   QAD_K_GEMM_FC1_RECOMPUTE = 14, /* QAD_FLAG_RECOMPUTE: fc1 again in the dgrad call (Z1 only) */
-  QAD_K_COUNT = 15
+  QAD_K_DEPLOY_SCALES = 15,      /* QAD_FMT_NVFP4_E4M3: the deployed weight scales */
+  QAD_K_COUNT = 16
 };
 int qad_profile_enable(int on);
 int qad_profile_reset(void);

@@ -17,19 +17,21 @@ QAD_OK, QAD_ERR_INVALID_ARG, QAD_ERR_UNSUPPORTED, QAD_ERR_WORKSPACE, QAD_ERR_CUD
 QAD_ERR_SCRATCH_LIMIT = -6
 QAD_NOALLOC_MAX_EXPERTS, QAD_NOALLOC_MAX_PAIRS = 256, 262144
 QAD_FMT_NVFP4, QAD_FMT_INT4_G128, QAD_FMT_FP8_ROW, QAD_FMT_NVFP4A16, QAD_FMT_W8A8, QAD_FMT_W4AFP8 = range(6)
+QAD_FMT_NVFP4_E4M3 = 6
 QAD_DEV_BAD_INDEX, QAD_DEV_DUP_INDEX, QAD_DEV_TIMEOUT = 1, 2, 4
 QAD_FLAG_STASH_H, QAD_FLAG_NO_QUANT, QAD_FLAG_RECOMPUTE, QAD_FLAG_NATIVE_FP8 = 1, 2, 4, 8
 QAD_FLAG_SMEM_DEQUANT, QAD_FLAG_DEQUANT_DUMP = 16, 32
 VIEWS = ["HEADER", "OFFSETS", "COUNTS", "ROW_TOKEN", "ROW_SLOT", "ROW_OF", "W13_HAT", "W2_HAT", "A1", "Z1", "H",
          "H_HAT", "Y", "DY", "DZ1", "DA1", "XQ", "W13_CODES", "W2_CODES", "A1_CODES", "H_CODES", "A_SCALE",
-         "H_SCALE"]
+         "H_SCALE", "S13_DEPLOYED", "S2_DEPLOYED"]
 VIEW = {n: i for i, n in enumerate(VIEWS)}
-KERNELS = 15
+KERNELS = 16
 
 EXPORTS = ["qad_fakequant_fwd", "qad_moe_workspace_bytes", "qad_moe_fwd", "qad_moe_bwd_dgrad",
            "qad_moe_bwd_scalegrad", "qad_check_device_error", "qad_status_string", "qad_moe_debug_view",
            "qad_profile_enable", "qad_profile_reset", "qad_profile_read", "qad_kernel_name", "qad_launch_count",
-           "qad_debug_quotient", "qad_route_permute_noalloc", "qad_debug_wait_timeout", "qad_moe_combine"]
+           "qad_debug_quotient", "qad_route_permute_noalloc", "qad_debug_wait_timeout", "qad_moe_combine",
+           "qad_nvfp4_deploy_scales"]
 
 
 class QADError(RuntimeError):
@@ -80,6 +82,7 @@ def lib():
             "qad_route_permute_noalloc": (ctypes.c_int, [_P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P,
                                                          _P, _P, _P]),
             "qad_moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int32, _I64, _P]),
+            "qad_nvfp4_deploy_scales": (ctypes.c_int, [_P, _P, _I64, _I64, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -118,6 +121,11 @@ def shape(T, d, F, E, topk, fmt, flags=0):
 def qad_fakequant_fwd(fmt, w, scale, w_hat, E, N, K, stream=None):
     return _check(lib().qad_fakequant_fwd(int(fmt), _ptr(w), _ptr(scale), _ptr(w_hat), int(E), int(N), int(K),
                                           _stream(stream)), "qad_fakequant_fwd")
+
+
+def qad_nvfp4_deploy_scales(s, s_q, n_mat, per_mat, stream=None):
+    return _check(lib().qad_nvfp4_deploy_scales(_ptr(s), _ptr(s_q), int(n_mat), int(per_mat), _stream(stream)),
+                  "qad_nvfp4_deploy_scales")
 
 
 def qad_moe_workspace_bytes(s):

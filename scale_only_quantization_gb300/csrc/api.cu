@@ -90,7 +90,7 @@ void prof_end(int id, cudaStream_t st) {
 
 int layout_of(const qad_moe_shape& s, Layout* L) {
   if (s.T < 0 || s.d <= 0 || s.F <= 0 || s.E <= 0 || s.topk <= 0) return QAD_ERR_INVALID_ARG;
-  if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_W4AFP8) return QAD_ERR_INVALID_ARG;
+  if (s.fmt < QAD_FMT_NVFP4 || s.fmt > QAD_FMT_NVFP4_E4M3) return QAD_ERR_INVALID_ARG;
   if (s.reserved != 0 || (s.flags & ~(QAD_FLAG_STASH_H | QAD_FLAG_NO_QUANT | QAD_FLAG_RECOMPUTE |
                                        QAD_FLAG_NATIVE_FP8 | QAD_FLAG_SMEM_DEQUANT | QAD_FLAG_DEQUANT_DUMP)))
     return QAD_ERR_INVALID_ARG;
@@ -157,6 +157,9 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
     L->sa_tok = take(4 * (size_t)(s.T > 0 ? s.T : 1));
     L->sh_row = take(4 * (size_t)Rmax);
   }
+  L->deployed = s.fmt == QAD_FMT_NVFP4_E4M3;
+  L->s13q = L->deployed ? take(4 * (size_t)(E * 2 * F * (d / 16))) : 0;
+  L->s2q = L->deployed ? take(4 * (size_t)(E * d * (F / 16))) : 0;
   L->total = o;
   return QAD_OK;
 }
@@ -232,12 +235,21 @@ const char* qad_status_string(int status) {
 
 int qad_fakequant_fwd(int fmt, const void* w, const float* scale, void* w_hat, int64_t E, int64_t N, int64_t K,
                       qad_stream_t stream) {
-  if (fmt < QAD_FMT_NVFP4 || fmt > QAD_FMT_W4AFP8) return QAD_ERR_INVALID_ARG;
+  if (fmt < QAD_FMT_NVFP4 || fmt > QAD_FMT_NVFP4_E4M3) return QAD_ERR_INVALID_ARG;
+  if (fmt == QAD_FMT_NVFP4_E4M3) return QAD_ERR_UNSUPPORTED;  // deploy the scales, then QAD_FMT_NVFP4
   if (E < 0 || N < 0 || K <= 0) return QAD_ERR_INVALID_ARG;
   if (K % 16 || (weight_kind(fmt) == kQInt4 && K % 128)) return QAD_ERR_UNSUPPORTED;
   if (E * N == 0) return QAD_OK;
   if (!ok_ptr(w) || !ok_ptr(scale) || !ok_ptr(w_hat)) return QAD_ERR_INVALID_ARG;
   return to_status(launch_fakequant(fmt, w, scale, w_hat, E * N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qad_nvfp4_deploy_scales(const float* s, float* s_q, int64_t n_mat, int64_t per_mat, qad_stream_t stream) {
+  if (n_mat < 0 || per_mat <= 0 || per_mat % 4 || n_mat > 0x7fffffff) return QAD_ERR_INVALID_ARG;
+  if (n_mat == 0) return QAD_OK;
+  if (!ok_ptr(s) || !ok_ptr(s_q)) return QAD_ERR_INVALID_ARG;
+  return to_status(launch_deploy_scales(s, s_q, n_mat, per_mat, nullptr, nullptr, 0, 0,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t qad_moe_workspace_bytes(const qad_moe_shape* s) {
@@ -292,8 +304,13 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
   const bool f8 = L.native_fp8;  // E4M3 codes for the fp8 tensor path as well
   const int32_t* row_token = reinterpret_cast<const int32_t*>(wsb + L.row_token);
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
-  c.s13 = s13;
-  c.s2 = s2;
+  // deployed nvfp4: every consumer of the weight scales (the fake-quant pass or the in-GEMM
+  // dequant here, the dequant and the LSQ epilogues in the backward calls) reads s_q
+  const bool deploy = L.deployed && !no_quant;
+  const float* s13u = deploy ? reinterpret_cast<const float*>(wsb + L.s13q) : s13;
+  const float* s2u = deploy ? reinterpret_cast<const float*>(wsb + L.s2q) : s2;
+  c.s13 = s13u;
+  c.s2 = s2u;
   {
     // routing and the activation gather on the side stream, the weight fake-quant on the
     // caller's: the latency-bound routing hides under the fake-quant, and the two HBM-bound
@@ -308,15 +325,18 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
                                   row_token, L.T, (int)L.k, L.d, rpad, ss->s, f8 ? wsb + L.a1q : nullptr,
                                   f8 ? reinterpret_cast<float*>(wsb + L.sa_tok) : nullptr));
     QAD_TRY(cudaEventRecord(ss->join, ss->s));
+    if (deploy)
+      QAD_TRY(launch_deploy_scales(s13, const_cast<float*>(s13u), L.E, 2 * L.F * (L.d / 16), s2,
+                                   const_cast<float*>(s2u), L.E, L.d * (L.F / 16), st));
     if (!no_quant && !c.dq) {  // with QAD_FLAG_SMEM_DEQUANT the GEMMs fake-quantize the weights themselves
-      QAD_TRY(launch_fakequant(fmt, w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
-      QAD_TRY(launch_fakequant(fmt, w2, s2, wsb + L.w2h, L.E * L.d, L.F, st, f8 ? wsb + L.w2q : nullptr));
+      QAD_TRY(launch_fakequant(fmt, w13, s13u, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
+      QAD_TRY(launch_fakequant(fmt, w2, s2u, wsb + L.w2h, L.E * L.d, L.F, st, f8 ? wsb + L.w2q : nullptr));
     }
     QAD_TRY(cudaStreamWaitEvent(st, ss->join, 0));
   }
   QAD_TRY(gemm_prepare(c));
   QAD_TRY(gemm_fc1(c, (s->flags & QAD_FLAG_RECOMPUTE) ? kFc1NoZ1 : kFc1Full));
-  if (row_scaled(c.aq))
+  if (act_needs_row(c.aq))
     QAD_TRY(launch_act_quant_rows(c.aq, wsb + L.h, wsb + L.hh, L.Rmax, L.F, rpad, st, f8 ? wsb + L.hq : nullptr,
                                   f8 ? reinterpret_cast<float*>(wsb + L.sh_row) : nullptr));
   QAD_TRY(gemm_fc2(c));
@@ -342,8 +362,9 @@ int qad_moe_bwd_dgrad(const qad_moe_shape* s, const void* dout, const float* top
                             reinterpret_cast<const int32_t*>(wsb + L.row_token), wsb + L.y, wsb + L.dy, dprobs, L.T,
                             (int)L.k, L.d, rpad, st));
   GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
-  c.s13 = s13;
-  c.s2 = s2;
+  const bool deploy = L.deployed && !(s->flags & QAD_FLAG_NO_QUANT);  // the forward's s_q
+  c.s13 = deploy ? reinterpret_cast<const float*>(wsb + L.s13q) : s13;
+  c.s2 = deploy ? reinterpret_cast<const float*>(wsb + L.s2q) : s2;
   if (s->flags & QAD_FLAG_RECOMPUTE) QAD_TRY(gemm_fc1(c, kFc1Z1Only));  // Z1 again, after Y's last use
   QAD_TRY(gemm_dgrad_fc2(c));
   QAD_TRY(gemm_dgrad_fc1(c));
@@ -361,9 +382,14 @@ int qad_moe_bwd_scalegrad(const qad_moe_shape* s, const void* w13, const float* 
     return QAD_ERR_INVALID_ARG;
   if (s->flags & QAD_FLAG_NO_QUANT) return QAD_ERR_INVALID_ARG;  // no scales without quantizers
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  GemmCtx c = gemm_ctx(L, static_cast<uint8_t*>(ws), *s, w13, w2, st);
-  QAD_TRY(gemm_wgrad_fc2(c, w2, s2, ds2, accumulate ? 1 : 0));
-  QAD_TRY(gemm_wgrad_fc1(c, w13, s13, ds13, accumulate ? 1 : 0));
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  GemmCtx c = gemm_ctx(L, wsb, *s, w13, w2, st);
+  // deployed nvfp4: the LSQ factor is taken at the forward's s_q, and the gradient reaches s
+  // straight through the E4M3 rounding (ds13 / ds2 are the gradients of s_q)
+  const float* s13u = L.deployed ? reinterpret_cast<const float*>(wsb + L.s13q) : s13;
+  const float* s2u = L.deployed ? reinterpret_cast<const float*>(wsb + L.s2q) : s2;
+  QAD_TRY(gemm_wgrad_fc2(c, w2, s2u, ds2, accumulate ? 1 : 0));
+  QAD_TRY(gemm_wgrad_fc1(c, w13, s13u, ds13, accumulate ? 1 : 0));
   return QAD_OK;
 }
 
@@ -417,6 +443,8 @@ int qad_moe_debug_view(const qad_moe_shape* s, int which, size_t* byte_offset, i
     case QAD_VIEW_H_CODES: off = L.hq; n = L.native_fp8 ? Rm * F : 0; break;
     case QAD_VIEW_A_SCALE: off = L.sa_tok; n = L.native_fp8 ? L.T : 0; break;
     case QAD_VIEW_H_SCALE: off = L.sh_row; n = L.native_fp8 ? Rm : 0; break;
+    case QAD_VIEW_S13_DEPLOYED: off = L.s13q; n = L.deployed ? E * 2 * F * (d / 16) : 0; break;
+    case QAD_VIEW_S2_DEPLOYED: off = L.s2q; n = L.deployed ? E * d * (F / 16) : 0; break;
     default: return QAD_ERR_INVALID_ARG;
   }
   *byte_offset = off;
@@ -468,7 +496,7 @@ const char* qad_kernel_name(int id) {
                                            "gemm_fc1_swiglu_aq", "gemm_fc2", "combine", "dy_gather",
                                            "gemm_dgrad_fc2_swiglu_bwd", "gemm_dgrad_fc1", "dx_combine",
                                            "gemm_wgrad_fc2_scalegrad", "gemm_wgrad_fc1_scalegrad", "scale_reduce",
-                                           "gemm_fc1_recompute"};
+                                           "gemm_fc1_recompute", "deploy_scales"};
   return (id >= 0 && id < QAD_K_COUNT) ? names[id] : "unknown";
 }
 

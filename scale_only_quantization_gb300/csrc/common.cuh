@@ -26,24 +26,29 @@
 
 namespace qad {
 
-// element grids ("quantizer kinds")
-constexpr int kQNone = -1, kQE2M1 = 0, kQInt4 = 1, kQE4M3 = 2, kQInt8 = 3;
+// element grids ("quantizer kinds"); kQE2M1G: E2M1 elements whose per-16 block scales are
+// rounded to E4M3 under one fp32 scale of the row (deployed nvfp4 activations)
+constexpr int kQNone = -1, kQE2M1 = 0, kQInt4 = 1, kQE4M3 = 2, kQInt8 = 3, kQE2M1G = 4;
 
 // weight and activation grids of each public format (qad_fmt)
 __host__ __device__ constexpr int weight_kind(int fmt) {
-  return fmt == QAD_FMT_NVFP4 || fmt == QAD_FMT_NVFP4A16   ? kQE2M1
-         : fmt == QAD_FMT_INT4_G128 || fmt == QAD_FMT_W4AFP8 ? kQInt4
-         : fmt == QAD_FMT_FP8_ROW                            ? kQE4M3
-                                                             : kQInt8;
+  return fmt == QAD_FMT_NVFP4 || fmt == QAD_FMT_NVFP4A16 || fmt == QAD_FMT_NVFP4_E4M3 ? kQE2M1
+         : fmt == QAD_FMT_INT4_G128 || fmt == QAD_FMT_W4AFP8                         ? kQInt4
+         : fmt == QAD_FMT_FP8_ROW                                                    ? kQE4M3
+                                                                                     : kQInt8;
 }
 __host__ __device__ constexpr int act_kind(int fmt) {
   return fmt == QAD_FMT_NVFP4                              ? kQE2M1
          : fmt == QAD_FMT_FP8_ROW || fmt == QAD_FMT_W4AFP8 ? kQE4M3
          : fmt == QAD_FMT_W8A8                             ? kQInt8
+         : fmt == QAD_FMT_NVFP4_E4M3                       ? kQE2M1G
                                                            : kQNone;
 }
 // a scale per whole row (E4M3, INT8) rather than per block along K
 __host__ __device__ constexpr bool row_scaled(int kind) { return kind == kQE4M3 || kind == kQInt8; }
+// an activation grid whose scales depend on the whole row (the per-row grids, and the E2M1
+// blocks under a row scale): the fc1 epilogue cannot apply it tile by tile
+__host__ __device__ constexpr bool act_needs_row(int kind) { return row_scaled(kind) || kind == kQE2M1G; }
 
 // ---------------------------------------------------------------------------------- bf16
 
@@ -143,6 +148,15 @@ __device__ __forceinline__ float2 q_pair(float a, float b) {
   // the grid value keeps the sign of its input, also when it rounds to zero
   return make_float2(copysignf(r.x, a), copysignf(r.y, b));
 }
+
+// Deployed nvfp4 block scale: s_q = fp32(e4m3(fp32(s / g)) * g), E4M3 rounding to nearest even
+// with saturation at 448 (cvt.rn.satfinite), exact decode; g = 0 gives 0.  The sign of s is kept.
+__device__ __forceinline__ float deployed_scale(float s, float g) {
+  if (g == 0.0f) return 0.0f;
+  return __fmul_rn(q_e4m3x2(__fdiv_rn(s, g), 0.0f).x, g);
+}
+// the tensor scale g = fp32(amax / 448) of a set of block scales whose largest magnitude is amax
+__device__ __forceinline__ float deploy_tensor_scale(float amax) { return __fdiv_rn(amax, 448.0f); }
 
 template <int QK> struct Clip;
 template <> struct Clip<kQE2M1> { static constexpr float lo = -6.0f, hi = 6.0f; };

@@ -294,6 +294,87 @@ __global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restr
   }
 }
 
+// Deployed-nvfp4 activations (kQE2M1G): one warp per row.  The row's tensor scale g =
+// fp32(fp32(row amax / 6) / 448) (the largest of the row's block scales fp32(block amax / 6),
+// divided by 448: fp32 rounding is monotone, so it is the block scale of the row amax); then
+// each 16-element block is fake-quantized on E2M1 with s_q = fp32(e4m3(fp32(sb / g)) * g),
+// sb = fp32(block amax / 6).
+__global__ void __launch_bounds__(256) act_quant_row_e2m1g_kernel(const uint4* __restrict__ in,
+                                                                  uint4* __restrict__ out, int64_t rows,
+                                                                  int64_t cols, const int32_t* dev_rows) {
+  const int64_t nrows = dev_rows ? (int64_t)*dev_rows : rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t c16 = cols / 16;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows; r += warps) {
+    const uint4* src = in + r * c16 * 2;
+    float amax = 0.0f;
+    for (int64_t c = lane; c < c16; c += 32) {
+      float v[16];
+      unpack8(src[2 * c], v);
+      unpack8(src[2 * c + 1], v + 8);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const float g = deploy_tensor_scale(__fdiv_rn(warp_max(amax), 6.0f));
+    for (int64_t c = lane; c < c16; c += 32) {
+      float v[16];
+      unpack8(src[2 * c], v);
+      unpack8(src[2 * c + 1], v + 8);
+      float bmax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+      fakequant_act_inplace<kQE2M1, 16>(v, deployed_scale(__fdiv_rn(bmax, 6.0f), g));
+      out[r * c16 * 2 + 2 * c] = pack8(v);
+      out[r * c16 * 2 + 2 * c + 1] = pack8(v + 8);
+    }
+  }
+}
+
+// Deployed nvfp4 weight scales, one CTA per matrix of `per_mat` scales (two tensors in one
+// launch: blocks [0, a.n_mat) take tensor a, the rest tensor b).  Pass 1: the matrix's largest
+// |s| (block reduction); g = fp32(amax / 448).  Pass 2: s_q = fp32(e4m3(fp32(s / g)) * g), written
+// in place or to another buffer (plain loads: the buffers may be the same).
+struct DeployJob {
+  const float* s;
+  float* sq;
+  int64_t n_mat, per_mat;
+};
+
+__global__ void __launch_bounds__(1024) deploy_scales_kernel(DeployJob a, DeployJob b) {
+  __shared__ float red[32];
+  const bool second = blockIdx.x >= a.n_mat;
+  const float* s = second ? b.s : a.s;
+  float* sq = second ? b.sq : a.sq;
+  const int64_t per = second ? b.per_mat : a.per_mat;
+  const int64_t m = second ? (int64_t)blockIdx.x - a.n_mat : (int64_t)blockIdx.x;
+  const float4* src = reinterpret_cast<const float4*>(s + m * per);
+  float4* dst = reinterpret_cast<float4*>(sq + m * per);
+  const int64_t n4 = per / 4;
+  float amax = 0.0f;
+#pragma unroll 4
+  for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = src[i];
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.0f;
+    v = warp_max(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float g = deploy_tensor_scale(red[0]);
+#pragma unroll 4
+  for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = src[i];
+    dst[i] = make_float4(deployed_scale(v.x, g), deployed_scale(v.y, g), deployed_scale(v.z, g),
+                         deployed_scale(v.w, g));
+  }
+}
+
 // Zero the padding rows (row_token < 0) of a routed-row buffer below *dev_rpad: each warp
 // tests 32 rows at a time and clears the padding ones (c16 16-byte chunks per row).
 __device__ __forceinline__ void zero_pad_rows(uint4* __restrict__ dst, const int32_t* __restrict__ row_token,
@@ -357,8 +438,8 @@ __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __rest
   for (int64_t t = w0; t < T; t += warps) {
     const int32_t my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
     const uint4* src = x + t * nblk * 2;
-    float s_row = 0.0f;
-    if constexpr (AQ == kQE4M3 || AQ == kQInt8) {
+    float s_row = 0.0f;  // the row's scale (E4M3, INT8) or tensor scale g (kQE2M1G)
+    if constexpr (AQ == kQE4M3 || AQ == kQInt8 || AQ == kQE2M1G) {
       float amax = 0.0f;
       for (int64_t b = lane; b < nblk; b += 32) {
         float f[16];
@@ -367,7 +448,10 @@ __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __rest
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
       }
-      s_row = __fdiv_rn(warp_max(amax), AQ == kQE4M3 ? 448.0f : 127.0f);
+      if constexpr (AQ == kQE2M1G)
+        s_row = deploy_tensor_scale(__fdiv_rn(warp_max(amax), 6.0f));
+      else
+        s_row = __fdiv_rn(warp_max(amax), AQ == kQE4M3 ? 448.0f : 127.0f);
       if constexpr (CODES) {
         if (lane == 0) sa_tok[t] = s_row;
       }
@@ -392,18 +476,19 @@ __global__ void __launch_bounds__(256) scatter_tokens_kernel(const uint4* __rest
             unpack8(v[i][0], f);
             unpack8(v[i][1], f + 8);
             float sc = s_row;
-            if constexpr (AQ == kQE2M1) {
+            if constexpr (AQ == kQE2M1 || AQ == kQE2M1G) {
               float amax = 0.0f;
 #pragma unroll
               for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(f[e]));
               sc = __fdiv_rn(amax, 6.0f);
+              if constexpr (AQ == kQE2M1G) sc = deployed_scale(sc, s_row);
             }
             if constexpr (CODES) {
               uint32_t cw[4];
               fakequant_e4m3_codes<16, true>(f, sc, cw);
               cd[i] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
             } else {
-              fakequant_act_inplace<AQ, 16>(f, sc);
+              fakequant_act_inplace<AQ == kQE2M1G ? kQE2M1 : AQ, 16>(f, sc);
             }
             v[i][0] = pack8(f);
             v[i][1] = pack8(f + 8);
@@ -642,6 +727,17 @@ cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_deploy_scales(const float* s_a, float* sq_a, int64_t n_a, int64_t per_a, const float* s_b,
+                                 float* sq_b, int64_t n_b, int64_t per_b, cudaStream_t st) {
+  if (n_a + n_b == 0) return cudaSuccess;
+  if (n_a + n_b > 0x7fffffff) return cudaErrorInvalidValue;
+  prof_begin(QAD_K_DEPLOY_SCALES, st);
+  deploy_scales_kernel<<<(unsigned)(n_a + n_b), 1024, 0, st>>>(DeployJob{s_a, sq_a, n_a, per_a},
+                                                               DeployJob{s_b, sq_b, n_b, per_b});
+  prof_end(QAD_K_DEPLOY_SCALES, st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st) {
   return launch_route_ptrs(idx, L.R, (int)L.k, (int)L.E, L.nchunks, reinterpret_cast<int32_t*>(ws + L.header),
                            reinterpret_cast<int32_t*>(ws + L.chunk_counts), reinterpret_cast<int32_t*>(ws + L.chunk_base),
@@ -672,9 +768,13 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
 cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st, void* codes, float* row_scale) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  if (kind != kQE4M3 && kind != kQInt8) return cudaErrorInvalidValue;
+  if (kind != kQE4M3 && kind != kQInt8 && kind != kQE2M1G) return cudaErrorInvalidValue;
+  if (kind == kQE2M1G && (cols % 16 || codes)) return cudaErrorInvalidValue;
   prof_begin(QAD_K_ACT_QUANT, st);
-  if (kind == kQE4M3 && codes) {
+  if (kind == kQE2M1G) {
+    act_quant_row_e2m1g_kernel<<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
+  } else if (kind == kQE4M3 && codes) {
     act_quant_row_kernel<kQE4M3, true><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
         static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows, static_cast<uint2*>(codes),
         row_scale);
@@ -700,6 +800,8 @@ cudaError_t launch_scatter_tokens(int aq, const void* x, void* xq, void* a1, con
   uint4* a = static_cast<uint4*>(a1);
   const int64_t nblk = d / 16;
   if (aq == kQE2M1) scatter_tokens_kernel<kQE2M1><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
+  else if (aq == kQE2M1G)
+    scatter_tokens_kernel<kQE2M1G><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad);
   else if (aq == kQE4M3 && a1q)
     scatter_tokens_kernel<kQE4M3, true><<<grid, 256, 0, st>>>(xs, q, a, row_of, row_token, T, k, nblk, dev_rpad,
                                                               static_cast<uint4*>(a1q), sa_tok);

@@ -439,7 +439,7 @@ __device__ __forceinline__ void epi_fc1(const Params& p, const CUtensorMap* tm_z
   const int64_t row = ti.row_base + row_in_tile;
   const int y = (int)ti.row_base + 32 * q;
   __nv_bfloat16* hrow = p.out3 + row * p.ld_out2;
-  const bool row_aq = row_scaled(p.aq);
+  const bool row_aq = act_needs_row(p.aq);
   // tm_h is the H_hat map, or the H map for the per-row activation grids (whose H_hat is
   // made by a separate pass); with QAD_FLAG_STASH_H and a per-block grid H is also kept.
   const bool extra_h = (p.flags & QAD_FLAG_STASH_H) && !row_aq;
@@ -1527,7 +1527,7 @@ cudaError_t gemm_fc1(const GemmCtx& c, int mode) {
   p.out3 = at<__nv_bfloat16>(c.ws, L.h);
   CUtensorMap tz, th;
   if (!make_store_tmap(&tz, c.ws + L.z1, 2 * L.F, L.Rmax, 2 * L.F, 16)) return cudaErrorInvalidValue;
-  if (!make_store_tmap(&th, c.ws + (row_scaled(c.aq) ? L.h : L.hh), L.F, L.Rmax, L.F, 16)) return cudaErrorInvalidValue;
+  if (!make_store_tmap(&th, c.ws + (act_needs_row(c.aq) ? L.h : L.hh), L.F, L.Rmax, L.F, 16)) return cudaErrorInvalidValue;
   const int kid = mode == kFc1Z1Only ? QAD_K_GEMM_FC1_RECOMPUTE : QAD_K_GEMM_FC1;
   const int64_t tiles = (L.Rmax / BM) * (int64_t)p.n_ntiles;
   if (c.dq) {

@@ -23,6 +23,9 @@ struct Layout {
   bool native_fp8;
   bool w_copies;  // the W13_hat / W2_hat regions exist (not with QAD_FLAG_SMEM_DEQUANT unless dumped)
   size_t w13q, w2q, a1q, hq, sa_tok, sh_row;
+  // QAD_FMT_NVFP4_E4M3: the deployed weight scales (0 otherwise)
+  bool deployed;
+  size_t s13q, s2q;
   size_t total;
 };
 
@@ -42,6 +45,11 @@ int num_sms();
 // codes (E4M3 weights only, may be null): the E4M3 code byte of every element, [rows, K]
 cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, int64_t rows, int64_t K,
                              cudaStream_t st, void* codes = nullptr);
+// deployed nvfp4 weight scales of two tensors in one launch (n_b may be 0): for each of the
+// n matrices of `per` scales (per % 4 == 0, 16-byte aligned), s_q = fp32(e4m3(fp32(s / g)) * g),
+// g = fp32(max |s| / 448) of that matrix; s_q may alias s
+cudaError_t launch_deploy_scales(const float* s_a, float* sq_a, int64_t n_a, int64_t per_a, const float* s_b,
+                                 float* sq_b, int64_t n_b, int64_t per_b, cudaStream_t st);
 cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st);
 // the same three routing kernels on explicit buffers (hdr: int32[64], zeroed by the caller;
 // chunk_counts / chunk_base: int32[nchunks * E]; mtile_expert: int32[Rmax / 128])
@@ -49,8 +57,8 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
                               int32_t* chunk_counts, int32_t* chunk_base, int32_t* counts, int32_t* offs,
                               int32_t* mtile_expert, int32_t* row_token, int32_t* row_slot, int32_t* row_of,
                               cudaStream_t st);
-// out[r, :] = AQ(in[r, :]) with activation grid `kind` (kQE2M1: per 16, kQE4M3 / kQInt8: per
-// row) for r < rows (or < *dev_rows when dev_rows != nullptr)
+// out[r, :] = AQ(in[r, :]) with activation grid `kind` (kQE4M3 / kQInt8: per row; kQE2M1G: per
+// 16 under a row scale) for r < rows (or < *dev_rows when dev_rows != nullptr)
 cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st, void* codes = nullptr,
                                   float* row_scale = nullptr);

@@ -52,9 +52,9 @@ def test_workspace_size_and_views(lib):
 
 _ELEM = dict(HEADER=4, OFFSETS=4, COUNTS=4, ROW_TOKEN=4, ROW_SLOT=4, ROW_OF=4, W13_HAT=2, W2_HAT=2, A1=2, Z1=2,
              H=2, H_HAT=2, Y=2, DY=2, DZ1=2, DA1=2, XQ=2, W13_CODES=1, W2_CODES=1, A1_CODES=1, H_CODES=1,
-             A_SCALE=4, H_SCALE=4)
+             A_SCALE=4, H_SCALE=4, S13_DEPLOYED=4, S2_DEPLOYED=4)
 _ALL_FMTS = [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8,
-             Q.QAD_FMT_W4AFP8]
+             Q.QAD_FMT_W4AFP8, Q.QAD_FMT_NVFP4_E4M3]
 
 
 def _layouts():
@@ -198,7 +198,8 @@ def test_binding_constants_match_the_header(lib):
                      "QAD_FLAG_DEQUANT_DUMP": Q.QAD_FLAG_DEQUANT_DUMP}
     fmts = _enum("QAD_FMT_")
     assert fmts == {"QAD_FMT_NVFP4": 0, "QAD_FMT_INT4_G128": 1, "QAD_FMT_FP8_ROW": 2, "QAD_FMT_NVFP4A16": 3,
-                    "QAD_FMT_W8A8": 4, "QAD_FMT_W4AFP8": 5}
+                    "QAD_FMT_W8A8": 4, "QAD_FMT_W4AFP8": 5, "QAD_FMT_NVFP4_E4M3": 6}
+    assert Q.QAD_FMT_NVFP4_E4M3 == 6
 
 
 def test_smem_dequant_flag_drops_the_weight_copies(lib):
@@ -235,7 +236,7 @@ def test_shape_contract(lib):
     """d and F: multiples of 16, of 128 for the INT4 formats; the E4M3 tensor path and the in-GEMM
     dequant keep whole tiles (d % 256, F % 128).  Others are refused on the host."""
     ok = lambda T, d, F, fmt, flags=0: Q.qad_moe_workspace_bytes(Q.shape(T, d, F, 4, 2, fmt, flags)) > 0  # noqa
-    for fmt in (Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8):
+    for fmt in (Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8, Q.QAD_FMT_NVFP4_E4M3):
         assert ok(64, 272, 144, fmt) and ok(64, 2880, 2880, fmt) and ok(64, 16, 16, fmt)
         assert not ok(64, 264, 144, fmt) and not ok(64, 272, 136, fmt)
     for fmt in (Q.QAD_FMT_INT4_G128, Q.QAD_FMT_W4AFP8):
@@ -248,3 +249,26 @@ def test_shape_contract(lib):
     ws = ctypes.c_void_p(1 << 20)
     assert lib.qad_moe_fwd(ctypes.byref(s), None, None, None, None, None, None, None, None, ws, 1 << 30,
                            None) == Q.QAD_ERR_UNSUPPORTED
+
+
+def test_deployed_nvfp4_layout_and_host_checks(lib):
+    """QAD_FMT_NVFP4_E4M3 keeps the deployed weight scales in the workspace (E * 2F * d / 16 and
+    E * d * F / 16 fp32 more than nvfp4); the deploy entry point checks its sizes and pointers on
+    the host, and the standalone fake-quant refuses the format (it needs the deployed scales)."""
+    T, d, F, E, k = 512, 256, 128, 4, 2
+    up = lambda n: (n + 1023) // 1024 * 1024  # noqa: E731
+    base = Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4))
+    dep = Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4_E4M3)
+    assert Q.qad_moe_workspace_bytes(dep) - base == up(4 * E * 2 * F * d // 16) + up(4 * E * d * F // 16)
+    assert Q.qad_moe_debug_view(dep, "S13_DEPLOYED")[1] == E * 2 * F * d // 16
+    assert Q.qad_moe_debug_view(dep, "S2_DEPLOYED")[1] == E * d * F // 16
+    assert Q.qad_moe_debug_view(Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4), "S13_DEPLOYED")[1] == 0
+    P = 1 << 20  # a 16-byte aligned stand-in address; nothing is launched for these
+    assert lib.qad_nvfp4_deploy_scales(P, P, 4, 6, None) == Q.QAD_ERR_INVALID_ARG      # per_mat % 4
+    assert lib.qad_nvfp4_deploy_scales(P, P, -1, 8, None) == Q.QAD_ERR_INVALID_ARG
+    assert lib.qad_nvfp4_deploy_scales(P, P, 4, 0, None) == Q.QAD_ERR_INVALID_ARG
+    assert lib.qad_nvfp4_deploy_scales(P + 4, P, 4, 8, None) == Q.QAD_ERR_INVALID_ARG  # misaligned
+    assert lib.qad_nvfp4_deploy_scales(None, P, 4, 8, None) == Q.QAD_ERR_INVALID_ARG
+    assert lib.qad_nvfp4_deploy_scales(None, None, 0, 8, None) == Q.QAD_OK
+    assert lib.qad_fakequant_fwd(Q.QAD_FMT_NVFP4_E4M3, P, P, P, 1, 16, 64, None) == Q.QAD_ERR_UNSUPPORTED
+    assert lib.qad_fakequant_fwd(7, P, P, P, 1, 16, 64, None) == Q.QAD_ERR_INVALID_ARG

@@ -22,6 +22,8 @@ pytestmark = pytest.mark.gpu
 WORKLOADS = ["qwen3_30b_a3b_nvfp4", "qwen3_30b_a3b_w4a16", "qwen3_30b_a3b_fp8", "large_nvfp4",
              # the remaining formats of the support matrix on the same Qwen3-30B-A3B shapes
              "qwen3_30b_a3b_nvfp4:3", "qwen3_30b_a3b_nvfp4:4", "qwen3_30b_a3b_nvfp4:5",
+             # nvfp4 with deployed (E4M3-rounded) block scales
+             "qwen3_30b_a3b_nvfp4:6",
              # fp8 with the forward GEMMs on the fp8 tensor path (scales applied to the sums)
              "qwen3_30b_a3b_fp8+native"]
 

@@ -21,7 +21,7 @@ from gpu_util import (E2E_REL_L2, Run, assert_close, assert_scale_grad, bits, e4
 pytestmark = pytest.mark.gpu
 
 FMTS = [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8,
-        Q.QAD_FMT_W4AFP8]
+        Q.QAD_FMT_W4AFP8, Q.QAD_FMT_NVFP4_E4M3]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -39,6 +39,7 @@ def _special_weights(E, N, K, fmt, seed):
     w[0, 0, :8] = torch.tensor([0.5, -0.5, 0.0, -0.0, 1e-30, -1e-30, 3.0, -3.0], device="cuda")
     w[0, 1, :] = 0.0                                   # all-zero rows -> zero scales
     w[-1, -1, ::7] *= 40.0                             # outliers inside their block
+    w[0, 3, :] *= 2.0 ** -12                           # a row of tiny scales (deployed E4M3: subnormal)
     w = w.to(torch.bfloat16)
     s = synth.init_scales(w, fmt, g)
     s[0, 2] *= 0.25                                    # clipped weights
@@ -50,7 +51,15 @@ def _special_weights(E, N, K, fmt, seed):
 def test_fakequant_bit_exact(fmt, E, N, K):
     w, s = _special_weights(E, N, K, fmt, seed=100 + fmt)
     out = torch.empty_like(w)
-    Q.qad_fakequant_fwd(fmt, w, s, out, E, N, K)
+    if fmt == Q.QAD_FMT_NVFP4_E4M3:
+        # the deployed scales, then the plain nvfp4 fake-quant with them (the header's recipe)
+        with pytest.raises(Q.QADError):
+            Q.qad_fakequant_fwd(fmt, w, s, out, E, N, K)
+        sq = torch.empty_like(s)
+        Q.qad_nvfp4_deploy_scales(s, sq, E, s[0].numel())
+        Q.qad_fakequant_fwd(Q.QAD_FMT_NVFP4, w, sq, out, E, N, K)
+    else:
+        Q.qad_fakequant_fwd(fmt, w, s, out, E, N, K)
     torch.cuda.synchronize()
     want = OQ.f64_to_bf16_bits(OQ.fakequant_weight(fmt, bits(w), synth.to_numpy(s)))
     got = bits(out)

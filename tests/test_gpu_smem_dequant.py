@@ -20,7 +20,7 @@ from gpu_util import Run, bits, host_inputs
 pytestmark = pytest.mark.gpu
 
 FMTS = [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4A16, Q.QAD_FMT_W8A8,
-        Q.QAD_FMT_W4AFP8]
+        Q.QAD_FMT_W4AFP8, Q.QAD_FMT_NVFP4_E4M3]
 DQ = Q.QAD_FLAG_SMEM_DEQUANT
 
 
@@ -65,7 +65,7 @@ def test_dequantized_tiles_are_bit_exact_and_outputs_identical(fmt):
     assert b.view("H_HAT", torch.bfloat16).numel() == a.view("H_HAT", torch.bfloat16).numel()
 
 
-@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_INT4_G128, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4_E4M3])
 def test_every_dequantizing_gemm_converts_every_tile(fmt):
     """The forward's GEMMs (fc1, fc2) and the input-gradient GEMMs (dgrad fc2, dgrad fc1) each
     write the values they converted: after clearing the dump between the calls, the dgrad call
