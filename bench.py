@@ -131,17 +131,20 @@ def algorithmic_per_launch(cfg, native_fp8=False):
     fc1 = 2.0 * R * 2 * F * d
     fc2 = 2.0 * R * d * F
     bpe = {0: 2 + 4.0 / 16 + 2, 1: 2 + 4.0 / 128 + 2, 2: None, 3: 2 + 4.0 / 16 + 2, 4: None,
-           5: 2 + 4.0 / 128 + 2}[cfg["fmt"]]
+           5: 2 + 4.0 / 128 + 2, 6: 2 + 4.0 / 16 + 2}[cfg["fmt"]]
     n13, n2 = E * 2 * F * d, E * d * F
     if bpe is None:  # one fp32 scale per row
         per_el = 5.0 if native_fp8 else 4.0
         fq = (per_el * n13 + 4 * E * 2 * F + per_el * n2 + 4 * E * d) / 2
     else:
         fq = bpe * (n13 + n2) / 2  # average of the two launches
-    return {"gemm_fc1_swiglu_aq": ("tensor", fc1), "gemm_fc2": ("tensor", fc2),
-            "gemm_dgrad_fc2_swiglu_bwd": ("tensor", fc2), "gemm_dgrad_fc1": ("tensor", fc1),
-            "gemm_wgrad_fc2_scalegrad": ("tensor", fc2), "gemm_wgrad_fc1_scalegrad": ("tensor", fc1),
-            "fakequant_w": ("hbm", fq)}
+    alg = {"gemm_fc1_swiglu_aq": ("tensor", fc1), "gemm_fc2": ("tensor", fc2),
+           "gemm_dgrad_fc2_swiglu_bwd": ("tensor", fc2), "gemm_dgrad_fc1": ("tensor", fc1),
+           "gemm_wgrad_fc2_scalegrad": ("tensor", fc2), "gemm_wgrad_fc1_scalegrad": ("tensor", fc1),
+           "fakequant_w": ("hbm", fq)}
+    if cfg["fmt"] == 6:  # deployed scales: every fp32 block scale read once and written once
+        alg["deploy_scales"] = ("hbm", 2 * 4.0 * (n13 + n2) / 16)
+    return alg
 
 
 def _traffic(kernel, workload):

@@ -12,6 +12,7 @@ Workloads, named by what they are:
   qwen3_30b_a3b_w4a16   same shapes, INT4 group-128 weights, bf16 activations
   qwen3_30b_a3b_fp8     same shapes, fp8 W8A8 per-row, Zipf(1.2) expert popularity
   large_nvfp4           E=256, d=4096, F=1536, top-8, 32768 tokens, nvfp4, 0.1% outliers
+  qwen3_30b_a3b_nvfp4_deployed  the nvfp4 shapes with deployed (E4M3-rounded) block scales
 
 Any workload can be run in another format with workload(name, fmt=...): 3 nvfp4a16,
 4 w8a8, 5 w4afp8, 6 nvfp4 with deployed (E4M3-rounded) block scales.
@@ -36,6 +37,8 @@ WORKLOADS = {
                               outliers=0.0),
     "large_nvfp4": dict(E=256, d=4096, F=1536, topk=8, T=32768, fmt=FMT_NVFP4, routing="uniform",
                         outliers=0.001),
+    "qwen3_30b_a3b_nvfp4_deployed": dict(E=128, d=2048, F=768, topk=8, T=16384, fmt=FMT_NVFP4_E4M3,
+                                         routing="uniform", outliers=0.0),
 }
 
 # elements per weight scale along K (absent: one per row), and the divisor that turns a
