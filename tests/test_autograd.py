@@ -19,7 +19,7 @@ def test_module_holds_frozen_weights_and_learnable_scales():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW])
+@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4_E4M3])
 def test_autograd_gradients_equal_the_abi_calls(fmt):
     from gpu_util import Run
     from scale_only_quantization_gb300 import build

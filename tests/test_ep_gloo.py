@@ -28,9 +28,9 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _weights():
+def _weights(fmt=0):
     import synth
-    cfg = synth.workload("tiny_nvfp4", E=E, d=D, F=F, topk=K, T=T)
+    cfg = synth.workload("tiny_nvfp4", E=E, d=D, F=F, topk=K, T=T, fmt=fmt)
     return synth.make_inputs(cfg, seed=0, device="cpu")
 
 
@@ -89,7 +89,7 @@ class OracleExperts:
         return self._bf16(OM.combine(OQ.bf16_to_f64(self._bits(rows)), pw, ro))
 
 
-def _rank_main(rank, world, ep, port, out, skew=False):
+def _rank_main(rank, world, ep, port, out, skew=False, fmt=0):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -98,7 +98,7 @@ def _rank_main(rank, world, ep, port, out, skew=False):
     ep_groups = [dist.new_group(list(range(i * ep, (i + 1) * ep))) for i in range(edp)]
     edp_groups = [dist.new_group(list(range(j, world, ep))) for j in range(ep)]
     my_ep, my_pos = rank // ep, rank % ep
-    w = _weights()
+    w = _weights(fmt)
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     e_loc = E // ep
     lo = my_pos * e_loc
@@ -123,10 +123,10 @@ def _rank_main(rank, world, ep, port, out, skew=False):
     dist.destroy_process_group()
 
 
-def _single_process(ranks, skew=False):
+def _single_process(ranks, skew=False, fmt=0):
     """The oracle layer on the tokens of `ranks` concatenated, with every expert."""
     from oracle import moe as OM
-    w = _weights()
+    w = _weights(fmt)
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     toks = [_tokens(r, skew) for r in ranks]
     x = np.concatenate([bits(t["x"]) for t in toks])
@@ -145,16 +145,20 @@ def _bf16_bits(v):
     return OQ.f64_to_bf16_bits(v)
 
 
-@pytest.mark.parametrize("world, ep, skew", [(2, 2, False), (4, 4, False), (4, 2, False), (2, 2, True)],
-                         ids=["ep2", "ep4", "ep2-edp2", "ep2-owner-without-rows"])
-def test_expert_parallel_exchange_matches_one_process(world, ep, skew):
+@pytest.mark.parametrize("world, ep, skew, fmt", [(2, 2, False, 0), (4, 4, False, 0), (4, 2, False, 0),
+                                                   (2, 2, True, 0), (2, 2, False, 6)],
+                         ids=["ep2", "ep4", "ep2-edp2", "ep2-owner-without-rows", "ep2-deployed-nvfp4"])
+def test_expert_parallel_exchange_matches_one_process(world, ep, skew, fmt):
+    """fmt 6 (deployed nvfp4 scales): the weights' tensor scale is per expert matrix and the
+    activations' per row, so the split must leave every bit unchanged too."""
     port = _free_port()
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
-    mp.start_processes(_rank_main, args=(world, ep, port, out, skew), nprocs=world, start_method="spawn", join=True)
+    mp.start_processes(_rank_main, args=(world, ep, port, out, skew, fmt), nprocs=world, start_method="spawn",
+                       join=True)
     edp = world // ep
     e_loc = E // ep
-    refs = [_single_process(list(range(i * ep, (i + 1) * ep)), skew) for i in range(edp)]
+    refs = [_single_process(list(range(i * ep, (i + 1) * ep)), skew, fmt) for i in range(edp)]
     if skew:
         assert int(np.sum(out[1]["counts"])) == 0  # rank 1 owned experts nobody was routed to
     for rank in range(world):

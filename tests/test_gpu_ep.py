@@ -43,6 +43,7 @@ def test_combine_against_the_oracle(T, k, d):
 
 
 @pytest.mark.parametrize("fmt, name", [(Q.QAD_FMT_NVFP4, "tiny_nvfp4"), (Q.QAD_FMT_FP8_ROW, "tiny_nvfp4"),
+                                       (Q.QAD_FMT_NVFP4_E4M3, "tiny_nvfp4"),
                                        (Q.QAD_FMT_NVFP4, "qwen3_30b_a3b_nvfp4")])
 def test_single_rank_expert_parallel_layer_equals_the_layer(fmt, name):
     inp = synth.make_inputs(synth.workload(name, fmt=fmt), seed=3, device="cuda")

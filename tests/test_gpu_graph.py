@@ -57,6 +57,7 @@ INPUTS = ("x", "dout", "topk_idx", "topk_w", "w13", "s13", "w2", "s2")
     (Q.QAD_FMT_NVFP4, 0),
     (Q.QAD_FMT_NVFP4, Q.QAD_FLAG_RECOMPUTE),
     (Q.QAD_FMT_FP8_ROW, Q.QAD_FLAG_NATIVE_FP8),
+    (Q.QAD_FMT_NVFP4_E4M3, 0),
 ])
 def test_step_captured_in_a_cuda_graph_replays_bit_identically(fmt, flags):
     cfg = synth.workload("tiny_nvfp4", fmt=fmt, T=1536, E=8)
