@@ -149,15 +149,6 @@ __device__ __forceinline__ float2 q_pair(float a, float b) {
   return make_float2(copysignf(r.x, a), copysignf(r.y, b));
 }
 
-// Deployed nvfp4 block scale: s_q = fp32(e4m3(fp32(s / g)) * g), E4M3 rounding to nearest even
-// with saturation at 448 (cvt.rn.satfinite), exact decode; g = 0 gives 0.  The sign of s is kept.
-__device__ __forceinline__ float deployed_scale(float s, float g) {
-  if (g == 0.0f) return 0.0f;
-  return __fmul_rn(q_e4m3x2(__fdiv_rn(s, g), 0.0f).x, g);
-}
-// the tensor scale g = fp32(amax / 448) of a set of block scales whose largest magnitude is amax
-__device__ __forceinline__ float deploy_tensor_scale(float amax) { return __fdiv_rn(amax, 448.0f); }
-
 template <int QK> struct Clip;
 template <> struct Clip<kQE2M1> { static constexpr float lo = -6.0f, hi = 6.0f; };
 template <> struct Clip<kQInt4> { static constexpr float lo = -8.0f, hi = 7.0f; };
@@ -168,6 +159,40 @@ template <> struct Clip<kQInt8> { static constexpr float lo = -128.0f, hi = 127.
 __device__ __forceinline__ float quotient(float w, float s) {
   return s == 0.0f ? copysignf(0.0f, w) : __fdiv_rn(w, s);
 }
+
+// One 32-byte sector (16 bf16) of read-only global memory with a 256-bit load that allocates no
+// L1 line (ptr 32-byte aligned).  Used where a warp's load touches 32 different rows.
+__device__ __forceinline__ void ld_nc_256(const void* ptr, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+               : "l"(ptr));
+}
+
+// x = fp32(w / s) from r = RN(1 / s) (computed once by the caller for many w): Markstein's
+// correction, with the range guards of quotients<N> below; outside them the IEEE division.
+__device__ __forceinline__ float quotient_r(float w, float s, float r) {
+  const float q = __fmul_rn(w, r);
+  const float e = __fmaf_rn(-q, s, w);
+  const float x = copysignf(__fmaf_rn(e, r, q), w);
+  const float aw = fabsf(w);
+  const bool ok = s >= 1.17549435e-38f && s <= 0x1p20f && (aw >= 0x1p-80f || aw == 0.0f) && fabsf(x) <= 3.0e38f;
+  return ok ? x : quotient(w, s);
+}
+
+// Deployed nvfp4 block scale: s_q = fp32(e4m3(fp32(s / g)) * g), E4M3 rounding to nearest even
+// with saturation at 448 (cvt.rn.satfinite), exact decode; g = 0 gives 0.  The sign of s is kept.
+__device__ __forceinline__ float deployed_scale(float s, float g) {
+  if (g == 0.0f) return 0.0f;
+  return __fmul_rn(q_e4m3x2(__fdiv_rn(s, g), 0.0f).x, g);
+}
+// the same from r = RN(1 / g), for many scales under one g
+__device__ __forceinline__ float deployed_scale_r(float s, float g, float r) {
+  if (g == 0.0f) return 0.0f;
+  return __fmul_rn(q_e4m3x2(quotient_r(s, g, r), 0.0f).x, g);
+}
+// the tensor scale g = fp32(amax / 448) of a set of block scales whose largest magnitude is amax
+__device__ __forceinline__ float deploy_tensor_scale(float amax) { return __fdiv_rn(amax, 448.0f); }
+
 
 // The same correctly rounded quotients from r = RN(1 / s), without a division per element.
 // Markstein's theorem (P. Markstein, "IA-64 and Elementary Functions", 2000; also

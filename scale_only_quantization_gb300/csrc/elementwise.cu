@@ -294,6 +294,78 @@ __global__ void __launch_bounds__(256) act_quant_row_kernel(const uint4* __restr
   }
 }
 
+// Activation fake-quant of rows of at most LPR * 16 * NB elements (the per-row grids E4M3 /
+// INT8, and kQE2M1G), LPR lanes per row (a warp takes 32 / LPR rows at once), the row held in
+// registers between the amax and the quantization: sub-lane l of a row holds its 16-element
+// blocks l, l + LPR, ... (one 256-bit load each).  CODES (E4M3): also the row's code bytes and
+// scale.
+template <int AQ, int LPR, int NB, bool CODES = false>
+__global__ void __launch_bounds__(256) act_quant_row_reg_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                                                int64_t rows, int64_t cols, const int32_t* dev_rows,
+                                                                uint4* __restrict__ codes = nullptr,
+                                                                float* __restrict__ row_scale = nullptr) {
+  constexpr int RPW = 32 / LPR;  // rows per warp at once
+  const int64_t nrows = dev_rows ? (int64_t)*dev_rows : rows;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % LPR;
+  const int64_t groups = (int64_t)gridDim.x * (blockDim.x / 32) * RPW;
+  const int nb = (int)(cols / 16);
+  for (int64_t r0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * RPW; r0 < nrows; r0 += groups) {
+    const int64_t r = r0 + lane / LPR;
+    const bool live = r < nrows;  // the warp stays together for the shuffles; dead rows load nothing
+    const uint4* src = in + r * nb * 2;
+    uint4 v[NB][2];
+    float bmax[NB];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int b = sub + LPR * i;
+      bmax[i] = 0.0f;
+      if (live && b < nb) {
+        ld_nc_256(src + 2 * b, v[i][0], v[i][1]);
+        float f[16];
+        unpack8(v[i][0], f);
+        unpack8(v[i][1], f + 8);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) bmax[i] = fmaxf(bmax[i], fabsf(f[e]));
+        amax = fmaxf(amax, bmax[i]);
+      }
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float s_row, r_g = 0.0f;
+    if constexpr (AQ == kQE2M1G) {
+      s_row = deploy_tensor_scale(__fdiv_rn(amax, 6.0f));  // the row's tensor scale g
+      r_g = s_row == 0.0f ? 0.0f : __frcp_rn(s_row);
+    } else {
+      s_row = __fdiv_rn(amax, AQ == kQE4M3 ? 448.0f : 127.0f);
+    }
+    if constexpr (CODES) {
+      if (live && sub == 0) row_scale[r] = s_row;
+    }
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int b = sub + LPR * i;
+      if (live && b < nb) {
+        float f[16];
+        unpack8(v[i][0], f);
+        unpack8(v[i][1], f + 8);
+        if constexpr (AQ == kQE2M1G) {
+          fakequant_act_inplace<kQE2M1, 16>(f, deployed_scale_r(__fdiv_rn(bmax[i], 6.0f), s_row, r_g));
+        } else if constexpr (CODES) {
+          uint32_t cw[4];
+          fakequant_e4m3_codes<16, true>(f, s_row, cw);
+          codes[r * nb + b] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        } else {
+          fakequant_act_inplace<AQ, 16>(f, s_row);
+        }
+        out[r * nb * 2 + 2 * b] = pack8(f);
+        out[r * nb * 2 + 2 * b + 1] = pack8(f + 8);
+      }
+    }
+  }
+}
+
 // Deployed-nvfp4 activations (kQE2M1G): one warp per row.  The row's tensor scale g =
 // fp32(fp32(row amax / 6) / 448) (the largest of the row's block scales fp32(block amax / 6),
 // divided by 448: fp32 rounding is monotone, so it is the block scale of the row amax); then
@@ -367,11 +439,12 @@ __global__ void __launch_bounds__(1024) deploy_scales_kernel(DeployJob a, Deploy
   }
   __syncthreads();
   const float g = deploy_tensor_scale(red[0]);
+  const float r = g == 0.0f ? 0.0f : __frcp_rn(g);
 #pragma unroll 4
   for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
     const float4 v = src[i];
-    dst[i] = make_float4(deployed_scale(v.x, g), deployed_scale(v.y, g), deployed_scale(v.z, g),
-                         deployed_scale(v.w, g));
+    dst[i] = make_float4(deployed_scale_r(v.x, g, r), deployed_scale_r(v.y, g, r), deployed_scale_r(v.z, g, r),
+                         deployed_scale_r(v.w, g, r));
   }
 }
 
@@ -765,25 +838,52 @@ cudaError_t launch_route_ptrs(const int32_t* idx, int64_t R, int k, int E, int64
   return cudaGetLastError();
 }
 
+namespace {
+template <int LPR, int NB>
+void act_quant_rows_reg(int kind, const uint4* in, uint4* out, int64_t rows, int64_t cols, const int32_t* dev_rows,
+                        uint4* codes, float* row_scale, cudaStream_t st) {
+  const int grid = grid_for((rows * LPR + 31) / 32 * 32, 256, 8);
+  if (kind == kQE2M1G)
+    act_quant_row_reg_kernel<kQE2M1G, LPR, NB><<<grid, 256, 0, st>>>(in, out, rows, cols, dev_rows);
+  else if (kind == kQE4M3 && codes)
+    act_quant_row_reg_kernel<kQE4M3, LPR, NB, true><<<grid, 256, 0, st>>>(in, out, rows, cols, dev_rows, codes,
+                                                                          row_scale);
+  else if (kind == kQE4M3)
+    act_quant_row_reg_kernel<kQE4M3, LPR, NB><<<grid, 256, 0, st>>>(in, out, rows, cols, dev_rows);
+  else
+    act_quant_row_reg_kernel<kQInt8, LPR, NB><<<grid, 256, 0, st>>>(in, out, rows, cols, dev_rows);
+}
+}  // namespace
+
 cudaError_t launch_act_quant_rows(int kind, const void* in, void* out, int64_t rows, int64_t cols,
                                   const int32_t* dev_rows, cudaStream_t st, void* codes, float* row_scale) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   if (kind != kQE4M3 && kind != kQInt8 && kind != kQE2M1G) return cudaErrorInvalidValue;
   if (kind == kQE2M1G && (cols % 16 || codes)) return cudaErrorInvalidValue;
   prof_begin(QAD_K_ACT_QUANT, st);
-  if (kind == kQE2M1G) {
-    act_quant_row_e2m1g_kernel<<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
-        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
+  const int grid = grid_for(rows * 32, 256, 8);
+  const uint4* src = static_cast<const uint4*>(in);
+  uint4* dst = static_cast<uint4*>(out);
+  const int64_t nb = cols / 16;
+  uint4* cd = static_cast<uint4*>(codes);
+  if (cols % 16 == 0 && nb <= 128) {
+    // rows of up to 2048 elements stay in registers between the row amax and the quantization;
+    // up to 768 elements two rows per warp (16 lanes each), so each warp has more loads in flight
+    if (nb <= 48)
+      act_quant_rows_reg<16, 3>(kind, src, dst, rows, cols, dev_rows, cd, row_scale, st);
+    else if (nb <= 96)
+      act_quant_rows_reg<32, 3>(kind, src, dst, rows, cols, dev_rows, cd, row_scale, st);
+    else
+      act_quant_rows_reg<32, 4>(kind, src, dst, rows, cols, dev_rows, cd, row_scale, st);
+  } else if (kind == kQE2M1G) {
+    act_quant_row_e2m1g_kernel<<<grid, 256, 0, st>>>(src, dst, rows, cols, dev_rows);
   } else if (kind == kQE4M3 && codes) {
-    act_quant_row_kernel<kQE4M3, true><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
-        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows, static_cast<uint2*>(codes),
-        row_scale);
+    act_quant_row_kernel<kQE4M3, true><<<grid, 256, 0, st>>>(src, dst, rows, cols, dev_rows,
+                                                            static_cast<uint2*>(codes), row_scale);
   } else if (kind == kQE4M3) {
-    act_quant_row_kernel<kQE4M3><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
-        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
+    act_quant_row_kernel<kQE4M3><<<grid, 256, 0, st>>>(src, dst, rows, cols, dev_rows);
   } else {
-    act_quant_row_kernel<kQInt8><<<grid_for(rows * 32, 256, 8), 256, 0, st>>>(
-        static_cast<const uint4*>(in), static_cast<uint4*>(out), rows, cols, dev_rows);
+    act_quant_row_kernel<kQInt8><<<grid, 256, 0, st>>>(src, dst, rows, cols, dev_rows);
   }
   prof_end(QAD_K_ACT_QUANT, st);
   return cudaGetLastError();

@@ -614,11 +614,6 @@ __device__ __forceinline__ Z1Cursor z1_cursor(const Params& p, const Tile& ti, i
 // takes: with 16-byte loads through L1 the line allocations throttled the loads and the
 // kernel ran ~11% slower.  Alignment: Z1 rows are 4F bytes apart (F % 128 == 0) from a
 // 256-byte aligned region, and the columns start at multiples of 16 elements.
-__device__ __forceinline__ void ld_nc_256(const void* ptr, uint4& lo, uint4& hi) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
-               : "l"(ptr));
-}
 __device__ __forceinline__ void z1_load(const Params& p, const Z1Cursor& c, int step, uint4 (&slot)[4]) {
   ld_nc_256(c.row + c.f_first + 16 * step, slot[0], slot[1]);
   ld_nc_256(c.row + p.F + c.f_first + 16 * step, slot[2], slot[3]);
