@@ -558,7 +558,10 @@ def test_bounded_wait_reports_timeout_and_leaves_the_context_usable():
 
 @pytest.mark.parametrize("fmt, d, F", [
     (Q.QAD_FMT_NVFP4, 272, 144), (Q.QAD_FMT_FP8_ROW, 272, 144), (Q.QAD_FMT_NVFP4A16, 272, 144),
-    (Q.QAD_FMT_W8A8, 272, 144),
+    (Q.QAD_FMT_W8A8, 272, 144), (Q.QAD_FMT_NVFP4_E4M3, 272, 144),
+    # the row quantizer of H with 16 lanes per row (F <= 768), 32 lanes and 3 blocks per lane
+    # (F <= 1536), 32 lanes and 4 blocks (F <= 2048)
+    (Q.QAD_FMT_NVFP4_E4M3, 256, 1040), (Q.QAD_FMT_FP8_ROW, 256, 1536), (Q.QAD_FMT_W8A8, 272, 2032),
     # INT4 weights need multiples of 128 (group-128 scales along d and F): 384 is not a whole 256 tile
     (Q.QAD_FMT_INT4_G128, 384, 384), (Q.QAD_FMT_W4AFP8, 384, 384)])
 def test_layer_stagewise_partial_tiles(fmt, d, F):
@@ -574,9 +577,13 @@ def test_layer_stagewise_partial_tiles(fmt, d, F):
     _stagewise(run, host_inputs(inp))
 
 
-def test_layer_stagewise_gpt_oss_like_width():
-    """A layer as wide as GPT-OSS's experts (d = F = 2880: 11.25 tiles of 256 columns), nvfp4."""
-    inp = synth.make_inputs(synth.workload("tiny_nvfp4", E=16, d=2880, F=2880, topk=4, T=1024), seed=13,
+@pytest.mark.parametrize("fmt", [Q.QAD_FMT_NVFP4, Q.QAD_FMT_FP8_ROW, Q.QAD_FMT_NVFP4_E4M3])
+def test_layer_stagewise_gpt_oss_like_width(fmt):
+    """A layer as wide as GPT-OSS's experts (d = F = 2880: 11.25 tiles of 256 columns).  With the
+    per-row activation grids (fp8, deployed nvfp4) the H rows (2880 > 2048 columns) take the
+    row quantizer's two-pass form instead of the register-held one."""
+    E, T = (16, 1024) if fmt == Q.QAD_FMT_NVFP4 else (8, 384)  # the oracle's GEMMs dominate the test's time
+    inp = synth.make_inputs(synth.workload("tiny_nvfp4", fmt=fmt, E=E, d=2880, F=2880, topk=4, T=T), seed=13,
                             device="cuda")
     run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
     assert run.error == 0
