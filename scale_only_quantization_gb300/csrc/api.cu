@@ -160,6 +160,7 @@ int layout_of(const qad_moe_shape& s, Layout* L) {
   L->deployed = s.fmt == QAD_FMT_NVFP4_E4M3;
   L->s13q = L->deployed ? take(4 * (size_t)(E * 2 * F * (d / 16))) : 0;
   L->s2q = L->deployed ? take(4 * (size_t)(E * d * (F / 16))) : 0;
+  L->deploy_tmp = L->deployed ? take(4 * (size_t)(2 * E) + 8 * (size_t)(2 * E)) : 0;
   L->total = o;
   return QAD_OK;
 }
@@ -325,10 +326,23 @@ int qad_moe_fwd(const qad_moe_shape* s, const void* x, const int32_t* topk_idx, 
                                   row_token, L.T, (int)L.k, L.d, rpad, ss->s, f8 ? wsb + L.a1q : nullptr,
                                   f8 ? reinterpret_cast<float*>(wsb + L.sa_tok) : nullptr));
     QAD_TRY(cudaEventRecord(ss->join, ss->s));
-    if (deploy)
-      QAD_TRY(launch_deploy_scales(s13, const_cast<float*>(s13u), L.E, 2 * L.F * (L.d / 16), s2,
-                                   const_cast<float*>(s2u), L.E, L.d * (L.F / 16), st));
-    if (!no_quant && !c.dq) {  // with QAD_FLAG_SMEM_DEQUANT the GEMMs fake-quantize the weights themselves
+    if (deploy) {
+      // the tensor scale of each expert matrix; the deployed block scales are then made by the
+      // weight fake-quant pass itself (or, with the in-GEMM dequant, by a rounding pass)
+      uint32_t* amax_bits = reinterpret_cast<uint32_t*>(wsb + L.deploy_tmp);
+      const float2* gr = reinterpret_cast<const float2*>(wsb + L.deploy_tmp + 4 * 2 * L.E);
+      QAD_TRY(launch_deploy_tensor_scales(s13, L.E, 2 * L.F * (L.d / 16), s2, L.E, L.d * (L.F / 16), amax_bits,
+                                          const_cast<float2*>(gr), st));
+      if (c.dq) {
+        QAD_TRY(launch_deploy_round(s13, const_cast<float*>(s13u), L.E, 2 * L.F * (L.d / 16), s2,
+                                    const_cast<float*>(s2u), L.E, L.d * (L.F / 16), gr, st));
+      } else {
+        QAD_TRY(launch_fakequant_deployed(w13, s13, wsb + L.w13h, L.E * 2 * L.F, L.d, 2 * L.F, gr,
+                                          const_cast<float*>(s13u), st));
+        QAD_TRY(launch_fakequant_deployed(w2, s2, wsb + L.w2h, L.E * L.d, L.F, L.d, gr + L.E, const_cast<float*>(s2u),
+                                          st));
+      }
+    } else if (!no_quant && !c.dq) {  // with QAD_FLAG_SMEM_DEQUANT the GEMMs fake-quantize the weights themselves
       QAD_TRY(launch_fakequant(fmt, w13, s13u, wsb + L.w13h, L.E * 2 * L.F, L.d, st, f8 ? wsb + L.w13q : nullptr));
       QAD_TRY(launch_fakequant(fmt, w2, s2u, wsb + L.w2h, L.E * L.d, L.F, st, f8 ? wsb + L.w2q : nullptr));
     }

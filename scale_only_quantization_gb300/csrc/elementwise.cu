@@ -52,25 +52,44 @@ __device__ __forceinline__ void fakequant_chunk(const uint4& u0, const uint4& u1
   }
 }
 
-template <int QK, bool CODES = false>
+// DEPLOY (deployed nvfp4, one scale per chunk): the chunk's scale is first rounded as deployed
+// NVFP4 stores it, s_q = fp32(e4m3(fp32(s / g)) * g) with gr[m] = (g, RN(1 / g)) of its matrix
+// m = c / cpm, and s_q is also written to sq[c] (the backward calls read it).
+__device__ __forceinline__ float deploy_chunk(float s, const float2* __restrict__ gr, uint32_t cpm,
+                                              float* __restrict__ sq, uint64_t c) {
+  const float2 g = __ldg(gr + (uint32_t)c / cpm);
+  const float v = deployed_scale_r(s, g.x, g.y);
+  sq[c] = v;
+  return v;
+}
+
+template <int QK, bool CODES = false, bool DEPLOY = false>
 __global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict__ w, const float* __restrict__ s,
                                                         uint4* __restrict__ out, uint64_t nchunks, uint32_t cps,
-                                                        uint4* __restrict__ codes = nullptr) {
+                                                        uint4* __restrict__ codes = nullptr,
+                                                        const float2* __restrict__ gr = nullptr, uint32_t cpm = 1,
+                                                        float* __restrict__ sq = nullptr) {
+  static_assert(!DEPLOY || (QK == kQE2M1 && !CODES), "deployed scales: nvfp4 weights, one scale per chunk");
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (; c + stride < nchunks; c += 2 * stride) {  // two chunks (64 bytes) per thread in flight
     const uint64_t c2 = c + stride;
     const uint4 u0 = ld_stream(w + 2 * c), u1 = ld_stream(w + 2 * c + 1);
     const uint4 u2 = ld_stream(w + 2 * c2), u3 = ld_stream(w + 2 * c2 + 1);
-    const float sc = __ldg(s + (cps == 1 ? c : c / cps));
-    const float sc2 = __ldg(s + (cps == 1 ? c2 : c2 / cps));
+    float sc = __ldg(s + (cps == 1 ? c : c / cps));
+    float sc2 = __ldg(s + (cps == 1 ? c2 : c2 / cps));
+    if constexpr (DEPLOY) {
+      sc = deploy_chunk(sc, gr, cpm, sq, c);
+      sc2 = deploy_chunk(sc2, gr, cpm, sq, c2);
+    }
     fakequant_chunk<QK, CODES>(u0, u1, sc, out, codes, c);
     fakequant_chunk<QK, CODES>(u2, u3, sc2, out, codes, c2);
   }
   for (; c < nchunks; c += stride) {
     const uint4 u0 = ld_stream(w + 2 * c);
     const uint4 u1 = ld_stream(w + 2 * c + 1);
-    const float sc = __ldg(s + (cps == 1 ? c : c / cps));
+    float sc = __ldg(s + (cps == 1 ? c : c / cps));
+    if constexpr (DEPLOY) sc = deploy_chunk(sc, gr, cpm, sq, c);
     fakequant_chunk<QK, CODES>(u0, u1, sc, out, codes, c);
   }
 }
@@ -448,6 +467,70 @@ __global__ void __launch_bounds__(1024) deploy_scales_kernel(DeployJob a, Deploy
   }
 }
 
+// The same in parallel over many CTAs, for the layer calls (their workspace holds the
+// per-matrix words): grid (parts, matrices of a then b).  deploy_amax_kernel: each CTA's slice
+// max |s|, combined per matrix with atomicMax on the bit patterns (non-negative floats order as
+// their bits; amax_bits zeroed first); deploy_g_kernel: gr[m] = (g, RN(1 / g)), g = fp32(amax /
+// 448); deploy_round_kernel: s_q for every scale (the fake-quant pass does the same inline).
+__device__ __forceinline__ void deploy_job(const DeployJob& a, const DeployJob& b, int m_all, const float** s,
+                                           float** sq, int64_t* per) {
+  const bool second = m_all >= a.n_mat;
+  const int64_t m = second ? m_all - a.n_mat : m_all;
+  *per = second ? b.per_mat : a.per_mat;
+  *s = (second ? b.s : a.s) + m * *per;
+  float* base = second ? b.sq : a.sq;
+  *sq = base ? base + m * *per : nullptr;
+}
+
+__global__ void __launch_bounds__(256) deploy_amax_kernel(DeployJob a, DeployJob b, uint32_t* __restrict__ amax_bits) {
+  __shared__ float red[8];
+  const float* s;
+  float* sq;
+  int64_t per;
+  deploy_job(a, b, (int)blockIdx.y, &s, &sq, &per);
+  const int64_t n4 = per / 4;
+  const int64_t slice = (n4 + gridDim.x - 1) / gridDim.x;
+  const int64_t lo = (int64_t)blockIdx.x * slice, hi = lo + slice < n4 ? lo + slice : n4;
+  const float4* src = reinterpret_cast<const float4*>(s);
+  float amax = 0.0f;
+#pragma unroll 4
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    const float4 v = __ldg(src + i);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = red[0];
+    for (int i = 1; i < (int)(blockDim.x / 32); ++i) v = fmaxf(v, red[i]);
+    if (lo < hi) atomicMax(amax_bits + blockIdx.y, __float_as_uint(v));
+  }
+}
+
+__global__ void deploy_g_kernel(const uint32_t* __restrict__ amax_bits, float2* __restrict__ gr, int n) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m < n) {
+    const float g = deploy_tensor_scale(__uint_as_float(amax_bits[m]));
+    gr[m] = make_float2(g, g == 0.0f ? 0.0f : __frcp_rn(g));
+  }
+}
+
+__global__ void __launch_bounds__(256) deploy_round_kernel(DeployJob a, DeployJob b, const float2* __restrict__ gr) {
+  const float* s;
+  float* sq;
+  int64_t per;
+  deploy_job(a, b, (int)blockIdx.y, &s, &sq, &per);
+  const float2 g = gr[blockIdx.y];
+  const float4* src = reinterpret_cast<const float4*>(s);
+  float4* dst = reinterpret_cast<float4*>(sq);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per / 4; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = __ldg(src + i);
+    dst[i] = make_float4(deployed_scale_r(v.x, g.x, g.y), deployed_scale_r(v.y, g.x, g.y),
+                         deployed_scale_r(v.z, g.x, g.y), deployed_scale_r(v.w, g.x, g.y));
+  }
+}
+
 // Zero the padding rows (row_token < 0) of a routed-row buffer below *dev_rpad: each warp
 // tests 32 rows at a time and clears the padding ones (c16 16-byte chunks per row).
 __device__ __forceinline__ void zero_pad_rows(uint4* __restrict__ dst, const int32_t* __restrict__ row_token,
@@ -808,6 +891,52 @@ cudaError_t launch_deploy_scales(const float* s_a, float* sq_a, int64_t n_a, int
   deploy_scales_kernel<<<(unsigned)(n_a + n_b), 1024, 0, st>>>(DeployJob{s_a, sq_a, n_a, per_a},
                                                                DeployJob{s_b, sq_b, n_b, per_b});
   prof_end(QAD_K_DEPLOY_SCALES, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_deploy_tensor_scales(const float* s_a, int64_t n_a, int64_t per_a, const float* s_b, int64_t n_b,
+                                        int64_t per_b, uint32_t* amax_bits, float2* gr, cudaStream_t st) {
+  const int64_t n = n_a + n_b;
+  if (n == 0) return cudaSuccess;
+  if (n > 65535) return cudaErrorInvalidValue;
+  prof_begin(QAD_K_DEPLOY_SCALES, st);
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t) * (size_t)n, st);
+  if (e != cudaSuccess) return e;
+  const int64_t per4 = (per_a > per_b ? per_a : per_b) / 4;
+  const int parts = (int)((per4 + 2047) / 2048);  // ~8 float4 per thread of a 256-thread CTA
+  deploy_amax_kernel<<<dim3((unsigned)(parts > 0 ? parts : 1), (unsigned)n), 256, 0, st>>>(
+      DeployJob{s_a, nullptr, n_a, per_a}, DeployJob{s_b, nullptr, n_b, per_b}, amax_bits);
+  deploy_g_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(amax_bits, gr, (int)n);
+  prof_end(QAD_K_DEPLOY_SCALES, st);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_deploy_round(const float* s_a, float* sq_a, int64_t n_a, int64_t per_a, const float* s_b,
+                                float* sq_b, int64_t n_b, int64_t per_b, const float2* gr, cudaStream_t st) {
+  const int64_t n = n_a + n_b;
+  if (n == 0) return cudaSuccess;
+  if (n > 65535) return cudaErrorInvalidValue;
+  prof_begin(QAD_K_DEPLOY_SCALES, st);
+  const int64_t per4 = (per_a > per_b ? per_a : per_b) / 4;
+  const int64_t want = (per4 + 1023) / 1024;  // ~4 float4 per thread
+  deploy_round_kernel<<<dim3((unsigned)(want > 0 ? want : 1), (unsigned)n), 256, 0, st>>>(
+      DeployJob{s_a, sq_a, n_a, per_a}, DeployJob{s_b, sq_b, n_b, per_b}, gr);
+  prof_end(QAD_K_DEPLOY_SCALES, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fakequant_deployed(const void* w, const float* s, void* out, int64_t rows, int64_t K,
+                                      int64_t rows_per_mat, const float2* gr, float* sq, cudaStream_t st) {
+  const uint64_t nchunks = (uint64_t)rows * (uint64_t)(K / 16);
+  if (nchunks == 0) return cudaSuccess;
+  if (nchunks >= (1ull << 32) || rows_per_mat <= 0) return cudaErrorInvalidValue;  // 32-bit chunk -> matrix map
+  const int grid = grid_for((int64_t)nchunks, 256, 8);
+  prof_begin(QAD_K_FAKEQUANT, st);
+  fakequant_kernel<kQE2M1, false, true><<<grid, 256, 0, st>>>(static_cast<const uint4*>(w), s,
+                                                              static_cast<uint4*>(out), nchunks, 1u, nullptr, gr,
+                                                              (uint32_t)(rows_per_mat * (K / 16)), sq);
+  prof_end(QAD_K_FAKEQUANT, st);
   return cudaGetLastError();
 }
 

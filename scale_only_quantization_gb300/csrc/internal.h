@@ -25,7 +25,7 @@ struct Layout {
   size_t w13q, w2q, a1q, hq, sa_tok, sh_row;
   // QAD_FMT_NVFP4_E4M3: the deployed weight scales (0 otherwise)
   bool deployed;
-  size_t s13q, s2q;
+  size_t s13q, s2q, deploy_tmp;  // deploy_tmp: 2E words of matrix amax bits, then 2E (g, 1/g) pairs
   size_t total;
 };
 
@@ -50,6 +50,16 @@ cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, 
 // g = fp32(max |s| / 448) of that matrix; s_q may alias s
 cudaError_t launch_deploy_scales(const float* s_a, float* sq_a, int64_t n_a, int64_t per_a, const float* s_b,
                                  float* sq_b, int64_t n_b, int64_t per_b, cudaStream_t st);
+// the same for the layer calls, in parallel: gr[m] = (g, RN(1 / g)) of each of the n_a + n_b
+// (<= 65535) matrices (amax_bits: n_a + n_b words of scratch), then s_q either by
+// launch_deploy_round or inside the weight fake-quant (launch_fakequant_deployed: nvfp4, writes
+// s_q to sq besides w_hat; rows_per_mat rows of K per matrix)
+cudaError_t launch_deploy_tensor_scales(const float* s_a, int64_t n_a, int64_t per_a, const float* s_b, int64_t n_b,
+                                        int64_t per_b, uint32_t* amax_bits, float2* gr, cudaStream_t st);
+cudaError_t launch_deploy_round(const float* s_a, float* sq_a, int64_t n_a, int64_t per_a, const float* s_b,
+                                float* sq_b, int64_t n_b, int64_t per_b, const float2* gr, cudaStream_t st);
+cudaError_t launch_fakequant_deployed(const void* w, const float* s, void* out, int64_t rows, int64_t K,
+                                      int64_t rows_per_mat, const float2* gr, float* sq, cudaStream_t st);
 cudaError_t launch_route(const int32_t* idx, const Layout& L, uint8_t* ws, cudaStream_t st);
 // the same three routing kernels on explicit buffers (hdr: int32[64], zeroed by the caller;
 // chunk_counts / chunk_base: int32[nchunks * E]; mtile_expert: int32[Rmax / 128])

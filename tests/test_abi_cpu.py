@@ -259,7 +259,8 @@ def test_deployed_nvfp4_layout_and_host_checks(lib):
     up = lambda n: (n + 1023) // 1024 * 1024  # noqa: E731
     base = Q.qad_moe_workspace_bytes(Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4))
     dep = Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4_E4M3)
-    assert Q.qad_moe_workspace_bytes(dep) - base == up(4 * E * 2 * F * d // 16) + up(4 * E * d * F // 16)
+    # the deployed scales, and 2E matrix amax words plus 2E (g, 1/g) pairs
+    assert Q.qad_moe_workspace_bytes(dep) - base == up(4 * E * 2 * F * d // 16) + up(4 * E * d * F // 16) + up(24 * E)
     assert Q.qad_moe_debug_view(dep, "S13_DEPLOYED")[1] == E * 2 * F * d // 16
     assert Q.qad_moe_debug_view(dep, "S2_DEPLOYED")[1] == E * d * F // 16
     assert Q.qad_moe_debug_view(Q.shape(T, d, F, E, k, Q.QAD_FMT_NVFP4), "S13_DEPLOYED")[1] == 0
