@@ -66,3 +66,21 @@ def test_kernel_table_fractions_and_shares():
     assert abs(f["frac_of_nominal_8tbs"] - 0.5) < 1e-12
     assert "combine" not in k and k["route_permute"]["share"] is None
     assert abs(g["share"] - 2.0 / 3.0) < 1e-12 and abs(f["share"] - 1.0 / 3.0) < 1e-12
+
+
+def test_algorithmic_bytes_and_flops_per_launch():
+    """2 R N K FLOPs per GEMM launch over the routed rows; the weight fake-quant moves 2 B read +
+    the fp32 scale share + 2 B written per weight (averaged over its two launches); the deployed
+    nvfp4 format adds the read and the write of each fp32 block scale."""
+    b = _bench_module()
+    cfg = dict(T=16384, topk=8, d=2048, F=768, E=128, fmt=0)
+    alg = b.algorithmic_per_launch(cfg)
+    R = 16384 * 8
+    assert alg["gemm_fc1_swiglu_aq"] == ("tensor", 2.0 * R * 1536 * 2048)
+    assert alg["gemm_fc2"] == ("tensor", 2.0 * R * 2048 * 768)
+    n = 128 * 1536 * 2048 + 128 * 2048 * 768
+    assert alg["fakequant_w"] == ("hbm", (2 + 0.25 + 2) * n / 2)
+    assert "deploy_scales" not in alg
+    dep = b.algorithmic_per_launch(dict(cfg, fmt=6))
+    assert dep["fakequant_w"] == alg["fakequant_w"]
+    assert dep["deploy_scales"] == ("hbm", 2 * 4.0 * n / 16)
