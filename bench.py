@@ -130,8 +130,9 @@ def algorithmic_per_launch(cfg, native_fp8=False):
     d, F, E = cfg["d"], cfg["F"], cfg["E"]
     fc1 = 2.0 * R * 2 * F * d
     fc2 = 2.0 * R * d * F
+    # format 6 (deployed nvfp4): the fake-quant pass also writes each deployed fp32 block scale
     bpe = {0: 2 + 4.0 / 16 + 2, 1: 2 + 4.0 / 128 + 2, 2: None, 3: 2 + 4.0 / 16 + 2, 4: None,
-           5: 2 + 4.0 / 128 + 2, 6: 2 + 4.0 / 16 + 2}[cfg["fmt"]]
+           5: 2 + 4.0 / 128 + 2, 6: 2 + 2 * 4.0 / 16 + 2}[cfg["fmt"]]
     n13, n2 = E * 2 * F * d, E * d * F
     if bpe is None:  # one fp32 scale per row
         per_el = 5.0 if native_fp8 else 4.0
@@ -142,8 +143,8 @@ def algorithmic_per_launch(cfg, native_fp8=False):
            "gemm_dgrad_fc2_swiglu_bwd": ("tensor", fc2), "gemm_dgrad_fc1": ("tensor", fc1),
            "gemm_wgrad_fc2_scalegrad": ("tensor", fc2), "gemm_wgrad_fc1_scalegrad": ("tensor", fc1),
            "fakequant_w": ("hbm", fq)}
-    if cfg["fmt"] == 6:  # deployed scales: every fp32 block scale read once and written once
-        alg["deploy_scales"] = ("hbm", 2 * 4.0 * (n13 + n2) / 16)
+    if cfg["fmt"] == 6:  # the matrices' tensor scales: every fp32 block scale read once
+        alg["deploy_scales"] = ("hbm", 4.0 * (n13 + n2) / 16)
     return alg
 
 

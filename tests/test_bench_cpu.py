@@ -70,8 +70,8 @@ def test_kernel_table_fractions_and_shares():
 
 def test_algorithmic_bytes_and_flops_per_launch():
     """2 R N K FLOPs per GEMM launch over the routed rows; the weight fake-quant moves 2 B read +
-    the fp32 scale share + 2 B written per weight (averaged over its two launches); the deployed
-    nvfp4 format adds the read and the write of each fp32 block scale."""
+    the fp32 scale share + 2 B written per weight (averaged over its two launches); with deployed
+    nvfp4 scales it also writes each deployed scale, and the tensor-scale pass reads each scale."""
     b = _bench_module()
     cfg = dict(T=16384, topk=8, d=2048, F=768, E=128, fmt=0)
     alg = b.algorithmic_per_launch(cfg)
@@ -82,5 +82,5 @@ def test_algorithmic_bytes_and_flops_per_launch():
     assert alg["fakequant_w"] == ("hbm", (2 + 0.25 + 2) * n / 2)
     assert "deploy_scales" not in alg
     dep = b.algorithmic_per_launch(dict(cfg, fmt=6))
-    assert dep["fakequant_w"] == alg["fakequant_w"]
-    assert dep["deploy_scales"] == ("hbm", 2 * 4.0 * n / 16)
+    assert dep["fakequant_w"] == ("hbm", (2 + 0.5 + 2) * n / 2)
+    assert dep["deploy_scales"] == ("hbm", 4.0 * n / 16)
