@@ -121,3 +121,24 @@ def test_deployed_recompute_is_bit_identical():
     for x, y in ((a.out, b.out), (a.dx, b.dx)):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
     assert torch.equal(a.ds13, b.ds13) and torch.equal(a.ds2, b.ds2)
+
+
+def test_deployed_layer_with_a_zero_matrix_and_negative_scales():
+    """An expert whose w13 scales are all zero (its tensor scale is 0, so every deployed scale is 0
+    and its fake-quantized gate/up weights are signed zeros) and a few negative w2 scales (rounded
+    as their magnitude, sign kept): the layer stage by stage against the oracle, and the deployed
+    scale views."""
+    inp = _structured(seed=6)
+    inp["s13"][1].zero_()
+    inp["s2"][2, :5, :3] *= -1.0
+    run = Run(inp, flags=Q.QAD_FLAG_STASH_H)
+    assert run.error == 0
+    host = host_inputs(inp)
+    _stagewise(run, host)
+    E, d, F = inp["E"], inp["d"], inp["F"]
+    s13q = synth.to_numpy(run.view("S13_DEPLOYED", torch.float32)).astype(np.float64).reshape(E, 2 * F, d // 16)
+    s2q = synth.to_numpy(run.view("S2_DEPLOYED", torch.float32)).astype(np.float64).reshape(E, d, F // 16)
+    assert np.all(s13q[1] == 0)
+    assert np.array_equal(s13q, OQ.effective_weight_scales(FMT, host["s13"]))
+    assert np.array_equal(s2q, OQ.effective_weight_scales(FMT, host["s2"]))
+    assert np.all(s2q[2, :5, :3] < 0)
