@@ -745,3 +745,23 @@ def test_deploy_scales_all_zero_matrix_and_row():
     assert np.all(s_a[0] == 0) and np.all(s_a[1, 16:] == 0)
     assert np.all(s_a[1, :16] == Q.round_f32(Q.round_f32(Q.round_f32(1.5 / 6.0) / 448.0) * 448.0))
     assert np.array_equal(Q.fakequant_act(Q.FMT_NVFP4_E4M3, a)[1, 3], 1.5)
+
+
+def test_deployed_activation_scales_against_torch_cast():
+    """Format 6 activations: per 16-block fp32(amax / 6), rounded as deployed NVFP4 stores it under
+    one fp32 scale per row (the row's largest block scale / 448), the E4M3 rounding done by torch's
+    float8_e4m3fn cast; rows spanning many binades, a zero block and a zero row included."""
+    rng = np.random.default_rng(32)
+    a = rng.standard_normal((7, 256)) * 2.0 ** rng.integers(-20, 4, (7, 16)).repeat(16, axis=1)
+    a[2, 32:48] = 0.0
+    a[5] = 0.0
+    a = Q.round_bf16(a)
+    got = Q.act_scale(Q.FMT_NVFP4_E4M3, a)[:, ::16]
+    at = torch.from_numpy(a).float()
+    sb = at.abs().reshape(7, 16, 16).amax(-1) / 6.0
+    g = sb.amax(-1, keepdim=True) / 448.0
+    safe = torch.where(g == 0, torch.ones_like(g), g)
+    sq = ((sb / safe).to(torch.float8_e4m3fn).float() * g)
+    want = torch.where(g == 0, torch.zeros_like(sq), sq).double().numpy()
+    assert np.array_equal(got, want)
+    assert np.all(got[5] == 0) and got[2, 2] == 0
