@@ -471,22 +471,30 @@ def run_ours(args):
 
 def other_configs(Q, args, dev, stream, barrier, local, tf_burst, tf_sust, hbm, peak_src):
     """A short timed run of every other workload (same step, default flags): tokens/s, ms per
-    step, and the dominant kernel against the peak of that run's own clock regime."""
+    step, and the dominant kernel against the peak of that run's own clock regime.  The fp8
+    workloads run once more with the forward GEMMs on the E4M3 tensor path (QAD_FLAG_NATIVE_FP8,
+    key suffix "+native_fp8")."""
     res = {}
+    runs = []
     for name in sorted(synth.WORKLOADS):
-        if name == args.workload:
-            continue
+        if name != args.workload:
+            runs.append((name, name, 0))
+        if synth.WORKLOADS[name]["fmt"] == synth.FMT_FP8_ROW and not args.native_fp8:
+            runs.append((name + "+native_fp8", name, Q.QAD_FLAG_NATIVE_FP8))
+    for key, name, flags in runs:
         cfg = synth.workload(name)
         inp = synth.make_inputs(cfg, seed=0, device=dev)
-        layer = Layer(Q, inp, 0, dev)
+        layer = Layer(Q, inp, flags, dev)
+        native = (flags & Q.QAD_FLAG_NATIVE_FP8) != 0
         ms, prof, launches, clk = timed_steps(Q, layer, stream, dev, args.config_steps, 3, barrier, local)
         clocks = clk.summary()
         peak, peak_name = tensor_peak(clocks, tf_burst, tf_sust)
-        alg = algorithmic_per_launch(cfg)
-        kernels = kernel_table(prof, args.config_steps, alg, peak, tf_burst, tf_sust, hbm)
-        roof = dominant_roofline(kernels, alg, peak, peak_name, hbm, peak_src, (), name)
+        alg = algorithmic_per_launch(cfg, native_fp8=native)
+        f8_kernels = ("gemm_fc1_swiglu_aq", "gemm_fc2") if native else ()
+        kernels = kernel_table(prof, args.config_steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels)
+        roof = dominant_roofline(kernels, alg, peak, peak_name, hbm, peak_src, f8_kernels, name)
         step_tf = synth.tokens_to_flops(cfg) / (ms / 1e3) / 1e12
-        res[name] = {"value": cfg["T"] / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+        res[key] = {"value": cfg["T"] / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
                      "steps": args.config_steps, "format": FMT_NAME[cfg["fmt"]],
                      "routing": cfg.get("routing", "uniform"), "step_tflops": step_tf,
                      "step_tensor_frac": step_tf / peak, "gpu_launches": int(launches),
