@@ -148,6 +148,15 @@ def algorithmic_per_launch(cfg, native_fp8=False):
     return alg
 
 
+def side_stream_bytes(cfg):
+    """Bytes per step that the routing and the token scatter move on the library's side stream
+    while the weight fake-quant runs: the routing indices read and the pair-to-row maps written
+    (int32), every token row read once and written to each of its routed rows (bf16)."""
+    T, k, d = cfg["T"], cfg["topk"], cfg["d"]
+    R = T * k
+    return 4.0 * R + 4.0 * 3 * R + 2.0 * T * d + 2.0 * R * d
+
+
 def _traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary (profiles/traffic.txt), or None
     when the kernel's sources have changed since the counters were taken."""
@@ -186,9 +195,12 @@ def tensor_peak(clocks, tf_burst, tf_sust):
         sm, mx, ",".join(reasons) or "none")
 
 
-def kernel_table(prof, steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels=()):
+def kernel_table(prof, steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels=(), side_bytes=None):
     """Per kernel: time per launch, launches per step, share of the step's serial kernel time,
-    and for the GEMMs and the weight fake-quant the achieved rate against the peaks."""
+    and for the GEMMs and the weight fake-quant the achieved rate against the peaks.  With
+    `side_bytes` (bytes per step of the side-stream kernels that run beside the fake-quant), the
+    fake-quant entry also gives the rate of the whole memory phase: its own bytes and those over
+    the fake-quant launches' time."""
     kernels = {}
     for name, (tot, n) in prof.items():
         if n == 0:
@@ -209,6 +221,13 @@ def kernel_table(prof, steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels=()):
                 entry.update(achieved_gbs=per_s / 1e9, frac=per_s / 1e9 / hbm,
                              frac_of_nominal_8tbs=per_s / 1e9 / NOMINAL_HBM_GBS)
         kernels[name] = entry
+    fq = kernels.get("fakequant_w")
+    if fq is not None and side_bytes and "fakequant_w" in alg and any(
+            "overlapped_with" in v for v in kernels.values()):
+        n = fq["launches_per_step"]
+        moved = alg["fakequant_w"][1] * n + side_bytes
+        rate = moved / (fq["ms_per_launch"] * n / 1e3) / 1e9
+        fq["with_side_stream"] = {"bytes_per_step": moved, "achieved_gbs": rate, "frac": rate / hbm}
     total_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values() if "overlapped_with" not in v)
     for v in kernels.values():
         if "overlapped_with" not in v:
@@ -407,7 +426,8 @@ def run_ours(args):
     peak, peak_name = tensor_peak(clocks, tf_burst, tf_sust)
     alg = algorithmic_per_launch(cfg, native_fp8=args.native_fp8)
     f8_kernels = ("gemm_fc1_swiglu_aq", "gemm_fc2") if args.native_fp8 else ()
-    kernels = kernel_table(prof, args.steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels)
+    kernels = kernel_table(prof, args.steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels,
+                           side_bytes=side_stream_bytes(cfg))
     roof = dominant_roofline(kernels, alg, peak, peak_name, hbm, peak_src, f8_kernels, args.workload)
     flops_step = synth.tokens_to_flops(cfg)
     step_tf = flops_step / (ms / 1e3) / 1e12
@@ -491,7 +511,8 @@ def other_configs(Q, args, dev, stream, barrier, local, tf_burst, tf_sust, hbm, 
         peak, peak_name = tensor_peak(clocks, tf_burst, tf_sust)
         alg = algorithmic_per_launch(cfg, native_fp8=native)
         f8_kernels = ("gemm_fc1_swiglu_aq", "gemm_fc2") if native else ()
-        kernels = kernel_table(prof, args.config_steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels)
+        kernels = kernel_table(prof, args.config_steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels,
+                               side_bytes=side_stream_bytes(cfg))
         roof = dominant_roofline(kernels, alg, peak, peak_name, hbm, peak_src, f8_kernels, name)
         step_tf = synth.tokens_to_flops(cfg) / (ms / 1e3) / 1e12
         res[key] = {"value": cfg["T"] / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,

@@ -84,3 +84,20 @@ def test_algorithmic_bytes_and_flops_per_launch():
     dep = b.algorithmic_per_launch(dict(cfg, fmt=6))
     assert dep["fakequant_w"] == ("hbm", (2 + 0.5 + 2) * n / 2)
     assert dep["deploy_scales"] == ("hbm", 4.0 * n / 16)
+
+
+def test_memory_phase_with_the_side_stream():
+    """The fake-quant entry's memory-phase rate: its own bytes over its launches plus the bytes of
+    the side-stream kernels (routing maps, token rows read once and written to each routed row),
+    over the fake-quant launches' time; absent when nothing ran beside it."""
+    b = _bench_module()
+    cfg = dict(T=16384, topk=8, d=2048, F=768, E=128, fmt=0)
+    R = 16384 * 8
+    assert b.side_stream_bytes(cfg) == 4.0 * R + 12.0 * R + 2.0 * 16384 * 2048 + 2.0 * R * 2048
+    alg = {"fakequant_w": ("hbm", 1e9)}
+    prof = {"fakequant_w": (1.0, 4), "route_permute": (0.5, 2)}
+    k = b.kernel_table(prof, 2, alg, 2000.0, 2000.0, 1000.0, 5000.0, side_bytes=1e9)
+    ph = k["fakequant_w"]["with_side_stream"]
+    assert ph["bytes_per_step"] == 3e9 and abs(ph["achieved_gbs"] - 6000.0) < 1e-9 and abs(ph["frac"] - 1.2) < 1e-12
+    k = b.kernel_table({"fakequant_w": (1.0, 4)}, 2, alg, 2000.0, 2000.0, 1000.0, 5000.0, side_bytes=1e9)
+    assert "with_side_stream" not in k["fakequant_w"]
