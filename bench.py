@@ -198,9 +198,10 @@ def tensor_peak(clocks, tf_burst, tf_sust):
 def kernel_table(prof, steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels=(), side_bytes=None):
     """Per kernel: time per launch, launches per step, share of the step's serial kernel time,
     and for the GEMMs and the weight fake-quant the achieved rate against the peaks.  With
-    `side_bytes` (bytes per step of the side-stream kernels that run beside the fake-quant), the
+    `side_bytes` (bytes per step of the side-stream kernels that start beside the fake-quant), the
     fake-quant entry also gives the rate of the whole memory phase: its own bytes and those over
-    the fake-quant launches' time."""
+    the phase's time, the longer of the fake-quant launches and the side-stream launches (both
+    start at the fork; the GEMMs wait for both)."""
     kernels = {}
     for name, (tot, n) in prof.items():
         if n == 0:
@@ -226,8 +227,11 @@ def kernel_table(prof, steps, alg, peak, tf_burst, tf_sust, hbm, f8_kernels=(), 
             "overlapped_with" in v for v in kernels.values()):
         n = fq["launches_per_step"]
         moved = alg["fakequant_w"][1] * n + side_bytes
-        rate = moved / (fq["ms_per_launch"] * n / 1e3) / 1e9
-        fq["with_side_stream"] = {"bytes_per_step": moved, "achieved_gbs": rate, "frac": rate / hbm}
+        side_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values() if "overlapped_with" in v)
+        phase_ms = max(fq["ms_per_launch"] * n, side_ms)
+        rate = moved / (phase_ms / 1e3) / 1e9
+        fq["with_side_stream"] = {"bytes_per_step": moved, "phase_ms": phase_ms, "achieved_gbs": rate,
+                                  "frac": rate / hbm}
     total_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for v in kernels.values() if "overlapped_with" not in v)
     for v in kernels.values():
         if "overlapped_with" not in v:

@@ -63,34 +63,45 @@ __device__ __forceinline__ float deploy_chunk(float s, const float2* __restrict_
   return v;
 }
 
+// A persistent grid of three 256-thread CTAs per SM (the registers of three fit; see the
+// launchers): with the next two chunks of each thread loaded ahead of the current two, ~96 KB
+// of weights per SM are in flight, which the memory system needs to run near its copy rate
+// (with one pair per thread at a time and eight CTAs per SM the pass ran ~10% slower).
 template <int QK, bool CODES = false, bool DEPLOY = false>
-__global__ void __launch_bounds__(256) fakequant_kernel(const uint4* __restrict__ w, const float* __restrict__ s,
-                                                        uint4* __restrict__ out, uint64_t nchunks, uint32_t cps,
-                                                        uint4* __restrict__ codes = nullptr,
-                                                        const float2* __restrict__ gr = nullptr, uint32_t cpm = 1,
-                                                        float* __restrict__ sq = nullptr) {
+__global__ void __launch_bounds__(256, 3) fakequant_kernel(const uint4* __restrict__ w, const float* __restrict__ s,
+                                                           uint4* __restrict__ out, uint64_t nchunks, uint32_t cps,
+                                                           uint4* __restrict__ codes = nullptr,
+                                                           const float2* __restrict__ gr = nullptr, uint32_t cpm = 1,
+                                                           float* __restrict__ sq = nullptr) {
   static_assert(!DEPLOY || (QK == kQE2M1 && !CODES), "deployed scales: nvfp4 weights, one scale per chunk");
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; c + stride < nchunks; c += 2 * stride) {  // two chunks (64 bytes) per thread in flight
-    const uint64_t c2 = c + stride;
-    const uint4 u0 = ld_stream(w + 2 * c), u1 = ld_stream(w + 2 * c + 1);
-    const uint4 u2 = ld_stream(w + 2 * c2), u3 = ld_stream(w + 2 * c2 + 1);
-    float sc = __ldg(s + (cps == 1 ? c : c / cps));
-    float sc2 = __ldg(s + (cps == 1 ? c2 : c2 / cps));
-    if constexpr (DEPLOY) {
-      sc = deploy_chunk(sc, gr, cpm, sq, c);
-      sc2 = deploy_chunk(sc2, gr, cpm, sq, c2);
+  // two chunks (64 bytes) per thread per iteration, and the next iteration's two chunks loaded
+  // before this one's arithmetic: 128 bytes of weights per thread in flight
+  auto load = [&](uint64_t cc, uint4& x0, uint4& x1, float& sc) {
+    x0 = ld_stream(w + 2 * cc);
+    x1 = ld_stream(w + 2 * cc + 1);
+    sc = __ldg(s + (cps == 1 ? cc : cc / cps));
+  };
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  uint4 a0 = z4, a1 = z4, b0 = z4, b1 = z4;
+  float sa = 0.0f, sb = 0.0f;
+  if (c < nchunks) load(c, a0, a1, sa);
+  if (c + stride < nchunks) load(c + stride, b0, b1, sb);
+  for (; c < nchunks; c += 2 * stride) {
+    const uint64_t c2 = c + stride, n = c + 2 * stride;
+    uint4 na0 = z4, na1 = z4, nb0 = z4, nb1 = z4;
+    float nsa = 0.0f, nsb = 0.0f;
+    if (n < nchunks) load(n, na0, na1, nsa);
+    if (n + stride < nchunks) load(n + stride, nb0, nb1, nsb);
+    if constexpr (DEPLOY) sa = deploy_chunk(sa, gr, cpm, sq, c);
+    fakequant_chunk<QK, CODES>(a0, a1, sa, out, codes, c);
+    if (c2 < nchunks) {
+      if constexpr (DEPLOY) sb = deploy_chunk(sb, gr, cpm, sq, c2);
+      fakequant_chunk<QK, CODES>(b0, b1, sb, out, codes, c2);
     }
-    fakequant_chunk<QK, CODES>(u0, u1, sc, out, codes, c);
-    fakequant_chunk<QK, CODES>(u2, u3, sc2, out, codes, c2);
-  }
-  for (; c < nchunks; c += stride) {
-    const uint4 u0 = ld_stream(w + 2 * c);
-    const uint4 u1 = ld_stream(w + 2 * c + 1);
-    float sc = __ldg(s + (cps == 1 ? c : c / cps));
-    if constexpr (DEPLOY) sc = deploy_chunk(sc, gr, cpm, sq, c);
-    fakequant_chunk<QK, CODES>(u0, u1, sc, out, codes, c);
+    a0 = na0; a1 = na1; b0 = nb0; b1 = nb1;
+    sa = nsa; sb = nsb;
   }
 }
 
@@ -863,7 +874,7 @@ cudaError_t launch_fakequant(int fmt, const void* w, const float* s, void* out, 
                              cudaStream_t st, void* codes) {
   const uint64_t nchunks = (uint64_t)rows * (uint64_t)(K / 16);
   if (nchunks == 0) return cudaSuccess;
-  const int grid = grid_for((int64_t)nchunks, 256, 8);
+  const int grid = grid_for((int64_t)nchunks, 256, 3);
   const uint4* wi = static_cast<const uint4*>(w);
   uint4* o = static_cast<uint4*>(out);
   prof_begin(QAD_K_FAKEQUANT, st);
@@ -931,7 +942,7 @@ cudaError_t launch_fakequant_deployed(const void* w, const float* s, void* out, 
   const uint64_t nchunks = (uint64_t)rows * (uint64_t)(K / 16);
   if (nchunks == 0) return cudaSuccess;
   if (nchunks >= (1ull << 32) || rows_per_mat <= 0) return cudaErrorInvalidValue;  // 32-bit chunk -> matrix map
-  const int grid = grid_for((int64_t)nchunks, 256, 8);
+  const int grid = grid_for((int64_t)nchunks, 256, 3);
   prof_begin(QAD_K_FAKEQUANT, st);
   fakequant_kernel<kQE2M1, false, true><<<grid, 256, 0, st>>>(static_cast<const uint4*>(w), s,
                                                               static_cast<uint4*>(out), nchunks, 1u, nullptr, gr,

@@ -89,7 +89,8 @@ def test_algorithmic_bytes_and_flops_per_launch():
 def test_memory_phase_with_the_side_stream():
     """The fake-quant entry's memory-phase rate: its own bytes over its launches plus the bytes of
     the side-stream kernels (routing maps, token rows read once and written to each routed row),
-    over the fake-quant launches' time; absent when nothing ran beside it."""
+    over the phase (the longer of the fake-quant launches and the side-stream launches); absent
+    when nothing ran beside it."""
     b = _bench_module()
     cfg = dict(T=16384, topk=8, d=2048, F=768, E=128, fmt=0)
     R = 16384 * 8
@@ -99,5 +100,9 @@ def test_memory_phase_with_the_side_stream():
     k = b.kernel_table(prof, 2, alg, 2000.0, 2000.0, 1000.0, 5000.0, side_bytes=1e9)
     ph = k["fakequant_w"]["with_side_stream"]
     assert ph["bytes_per_step"] == 3e9 and abs(ph["achieved_gbs"] - 6000.0) < 1e-9 and abs(ph["frac"] - 1.2) < 1e-12
+    # a side stream longer than the fake-quant sets the phase: 0.5 + 0.25 ms
+    prof = {"fakequant_w": (1.0, 4), "route_permute": (1.0, 2), "gather_rows": (0.5, 2)}
+    ph = b.kernel_table(prof, 2, alg, 2000.0, 2000.0, 1000.0, 5000.0, side_bytes=1e9)["fakequant_w"]["with_side_stream"]
+    assert abs(ph["phase_ms"] - 0.75) < 1e-12 and abs(ph["achieved_gbs"] - 4000.0) < 1e-9
     k = b.kernel_table({"fakequant_w": (1.0, 4)}, 2, alg, 2000.0, 2000.0, 1000.0, 5000.0, side_bytes=1e9)
     assert "with_side_stream" not in k["fakequant_w"]
