@@ -47,7 +47,10 @@ def _special_weights(E, N, K, fmt, seed):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("E,N,K", [(3, 64, 512), (1, 5, 256), (2, 128, 2048)])
+# the last shape has more 16-element chunks (277,560) than two passes of the persistent grid's
+# threads over them (3 CTAs x 256 threads x 152 SMs = 116,736 per pass), and not a multiple of
+# that: every thread runs several iterations of its load-ahead loop and the last ones are ragged
+@pytest.mark.parametrize("E,N,K", [(3, 64, 512), (1, 5, 256), (2, 128, 2048), (5, 771, 1152)])
 def test_fakequant_bit_exact(fmt, E, N, K):
     w, s = _special_weights(E, N, K, fmt, seed=100 + fmt)
     out = torch.empty_like(w)
