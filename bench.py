@@ -259,15 +259,27 @@ class Layer:
                                                          device=self.ws.device),
                 torch.empty_like(inp["s13"]), torch.empty_like(inp["s2"]))
 
-    def step(self, stream, x, idx, p, dout, outs=None, average=None):
-        Q, inp = self.Q, self.inp
-        out, dx, dprobs, ds13, ds2 = outs if outs is not None else self.outs
-        Q.qad_moe_fwd(self.s, x, idx, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], out, self.ws, stream)
-        Q.qad_moe_bwd_dgrad(self.s, dout, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], dx, dprobs, self.ws,
-                            stream)
-        Q.qad_moe_bwd_scalegrad(self.s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], ds13, ds2, 0, self.ws, stream)
+    def fwd(self, stream, x, idx, p, outs):
+        inp = self.inp
+        self.Q.qad_moe_fwd(self.s, x, idx, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], outs[0], self.ws, stream)
+
+    def dgrad(self, stream, p, dout, outs):
+        inp = self.inp
+        self.Q.qad_moe_bwd_dgrad(self.s, dout, p, inp["w13"], inp["s13"], inp["w2"], inp["s2"], outs[1], outs[2],
+                                 self.ws, stream)
+
+    def scalegrad(self, stream, outs, average=None):
+        inp = self.inp
+        self.Q.qad_moe_bwd_scalegrad(self.s, inp["w13"], inp["s13"], inp["w2"], inp["s2"], outs[3], outs[4], 0,
+                                     self.ws, stream)
         if average is not None:
-            average([ds13, ds2])
+            average([outs[3], outs[4]])
+
+    def step(self, stream, x, idx, p, dout, outs=None, average=None):
+        outs = outs if outs is not None else self.outs
+        self.fwd(stream, x, idx, p, outs)
+        self.dgrad(stream, p, dout, outs)
+        self.scalegrad(stream, outs, average)
 
 
 def timed_steps(Q, layer, stream, dev, steps, warmup, barrier, local, average=None):
@@ -303,10 +315,14 @@ def timed_steps(Q, layer, stream, dev, steps, warmup, barrier, local, average=No
 def e2e_steps(layer, stream, dev, steps, warmup, barrier, local, average=None):
     """The same step end to end through the public calls: every step copies its inputs (x,
     topk_idx, topk_w, dout) from pinned host memory and reads its results (out, dx, dprobs,
-    ds13, ds2) back to pinned host memory.  Double-buffered as an input pipeline runs it:
-    one copy stream moves step i+1's inputs to the device while the compute stream runs step
-    i, and a second copy stream moves step i's results to the host, so the two directions of
-    the host link run at the same time.  Returns (ms per step, H2D bytes, D2H bytes, clocks)."""
+    ds13, ds2) back to pinned host memory.  Double-buffered as an input pipeline runs it: one
+    copy stream moves step i+1's inputs to the device while the compute stream runs step i (the
+    forward's inputs first, dout after them: the forward waits only for its own), and a second
+    copy stream moves each result down as soon as the call that writes it has finished (out after
+    the forward, dx and dprobs after the input gradient, the scale gradients after the last
+    call), so the two directions of the host link run at the same time and a short run's first
+    and last steps wait for as few bytes as possible.  Returns (ms per step, H2D bytes, D2H
+    bytes, clocks)."""
     inp = layer.inp
     args_dev = (inp["x"], inp["topk_idx"], inp["topk_w"], inp["dout"])
     host_in = [[a.cpu().pin_memory() for a in args_dev] for _ in range(2)]
@@ -316,37 +332,57 @@ def e2e_steps(layer, stream, dev, steps, warmup, barrier, local, average=None):
     h2d = sum(a.numel() * a.element_size() for a in host_in[0])
     d2h = sum(a.numel() * a.element_size() for a in host_out[0])
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_read = [torch.cuda.Event() for _ in range(2)]
+    ev = {name: [torch.cuda.Event() for _ in range(2)]
+          for name in ("in_fwd", "in_bwd", "fwd", "dgrad", "done", "out", "dx", "ds")}
+
+    def copy(dsts, srcs):
+        for dst, src in zip(dsts, srcs):
+            dst.copy_(src, non_blocking=True)
+
+    def inputs_up(b):
+        with torch.cuda.stream(up):
+            copy(dev_in[b][:3], host_in[b][:3])  # x, topk_idx, topk_w: the forward's inputs
+            ev["in_fwd"][b].record(up)
+            copy(dev_in[b][3:], host_in[b][3:])  # dout
+            ev["in_bwd"][b].record(up)
 
     def run(n):
         up.wait_stream(stream)
         down.wait_stream(stream)
-        with torch.cuda.stream(up):
-            for dst, src in zip(dev_in[0], host_in[0]):
-                dst.copy_(src, non_blocking=True)
-            ev_in[0].record(up)
+        inputs_up(0)
         for i in range(n):
             b = i % 2
-            stream.wait_event(ev_in[b])
+            x, idx, p, dout = dev_in[b]
+            outs = dev_out[b]
+            stream.wait_event(ev["in_fwd"][b])
             if i >= 2:
-                stream.wait_event(ev_read[b])  # step i-2's results have left dev_out[b]
-            layer.step(stream, *dev_in[b], outs=dev_out[b], average=average)
-            ev_done[b].record(stream)
+                stream.wait_event(ev["out"][b])  # step i-2's out has left dev_out[b]
+            layer.fwd(stream, x, idx, p, outs)
+            ev["fwd"][b].record(stream)
+            stream.wait_event(ev["in_bwd"][b])
+            if i >= 2:
+                stream.wait_event(ev["dx"][b])
+            layer.dgrad(stream, p, dout, outs)
+            ev["dgrad"][b].record(stream)
+            if i >= 2:
+                stream.wait_event(ev["ds"][b])
+            layer.scalegrad(stream, outs, average)
+            ev["done"][b].record(stream)
             if i + 1 < n:
                 nb = (i + 1) % 2
-                with torch.cuda.stream(up):
-                    if i >= 1:
-                        up.wait_event(ev_done[nb])  # step i-1 has finished reading dev_in[nb]
-                    for dst, src in zip(dev_in[nb], host_in[nb]):
-                        dst.copy_(src, non_blocking=True)
-                    ev_in[nb].record(up)
+                if i >= 1:
+                    up.wait_event(ev["dgrad"][nb])  # step i-1 has finished reading dev_in[nb]
+                inputs_up(nb)
             with torch.cuda.stream(down):
-                down.wait_event(ev_done[b])
-                for dst, src in zip(host_out[b], dev_out[b]):
-                    dst.copy_(src, non_blocking=True)
-                ev_read[b].record(down)
+                down.wait_event(ev["fwd"][b])
+                copy(host_out[b][:1], outs[:1])
+                ev["out"][b].record(down)
+                down.wait_event(ev["dgrad"][b])
+                copy(host_out[b][1:3], outs[1:3])
+                ev["dx"][b].record(down)
+                down.wait_event(ev["done"][b])
+                copy(host_out[b][3:], outs[3:])
+                ev["ds"][b].record(down)
         stream.wait_stream(up)
         stream.wait_stream(down)
 
@@ -462,8 +498,9 @@ def run_ours(args):
         "e2e": {"value": T * world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "link_gbs": (h2d + d2h) / (ms_e2e / 1e3) / 1e9, "clocks": clk_e2e.summary(),
-                "note": "pinned host buffers; step i+1's inputs go up on one copy stream and step i's results "
-                        "come down on another while step i+1 computes"},
+                "note": "pinned host buffers; step i+1's inputs go up on one copy stream (the forward's first, "
+                        "dout after them) while step i computes, and each of step i's results comes down on "
+                        "another as soon as the call that writes it has finished"},
     }
     del layer
     torch.cuda.empty_cache()
