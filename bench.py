@@ -312,7 +312,7 @@ def timed_steps(Q, layer, stream, dev, steps, warmup, barrier, local, average=No
     return ms, prof, launches, clk
 
 
-def e2e_steps(layer, stream, dev, steps, warmup, barrier, local, average=None):
+def e2e_steps(layer, stream, dev, steps, warmup, barrier, local, average=None, host_in=None, results=None):
     """The same step end to end through the public calls: every step copies its inputs (x,
     topk_idx, topk_w, dout) from pinned host memory and reads its results (out, dx, dprobs,
     ds13, ds2) back to pinned host memory.  Double-buffered as an input pipeline runs it: one
@@ -322,10 +322,13 @@ def e2e_steps(layer, stream, dev, steps, warmup, barrier, local, average=None):
     the forward, dx and dprobs after the input gradient, the scale gradients after the last
     call), so the two directions of the host link run at the same time and a short run's first
     and last steps wait for as few bytes as possible.  Returns (ms per step, H2D bytes, D2H
-    bytes, clocks)."""
+    bytes, clocks).  `host_in` (two lists of pinned x, topk_idx, topk_w, dout) replaces the
+    layer's own inputs in the two buffers (step i uses buffer i % 2); with `results` (a list)
+    the two buffers' host results are appended to it after the run."""
     inp = layer.inp
     args_dev = (inp["x"], inp["topk_idx"], inp["topk_w"], inp["dout"])
-    host_in = [[a.cpu().pin_memory() for a in args_dev] for _ in range(2)]
+    if host_in is None:
+        host_in = [[a.cpu().pin_memory() for a in args_dev] for _ in range(2)]
     dev_in = [[torch.empty_like(a) for a in args_dev] for _ in range(2)]
     dev_out = [layer.new_outputs() for _ in range(2)]
     host_out = [[torch.empty(a.shape, dtype=a.dtype, pin_memory=True) for a in dev_out[0]] for _ in range(2)]
@@ -395,6 +398,8 @@ def e2e_steps(layer, stream, dev, steps, warmup, barrier, local, average=None):
         run(steps)
         e1.record(stream)
         barrier()
+    if results is not None:
+        results.extend(host_out)
     return e0.elapsed_time(e1) / steps, h2d, d2h, clk
 
 
